@@ -1,0 +1,314 @@
+"""Thin Python binding of the C ABI in include/eagle.h (argument marshalling
+only: every step of the path runs in the library's CUDA kernels).
+
+The functions carry the C names.  Tensors are torch tensors on the current
+CUDA device; workspaces are uint8 tensors that the binding allocates
+zero-filled when the caller passes none.  If the library is missing the
+first call raises: there is no fallback path.
+"""
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle.so")
+
+EAGLE_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape",
+                3: "workspace too small", 4: "CUDA error", 5: "device wait timed out",
+                6: "device invariant violated"}
+EAGLE_F32 = 0
+EAGLE_BF16 = 1
+MAX_TOP_K = 64
+MAX_DEPTH = 16
+MAX_CANDIDATES = 2048
+MAX_TREE = 256
+MAX_BATCH = 32
+
+
+class EagleError(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status})")
+        self.status = status
+
+
+class CTree(ctypes.Structure):
+    _fields_ = [("parents", ctypes.c_void_p), ("tokens", ctypes.c_void_p),
+                ("depth", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("mask", ctypes.c_void_p), ("values", ctypes.c_void_p),
+                ("m", ctypes.c_int32), ("mask_words", ctypes.c_int32)]
+
+
+class CSampling(ctypes.Structure):
+    _fields_ = [("greedy", ctypes.c_int32), ("temperature", ctypes.c_float),
+                ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
+
+class CAttnItem(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p),
+                ("v_cache", ctypes.c_void_p), ("tree_k", ctypes.c_void_p),
+                ("tree_v", ctypes.c_void_p), ("mask", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("cache_head_stride", ctypes.c_int64),
+                ("prefix_len", ctypes.c_int32), ("m", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_U64 = ctypes.c_uint64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+EXPORTS = {
+    "eagle_status_string": (ctypes.c_char_p, [_I32]),
+    "eagle_version": (_I32, []),
+    "eagle_workspace_init": (_I32, [_P, _SZ, _P]),
+    "eagle_workspace_error": (_I32, [_P, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "eagle_tree_build_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "eagle_tree_build": (_I32, [_P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, CTree, _P, _SZ, _P]),
+    "eagle_tree_build_batched": (_I32, [_I32, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P,
+                                        _P, _SZ, _P]),
+    "eagle_tree_attn_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "eagle_tree_attn": (_I32, [_P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
+                               _F, _P, _P, _SZ, _P]),
+    "eagle_tree_attn_batched_workspace_size": (_SZ, [_P, _I32, _I32, _I32, _I32, _I32]),
+    "eagle_tree_attn_batched": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _F, _P, _SZ, _P]),
+    "eagle_tree_verify_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "eagle_tree_verify": (_I32, [_P, _I64, _I32, CTree, ctypes.POINTER(CSampling), _U64, _U64,
+                                 _P, _P, _P, _P, _SZ, _P]),
+    "eagle_tree_verify_batched": (_I32, [_I32, _P, _I64, _I32, _P, _P, _P, _U64, _P, _P, _P,
+                                         _P, _SZ, _P]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded C library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status, what):
+    if status != EAGLE_OK:
+        raise EagleError(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def workspace(nbytes, device=None):
+    """Zero-filled uint8 workspace of at least nbytes (256-byte aligned)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8,
+                       device=device or torch.device("cuda"))
+
+
+def workspace_error(ws, stream=None):
+    st, detail = _I32(0), _I32(0)
+    _check(lib().eagle_workspace_error(_ptr(ws), _stream(stream), ctypes.byref(st),
+                                       ctypes.byref(detail)), "eagle_workspace_error")
+    return st.value, detail.value
+
+
+class Tree:
+    """Device arrays of one draft tree (see eagle_tree in include/eagle.h)."""
+
+    def __init__(self, m, device=None, with_values=True):
+        dev = device or torch.device("cuda")
+        self.m = int(m)
+        self.mask_words = (self.m + 63) // 64
+        self.parents = torch.empty(self.m, dtype=torch.int32, device=dev)
+        self.tokens = torch.empty(self.m, dtype=torch.int32, device=dev)
+        self.depth = torch.empty(self.m, dtype=torch.int32, device=dev)
+        self.pos = torch.empty(self.m, dtype=torch.int32, device=dev)
+        self.mask = torch.empty(self.m * self.mask_words, dtype=torch.int64, device=dev)
+        self.values = torch.empty(self.m, dtype=torch.float64, device=dev) if with_values else None
+
+    def c(self):
+        return CTree(self.parents.data_ptr(), self.tokens.data_ptr(), self.depth.data_ptr(),
+                     self.pos.data_ptr(), self.mask.data_ptr(),
+                     self.values.data_ptr() if self.values is not None else 0,
+                     self.m, self.mask_words)
+
+    @staticmethod
+    def from_arrays(parents, tokens, device=None):
+        """Tree with given parents/tokens (other arrays left unset)."""
+        parents = torch.as_tensor(parents, dtype=torch.int32)
+        t = Tree(parents.numel(), device, with_values=False)
+        t.parents.copy_(parents)
+        t.tokens.copy_(torch.as_tensor(tokens, dtype=torch.int32))
+        return t
+
+    def mask_u64(self):
+        """mask as a host numpy uint64 array [m, mask_words]."""
+        return self.mask.cpu().numpy().view("uint64").reshape(self.m, self.mask_words)
+
+
+# ------------------------------------------------------------------ build
+def eagle_tree_build_workspace_size(n_items, n_rows, vocab, top_k, depth, total_tokens):
+    return lib().eagle_tree_build_workspace_size(n_items, n_rows, vocab, top_k, depth,
+                                                 total_tokens)
+
+
+def eagle_tree_build(draft_logits, top_k, depth, total_tokens, root_token, out=None, ws=None,
+                     stream=None):
+    """draft_logits: fp32 CUDA tensor [n_rows, vocab] (row stride may exceed vocab)."""
+    n_rows, vocab = draft_logits.shape
+    out = out or Tree(total_tokens, draft_logits.device)
+    if ws is None:
+        ws = workspace(eagle_tree_build_workspace_size(1, n_rows, vocab, top_k, depth,
+                                                       total_tokens), draft_logits.device)
+    _check(lib().eagle_tree_build(_ptr(draft_logits), draft_logits.stride(0), n_rows, vocab,
+                                  top_k, depth, total_tokens, int(root_token), out.c(), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "eagle_tree_build")
+    return out
+
+
+def eagle_tree_build_batched(draft_logits, top_k, depth, total_tokens, root_tokens, outs=None,
+                             ws=None, stream=None):
+    """draft_logits: list of fp32 CUDA tensors [n_rows, vocab], same shape/stride."""
+    n = len(draft_logits)
+    n_rows, vocab = draft_logits[0].shape
+    outs = outs or [Tree(total_tokens, draft_logits[0].device) for _ in range(n)]
+    if ws is None:
+        ws = workspace(eagle_tree_build_workspace_size(n, n_rows, vocab, top_k, depth,
+                                                       total_tokens), draft_logits[0].device)
+    ptrs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in draft_logits])
+    roots = (ctypes.c_int32 * n)(*[int(r) for r in root_tokens])
+    trees = (CTree * n)(*[o.c() for o in outs])
+    _check(lib().eagle_tree_build_batched(n, ptrs, draft_logits[0].stride(0), n_rows, vocab,
+                                          top_k, depth, total_tokens, roots, trees, _ptr(ws),
+                                          ws.numel(), _stream(stream)),
+           "eagle_tree_build_batched")
+    return outs
+
+
+# -------------------------------------------------------------- attention
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return EAGLE_F32
+    if t.dtype == torch.bfloat16:
+        return EAGLE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def attn_item(q, k_cache, v_cache, tree_k, tree_v, mask, out, prefix_len=None):
+    """C item for one attention problem (k/v cache [Hkv, cap, d])."""
+    S = k_cache.shape[1] if prefix_len is None else int(prefix_len)
+    return CAttnItem(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), tree_k.data_ptr(),
+                     tree_v.data_ptr(), mask.data_ptr(), out.data_ptr(), k_cache.stride(0), S,
+                     q.shape[0])
+
+
+def eagle_tree_attn_workspace_size(m, n_q_heads, n_kv_heads, head_dim, prefix_len, dtype):
+    return lib().eagle_tree_attn_workspace_size(m, n_q_heads, n_kv_heads, head_dim, prefix_len,
+                                                dtype)
+
+
+def eagle_tree_attn(q, k_cache, v_cache, tree_k, tree_v, mask, prefix_len=None, scale=0.0,
+                    out=None, ws=None, stream=None):
+    """q [m, Hq, d]; k/v_cache [Hkv, cap, d]; tree_k/v [m, Hkv, d]; mask int64 [m * W].
+    Returns fp32 [m, Hq, d]."""
+    m, hq, d = q.shape
+    hkv = k_cache.shape[0]
+    S = k_cache.shape[1] if prefix_len is None else int(prefix_len)
+    dt = _dtype_code(q)
+    out = out if out is not None else torch.empty(m, hq, d, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(eagle_tree_attn_workspace_size(m, hq, hkv, d, S, dt), q.device)
+    _check(lib().eagle_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0),
+                                 _ptr(tree_k), _ptr(tree_v), _ptr(mask), m, hq, hkv, d, S, dt,
+                                 float(scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "eagle_tree_attn")
+    return out
+
+
+def eagle_tree_attn_batched_workspace_size(items, n_q_heads, n_kv_heads, head_dim, dtype):
+    arr = (CAttnItem * len(items))(*items)
+    return lib().eagle_tree_attn_batched_workspace_size(arr, len(items), n_q_heads, n_kv_heads,
+                                                        head_dim, dtype)
+
+
+def eagle_tree_attn_batched(items, n_q_heads, n_kv_heads, head_dim, dtype, scale=0.0, ws=None,
+                            stream=None, device=None):
+    """items: list of CAttnItem (see attn_item)."""
+    arr = (CAttnItem * len(items))(*items)
+    if ws is None:
+        ws = workspace(eagle_tree_attn_batched_workspace_size(items, n_q_heads, n_kv_heads,
+                                                              head_dim, dtype), device)
+    _check(lib().eagle_tree_attn_batched(arr, len(items), n_q_heads, n_kv_heads, head_dim,
+                                         dtype, float(scale), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "eagle_tree_attn_batched")
+
+
+# ----------------------------------------------------------------- verify
+def eagle_tree_verify_workspace_size(n_items, m, vocab):
+    return lib().eagle_tree_verify_workspace_size(n_items, m, vocab)
+
+
+def sampling(greedy=True, temperature=1.0, top_k=0, top_p=1.0):
+    return CSampling(int(bool(greedy)), float(temperature), int(top_k), float(top_p))
+
+
+def eagle_tree_verify(target_logits, tree, params=None, seed=0, step=0, accepted=None,
+                      n_accepted=None, bonus_token=None, ws=None, stream=None):
+    """target_logits fp32 [m, vocab].  Returns (accepted [m], n_accepted [1], bonus [1])
+    as int32 CUDA tensors."""
+    m, vocab = target_logits.shape
+    dev = target_logits.device
+    params = params or sampling()
+    accepted = accepted if accepted is not None else torch.full((m,), -1, dtype=torch.int32,
+                                                                device=dev)
+    n_accepted = n_accepted if n_accepted is not None else torch.zeros(1, dtype=torch.int32,
+                                                                       device=dev)
+    bonus_token = bonus_token if bonus_token is not None else torch.zeros(1, dtype=torch.int32,
+                                                                          device=dev)
+    if ws is None:
+        ws = workspace(eagle_tree_verify_workspace_size(1, m, vocab), dev)
+    _check(lib().eagle_tree_verify(_ptr(target_logits), target_logits.stride(0), vocab, tree.c(),
+                                   ctypes.byref(params), seed, step, _ptr(accepted),
+                                   _ptr(n_accepted), _ptr(bonus_token), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "eagle_tree_verify")
+    return accepted, n_accepted, bonus_token
+
+
+def eagle_tree_verify_batched(target_logits, trees, params, seeds, step=0, accepted=None,
+                              n_accepted=None, bonus_tokens=None, ws=None, stream=None):
+    n = len(target_logits)
+    m, vocab = target_logits[0].shape
+    dev = target_logits[0].device
+    accepted = accepted or [torch.full((m,), -1, dtype=torch.int32, device=dev) for _ in range(n)]
+    n_accepted = n_accepted if n_accepted is not None else torch.zeros(n, dtype=torch.int32,
+                                                                       device=dev)
+    bonus_tokens = bonus_tokens if bonus_tokens is not None else torch.zeros(n, dtype=torch.int32,
+                                                                             device=dev)
+    if ws is None:
+        ws = workspace(eagle_tree_verify_workspace_size(n, m, vocab), dev)
+    lp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in target_logits])
+    tr = (CTree * n)(*[t.c() for t in trees])
+    pa = (CSampling * n)(*params)
+    sd = (ctypes.c_uint64 * n)(*[int(s) for s in seeds])
+    ac = (ctypes.c_void_p * n)(*[a.data_ptr() for a in accepted])
+    _check(lib().eagle_tree_verify_batched(n, lp, target_logits[0].stride(0), vocab, tr, pa, sd,
+                                           step, ac, _ptr(n_accepted), _ptr(bonus_tokens),
+                                           _ptr(ws), ws.numel(), _stream(stream)),
+           "eagle_tree_verify_batched")
+    return accepted, n_accepted, bonus_tokens

@@ -1,0 +1,49 @@
+// Launch plan shared by the attention kernels (CUDA-core path, merge, and the
+// tcgen05 tensor-core path).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "eagle_common.cuh"
+
+namespace eagle {
+
+constexpr int kAttnMaxItems = 32;  // items per launch (more are chunked)
+// Split plans are sized for a 152-SM part independently of the device the
+// call runs on, so workspace sizes do not depend on the device.
+constexpr int kPlanSMs = 152;
+
+struct AttnItemDev {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* tree_k;
+  const void* tree_v;
+  const uint64_t* mask;
+  float* out;
+  int64_t cache_head_stride;
+  int32_t prefix_len;
+  int32_t m;
+};
+
+struct AttnPlan {
+  AttnItemDev items[kAttnMaxItems];
+  int splits[kAttnMaxItems];
+  int unit_start[kAttnMaxItems + 1];     // first CTA of each item
+  int64_t row_start[kAttnMaxItems + 1];  // first output row (query x q head)
+  int64_t part_start[kAttnMaxItems];     // first partial float of each item
+  int64_t part_floats;
+  int n_items, n_q_heads, n_kv_heads, head_dim;
+  float scale;
+  int32_t* err;
+  float* partials;
+};
+
+// tensor-core path (eagle_attn_tc.cu)
+bool tc_supported(int head_dim);
+size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms);
+eagle_status attn_tc_launch(const eagle_attn_item* items, int n, int hq, int hkv, int d,
+                            float scale, void* ws, size_t ws_bytes, cudaStream_t stream, int sms);
+
+}  // namespace eagle

@@ -1,0 +1,379 @@
+// eagle_tree_build: draft logits -> dynamic draft tree, one fused launch.
+//
+// Sources: "EAGLE-2: Feature-Level Speculative Decoding Guide", "The
+// Recurrent Feature Drafting Step" (draft distribution = softmax of the
+// LM-head logits; its listing takes the top candidates of that softmax) and
+// "Context-Aware Dynamic Tree Construction"; "Support Eagle-3 Speculative
+// Decoding in llama.cpp", reply on the dynamic tree (node value = draft
+// confidence, tree grown per drafting step and pruned at the end).
+//
+// Phase 1 (all CTAs, eagle_rowstream.cuh): one HBM pass over the R draft
+// rows -> per row the top_k (value desc, token id asc) and logsumexp.
+// Phase 2 (the CTA that finalizes an item's last row): candidate values
+// value = parent value + (logit - logsumexp), in fp64; per depth the top_k
+// frontier (ranks by binary search over the per-slot sorted child lists);
+// final best m-1 by an MSB radix select on order-preserving 64-bit keys
+// (ties -> lower candidate index); node ids by a block scan; ancestor mask
+// by walking parent pointers (depth <= 16).
+#include "eagle_stream_host.h"
+
+namespace eagle {
+
+struct BuildArgs {
+  RowStream rs;
+  int top_k, depth, total_tokens, n_cand;
+  int root_token[kMaxItems];
+  eagle_tree out[kMaxItems];
+};
+
+__device__ __forceinline__ int cand_depth(int a, int k) { return a < k ? 1 : 2 + (a - k) / (k * k); }
+
+// Block-wide exclusive scan of per-thread counts (blockDim == kThreads).
+__device__ int block_excl_scan(int v, int* warp_tot, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int off = 0;
+  total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) off += warp_tot[w];
+    total += warp_tot[w];
+  }
+  __syncthreads();
+  return off + incl - v;
+}
+
+__device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = A.top_k, D = A.depth, m = A.total_tokens, C = A.n_cand;
+  const int R = 1 + (D - 1) * k;
+  const int rk = A.rs.rec_k;
+  const int rb = rec_bytes(rk);
+  char* rows = A.rs.rows + static_cast<int64_t>(item) * A.rs.rows_per_item * rb;
+  const eagle_tree out = A.out[item];
+
+  // scratch carved from the (now idle) ring buffers: <= 60 KB for C <= 2048
+  char* p = reinterpret_cast<char*>(S.buf);
+  double* val = reinterpret_cast<double*>(p);
+  p += sizeof(double) * C;
+  uint64_t* key = reinterpret_cast<uint64_t*>(p);
+  p += sizeof(uint64_t) * C;
+  double* lse = reinterpret_cast<double*>(p);
+  p += sizeof(double) * R;
+  int* tok = reinterpret_cast<int*>(p);
+  p += sizeof(int) * C;
+  int* par = reinterpret_cast<int*>(p);
+  p += sizeof(int) * C;
+  int* node = reinterpret_cast<int*>(p);
+  p += sizeof(int) * C;
+  int* npar = reinterpret_cast<int*>(p);
+  p += sizeof(int) * EAGLE_MAX_TREE;
+  int* fr = reinterpret_cast<int*>(p);
+  p += sizeof(int) * kKMax;
+  int* fr_next = reinterpret_cast<int*>(p);
+  p += sizeof(int) * kKMax;
+  int* hist = reinterpret_cast<int*>(p);
+  p += sizeof(int) * 256;
+  int* misc = reinterpret_cast<int*>(p);  // [0] digit, [1] count above, [2] done flag
+  p += sizeof(int) * 8;
+  int* warp_tot = reinterpret_cast<int*>(p);
+
+  for (int r = tid; r < R; r += kThreads) {
+    const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rows + r * rb);
+    lse[r] = static_cast<double>(h->max) + log(h->sum);
+  }
+  __syncthreads();
+  auto row_logit = [&](int r, int c) { return __ldcg(rec_val(rows + r * rb) + c); };
+  auto row_token = [&](int r, int c) { return __ldcg(rec_idx(rows + r * rb, rk) + c); };
+
+  // depth 1: the root's top_k, rank order
+  for (int c = tid; c < k; c += kThreads) {
+    val[c] = static_cast<double>(row_logit(0, c)) - lse[0];
+    tok[c] = row_token(0, c);
+    par[c] = -1;
+    fr[c] = c;
+  }
+  __syncthreads();
+
+  int level_base = 0;
+  for (int l = 1; l < D; ++l) {
+    const int child_base = (l == 1) ? k : level_base + k * k;
+    for (int e = tid; e < k * k; e += kThreads) {
+      const int s = e / k, c = e - s * k;
+      const int r = 1 + (l - 1) * k + s;
+      const int a = child_base + e;
+      const int pa = fr[s];
+      val[a] = val[pa] + (static_cast<double>(row_logit(r, c)) - lse[r]);
+      tok[a] = row_token(r, c);
+      par[a] = pa;
+    }
+    __syncthreads();
+    level_base = child_base;
+    if (l + 1 < D) {
+      // frontier of depth l+1: best k of the k sorted child lists
+      for (int e = tid; e < k * k; e += kThreads) {
+        const int s = e / k, c = e - s * k;
+        const double v = val[level_base + e];
+        int rank = c;
+        for (int s2 = 0; s2 < k && rank < k; ++s2) {
+          if (s2 == s) continue;
+          const double* lst = val + level_base + s2 * k;
+          int lo = 0, hi = k;
+          if (s2 < s) {  // lower indices: entries with value >= v come first
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (lst[mid] >= v) lo = mid + 1; else hi = mid;
+            }
+          } else {
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (lst[mid] > v) lo = mid + 1; else hi = mid;
+            }
+          }
+          rank += lo;
+        }
+        if (rank < k) fr_next[rank] = level_base + e;
+      }
+      __syncthreads();
+      for (int c = tid; c < k; c += kThreads) fr[c] = fr_next[c];
+      __syncthreads();
+    }
+  }
+
+  // final rerank: best need = m-1 of C candidates
+  const int need = m - 1;
+  uint64_t prefix = 0, pmask = 0;
+  int rem = need;
+  bool all_in = (need >= C);
+  if (need > 0 && !all_in) {
+    for (int a = tid; a < C; a += kThreads) key[a] = order_key(val[a]);
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      for (int a = tid; a < C; a += kThreads)
+        if ((key[a] & pmask) == prefix) atomicAdd(&hist[(key[a] >> shift) & 255], 1);
+      __syncthreads();
+      if (warp == 0) {
+        // lane l owns digits 255-8l .. 248-8l (descending)
+        int cnt[8];
+        int lsum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          cnt[j] = hist[255 - 8 * lane - j];
+          lsum += cnt[j];
+        }
+        int incl = lsum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int above = incl - lsum;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (above < rem && rem <= above + cnt[j]) {
+            misc[0] = 255 - 8 * lane - j;
+            misc[1] = above;
+          }
+          above += cnt[j];
+        }
+      }
+      __syncthreads();
+      const int d = misc[0];
+      rem -= misc[1];
+      prefix |= static_cast<uint64_t>(d) << shift;
+      pmask |= 0xFFull << shift;
+      const bool done = (hist[d] == rem);
+      __syncthreads();
+      if (done) {
+        all_in = true;
+        break;
+      }
+    }
+  }
+
+  // selection flags in candidate order -> node ids (1 + exclusive count)
+  const int per = (C + kThreads - 1) / kThreads;
+  const int a0 = tid * per, a1 = min(C, a0 + per);
+  int cnt_local = 0;
+  for (int a = a0; a < a1; ++a) {
+    bool sel;
+    if (need <= 0) sel = false;
+    else if (need >= C) sel = true;
+    else {
+      const uint64_t top = key[a] & pmask;
+      sel = top > prefix;
+      if (top == prefix) {
+        if (all_in) sel = true;
+        else {  // fully equal keys: lowest candidate indices first
+          int before_cnt = 0;
+          for (int b = 0; b < a; ++b) before_cnt += (key[b] == prefix) ? 1 : 0;
+          sel = before_cnt < rem;
+        }
+      }
+    }
+    node[a] = sel ? 1 : 0;
+    cnt_local += sel ? 1 : 0;
+  }
+  int total = 0;
+  int off = block_excl_scan(cnt_local, warp_tot, total);
+  for (int a = a0; a < a1; ++a) {
+    if (node[a]) node[a] = 1 + off++;
+    else node[a] = 0;
+  }
+  __syncthreads();
+  if (tid == 0 && total != (need > 0 ? min(need, C) : 0)) record_error(A.rs.err, kDevAssert, 10);
+
+  // node arrays
+  if (tid == 0) {
+    out.parents[0] = -1;
+    out.tokens[0] = A.root_token[item];
+    out.depth[0] = 0;
+    out.pos[0] = 0;
+    if (out.values) out.values[0] = 0.0;
+    npar[0] = -1;
+  }
+  for (int a = tid; a < C; a += kThreads) {
+    const int n = node[a];
+    if (!n) continue;
+    int pn = 0;
+    if (par[a] >= 0) {
+      pn = node[par[a]];
+      if (pn == 0) {
+        record_error(A.rs.err, kDevAssert, 11);  // kept set not ancestor-closed
+        pn = 0;
+      }
+    }
+    const int dep = cand_depth(a, k);
+    out.parents[n] = pn;
+    out.tokens[n] = tok[a];
+    out.depth[n] = dep;
+    out.pos[n] = dep;
+    if (out.values) out.values[n] = val[a];
+    npar[n] = pn;
+  }
+  __syncthreads();
+  const int W = out.mask_words;
+  for (int n = tid; n < m; n += kThreads) {
+    uint64_t w[EAGLE_MAX_TREE / 64] = {0, 0, 0, 0};
+    int q = n;
+    for (int guard = 0; q >= 0 && guard <= EAGLE_MAX_DEPTH + 1; ++guard) {
+      w[q >> 6] |= 1ull << (q & 63);
+      q = npar[q];
+    }
+    for (int i = 0; i < W; ++i) out.mask[static_cast<int64_t>(n) * W + i] = w[i];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads) build_kernel(const __grid_constant__ BuildArgs A) {
+  extern __shared__ __align__(128) char smem_raw[];
+  StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
+  run_stream(A.rs, S);
+  const int n_done = S.n_done_items;
+  for (int d = 0; d < n_done; ++d) {
+    assemble_tree(A, S.done_items[d], S);
+    __syncthreads();
+  }
+}
+
+static int build_ctas_per_sm() {
+  int occ = 0;
+  const size_t smem = sizeof(StreamSmem);
+  if (cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, build_kernel, kThreads, smem) !=
+      cudaSuccess)
+    return 0;
+  return occ;
+}
+
+static eagle_status build_impl(int32_t n_items, const float* const* logits, int64_t row_stride,
+                               int32_t n_rows, int32_t vocab, int32_t top_k, int32_t depth,
+                               int32_t total_tokens, const int32_t* roots,
+                               const eagle_tree* outs, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  EAGLE_CHECK_ARG(logits && roots && outs && ws);
+  EAGLE_CHECK_ARG(n_items >= 1 && vocab >= 1 && n_rows >= 1 && top_k >= 1 && depth >= 1 &&
+                  total_tokens >= 1);
+  EAGLE_CHECK_SHAPE(n_items <= kMaxItems);
+  EAGLE_CHECK_SHAPE(top_k <= kKMax && top_k <= vocab && depth <= EAGLE_MAX_DEPTH);
+  const int64_t C = top_k + static_cast<int64_t>(depth - 1) * top_k * top_k;
+  EAGLE_CHECK_SHAPE(C <= EAGLE_MAX_CANDIDATES);
+  EAGLE_CHECK_SHAPE(total_tokens <= EAGLE_MAX_TREE && total_tokens <= 1 + C);
+  const int R = 1 + (depth - 1) * top_k;
+  EAGLE_CHECK_ARG(n_rows >= R);
+  EAGLE_CHECK_ARG(row_stride >= vocab && row_stride % 4 == 0);
+  for (int i = 0; i < n_items; ++i) {
+    EAGLE_CHECK_ARG(logits[i] && aligned16(logits[i]));
+    const eagle_tree& t = outs[i];
+    EAGLE_CHECK_ARG(t.parents && t.tokens && t.depth && t.pos && t.mask);
+    EAGLE_CHECK_ARG(t.m == total_tokens && t.mask_words == (total_tokens + 63) / 64);
+  }
+  const StreamLayout L = stream_layout(n_items, R, vocab, top_k, false);
+  if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+
+  BuildArgs A;
+  memset(&A, 0, sizeof(A));
+  const int occ = build_ctas_per_sm();
+  if (occ <= 0) return EAGLE_ERR_CUDA;
+  const int grid = stream_grid(L, occ);
+  fill_stream(A.rs, L, static_cast<char*>(ws), n_items, R, vocab, row_stride, grid, false);
+  for (int i = 0; i < n_items; ++i) {
+    A.rs.base[i] = logits[i];
+    A.rs.exp_scale[i] = 1.0f;
+    A.rs.topk[i] = static_cast<int16_t>(top_k);
+    A.rs.flags[i] = kWantSum;
+    A.root_token[i] = roots[i];
+    A.out[i] = outs[i];
+  }
+  A.top_k = top_k;
+  A.depth = depth;
+  A.total_tokens = total_tokens;
+  A.n_cand = static_cast<int>(C);
+  build_kernel<<<grid, kThreads, sizeof(StreamSmem), stream>>>(A);
+  return launch_status();
+}
+
+}  // namespace eagle
+
+using namespace eagle;
+
+extern "C" size_t eagle_tree_build_workspace_size(int32_t n_items, int32_t n_rows, int32_t vocab,
+                                                  int32_t top_k, int32_t depth,
+                                                  int32_t total_tokens) {
+  (void)n_rows;
+  (void)total_tokens;
+  if (n_items < 1 || vocab < 1 || top_k < 1 || depth < 1) return 0;
+  const int R = 1 + (depth - 1) * top_k;
+  return stream_layout(n_items, R, vocab, top_k, false).total;
+}
+
+extern "C" eagle_status eagle_tree_build(const float* draft_logits, int64_t row_stride,
+                                         int32_t n_rows, int32_t vocab, int32_t top_k,
+                                         int32_t depth, int32_t total_tokens,
+                                         int32_t root_token, eagle_tree out, void* ws,
+                                         size_t ws_bytes, eagle_stream stream) {
+  return build_impl(1, &draft_logits, row_stride, n_rows, vocab, top_k, depth, total_tokens,
+                    &root_token, &out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" eagle_status eagle_tree_build_batched(int32_t n_items,
+                                                 const float* const* draft_logits,
+                                                 int64_t row_stride, int32_t n_rows,
+                                                 int32_t vocab, int32_t top_k, int32_t depth,
+                                                 int32_t total_tokens,
+                                                 const int32_t* root_tokens,
+                                                 const eagle_tree* outs, void* ws,
+                                                 size_t ws_bytes, eagle_stream stream) {
+  return build_impl(n_items, draft_logits, row_stride, n_rows, vocab, top_k, depth,
+                    total_tokens, root_tokens, outs, ws, ws_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}

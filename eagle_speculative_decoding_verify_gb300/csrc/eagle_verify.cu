@@ -1,0 +1,447 @@
+// eagle_tree_verify: target logits + draft tree -> accepted path and bonus
+// token, one fused launch.
+//
+// Sources: "EAGLE-2: Feature-Level Speculative Decoding Guide", "Single-Pass
+// Tree Verification" (the target scores every node at once; the verifier
+// walks from the root accepting matching tokens until the first discrepancy;
+// the output equals vanilla decoding) and "True Lossless Acceleration";
+// "Support Eagle-3 Speculative Decoding in llama.cpp", proposal (acceptance /
+// rejection strategy = speculative sampling); "EAGLE-2 Speculative Decoding
+// Support for llama.cpp - Phase 1", "Performance Notes" (temperature + top_k
+// + top_p).
+//
+// Phase 1 (all CTAs, eagle_rowstream.cuh): one HBM pass over the m target
+// rows of every item -> per row the argmax (greedy), the top_k logits
+// (sampling with top_k) or the max, sum of exp((x-max)/T) and per-tile sums
+// (sampling over the full vocabulary).
+// Phase 2 (the CTA that finalizes an item's last row, one warp): the walk.
+// Sampling follows recursive speculative sampling with one-hot draft
+// distributions (tree children are deterministic top-k picks): accept child j
+// iff u_j (1 - rho) < p(token_j), else rho += p(token_j); on rejection of all
+// children (or at a leaf) draw the bonus token by inverse CDF over token ids
+// ascending with the rejected tokens removed.  Probabilities of individual
+// tokens and all decisions are fp64.
+#include "eagle_philox.cuh"
+#include "eagle_stream_host.h"
+
+namespace eagle {
+
+enum : int { kModeGreedy = 0, kModeTopK = 1, kModeFull = 2 };
+
+struct VerifyArgs {
+  RowStream rs;
+  int m;
+  int mode[kMaxItems];
+  float temperature[kMaxItems];
+  float top_p[kMaxItems];
+  int top_k[kMaxItems];
+  const int32_t* parents[kMaxItems];
+  const int32_t* tokens[kMaxItems];
+  int32_t* accepted[kMaxItems];
+  uint64_t seed[kMaxItems];
+  uint64_t step;
+  int32_t* n_accepted;
+  int32_t* bonus;
+};
+
+__device__ __forceinline__ double warp_incl_scan_d(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// p(t) under the full-vocabulary target distribution (lane-local).
+__device__ __forceinline__ double full_prob(const float* lrow, int t, double rowmax, double T,
+                                            double zsum) {
+  return exp((static_cast<double>(__ldg(lrow + t)) - rowmax) / T) / zsum;
+}
+
+// The walk; executed by warp 0 of the CTA.
+__device__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
+  const int lane = threadIdx.x & 31;
+  const int m = A.m;
+  const int rk = A.rs.rec_k;
+  const int rb = rec_bytes(rk);
+  const int TR = A.rs.tiles_per_row;
+  char* rows = A.rs.rows + static_cast<int64_t>(item) * m * rb;
+  const int mode = A.mode[item];
+  const double T = static_cast<double>(A.temperature[item]);
+  const double top_p = static_cast<double>(A.top_p[item]);
+  const int K = A.top_k[item];
+  const uint64_t seed = A.seed[item];
+  int32_t* acc = A.accepted[item];
+
+  int* par = reinterpret_cast<int*>(S.buf[0]);
+  int* tok = par + EAGLE_MAX_TREE;
+  int* rejected = tok + EAGLE_MAX_TREE;        // tokens rejected at the current node
+  double* kp = reinterpret_cast<double*>(S.buf[1]);  // kept probabilities (top-k mode)
+  int* kid = reinterpret_cast<int*>(kp + kKMax);     // kept ids
+  double* sp = reinterpret_cast<double*>(kid + kKMax);  // kept probs sorted by id
+  int* sid = reinterpret_cast<int*>(sp + kKMax);
+  for (int i = lane; i < m; i += 32) {
+    par[i] = A.parents[item][i];
+    tok[i] = A.tokens[item][i];
+  }
+  __syncwarp();
+
+  int node = 0, n_acc = 0, bonus = -1;
+  if (lane == 0) acc[0] = 0;
+  for (int guard = 0; guard < m; ++guard) {
+    char* rec = rows + static_cast<int64_t>(node) * rb;
+    const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rec);
+    if (mode == kModeGreedy) {
+      const int a = __ldcg(rec_idx(rec, rk));
+      int child = -1;
+      for (int base = node + 1; base < m && child < 0; base += 32) {
+        const int i = base + lane;
+        const bool hit = i < m && par[i] == node && tok[i] == a;
+        const unsigned bal = __ballot_sync(0xffffffffu, hit);
+        if (bal) child = base + __ffs(bal) - 1;
+      }
+      if (child < 0) {
+        bonus = a;
+        break;
+      }
+      node = child;
+      ++n_acc;
+      if (lane == 0) acc[n_acc] = node;
+      continue;
+    }
+
+    // ---- the warped target distribution at this node
+    const float* lrow = A.rs.base[item] + static_cast<int64_t>(node) * A.rs.row_stride;
+    double rowmax = 0.0, zsum = 1.0;
+    int nkeep = 0;
+    if (mode == kModeTopK) {
+      int cnt = h->count;
+      if (cnt > K) cnt = K;
+      double z[2], pr[2];
+      int id[2];
+      const double z0 = static_cast<double>(__ldcg(rec_val(rec))) / T;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int e = lane + 32 * hh;
+        if (e < cnt) {
+          z[hh] = static_cast<double>(__ldcg(rec_val(rec) + e)) / T;
+          id[hh] = __ldcg(rec_idx(rec, rk) + e);
+          pr[hh] = exp(z[hh] - z0);
+        } else {
+          pr[hh] = 0.0;
+          id[hh] = 0x7fffffff;
+        }
+      }
+      const double tot = warp_sum_d(pr[0] + pr[1]);
+      pr[0] /= tot;
+      pr[1] /= tot;
+      nkeep = cnt;
+      if (top_p < 1.0) {
+        // entries are in probability order; keep the shortest prefix whose
+        // cumulative mass reaches top_p (the crossing entry included)
+        const double c0 = warp_incl_scan_d(pr[0]);
+        const double t0 = __shfl_sync(0xffffffffu, c0, 31);
+        const double c1 = warp_incl_scan_d(pr[1]) + t0;
+        const unsigned b0 = __ballot_sync(0xffffffffu, lane < cnt && c0 >= top_p);
+        const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < cnt && c1 >= top_p);
+        int last = cnt - 1;
+        if (b0) last = __ffs(b0) - 1;
+        else if (b1) last = 32 + __ffs(b1) - 1;
+        nkeep = last + 1;
+        if (lane > last) pr[0] = 0.0;
+        if (lane + 32 > last) pr[1] = 0.0;
+        const double tot2 = warp_sum_d(pr[0] + pr[1]);
+        pr[0] /= tot2;
+        pr[1] /= tot2;
+      }
+      kp[lane] = pr[0];
+      kid[lane] = lane < nkeep ? id[0] : 0x7fffffff;
+      kp[lane + 32] = pr[1];
+      kid[lane + 32] = lane + 32 < nkeep ? id[1] : 0x7fffffff;
+      __syncwarp();
+    } else {  // full vocabulary
+      rowmax = static_cast<double>(h->max);
+      zsum = h->sum;
+    }
+    auto prob_of = [&](int t) -> double {  // warp-uniform result
+      if (mode == kModeTopK) {
+        double v = 0.0;
+        if (kid[lane] == t) v = kp[lane];
+        if (kid[lane + 32] == t) v = kp[lane + 32];
+        return warp_sum_d(v);
+      }
+      return full_prob(lrow, t, rowmax, T, zsum);
+    };
+
+    // ---- children in node order: recursive speculative sampling
+    double rho = 0.0;
+    int n_rej = 0, child = -1, j = 0;
+    for (int base = node + 1; base < m && child < 0; base += 32) {
+      const int i = base + lane;
+      unsigned bal = __ballot_sync(0xffffffffu, i < m && par[i] == node);
+      while (bal && child < 0) {
+        const int c = base + __ffs(bal) - 1;
+        bal &= bal - 1;
+        const int t = tok[c];
+        const double pt = prob_of(t);
+        const double u = philox_uniform(seed, A.step, static_cast<uint32_t>(node),
+                                        static_cast<uint32_t>(j));
+        if (u * (1.0 - rho) < pt) {
+          child = c;
+        } else {
+          rho += pt;
+          if (lane == 0 && n_rej < EAGLE_MAX_TREE) rejected[n_rej] = t;
+          ++n_rej;
+        }
+        ++j;
+      }
+    }
+    __syncwarp();
+    if (child >= 0) {
+      node = child;
+      ++n_acc;
+      if (lane == 0) acc[n_acc] = node;
+      continue;
+    }
+
+    // ---- residual / bonus draw: inverse CDF over ids ascending
+    const double thr =
+        philox_uniform(seed, A.step, static_cast<uint32_t>(node), kResidualChild) * (1.0 - rho);
+    auto is_rejected = [&](int t) {
+      for (int r = 0; r < n_rej && r < EAGLE_MAX_TREE; ++r)
+        if (rejected[r] == t) return true;
+      return false;
+    };
+    if (mode == kModeTopK) {
+      // sort the kept entries by token id (rank by counting)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int e = lane + 32 * hh;
+        if (e < nkeep) {
+          int r = 0;
+          for (int f = 0; f < nkeep; ++f) r += kid[f] < kid[e] ? 1 : 0;
+          sid[r] = kid[e];
+          sp[r] = is_rejected(kid[e]) ? 0.0 : kp[e];
+        }
+      }
+      __syncwarp();
+      int pick_id = 0;
+      if (lane == 0) {
+        double cum = 0.0;
+        int pick = -1, last_pos = -1;
+        for (int r = 0; r < nkeep; ++r) {
+          cum += sp[r];
+          if (sp[r] > 0.0) last_pos = r;
+          if (cum > thr) {
+            pick = r;
+            break;
+          }
+        }
+        if (pick < 0) pick = last_pos >= 0 ? last_pos : nkeep - 1;
+        pick_id = sid[pick];
+      }
+      bonus = __shfl_sync(0xffffffffu, pick_id, 0);
+      __syncwarp();
+    } else {
+      // tile masses (tile sums were taken relative to each tile's max)
+      const float2* ts = A.rs.tile_sums + (static_cast<int64_t>(item) * m + node) * TR;
+      const double c2 = static_cast<double>(A.rs.exp_scale[item]) * 1.4426950408889634;
+      double cum = 0.0;
+      int tile = -1;
+      double before_tile = 0.0;
+      for (int base = 0; base < TR && tile < 0; base += 32) {
+        const int t = base + lane;
+        double mass = 0.0;
+        if (t < TR) {
+          const float2 v = __ldcg(ts + t);
+          if (v.y > 0.f) mass = static_cast<double>(v.y) * exp2((static_cast<double>(v.x) - rowmax) * c2) / zsum;
+          for (int r = 0; r < n_rej && r < EAGLE_MAX_TREE; ++r)
+            if (rejected[r] / kTile == t) mass -= full_prob(lrow, rejected[r], rowmax, T, zsum);
+          if (mass < 0.0) mass = 0.0;
+        }
+        const double incl = warp_incl_scan_d(mass) + cum;
+        const unsigned bal = __ballot_sync(0xffffffffu, t < TR && incl > thr);
+        if (bal) {
+          const int l = __ffs(bal) - 1;
+          tile = base + l;
+          before_tile = __shfl_sync(0xffffffffu, incl - mass, l);
+        }
+        cum = __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (tile < 0) tile = TR - 1, before_tile = cum;  // rounding: take the last tile
+      // scan inside the tile: lane owns 32 consecutive tokens
+      const int v0 = tile * kTile + lane * 32;
+      double lm[32];
+      double lsum = 0.0;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int t = v0 + q;
+        double mass = 0.0;
+        if (t < A.rs.vocab && !is_rejected(t)) {
+          const float x = __ldg(lrow + t);
+          mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) / zsum;
+        }
+        lm[q] = mass;
+        lsum += mass;
+      }
+      const double incl = warp_incl_scan_d(lsum) + before_tile;
+      const unsigned bal = __ballot_sync(0xffffffffu, incl > thr);
+      int pick = -1;
+      if (bal) {
+        const int l = __ffs(bal) - 1;
+        if (lane == l) {
+          double c = incl - lsum;
+          for (int q = 0; q < 32; ++q) {
+            c += lm[q];
+            if (lm[q] > 0.0 && c > thr) {
+              pick = v0 + q;
+              break;
+            }
+          }
+          if (pick < 0) pick = v0 + 31;
+        }
+        pick = __shfl_sync(0xffffffffu, pick, l);
+      } else {  // rounding: last token of the tile with mass
+        int last = -1;
+        for (int q = 31; q >= 0; --q)
+          if (lm[q] > 0.0) {
+            last = v0 + q;
+            break;
+          }
+        const unsigned b2 = __ballot_sync(0xffffffffu, last >= 0);
+        const int l = b2 ? 31 - __clz(b2) : 0;
+        pick = __shfl_sync(0xffffffffu, last, l);
+        if (pick < 0) pick = tile * kTile;
+      }
+      bonus = pick;
+    }
+    break;
+  }
+  if (lane == 0) {
+    A.n_accepted[item] = n_acc;
+    A.bonus[item] = bonus;
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyArgs A) {
+  extern __shared__ __align__(128) char smem_raw[];
+  StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
+  run_stream(A.rs, S);
+  const int n_done = S.n_done_items;
+  for (int d = 0; d < n_done; ++d) {
+    if (threadIdx.x < 32) walk(A, S.done_items[d], S);
+    __syncthreads();
+  }
+}
+
+static int verify_ctas_per_sm() {
+  int occ = 0;
+  const size_t smem = sizeof(StreamSmem);
+  if (cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, verify_kernel, kThreads, smem) !=
+      cudaSuccess)
+    return 0;
+  return occ;
+}
+
+static eagle_status verify_impl(int32_t n_items, const float* const* logits, int64_t row_stride,
+                                int32_t vocab, const eagle_tree* trees,
+                                const eagle_sampling* params, const uint64_t* seeds,
+                                uint64_t step, int32_t* const* accepted, int32_t* n_accepted,
+                                int32_t* bonus, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
+  EAGLE_CHECK_ARG(logits && trees && params && seeds && accepted && n_accepted && bonus && ws);
+  EAGLE_CHECK_ARG(n_items >= 1 && vocab >= 1);
+  EAGLE_CHECK_SHAPE(n_items <= kMaxItems);
+  EAGLE_CHECK_ARG(row_stride >= vocab && row_stride % 4 == 0);
+  const int m = trees[0].m;
+  EAGLE_CHECK_ARG(m >= 1);
+  EAGLE_CHECK_SHAPE(m <= EAGLE_MAX_TREE);
+  VerifyArgs A;
+  memset(&A, 0, sizeof(A));
+  int rec_k = 1;
+  bool any_full = false;
+  for (int i = 0; i < n_items; ++i) {
+    EAGLE_CHECK_ARG(logits[i] && aligned16(logits[i]) && accepted[i]);
+    EAGLE_CHECK_ARG(trees[i].parents && trees[i].tokens && trees[i].m == m);
+    const eagle_sampling& p = params[i];
+    int mode, k = 0;
+    if (p.greedy) {
+      mode = kModeGreedy;
+      k = 1;
+    } else {
+      EAGLE_CHECK_ARG(p.temperature > 0.f && p.top_p > 0.f && p.top_p <= 1.f && p.top_k >= 0);
+      k = p.top_k >= vocab ? (vocab <= kKMax ? vocab : 0) : p.top_k;
+      EAGLE_CHECK_SHAPE(k <= kKMax);
+      EAGLE_CHECK_SHAPE(k > 0 || p.top_p >= 1.f);  // nucleus needs a top_k bound
+      mode = k > 0 ? kModeTopK : kModeFull;
+    }
+    A.mode[i] = mode;
+    A.top_k[i] = k;
+    A.temperature[i] = p.greedy ? 1.f : p.temperature;
+    A.top_p[i] = p.greedy ? 1.f : p.top_p;
+    A.parents[i] = trees[i].parents;
+    A.tokens[i] = trees[i].tokens;
+    A.accepted[i] = accepted[i];
+    A.seed[i] = seeds[i];
+    A.rs.base[i] = logits[i];
+    A.rs.exp_scale[i] = p.greedy ? 1.f : 1.f / p.temperature;
+    A.rs.topk[i] = static_cast<int16_t>(mode == kModeFull ? 0 : k);
+    A.rs.flags[i] = mode == kModeFull ? (kWantSum | kWantTileSums) : 0;
+    if (k > rec_k) rec_k = k;
+    any_full |= mode == kModeFull;
+  }
+  (void)any_full;
+  const StreamLayout L = stream_layout(n_items, m, vocab, kKMax, true);
+  if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  const int occ = verify_ctas_per_sm();
+  if (occ <= 0) return EAGLE_ERR_CUDA;
+  const int grid = stream_grid(L, occ);
+  fill_stream(A.rs, L, static_cast<char*>(ws), n_items, m, vocab, row_stride, grid, true);
+  A.m = m;
+  A.step = step;
+  A.n_accepted = n_accepted;
+  A.bonus = bonus;
+  verify_kernel<<<grid, kThreads, sizeof(StreamSmem), stream>>>(A);
+  return launch_status();
+}
+
+}  // namespace eagle
+
+using namespace eagle;
+
+extern "C" size_t eagle_tree_verify_workspace_size(int32_t n_items, int32_t m, int32_t vocab) {
+  if (n_items < 1 || m < 1 || vocab < 1) return 0;
+  return stream_layout(n_items, m, vocab, kKMax, true).total;
+}
+
+extern "C" eagle_status eagle_tree_verify(const float* target_logits, int64_t row_stride,
+                                          int32_t vocab, eagle_tree tree,
+                                          const eagle_sampling* params, uint64_t seed,
+                                          uint64_t step, int32_t* accepted,
+                                          int32_t* n_accepted, int32_t* bonus_token, void* ws,
+                                          size_t ws_bytes, eagle_stream stream) {
+  return verify_impl(1, &target_logits, row_stride, vocab, &tree, params, &seed, step,
+                     &accepted, n_accepted, bonus_token, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" eagle_status eagle_tree_verify_batched(int32_t n_items,
+                                                  const float* const* target_logits,
+                                                  int64_t row_stride, int32_t vocab,
+                                                  const eagle_tree* trees,
+                                                  const eagle_sampling* params,
+                                                  const uint64_t* seeds, uint64_t step,
+                                                  int32_t* const* accepted,
+                                                  int32_t* n_accepted, int32_t* bonus_tokens,
+                                                  void* ws, size_t ws_bytes,
+                                                  eagle_stream stream) {
+  return verify_impl(n_items, target_logits, row_stride, vocab, trees, params, seeds, step,
+                     accepted, n_accepted, bonus_tokens, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,270 @@
+/*
+ * eagle.h -- C ABI of the GB300 (sm_103a) library for the hot path of one
+ * EAGLE-2 speculative-decoding verify step:
+ *
+ *   eagle_tree_build   draft logits            -> dynamic draft tree
+ *   eagle_tree_attn    tree queries + KV cache -> tree-masked attention output
+ *   eagle_tree_verify  target logits + tree    -> accepted path + bonus token
+ *
+ * Sources (page title and section):
+ *   [blog]  "EAGLE-2: Feature-Level Speculative Decoding Guide":
+ *           "The Recurrent Feature Drafting Step" (draft distribution =
+ *           softmax of LM-head logits), "Context-Aware Dynamic Tree
+ *           Construction", "Single-Pass Tree Verification" (ancestor-only
+ *           tree mask, root-to-leaf acceptance, lossless output).
+ *   [disc]  "Support Eagle-3 Speculative Decoding in llama.cpp": reply on the
+ *           dynamic tree (valued by draft confidence, pruned at the end of
+ *           drafting), the acceptance / rejection strategy, and the reply on
+ *           KV caches (target keeps the accepted context).
+ *   [pr]    "EAGLE-2 Speculative Decoding Support for llama.cpp - Phase 1",
+ *           "Performance Notes": mixed sampling = temperature + top_k + top_p.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless marked "host".  The
+ *     caller owns every buffer, including the workspace `ws`; the library
+ *     allocates nothing and keeps no global state.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream); nothing synchronises with the host.  Calls on one stream run
+ *     in order; two calls that share a workspace must not overlap.
+ *   - Arguments are validated on the host before anything is launched; on a
+ *     bad argument nothing is enqueued.  Launch failures return
+ *     EAGLE_ERR_CUDA.  Device-side problems (a bounded wait that ran out, a
+ *     violated invariant) do not fail the call: they are recorded in the
+ *     workspace's error word, read with eagle_workspace_error().
+ *   - Workspaces must be zero-filled once before first use (for example with
+ *     eagle_workspace_init); every successful call leaves its workspace
+ *     ready for the next call.  After a recorded device error, re-initialise.
+ *   - Floating-point inputs must be finite (no NaN / +-inf).
+ */
+#ifndef EAGLE_H
+#define EAGLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* eagle_stream;
+
+typedef enum {
+  EAGLE_OK = 0,
+  EAGLE_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad stride/alignment   */
+  EAGLE_ERR_UNSUPPORTED_SHAPE = 2,   /* valid but outside the library's limits (below)      */
+  EAGLE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < the matching *_workspace_size()          */
+  EAGLE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed                 */
+  EAGLE_ERR_TIMEOUT = 5,             /* device error word: a bounded wait expired            */
+  EAGLE_ERR_DEVICE_ASSERT = 6        /* device error word: an internal invariant was broken  */
+} eagle_status;
+
+typedef enum { EAGLE_F32 = 0, EAGLE_BF16 = 1 } eagle_dtype;
+
+/* Library limits (EAGLE_ERR_UNSUPPORTED_SHAPE beyond them). */
+#define EAGLE_MAX_TOP_K 64        /* draft top_k and sampling top_k             */
+#define EAGLE_MAX_DEPTH 16
+#define EAGLE_MAX_CANDIDATES 2048 /* C = top_k + (depth-1)*top_k^2             */
+#define EAGLE_MAX_TREE 256        /* m = total_tokens                          */
+#define EAGLE_MAX_BATCH 32        /* items per batched build / verify call     */
+
+/*
+ * Draft tree, one per sequence ([blog] "Context-Aware Dynamic Tree
+ * Construction" and "Single-Pass Tree Verification").  All arrays are device
+ * arrays of length m (mask: m * mask_words words), written by
+ * eagle_tree_build and read by eagle_tree_verify.
+ *   node 0 is the root (parents[0] = -1, tokens[0] = root token, depth 0);
+ *   nodes 1..m-1 are the selected draft candidates in candidate order, so
+ *   parents[i] < i and siblings appear in draft-rank order;
+ *   mask[i*mask_words + w] bit b  <=>  node 64*w+b is node i or an ancestor;
+ *   pos[i] = depth[i] (the caller adds its prefix length);
+ *   values[i] = cumulative draft log-probability of node i (optional, may be
+ *   NULL; 0 for the root).
+ */
+typedef struct {
+  int32_t*  parents;
+  int32_t*  tokens;
+  int32_t*  depth;
+  int32_t*  pos;
+  uint64_t* mask;
+  double*   values;
+  int32_t   m;          /* total_tokens, root included */
+  int32_t   mask_words; /* must equal (m + 63) / 64    */
+} eagle_tree;
+
+/* Target sampling parameters ([pr] "Performance Notes").  greedy != 0 walks
+ * by argmax and ignores the rest.  Otherwise: logits / temperature (> 0),
+ * keep the top_k largest (0 = all, at most EAGLE_MAX_TOP_K), softmax, then
+ * nucleus top_p in (0, 1] (top_p < 1 needs top_k > 0), renormalise. */
+typedef struct {
+  int32_t greedy;
+  float   temperature;
+  int32_t top_k;
+  float   top_p;
+} eagle_sampling;
+
+const char* eagle_status_string(eagle_status status);
+int32_t eagle_version(void);
+
+/* Zero-fill a workspace (cudaMemsetAsync on `stream`). */
+eagle_status eagle_workspace_init(void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* Synchronise `stream`, then read the workspace's device error word into
+ * *status (EAGLE_OK, EAGLE_ERR_TIMEOUT or EAGLE_ERR_DEVICE_ASSERT) and
+ * *detail (where it happened).  Debug / test use: it blocks the host. */
+eagle_status eagle_workspace_error(const void* ws, eagle_stream stream,
+                                   int32_t* status, int32_t* detail);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_build -- [blog] "The Recurrent Feature Drafting Step" and
+ * "Context-Aware Dynamic Tree Construction"; [disc] reply on the dynamic
+ * tree (value = draft confidence, grow per step, prune at the end).
+ *
+ * draft_logits: fp32 [n_rows][row_stride] row-major, 16-byte aligned,
+ *   row_stride % 4 == 0, row_stride >= vocab.  n_rows >= R where
+ *   R = 1 + (depth-1)*top_k.  Row 0 belongs to the root; the draft row of
+ *   the j-th node of the depth-l frontier is 1 + (l-1)*top_k + j.
+ * Per row: log-probabilities = logit - logsumexp(row) (draft temperature 1)
+ * and the top_k tokens (ties -> lower token id).  Node value = parent value +
+ * log-probability (root 0).  Depth-1 candidates are the root's top_k; at
+ * each depth l = 2..depth-1 the frontier is the top_k candidates of depth l
+ * by value (ties -> lower candidate index), ordered best first, and each
+ * frontier node is expanded by its row's top_k.  The tree keeps the root plus
+ * the best total_tokens-1 candidates overall (ties -> lower candidate index);
+ * the kept set is closed under ancestors because values never increase
+ * along a path.
+ * Limits: 1 <= top_k <= min(64, vocab); 1 <= depth <= 16;
+ *   C = top_k + (depth-1)*top_k^2 <= 2048; 1 <= total_tokens <= min(1+C, 256).
+ * out: device arrays sized for m = total_tokens; out.m must equal
+ *   total_tokens and out.mask_words (m+63)/64.
+ * ws: at least eagle_tree_build_workspace_size(1, n_rows, vocab, top_k,
+ *   depth, total_tokens) bytes, zero-filled before first use.
+ * ------------------------------------------------------------------------ */
+size_t eagle_tree_build_workspace_size(int32_t n_items, int32_t n_rows, int32_t vocab,
+                                       int32_t top_k, int32_t depth, int32_t total_tokens);
+
+eagle_status eagle_tree_build(const float* draft_logits, int64_t row_stride,
+                              int32_t n_rows, int32_t vocab, int32_t top_k,
+                              int32_t depth, int32_t total_tokens, int32_t root_token,
+                              eagle_tree out, void* ws, size_t ws_bytes,
+                              eagle_stream stream);
+
+/* n_items independent sequences in one launch: draft_logits (host array of
+ * n_items device pointers, same row_stride / n_rows / vocab), root_tokens
+ * (host array), outs (host array of n_items trees, same total_tokens). */
+eagle_status eagle_tree_build_batched(int32_t n_items, const float* const* draft_logits,
+                                      int64_t row_stride, int32_t n_rows, int32_t vocab,
+                                      int32_t top_k, int32_t depth, int32_t total_tokens,
+                                      const int32_t* root_tokens, const eagle_tree* outs,
+                                      void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_attn -- [blog] "Single-Pass Tree Verification" (a tree token
+ * attends to its ancestors and itself, never to other branches) over the
+ * target's KV cache of the accepted prefix ([disc] reply on KV caches).
+ *
+ *   out[i][h] = sum_j softmax_j(scale * q[i][h] . k_j) v_j,
+ *   j over the prefix keys of kv head h / (n_q_heads / n_kv_heads) plus the
+ *   tree keys t with mask bit (i, t) set.
+ *
+ * q:        [m][n_q_heads][head_dim]
+ * k_cache,
+ * v_cache:  [n_kv_heads][cache_head_stride] -- head h starts at
+ *           h*cache_head_stride elements; its rows (one per prefix token,
+ *           head_dim elements each) are contiguous; rows 0..prefix_len-1
+ *           are read.  cache_head_stride >= prefix_len*head_dim, multiple
+ *           of 8 elements; the pointers 16-byte aligned.
+ * tree_k,
+ * tree_v:   [m][n_kv_heads][head_dim]: keys / values of the tree tokens.
+ * mask:     [m][(m+63)/64] ancestor bitmask (as written by eagle_tree_build).
+ * out:      fp32 [m][n_q_heads][head_dim].
+ * dtype:    element type of q / caches / tree k,v: EAGLE_BF16 (tensor-core
+ *           path, head_dim 64 or 128) or EAGLE_F32 (CUDA-core path, head_dim
+ *           <= 128, multiple of 4).
+ * scale:    0 selects 1/sqrt(head_dim).
+ * Limits: 1 <= m <= 256; n_q_heads % n_kv_heads == 0; prefix_len >= 0.
+ * ------------------------------------------------------------------------ */
+size_t eagle_tree_attn_workspace_size(int32_t m, int32_t n_q_heads, int32_t n_kv_heads,
+                                      int32_t head_dim, int32_t prefix_len,
+                                      eagle_dtype dtype);
+
+eagle_status eagle_tree_attn(const void* q, const void* k_cache, const void* v_cache,
+                             int64_t cache_head_stride, const void* tree_k,
+                             const void* tree_v, const uint64_t* mask, int32_t m,
+                             int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                             int32_t prefix_len, eagle_dtype dtype, float scale,
+                             float* out, void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* One independent attention problem per item (a layer, or a sequence of a
+ * ragged batch), all in one launch.  Same head counts, head_dim and dtype for
+ * every item; each item has its own pointers, m, prefix_len and cache stride. */
+typedef struct {
+  const void*     q;
+  const void*     k_cache;
+  const void*     v_cache;
+  const void*     tree_k;
+  const void*     tree_v;
+  const uint64_t* mask;
+  float*          out;
+  int64_t         cache_head_stride;
+  int32_t         prefix_len;
+  int32_t         m;
+} eagle_attn_item;
+
+/* items: host array; only m and prefix_len are read here. */
+size_t eagle_tree_attn_batched_workspace_size(const eagle_attn_item* items, int32_t n_items,
+                                              int32_t n_q_heads, int32_t n_kv_heads,
+                                              int32_t head_dim, eagle_dtype dtype);
+
+eagle_status eagle_tree_attn_batched(const eagle_attn_item* items, int32_t n_items,
+                                     int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                     eagle_dtype dtype, float scale,
+                                     void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_verify -- [blog] "Single-Pass Tree Verification" (walk from the
+ * root, accept matching tokens until the first discrepancy; lossless) and
+ * [disc] proposal (acceptance / rejection by speculative sampling).
+ *
+ * target_logits: fp32 [tree.m][row_stride] (16-byte aligned, row_stride % 4
+ *   == 0); row i predicts the token that follows node i.
+ * tree: as written by eagle_tree_build (parents, tokens and m are read).
+ * params (host): greedy -> follow the argmax (ties -> lower id); the bonus
+ *   token is the argmax at the last accepted node.  Sampling -> recursive
+ *   speculative sampling over the children of the current node in node
+ *   order with one-hot draft distributions: u_j = U(seed, step, node, j);
+ *   accept child j iff u_j * (1 - rho) < p(token_j), else rho += p(token_j);
+ *   with no child accepted (or at a leaf) the bonus token is the first token
+ *   (ids ascending, rejected tokens removed) whose cumulative p exceeds
+ *   U(seed, step, node, 0xffffffff) * (1 - rho).  U is Philox4x32-10 with
+ *   key (seed lo, seed hi), counter (step lo, step hi, node, child), u =
+ *   (word0 >> 8) * 2^-24.
+ * accepted: device int32 [tree.m]: node ids of the accepted path starting
+ *   with the root (entries past *n_accepted + 1 are left untouched).
+ * n_accepted, bonus_token: device int32 scalars (accepted draft tokens,
+ *   0..depth; the token to emit after them).
+ * ------------------------------------------------------------------------ */
+size_t eagle_tree_verify_workspace_size(int32_t n_items, int32_t m, int32_t vocab);
+
+eagle_status eagle_tree_verify(const float* target_logits, int64_t row_stride, int32_t vocab,
+                               eagle_tree tree, const eagle_sampling* params,
+                               uint64_t seed, uint64_t step, int32_t* accepted,
+                               int32_t* n_accepted, int32_t* bonus_token,
+                               void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* n_items sequences (same m, row_stride, vocab) in one launch.  Host arrays:
+ * target_logits, trees, params, seeds, accepted (device pointers each).
+ * n_accepted, bonus_tokens: device int32 [n_items]. */
+eagle_status eagle_tree_verify_batched(int32_t n_items, const float* const* target_logits,
+                                       int64_t row_stride, int32_t vocab,
+                                       const eagle_tree* trees, const eagle_sampling* params,
+                                       const uint64_t* seeds, uint64_t step,
+                                       int32_t* const* accepted, int32_t* n_accepted,
+                                       int32_t* bonus_tokens,
+                                       void* ws, size_t ws_bytes, eagle_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EAGLE_H */

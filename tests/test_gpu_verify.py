@@ -1,0 +1,123 @@
+"""GPU parity of eagle_tree_verify against the oracle (bit-exact accepted
+path and bonus token; near ties reported), through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+from eagle_speculative_decoding_verify_gb300 import binding as eb
+from eagle_speculative_decoding_verify_gb300 import workloads as wl
+from oracle.tree_build import build_draft_tree
+from oracle.verify import verify_tree
+from tests.parity import path_matches
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(key, item=0):
+    w = wl.WORKLOADS[key]
+    ref = build_draft_tree(wl.draft_logits(w, item).numpy(), w.top_k, w.depth, w.total_tokens,
+                           wl.root_token(w, item))
+    target = wl.target_logits(w, ref["parents"], ref["tokens"], item)
+    return w, ref, target
+
+
+def _verify(target, ref, greedy=True, T=1.0, top_k=0, top_p=1.0, seed=0, step=0):
+    tree = eb.Tree.from_arrays(ref["parents"], ref["tokens"])
+    acc, n, bonus = eb.eagle_tree_verify(target.cuda(), tree,
+                                         eb.sampling(greedy, T, top_k, top_p), seed, step)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), int(n.item()), int(bonus.item())
+
+
+@pytest.mark.parametrize("key", ["c0", "c1", "c3"])
+def test_greedy_workloads(key):
+    w, ref, target = _case(key)
+    v = verify_tree(target.numpy(), ref["parents"], ref["tokens"])
+    acc, n, bonus = _verify(target, ref)
+    path_matches(acc, n, bonus, v, key)
+
+
+def test_greedy_forced_full_chain():
+    w, ref, target = _case("c1")
+    target = target.clone()
+    # force every node's argmax onto its first child: the walk accepts the
+    # whole first-child chain
+    kids = {}
+    for i in range(1, ref["m"]):
+        kids.setdefault(int(ref["parents"][i]), []).append(i)
+    for p, cs in kids.items():
+        target[p, int(ref["tokens"][cs[0]])] = 100.0
+    v = verify_tree(target.numpy(), ref["parents"], ref["tokens"])
+    acc, n, bonus = _verify(target, ref)
+    assert n == w.depth
+    path_matches(acc, n, bonus, v, "forced chain")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_sampling_topk_topp_qwen7b(seed):
+    w, ref, target = _case("c2")
+    _, T, k, p = w.sampling_of(0)
+    v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False, temperature=T,
+                    top_k=k, top_p=p, seed=seed, step=seed * 7)
+    acc, n, bonus = _verify(target, ref, False, T, k, p, seed, seed * 7)
+    path_matches(acc, n, bonus, v, f"seed{seed}")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_sampling_full_vocab(seed):
+    w, ref, target = _case("c4", item=8)
+    v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False, temperature=1.0,
+                    seed=seed, step=3)
+    acc, n, bonus = _verify(target, ref, False, 1.0, 0, 1.0, seed, 3)
+    path_matches(acc, n, bonus, v, f"full seed{seed}")
+
+
+@pytest.mark.parametrize("T,k,p", [(0.5, 1, 1.0), (1.3, 64, 1.0), (0.9, 7, 0.5), (2.0, 0, 1.0)])
+def test_sampling_variants_rejections(T, k, p):
+    # flat rows so that children get rejected and residual draws happen
+    w = wl.WORKLOADS["c0"]
+    ref = build_draft_tree(wl.draft_logits(w).numpy(), w.top_k, w.depth, w.total_tokens, 5)
+    g = torch.Generator().manual_seed(17)
+    target = torch.randn(w.total_tokens, 5003, generator=g) * 0.7
+    for seed in range(12):
+        v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False,
+                        temperature=T, top_k=k, top_p=p, seed=seed, step=1)
+        acc, n, bonus = _verify(target, ref, False, T, k, p, seed, 1)
+        path_matches(acc, n, bonus, v, f"T{T} k{k} p{p} seed{seed}")
+
+
+def test_batched_ragged16_mixed_modes():
+    w = wl.WORKLOADS["c4"]
+    refs, targets, trees, params = [], [], [], []
+    for b in range(w.items):
+        _, ref, target = _case("c4", b)
+        refs.append(ref)
+        targets.append(target)
+        trees.append(eb.Tree.from_arrays(ref["parents"], ref["tokens"]))
+        gr, T, k, p = w.sampling_of(b)
+        params.append(eb.sampling(gr, T, k, p))
+    seeds = [1000 + b for b in range(w.items)]
+    acc, n, bonus = eb.eagle_tree_verify_batched([t.cuda() for t in targets], trees, params,
+                                                 seeds, step=5)
+    torch.cuda.synchronize()
+    for b in range(w.items):
+        gr, T, k, p = w.sampling_of(b)
+        v = verify_tree(targets[b].numpy(), refs[b]["parents"], refs[b]["tokens"], greedy=bool(gr),
+                        temperature=T, top_k=k, top_p=p, seed=seeds[b], step=5)
+        path_matches(acc[b].cpu().numpy(), int(n[b]), int(bonus[b]), v, f"item{b}")
+
+
+def test_single_node_tree():
+    g = torch.Generator().manual_seed(3)
+    target = torch.randn(1, 3000, generator=g)
+    ref = dict(parents=np.array([-1]), tokens=np.array([7]))
+    acc, n, bonus = _verify(target, ref)
+    assert n == 0 and bonus == int(torch.argmax(target[0]))
+
+
+def test_rejects_nucleus_without_top_k():
+    _, ref, target = _case("c0")
+    with pytest.raises(eb.EagleError) as e:
+        _verify(target, ref, False, 1.0, 0, 0.9)
+    assert e.value.status == 2
