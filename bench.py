@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of one EAGLE-2 tree-verify step on GB300: draft-tree build,
+tree-masked GQA attention, acceptance walk (all three through the C ABI).
+
+Default workload: Qwen2-7B layer shape at 8K context (28 q / 4 kv heads,
+d 128, bf16 KV prefix 8192; vocab 152064; top_k 10, depth 6, 60-token tree;
+sampling T 0.7, top_k 50, top_p 0.9), synthetic seeded inputs.
+
+Prints ONE JSON line (rank 0).  `value` = microseconds per verify step with
+every input resident in HBM, L2 flushed before each step (inputs 86 MB < L2),
+step replayed as a CUDA graph; `e2e` = the same step with the per-step inputs
+copied from pinned host memory and the accepted path read back.
+--impl reference times the fp64 CPU oracle on the same workload (host cores).
+With torchrun (N > 1) every rank runs an independent replica (weak scaling).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per tree-verify step and tree-attn HBM GB/s (% of peak) at 8K ctx"
+NAMES = ("q", "k_cache", "v_cache", "tree_k", "tree_v")
+WORKLOAD_LABEL = {
+    "c0": "tiny: vocab 1000, 16-token tree, 4/2 heads d64 fp32, prefix 128, greedy",
+    "c1": "llama3-8b layer: vocab 128256, 60-token tree, 32/8 heads d128, prefix 2048, greedy",
+    "c2": "qwen2-7b layer: vocab 152064, 60-token tree (top_k 10, depth 6), 28/4 heads d128, "
+          "bf16 prefix 8192, sampling T0.7 top_k50 top_p0.9",
+    "c3": "llama3-8b, 32 layers x prefix 32768: vocab 128256, 60-token tree, greedy",
+    "c4": "16 ragged sequences, prefixes U[512,16384], 64/8 heads d128, vocab 128256",
+}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = self.rows
+        if self.window:
+            t0, t1 = self.window
+            inside = [r for r in rows if t0 - 0.06 <= r[0] <= t1 + 0.06]
+            rows = inside or rows
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, v in rows:
+            try:
+                sm.append(float(v[0]))
+                smax = max(smax, float(v[1]))
+                for n, flag in zip(names, v[4:8]):
+                    if flag.lower().startswith("active"):
+                        reasons.add(n)
+            except Exception:
+                pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def _kernel_source_hash():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "eagle_speculative_decoding_verify_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+class Step:
+    """Device buffers and the three calls of one verify step (single sequence)."""
+
+    def __init__(self, w, dev, eb, wl):
+        import torch
+        self.torch, self.eb, self.w = torch, eb, w
+        self.draft_h = wl.draft_logits(w)
+        self.root = wl.root_token(w)
+        a = wl.attention_inputs(w)
+        self.attn_h = {n: a[n] for n in NAMES}
+        self.draft = self.draft_h.to(dev)
+        self.attn = {n: t.to(dev) for n, t in self.attn_h.items()}
+        self.tree = eb.Tree(w.total_tokens, dev)
+        self.ws_build = eb.workspace(eb.eagle_tree_build_workspace_size(
+            1, w.n_rows, w.vocab, w.top_k, w.depth, w.total_tokens), dev)
+        dtype = eb.EAGLE_BF16 if w.dtype == "bf16" else eb.EAGLE_F32
+        self.out = torch.empty(w.total_tokens, w.n_q_heads, w.head_dim, device=dev)
+        self.ws_attn = eb.workspace(eb.eagle_tree_attn_workspace_size(
+            w.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.prefix, dtype), dev)
+        self.item = eb.attn_item(self.attn["q"], self.attn["k_cache"], self.attn["v_cache"],
+                                 self.attn["tree_k"], self.attn["tree_v"], self.tree.mask,
+                                 self.out)
+        self.attn_launches = eb.eagle_tree_attn_num_launches(
+            [self.item], w.n_q_heads, w.n_kv_heads, w.head_dim, dtype)
+        gr, T, k, p = w.sampling_of(0)
+        self.params = eb.sampling(gr, T, k, p)
+        # target logits depend on the tree: build it once (untimed) on the GPU
+        eb.eagle_tree_build(self.draft, w.top_k, w.depth, w.total_tokens, self.root,
+                            out=self.tree, ws=self.ws_build)
+        torch.cuda.synchronize()
+        self.target_h = wl.target_logits(w, self.tree.parents.cpu().tolist(),
+                                         self.tree.tokens.cpu().tolist())
+        self.target = self.target_h.to(dev)
+        self.ws_verify = eb.workspace(eb.eagle_tree_verify_workspace_size(
+            1, w.total_tokens, w.vocab), dev)
+        self.acc = torch.zeros(w.total_tokens, dtype=torch.int32, device=dev)
+        self.n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.bonus = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.launches = 1 + self.attn_launches + 1
+
+    def build(self, s):
+        w = self.w
+        self.eb.eagle_tree_build(self.draft, w.top_k, w.depth, w.total_tokens, self.root,
+                                 out=self.tree, ws=self.ws_build, stream=s)
+
+    def attention(self, s):
+        w = self.w
+        a = self.attn
+        self.eb.eagle_tree_attn(a["q"], a["k_cache"], a["v_cache"], a["tree_k"], a["tree_v"],
+                                self.tree.mask, out=self.out, ws=self.ws_attn, stream=s)
+
+    def verify(self, s, step=0):
+        self.eb.eagle_tree_verify(self.target, self.tree, self.params, 1234, step,
+                                  accepted=self.acc, n_accepted=self.n_acc,
+                                  bonus_token=self.bonus, ws=self.ws_verify, stream=s)
+
+    def run(self, s):
+        self.build(s)
+        self.attention(s)
+        self.verify(s)
+
+    # algorithmic bytes / flops
+    def bytes_build(self):
+        w = self.w
+        return w.n_rows * w.vocab * 4
+
+    def bytes_verify(self):
+        w = self.w
+        return w.total_tokens * w.vocab * 4
+
+    def bytes_attn(self):
+        w = self.w
+        el = 2 if w.dtype == "bf16" else 4
+        kv = 2 * w.prefix * w.n_kv_heads * w.head_dim * el
+        q = w.total_tokens * w.n_q_heads * w.head_dim * el
+        tkv = 2 * w.total_tokens * w.n_kv_heads * w.head_dim * el
+        out = w.total_tokens * w.n_q_heads * w.head_dim * 4
+        return kv + q + tkv + out
+
+    def flops_attn(self):
+        w = self.w
+        return 4.0 * w.total_tokens * w.n_q_heads * (w.prefix + w.total_tokens) * w.head_dim
+
+    def h2d_bytes(self):
+        return (self.draft_h.numel() * 4 + self.target_h.numel() * 4 +
+                sum(self.attn_h[n].numel() * self.attn_h[n].element_size()
+                    for n in ("q", "tree_k", "tree_v")))
+
+
+def _time_graph(torch, step, s, flush, K):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        step.run(s)          # warm the allocator-free path once outside capture
+    s.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        step.run(s)
+    times = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    with torch.cuda.stream(s):
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+    s.synchronize()
+    for e0, e1 in ev:
+        times.append(e0.elapsed_time(e1) * 1e3)
+    return times, g
+
+
+def _time_kernels(torch, step, s, flush, K):
+    """Per-call device times (µs) with events between the calls."""
+    per = {"build": [], "attn": [], "verify": []}
+    evs = []
+    with torch.cuda.stream(s):
+        for _ in range(K):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            flush.zero_()
+            e[0].record(s)
+            step.build(s)
+            e[1].record(s)
+            step.attention(s)
+            e[2].record(s)
+            step.verify(s)
+            e[3].record(s)
+            evs.append(e)
+    s.synchronize()
+    for e in evs:
+        per["build"].append(e[0].elapsed_time(e[1]) * 1e3)
+        per["attn"].append(e[1].elapsed_time(e[2]) * 1e3)
+        per["verify"].append(e[2].elapsed_time(e[3]) * 1e3)
+    return per
+
+
+def _time_e2e(torch, step, s, flush, K):
+    """Same step with per-step inputs from pinned host memory and the result
+    read back; device-timed around copies + calls."""
+    pin = {n: step.attn_h[n].pin_memory() for n in ("q", "tree_k", "tree_v")}
+    draft_p = step.draft_h.pin_memory()
+    target_p = step.target_h.pin_memory()
+    out_acc = torch.empty(step.acc.numel() + 2, dtype=torch.int32).pin_memory()
+    times = []
+    evs = []
+    with torch.cuda.stream(s):
+        for _ in range(K):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            step.draft.copy_(draft_p, non_blocking=True)
+            for n in ("q", "tree_k", "tree_v"):
+                step.attn[n].copy_(pin[n], non_blocking=True)
+            step.target.copy_(target_p, non_blocking=True)
+            step.run(s)
+            out_acc[: step.acc.numel()].copy_(step.acc, non_blocking=True)
+            out_acc[-2:-1].copy_(step.n_acc, non_blocking=True)
+            out_acc[-1:].copy_(step.bonus, non_blocking=True)
+            e1.record(s)
+            evs.append((e0, e1))
+    s.synchronize()
+    for e0, e1 in evs:
+        times.append(e0.elapsed_time(e1) * 1e3)
+    d2h = (step.acc.numel() + 2) * 4
+    return times, d2h
+
+
+# known ncu DRAM traffic per launch (bytes), keyed by kernel and source hash;
+# entries whose hash no longer matches the sources are reported as null
+TRAFFIC = {}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from eagle_speculative_decoding_verify_gb300 import _build
+    _build.build()
+    from eagle_speculative_decoding_verify_gb300 import binding as eb
+    from eagle_speculative_decoding_verify_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    step = Step(w, dev, eb, wl)
+    s = torch.cuda.Stream(device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x L2
+    with torch.cuda.stream(s):
+        for _ in range(max(args.warmup, 3)):
+            flush.zero_()
+            step.run(s)
+    s.synchronize()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local_rank] if vis else local_rank)
+    sampler.start()
+    time.sleep(0.15)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    try:
+        times, _ = _time_graph(torch, step, s, flush, args.steps)
+        graphed = True
+    except Exception as exc:  # capture refused: time the plain stream launches
+        print(f"cuda graph capture failed ({exc}); timing without a graph", file=sys.stderr)
+        torch.cuda.synchronize()
+        per0 = _time_kernels(torch, step, s, flush, args.steps)
+        times = [a + b + c for a, b, c in zip(per0["build"], per0["attn"], per0["verify"])]
+        graphed = False
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.window = (t_wall0, t_wall1)
+    per = _time_kernels(torch, step, s, flush, args.steps)
+    e2e_times, d2h = _time_e2e(torch, step, s, flush, args.steps)
+    time.sleep(0.1)
+    sampler.stop()
+
+    us = statistics.mean(times)
+    if world > 1:
+        t = torch.tensor([us], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        us = float(t.item())
+    hbm, tf, tf_sus, peak_src = _peaks()
+    k_us = {k: statistics.mean(v) for k, v in per.items()}
+    attn_gbs = step.bytes_attn() / (k_us["attn"] * 1e-6) / 1e9
+    attn_tflops = step.flops_attn() / (k_us["attn"] * 1e-6) / 1e12
+    dominant = max(k_us, key=k_us.get)
+    src_hash = _kernel_source_hash()
+    if dominant == "attn" and step.flops_attn() / step.bytes_attn() > tf * 1e12 / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": attn_tflops, "peak": tf, "unit": "TFLOP/s",
+                "frac": attn_tflops / tf}
+    else:
+        b = {"build": step.bytes_build(), "attn": step.bytes_attn(),
+             "verify": step.bytes_verify()}[dominant]
+        gbs = b / (k_us[dominant] * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
+    tr = TRAFFIC.get(f"{dominant}:{args.workload}")
+    roof.update({"kernel": dominant, "peak_source": peak_src,
+                 "traffic": tr[1] if tr and tr[0] == src_hash else None})
+    step_roof_us = (step.bytes_build() / (hbm * 1e3) + step.bytes_verify() / (hbm * 1e3) +
+                    max(step.bytes_attn() / (hbm * 1e3), step.flops_attn() / (tf * 1e6)))
+    line = {
+        "metric": METRIC, "value": round(us, 3), "unit": "us", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 logits + bf16 attention (fp32 accumulate)" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded generators; no dataset or weights)",
+        "config": {"workload": f"{args.workload} {WORKLOAD_LABEL[args.workload]}",
+                   "l2": "flushed before every step (512 MB write)", "cuda_graph": graphed,
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "step_roofline_us": round(step_roof_us, 3),
+        "step_roofline_frac": round(step_roof_us / us, 4),
+        "kernels_us": {k: round(v, 3) for k, v in k_us.items()},
+        "step_us_no_graph": round(sum(k_us.values()), 3),
+        "tree_attn": {"achieved_gbs": round(attn_gbs, 1), "frac_hbm": round(attn_gbs / hbm, 4),
+                      "achieved_tflops": round(attn_tflops, 1),
+                      "frac_tensor": round(attn_tflops / tf, 4), "peak_source": peak_src},
+        "e2e": {"value": round(statistics.mean(e2e_times), 3), "unit": "us",
+                "h2d_bytes_per_step": step.h2d_bytes(), "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, samples=1)
+    return line
+
+
+# ------------------------------------------------------------- oracle (CPU)
+def _oracle_step(w, wl, inputs):
+    from oracle.tree_attn import tree_attention
+    from oracle.tree_build import build_draft_tree
+    from oracle.verify import verify_tree
+    draft, attn, root = inputs
+    t = build_draft_tree(draft, w.top_k, w.depth, w.total_tokens, root)
+    target = wl.target_logits(w, t["parents"], t["tokens"]).numpy()   # input generation
+    t0 = time.perf_counter()
+    tree_attention(*(attn[n] for n in NAMES), t["mask"], w.prefix)
+    gr, T, k, p = w.sampling_of(0)
+    verify_tree(target, t["parents"], t["tokens"], greedy=bool(gr), temperature=T, top_k=k,
+                top_p=p, seed=1234, step=0)
+    return time.perf_counter() - t0
+
+
+def _oracle_inputs(w, wl):
+    a = wl.attention_inputs(w)
+    return (wl.draft_logits(w).numpy(), {n: a[n].double().numpy() for n in NAMES},
+            wl.root_token(w))
+
+
+def cpu_baseline(key, samples=1):
+    """Oracle step time on the host cores (build + attention + verify; the
+    target-logit generation between build and verify is not timed)."""
+    from oracle.tree_build import build_draft_tree
+    from eagle_speculative_decoding_verify_gb300 import workloads as wl
+    w = wl.WORKLOADS[key]
+    inputs = _oracle_inputs(w, wl)
+    ts = []
+    for _ in range(samples):
+        t0 = time.perf_counter()
+        build_draft_tree(inputs[0], w.top_k, w.depth, w.total_tokens, inputs[2])
+        tb = time.perf_counter() - t0
+        ts.append(tb + _oracle_step(w, wl, inputs))
+    return {"value": round(statistics.mean(ts) * 1e6, 1), "unit": "us", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{samples} full step(s) of workload {key}: fp64 numpy tree build, "
+                      "tree attention, acceptance walk"}
+
+
+def run_reference(args):
+    from eagle_speculative_decoding_verify_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    inputs = _oracle_inputs(w, wl)
+    from oracle.tree_build import build_draft_tree
+
+    def one():
+        t0 = time.perf_counter()
+        build_draft_tree(inputs[0], w.top_k, w.depth, w.total_tokens, inputs[2])
+        return time.perf_counter() - t0 + _oracle_step(w, wl, inputs)
+
+    for _ in range(min(args.warmup, 1)):
+        one()
+    budget = 150.0
+    ts = []
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        ts.append(one())
+        if time.perf_counter() - t_start > budget:
+            break
+    us = statistics.mean(ts) * 1e6
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us",
+        "n_gpus": 0, "steps": len(ts), "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generators; no dataset or weights)",
+        "config": {"workload": f"{args.workload} {WORKLOAD_LABEL[args.workload]}"},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{len(ts)} full oracle step(s) of workload {args.workload} "
+                                   "(timed steps capped at 150 s of host time)"},
+        "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2", choices=["c0", "c1", "c2"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

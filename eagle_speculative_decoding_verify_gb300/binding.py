@@ -73,6 +73,7 @@ EXPORTS = {
     "eagle_tree_attn": (_I32, [_P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                _F, _P, _P, _SZ, _P]),
     "eagle_tree_attn_batched_workspace_size": (_SZ, [_P, _I32, _I32, _I32, _I32, _I32]),
+    "eagle_tree_attn_num_launches": (_I32, [_P, _I32, _I32, _I32, _I32, _I32]),
     "eagle_tree_attn_batched": (_I32, [_P, _I32, _I32, _I32, _I32, _I32, _F, _P, _SZ, _P]),
     "eagle_tree_verify_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "eagle_tree_verify": (_I32, [_P, _I64, _I32, CTree, ctypes.POINTER(CSampling), _U64, _U64,
@@ -245,6 +246,12 @@ def eagle_tree_attn_batched_workspace_size(items, n_q_heads, n_kv_heads, head_di
     arr = (CAttnItem * len(items))(*items)
     return lib().eagle_tree_attn_batched_workspace_size(arr, len(items), n_q_heads, n_kv_heads,
                                                         head_dim, dtype)
+
+
+def eagle_tree_attn_num_launches(items, n_q_heads, n_kv_heads, head_dim, dtype):
+    arr = (CAttnItem * len(items))(*items)
+    return lib().eagle_tree_attn_num_launches(arr, len(items), n_q_heads, n_kv_heads, head_dim,
+                                              dtype)
 
 
 def eagle_tree_attn_batched(items, n_q_heads, n_kv_heads, head_dim, dtype, scale=0.0, ws=None,

@@ -279,9 +279,32 @@ static size_t attn_ws_size(const eagle_attn_item* items, int32_t n, int32_t hq, 
   return need;
 }
 
+static int32_t attn_num_launches(const eagle_attn_item* items, int32_t n, int32_t hq,
+                                 int32_t hkv, int32_t d, eagle_dtype dtype) {
+  if (!items || n < 1 || hq < 1 || hkv < 1 || d < 1) return 0;
+  int32_t count = 0;
+  for (int b0 = 0; b0 < n; b0 += kAttnMaxItems) {
+    const int nb = (n - b0) < kAttnMaxItems ? (n - b0) : kAttnMaxItems;
+    if (dtype == EAGLE_BF16 && tc_supported(d)) {
+      count += attn_tc_num_launches(items + b0, nb, hq, hkv, d);
+    } else {
+      AttnPlan P;
+      plan_simt(P, items + b0, nb, hq, hkv, d, 0.f, kPlanSMs);
+      count += 1 + (P.part_floats > 0 ? 1 : 0);
+    }
+  }
+  return count;
+}
+
 }  // namespace eagle
 
 using namespace eagle;
+
+extern "C" int32_t eagle_tree_attn_num_launches(const eagle_attn_item* items, int32_t n_items,
+                                                int32_t n_q_heads, int32_t n_kv_heads,
+                                                int32_t head_dim, eagle_dtype dtype) {
+  return attn_num_launches(items, n_items, n_q_heads, n_kv_heads, head_dim, dtype);
+}
 
 extern "C" size_t eagle_tree_attn_batched_workspace_size(const eagle_attn_item* items,
                                                          int32_t n_items, int32_t n_q_heads,

@@ -43,6 +43,7 @@ struct AttnPlan {
 // tensor-core path (eagle_attn_tc.cu)
 bool tc_supported(int head_dim);
 size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms);
+int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d);
 eagle_status attn_tc_launch(const eagle_attn_item* items, int n, int hq, int hkv, int d,
                             float scale, void* ws, size_t ws_bytes, cudaStream_t stream, int sms);
 

@@ -3,6 +3,7 @@
 
 namespace eagle {
 bool tc_supported(int) { return false; }
+int attn_tc_num_launches(const eagle_attn_item*, int, int, int, int) { return 0; }
 size_t attn_tc_ws_size(const eagle_attn_item*, int, int, int, int, int) { return 0; }
 eagle_status attn_tc_launch(const eagle_attn_item*, int, int, int, int, float, void*, size_t,
                             cudaStream_t, int) {

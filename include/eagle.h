@@ -216,6 +216,13 @@ size_t eagle_tree_attn_batched_workspace_size(const eagle_attn_item* items, int3
                                               int32_t n_q_heads, int32_t n_kv_heads,
                                               int32_t head_dim, eagle_dtype dtype);
 
+/* Number of kernels one eagle_tree_attn_batched call with these items
+ * launches (host-side planning only; items: host array, only m and
+ * prefix_len are read). */
+int32_t eagle_tree_attn_num_launches(const eagle_attn_item* items, int32_t n_items,
+                                     int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                     eagle_dtype dtype);
+
 eagle_status eagle_tree_attn_batched(const eagle_attn_item* items, int32_t n_items,
                                      int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                      eagle_dtype dtype, float scale,

@@ -85,12 +85,12 @@ def build_draft_tree(draft_logits, top_k, depth, total_tokens, root_token, log=N
     for r in range(R):
         row = logits[r].astype(np.float64)
         lse[r] = row_logsumexp(row)
-        ids = row_top_k(row, k)
+        ranked = row_top_k(row, min(k + 1, V))
+        ids = ranked[:k]
         top_ids[r] = ids
         top_logp[r] = row[ids] - lse[r]
         if V > k:   # k-th vs (k+1)-th logit: raw fp32 values, exact on both sides
-            nxt = row_top_k(row, k + 1)[-1]
-            log.check("draft_topk_cut", f"row{r}", row[ids[-1]], row[nxt], exact=True)
+            log.check("draft_topk_cut", f"row{r}", row[ids[-1]], row[ranked[k]], exact=True)
 
     value = np.zeros(C, dtype=np.float64)
     token = np.zeros(C, dtype=np.int64)

@@ -50,5 +50,16 @@ def path_matches(acc, n_acc, bonus, ref, what="verify"):
     return True
 
 
+def to_device_rows(x, stride=None):
+    """Copy fp32 rows [R, V] to the GPU with a row stride that is a multiple of
+    4 elements (the library's alignment rule); returns the [R, V] view."""
+    import torch
+    R, V = x.shape
+    stride = stride or (V + 3) // 4 * 4
+    full = torch.full((R, stride), -3.0e38, dtype=torch.float32, device="cuda")
+    full[:, :V] = x.to("cuda")
+    return full[:, :V]
+
+
 def max_abs(a, b):
     return float(np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64)).max())

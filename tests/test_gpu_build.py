@@ -8,7 +8,7 @@ import torch
 from eagle_speculative_decoding_verify_gb300 import binding as eb
 from eagle_speculative_decoding_verify_gb300 import workloads as wl
 from oracle.tree_build import build_draft_tree, tree_sizes
-from tests.parity import tree_matches
+from tests.parity import to_device_rows, tree_matches
 
 pytestmark = pytest.mark.gpu
 
@@ -25,15 +25,9 @@ def _rows(R, V, seed, stride=None):
 
 
 def _run(x, k, D, m, root=3):
-    """Copy x (possibly a column slice of a wider buffer) to the GPU with the
-    same row stride and build the tree there."""
-    dev = torch.device("cuda")
-    if x.is_contiguous():
-        xd = x.to(dev)
-    else:
-        full = torch.empty(x.shape[0], x.stride(0), dtype=torch.float32, device=dev)
-        full[:, : x.shape[1]] = x.to(dev)
-        xd = full[:, : x.shape[1]]
+    """Copy x to the GPU (row stride rounded up to 4 elements, or x's own
+    stride when it is a slice of a wider buffer) and build the tree there."""
+    xd = to_device_rows(x, x.stride(0) if not x.is_contiguous() else None)
     t = eb.eagle_tree_build(xd, k, D, m, root)
     torch.cuda.synchronize()
     return t
@@ -55,7 +49,7 @@ def test_workload_trees(key):
     (777, 3, 5, 30, 3),        # vocab below one tile
     (20000, 1, 6, 7, 4),       # top_k 1: a chain
     (3000, 9, 1, 10, 5),       # depth 1: a star
-    (2048, 3, 3, 40, 6),       # m = 1 + C: every candidate kept
+    (2048, 3, 3, 22, 6),       # m = 1 + C: every candidate kept
     (4096, 7, 3, 1, 7),        # root only
     (70001, 64, 1, 65, 8),     # maximum top_k
     (9000, 2, 16, 31, 9),      # maximum depth

@@ -9,7 +9,7 @@ from eagle_speculative_decoding_verify_gb300 import binding as eb
 from eagle_speculative_decoding_verify_gb300 import workloads as wl
 from oracle.tree_build import build_draft_tree
 from oracle.verify import verify_tree
-from tests.parity import path_matches
+from tests.parity import path_matches, to_device_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +24,7 @@ def _case(key, item=0):
 
 def _verify(target, ref, greedy=True, T=1.0, top_k=0, top_p=1.0, seed=0, step=0):
     tree = eb.Tree.from_arrays(ref["parents"], ref["tokens"])
-    acc, n, bonus = eb.eagle_tree_verify(target.cuda(), tree,
+    acc, n, bonus = eb.eagle_tree_verify(to_device_rows(target), tree,
                                          eb.sampling(greedy, T, top_k, top_p), seed, step)
     torch.cuda.synchronize()
     return acc.cpu().numpy(), int(n.item()), int(bonus.item())
@@ -50,7 +50,12 @@ def test_greedy_forced_full_chain():
         target[p, int(ref["tokens"][cs[0]])] = 100.0
     v = verify_tree(target.numpy(), ref["parents"], ref["tokens"])
     acc, n, bonus = _verify(target, ref)
-    assert n == w.depth
+    chain = 0       # length of the first-child chain from the root
+    node = 0
+    while node in kids:
+        node = kids[node][0]
+        chain += 1
+    assert n == chain
     path_matches(acc, n, bonus, v, "forced chain")
 
 
