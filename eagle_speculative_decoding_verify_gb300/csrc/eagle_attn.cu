@@ -156,6 +156,12 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__
 }
 
 // ------------------------------------------------------------------ host
+eagle_status launch_attn_merge(const AttnPlan& P, cudaStream_t stream) {
+  const int64_t rows = P.row_start[P.n_items];
+  attn_merge_kernel<<<static_cast<int>((rows + 3) / 4), 128, 0, stream>>>(P);
+  return launch_status();
+}
+
 static eagle_status validate(const eagle_attn_item* items, int n, int hq, int hkv, int d,
                              eagle_dtype dtype) {
   EAGLE_CHECK_ARG(items && n >= 1);
@@ -250,11 +256,7 @@ static eagle_status attn_batched_impl(const eagle_attn_item* items, int32_t n, i
     else
       attn_simt_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(P);
     if ((st = launch_status()) != EAGLE_OK) return st;
-    if (P.part_floats > 0) {
-      const int64_t rows = P.row_start[nb];
-      attn_merge_kernel<<<static_cast<int>((rows + 3) / 4), 128, 0, stream>>>(P);
-      if ((st = launch_status()) != EAGLE_OK) return st;
-    }
+    if (P.part_floats > 0 && (st = launch_attn_merge(P, stream)) != EAGLE_OK) return st;
   }
   return EAGLE_OK;
 }

@@ -40,6 +40,9 @@ struct AttnPlan {
   float* partials;
 };
 
+// Launch the split merge (eagle_attn.cu) for a plan whose partials are set.
+eagle_status launch_attn_merge(const AttnPlan& P, cudaStream_t stream);
+
 // tensor-core path (eagle_attn_tc.cu)
 bool tc_supported(int head_dim);
 size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms);

@@ -1,12 +1,602 @@
-// Tensor-core (tcgen05) path of eagle_tree_attn: not enabled yet.
+// Tensor-core path of eagle_tree_attn for bf16 Q/K/V (head_dim 64 or 128).
+//
+// Source: "EAGLE-2: Feature-Level Speculative Decoding Guide", "Single-Pass
+// Tree Verification" (one target pass over the tree; a token attends to its
+// ancestors and itself only) over the target's prefix KV cache.
+//
+// The m tree queries of one KV head times its g query heads form the M
+// dimension (row R = i*g + head-in-group), so the g heads that share a KV
+// head share every K/V byte.  One CTA = (item, kv head, pair of 128-row
+// query tiles, KV split) and runs warp-specialised:
+//   warp 0      TMA producer: K and V chunks of 128 keys (prefix from the
+//               cache tensor map, then the tree keys) into a 3-slot ring of
+//               128-byte-swizzled shared-memory tiles.
+//   warp 1      tensor-memory owner and MMA issuer: S_t = Q_t K^T (M 128,
+//               N 128, K = head_dim) and O_t += P_t V (M 128, N = head_dim,
+//               K 128) with tcgen05.mma kind::f16, fp32 accumulators in
+//               tensor memory (S_0, S_1, O_0, O_1 = 512 columns).
+//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1: one thread per
+//   / 8-11      query row reads its S row from tensor memory, applies scale,
+//               the prefix bound and the ancestor mask, updates the running
+//               max / sum (O rescaled in tensor memory only when the max
+//               grows by more than 2^8), writes P in bf16 to shared memory.
+// The epilogue writes the normalised row (one split) or an unnormalised
+// partial (o, max, sum) that attn_merge_kernel combines.  Every mbarrier
+// wait is bounded; on a timeout the CTA records the error, drains its own
+// copies and MMAs, frees tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "eagle_attn.h"
+#include "eagle_host.h"
+#include "eagle_tc.cuh"
 
 namespace eagle {
-bool tc_supported(int) { return false; }
-int attn_tc_num_launches(const eagle_attn_item*, int, int, int, int) { return 0; }
-size_t attn_tc_ws_size(const eagle_attn_item*, int, int, int, int, int) { return 0; }
-eagle_status attn_tc_launch(const eagle_attn_item*, int, int, int, int, float, void*, size_t,
-                            cudaStream_t, int) {
+
+constexpr int kTcMaxItems = 16;     // items per launch (tensor maps live in the params)
+constexpr int kTcThreads = 384;     // 12 warps
+constexpr int kChunk = 128;         // keys per K/V chunk
+constexpr int kSlots = 3;           // K/V ring depth
+constexpr uint32_t kTmemCols = 512;
+
+struct TcItem {
+  const __nv_bfloat16* q;
+  float* out;
+  const uint64_t* mask;
+  int m, prefix_len, splits, tile_pairs, unit_start;
+  int64_t part_start;
+};
+
+struct TcParams {
+  CUtensorMap kmap[kTcMaxItems];
+  CUtensorMap vmap[kTcMaxItems];
+  CUtensorMap tkmap[kTcMaxItems];
+  CUtensorMap tvmap[kTcMaxItems];
+  TcItem items[kTcMaxItems];
+  int n_items, hq, hkv, g, span_chunks, total_units;
+  float scale_log2;
+  float* partials;
+  int32_t* err;
+};
+
+template <int D>
+struct TcSmem {
+  static constexpr int kTileBytes = 128 * D * 2;      // one 128-row bf16 tile of width D
+  static constexpr int kPBytes = 128 * kChunk * 2;    // P tile: 128 rows x 128 keys
+  static constexpr int kQ = 0;
+  static constexpr int kP = kQ + 2 * kTileBytes;
+  static constexpr int kRing = kP + 2 * kPBytes;
+  static constexpr int kBars = kRing + kSlots * kTileBytes;
+  static constexpr int kBytes = kBars + 256;
+  static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
+};
+
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                             volatile int* abort_flag, int where) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, parity)) return true;
+  record_error(err, kDevTimeout, where);
+  *abort_flag = 1;
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams P) {
+  using L = TcSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint64_t* empty = full + kSlots;
+  uint64_t* s_full = empty + kSlots;    // [2]
+  uint64_t* p_full = s_full + 2;        // [2]
+  uint64_t* o_done = p_full + 2;        // [2]
+  uint64_t* drain = o_done + 2;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work unit
+  int item = 0;
+  while (item + 1 < P.n_items && static_cast<int>(blockIdx.x) >= P.items[item + 1].unit_start)
+    ++item;
+  const TcItem& it = P.items[item];
+  int u = blockIdx.x - it.unit_start;
+  const int split = u % it.splits;
+  u /= it.splits;
+  const int tp = u % it.tile_pairs;
+  const int kvh = u / it.tile_pairs;
+  const int g = P.g;
+  const int M = it.m * g;
+  const int n_tiles = (M - 256 * tp) > 128 ? 2 : 1;
+  const int split_start = split * P.span_chunks * kChunk;
+  const int split_end = min(it.prefix_len, split_start + P.span_chunks * kChunk);
+  const int n_pref = split_end > split_start ? (split_end - split_start + kChunk - 1) / kChunk : 0;
+  const bool last_split = split == it.splits - 1;
+  const int n_chunks = n_pref + (last_split ? (it.m + kChunk - 1) / kChunk : 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&P.kmap[item]);
+    tma_prefetch_map(&P.vmap[item]);
+    tma_prefetch_map(&P.tkmap[item]);
+    tma_prefetch_map(&P.tvmap[item]);
+  }
+
+  // ---- Q tiles -> shared memory (128-byte swizzle), mask rows -> registers
+  const int wg = warp >= 4 ? (warp - 4) >> 2 : -1;   // softmax warpgroup = query tile
+  const int row = (warp & 3) * 32 + lane;            // row within the tile = TMEM lane
+  const int R = 256 * tp + 128 * (wg < 0 ? 0 : wg) + row;
+  uint64_t mrow[4] = {~0ull, ~0ull, ~0ull, ~0ull};
+  if (wg >= 0) {
+    uint8_t* qt = smem + L::kQ + wg * L::kTileBytes;
+    const bool valid = R < M;
+    const int qi = valid ? R / g : 0;
+    const int hl = valid ? R - qi * g : 0;
+    const int4* src = reinterpret_cast<const int4*>(
+        it.q + (static_cast<int64_t>(qi) * P.hq + kvh * g + hl) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {   // 16-byte chunks of the row
+      const int4 v = valid ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+      const int half = c >> 3, cc = c & 7;
+      *reinterpret_cast<int4*>(qt + half * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+    }
+    if (valid) {
+      const int W = (it.m + 63) >> 6;
+      for (int w = 0; w < W; ++w) mrow[w] = __ldg(it.mask + static_cast<int64_t>(qi) * W + w);
+      for (int w = W; w < 4; ++w) mrow[w] = 0ull;
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_S = tmem;               // S_t at column 128 t
+  const uint32_t tmem_O = tmem + 256;         // O_t at column 256 + D t
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      constexpr uint32_t kBytesChunk = static_cast<uint32_t>(L::kTileBytes);
+      int issued = 0;
+      for (int n = 0; n < 2 * n_chunks; ++n) {
+        const int slot = n % kSlots, use = n / kSlots;
+        if (use > 0 && !bounded_wait(&empty[slot], (use - 1) & 1, P.err, abort_flag, 20)) break;
+        const int j = n >> 1;
+        const bool is_v = n & 1;
+        uint8_t* dst = smem + L::kRing + slot * L::kTileBytes;
+        mbar_arrive_expect_tx(&full[slot], kBytesChunk);
+        if (j < n_pref) {
+          const CUtensorMap* map = is_v ? &P.vmap[item] : &P.kmap[item];
+          const int y = split_start + j * kChunk;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * 128 * 128, map, 64 * h, y, kvh, &full[slot]);
+        } else {
+          const CUtensorMap* map = is_v ? &P.tvmap[item] : &P.tkmap[item];
+          const int z = (j - n_pref) * kChunk;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * 128 * 128, map, 64 * h, kvh, z, &full[slot]);
+        }
+        issued = n + 1;
+      }
+      // make sure no copy of ours is still landing when the CTA leaves
+      for (int n = (issued > kSlots ? issued - kSlots : 0); n < issued; ++n)
+        mbar_wait(&full[n % kSlots], (n / kSlots) & 1, 200000000ull);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kChunk, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      const uint32_t q_base = smem_addr(smem + L::kQ);
+      const uint32_t p_base = smem_addr(smem + L::kP);
+      const uint32_t ring_base = smem_addr(smem + L::kRing);
+      auto issue_s = [&](int t, int slot) {   // S_t = Q_t K^T
+        const uint32_t qa = q_base + t * L::kTileBytes;
+        const uint32_t kb = ring_base + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          mma_bf16(tmem_S + 128 * t, smem_desc_sw128(qa + off, 16, 1024),
+                   smem_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {   // O_t += P_t V
+        const uint32_t pa = p_base + t * L::kPBytes;
+        const uint32_t vb = ring_base + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          const uint32_t boff = kk * 2048;   // 16 keys = two 8-row groups
+          mma_bf16(tmem_O + D * t, smem_desc_sw128(pa + aoff, 16, 1024),
+                   smem_desc_sw128(vb + boff, 128 * 128, 1024), idesc_o, (acc || kk > 0));
+        }
+      };
+      bool ok = n_chunks > 0 && bounded_wait(&full[0], 0, P.err, abort_flag, 30);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < n_tiles; ++t) {
+          issue_s(t, 0);
+          mma_commit(&s_full[t]);
+        }
+        mma_commit(&empty[0]);
+      }
+      int fseq = 0;   // P fills consumed so far (per tile; every tile has the same schedule)
+      for (int j = 0; ok && j < n_chunks; ++j) {
+        const int nv = 2 * j + 1, nk = 2 * j + 2;
+        const int vslot = nv % kSlots, kslot = nk % kSlots;
+        const int nf = j < n_pref ? 1 : 2;   // tree keys: P = hi + lo
+        if (!bounded_wait(&full[vslot], (nv / kSlots) & 1, P.err, abort_flag, 31)) break;
+        tc_fence_after();
+        const bool more = j + 1 < n_chunks;
+        for (int t = 0; t < n_tiles && ok; ++t) {
+          for (int f = 0; f < nf; ++f) {
+            if (!bounded_wait(&p_full[t], (fseq + f) & 1, P.err, abort_flag, 32)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(t, vslot, j > 0 || f > 0);
+            mma_commit(&o_done[t]);
+          }
+          if (!ok) break;
+          if (more) {
+            if (t == 0) {
+              if (!bounded_wait(&full[kslot], (nk / kSlots) & 1, P.err, abort_flag, 33)) { ok = false; break; }
+              tc_fence_after();
+            }
+            issue_s(t, kslot);
+            mma_commit(&s_full[t]);
+          }
+        }
+        if (!ok) break;
+        fseq += nf;
+        if (more) mma_commit(&empty[kslot]);
+        mma_commit(&empty[vslot]);
+      }
+      // every MMA of this CTA has completed once `drain` flips
+      mma_commit(drain);
+      mbar_wait(drain, 0, 200000000ull);
+    }
+  } else if (wg >= 0 && wg < n_tiles) {
+    // ================================================================ softmax
+    const int t = wg;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem_S + 128 * t + lane_off;
+    const uint32_t o_addr = tmem_O + D * t + lane_off;
+    uint8_t* pt = smem + L::kP + t * L::kPBytes;
+    const float sl2 = P.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    int fseq = 0;   // P fills produced so far
+    for (int j = 0; j < n_chunks; ++j) {
+      if (!bounded_wait(&s_full[t], j & 1, P.err, abort_flag, 40)) { ok = false; break; }
+      tc_fence_after();
+      // key validity for this chunk: prefix bound, or the ancestor mask words
+      const bool pref = j < n_pref;
+      const int nvalid = pref ? min(kChunk, split_end - (split_start + j * kChunk)) : 0;
+      const int t0 = pref ? 0 : (j - n_pref) * kChunk;
+      const uint64_t wlo = t0 == 0 ? mrow[0] : mrow[2];
+      const uint64_t whi = t0 == 0 ? mrow[1] : mrow[3];
+      auto scaled = [&](float v, int c) {   // c is a compile-time column index
+        bool vis;
+        if (pref) vis = c < nvalid;
+        else vis = (t0 + c < it.m) && (((c < 64 ? wlo : whi) >> (c & 63)) & 1ull);
+        return vis ? v * sl2 : -INFINITY;
+      };
+      // pass 1: row max over the chunk
+      float mx = -INFINITY;
+#pragma unroll
+      for (int cb = 0; cb < kChunk / 32; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(s_addr + 32 * cb, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, scaled(__uint_as_float(r[e]), 32 * cb + e));
+      }
+      // previous PV of this tile must be done before P is overwritten / O rescaled
+      if (fseq > 0 && !bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 41)) { ok = false; break; }
+      tc_fence_after();
+      const float m_new = fmaxf(m_run, mx);
+      const bool grow = (j == 0) || (m_new > m_run + 8.0f);
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        const float f = grow ? exp2f(m_run - m_new) : 1.0f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + 32 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+          tmem_st32(o_addr + 32 * c, r);
+        }
+        tmem_wait_st();
+        if (grow) l_run *= f;
+      }
+      if (grow) m_run = m_new;
+      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+      // pass 2: P = 2^(s - m) in bf16 -> shared memory (K-major, 128-byte swizzle).
+      // Tree keys (few, possibly dominant) get a second pass with the bf16
+      // rounding residual, so that O accumulates hi + lo ~ P to 2^-17.
+      const int nf = pref ? 1 : 2;
+#pragma unroll 1
+      for (int f = 0; f < nf; ++f) {
+        if (f == 1) {
+          if (!bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 43)) { ok = false; break; }
+          tc_fence_after();
+        }
+        float lsum = 0.f;
+#pragma unroll 1
+        for (int cb = 0; cb < kChunk / 32; ++cb) {
+          uint32_t r[32];
+          tmem_ld32(s_addr + 32 * cb, r);
+          tmem_wait_ld();
+          const int h = cb >> 1;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {   // four 16-byte chunks of 8 keys
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 32 * cb + 8 * q + 2 * e;
+              float p0 = exp2f(scaled(__uint_as_float(r[8 * q + 2 * e]), c) - mref);
+              float p1 = exp2f(scaled(__uint_as_float(r[8 * q + 2 * e + 1]), c + 1) - mref);
+              lsum += p0 + p1;
+              if (f == 1) {   // residual of the bf16 rounding
+                p0 -= __bfloat162float(__float2bfloat16_rn(p0));
+                p1 -= __bfloat162float(__float2bfloat16_rn(p1));
+              }
+              w[e] = pack_bf16x2(p0, p1);
+            }
+            const int cc = ((32 * cb) & 63) / 8 + q;   // chunk index within the 128-byte row
+            *reinterpret_cast<uint4*>(pt + h * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        if (f == 0) l_run += lsum;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+        ++fseq;
+      }
+      if (!ok) break;
+    }
+    // ---- epilogue
+    if (ok && fseq > 0 && bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 42)) {
+      tc_fence_after();
+      const bool valid = R < M;
+      const int qi = valid ? R / g : 0, hl = valid ? R - qi * g : 0;
+      const int64_t orow = static_cast<int64_t>(qi) * P.hq + kvh * g + hl;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      float* part = P.partials + it.part_start + (orow * it.splits + split) * (D + 2);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(o_addr + 32 * c, r);
+        tmem_wait_ld();
+        if (!valid) continue;
+        if (it.splits == 1) {
+          float4* dst = reinterpret_cast<float4*>(it.out + orow * D + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                 __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) part[32 * c + e] = __uint_as_float(r[e]);
+        }
+      }
+      if (valid && it.splits > 1) {
+        part[D] = m_run;
+        part[D + 1] = l_run;
+      }
+    }
+  }
+
+  // ---- teardown: tensor memory is freed by the warp that allocated it
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map with a (64 x rows_box x 1) box, 128-byte swizzle.
+static bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1,
+                      uint32_t box2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1 ? d1 : 1, d2 ? d2 : 1};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_supported(int head_dim) { return head_dim == 64 || head_dim == 128; }
+
+struct TcPlan {
+  int span;
+  int splits[kTcMaxItems];
+  int tile_pairs[kTcMaxItems];
+  int units;
+  int64_t part_floats;
+};
+
+// Choose the KV span (chunks per CTA) that minimises waves x (span + 2),
+// the +2 standing for the per-CTA fixed work (Q tiles, tree chunk, epilogue).
+static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int d) {
+  TcPlan T;
+  memset(&T, 0, sizeof(T));
+  const int g = hq / hkv;
+  int max_nc = 1;
+  for (int b = 0; b < n; ++b) {
+    T.tile_pairs[b] = (items[b].m * g + 255) / 256;
+    max_nc = std::max(max_nc, (items[b].prefix_len + kChunk - 1) / kChunk);
+  }
+  int64_t best_cost = -1;
+  for (int span = 1; span <= max_nc; ++span) {
+    int64_t total = 0;
+    for (int b = 0; b < n; ++b) {
+      const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
+      total += static_cast<int64_t>(hkv) * T.tile_pairs[b] * std::max(1, (nc + span - 1) / span);
+    }
+    const int64_t waves = (total + kPlanSMs - 1) / kPlanSMs;
+    const int64_t cost = waves * (span + 2);
+    if (best_cost < 0 || cost <= best_cost) {
+      best_cost = cost;
+      T.span = span;
+    }
+  }
+  int64_t units = 0, part = 0;
+  for (int b = 0; b < n; ++b) {
+    const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
+    T.splits[b] = std::max(1, (nc + T.span - 1) / T.span);
+    units += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
+    if (T.splits[b] > 1) part += static_cast<int64_t>(items[b].m) * hq * T.splits[b] * (d + 2);
+  }
+  T.units = static_cast<int>(units);
+  T.part_floats = part;
+  return T;
+}
+
+int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d) {
+  int count = 0;
+  for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
+    const int nb = std::min(kTcMaxItems, n - b0);
+    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d);
+    count += 1 + (T.part_floats > 0 ? 1 : 0);
+  }
+  return count;
+}
+
+size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int d, int) {
+  size_t need = kWsHeader;
+  for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
+    const int nb = std::min(kTcMaxItems, n - b0);
+    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d);
+    need = std::max(need, align_up(kWsHeader + sizeof(float) * static_cast<size_t>(T.part_floats), 256));
+  }
+  return need;
+}
+
+template <int D>
+static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hkv, float scale,
+                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+  static_assert(sizeof(TcParams) < 32000, "kernel parameter block too large");
+  for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
+    const int nb = std::min(kTcMaxItems, n - b0);
+    const eagle_attn_item* its = items + b0;
+    const TcPlan T = plan_tc(its, nb, hq, hkv, D);
+    if (ws_bytes < align_up(kWsHeader + sizeof(float) * static_cast<size_t>(T.part_floats), 256))
+      return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+    TcParams P;
+    memset(&P, 0, sizeof(P));
+    AttnPlan M;   // plan of the merge kernel (same partial layout as the CUDA-core path)
+    memset(&M, 0, sizeof(M));
+    int64_t units = 0, part = 0, rows = 0;
+    for (int b = 0; b < nb; ++b) {
+      const eagle_attn_item& x = its[b];
+      const uint64_t S = static_cast<uint64_t>(x.prefix_len);
+      const void* kbase = x.prefix_len ? x.k_cache : x.tree_k;
+      const void* vbase = x.prefix_len ? x.v_cache : x.tree_v;
+      const uint64_t hs = static_cast<uint64_t>(x.cache_head_stride) * 2;
+      if (!encode_3d(&P.kmap[b], kbase, D, S, hkv, D * 2, x.prefix_len ? hs : D * 2, kChunk, 1) ||
+          !encode_3d(&P.vmap[b], vbase, D, S, hkv, D * 2, x.prefix_len ? hs : D * 2, kChunk, 1) ||
+          !encode_3d(&P.tkmap[b], x.tree_k, D, hkv, x.m, D * 2, static_cast<uint64_t>(hkv) * D * 2, 1, kChunk) ||
+          !encode_3d(&P.tvmap[b], x.tree_v, D, hkv, x.m, D * 2, static_cast<uint64_t>(hkv) * D * 2, 1, kChunk))
+        return EAGLE_ERR_CUDA;
+      TcItem& ti = P.items[b];
+      ti.q = static_cast<const __nv_bfloat16*>(x.q);
+      ti.out = x.out;
+      ti.mask = x.mask;
+      ti.m = x.m;
+      ti.prefix_len = x.prefix_len;
+      ti.splits = T.splits[b];
+      ti.tile_pairs = T.tile_pairs[b];
+      ti.unit_start = static_cast<int>(units);
+      ti.part_start = part;
+      units += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
+      // merge plan
+      M.items[b].out = x.out;
+      M.items[b].m = x.m;
+      M.splits[b] = T.splits[b];
+      M.row_start[b] = rows;
+      M.part_start[b] = part;
+      rows += static_cast<int64_t>(x.m) * hq;
+      if (T.splits[b] > 1) part += static_cast<int64_t>(x.m) * hq * T.splits[b] * (D + 2);
+    }
+    P.n_items = nb;
+    P.hq = hq;
+    P.hkv = hkv;
+    P.g = hq / hkv;
+    P.span_chunks = T.span;
+    P.total_units = static_cast<int>(units);
+    P.scale_log2 = (scale != 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D))) * 1.4426950408889634f;
+    P.err = static_cast<int32_t*>(ws);
+    P.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+    const size_t smem = TcSmem<D>::kAlloc;
+    EAGLE_CUDA(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem)));
+    attn_tc_kernel<D><<<static_cast<unsigned>(units), kTcThreads, smem, stream>>>(P);
+    eagle_status st = launch_status();
+    if (st != EAGLE_OK) return st;
+    if (part > 0) {
+      M.n_items = nb;
+      M.n_q_heads = hq;
+      M.n_kv_heads = hkv;
+      M.head_dim = D;
+      M.row_start[nb] = rows;
+      M.part_floats = part;
+      M.err = P.err;
+      M.partials = P.partials;
+      if ((st = launch_attn_merge(M, stream)) != EAGLE_OK) return st;
+    }
+  }
+  return EAGLE_OK;
+}
+
+eagle_status attn_tc_launch(const eagle_attn_item* items, int n, int hq, int hkv, int d,
+                            float scale, void* ws, size_t ws_bytes, cudaStream_t stream, int) {
+  if (d == 128) return launch_d<128>(items, n, hq, hkv, scale, ws, ws_bytes, stream);
+  if (d == 64) return launch_d<64>(items, n, hq, hkv, scale, ws, ws_bytes, stream);
   return EAGLE_ERR_UNSUPPORTED_SHAPE;
 }
+
 }  // namespace eagle

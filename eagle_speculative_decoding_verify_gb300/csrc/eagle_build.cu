@@ -29,7 +29,7 @@ struct BuildArgs {
 __device__ __forceinline__ int cand_depth(int a, int k) { return a < k ? 1 : 2 + (a - k) / (k * k); }
 
 // Block-wide exclusive scan of per-thread counts (blockDim == kThreads).
-__device__ int block_excl_scan(int v, int* warp_tot, int& total) {
+static __device__ int block_excl_scan(int v, int* warp_tot, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
 #pragma unroll
@@ -49,7 +49,7 @@ __device__ int block_excl_scan(int v, int* warp_tot, int& total) {
   return off + incl - v;
 }
 
-__device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
+static __device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = A.top_k, D = A.depth, m = A.total_tokens, C = A.n_cand;
   const int R = 1 + (D - 1) * k;
@@ -86,7 +86,7 @@ __device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
 
   for (int r = tid; r < R; r += kThreads) {
     const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rows + r * rb);
-    lse[r] = static_cast<double>(h->max) + log(h->sum);
+    lse[r] = static_cast<double>(h->max) + log_d(h->sum);
   }
   __syncthreads();
   auto row_logit = [&](int r, int c) { return __ldcg(rec_val(rows + r * rb) + c); };
@@ -116,16 +116,19 @@ __device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
     __syncthreads();
     level_base = child_base;
     if (l + 1 < D) {
-      // frontier of depth l+1: best k of the k sorted child lists
+      // frontier of depth l+1: best k of the k sorted child lists, compared on
+      // order-preserving integer keys (ties -> lower candidate index)
+      for (int e = tid; e < k * k; e += kThreads) key[level_base + e] = order_key(val[level_base + e]);
+      __syncthreads();
       for (int e = tid; e < k * k; e += kThreads) {
         const int s = e / k, c = e - s * k;
-        const double v = val[level_base + e];
+        const uint64_t v = key[level_base + e];
         int rank = c;
         for (int s2 = 0; s2 < k && rank < k; ++s2) {
           if (s2 == s) continue;
-          const double* lst = val + level_base + s2 * k;
+          const uint64_t* lst = key + level_base + s2 * k;
           int lo = 0, hi = k;
-          if (s2 < s) {  // lower indices: entries with value >= v come first
+          if (s2 < s) {  // lower indices: entries with key >= v come first
             while (lo < hi) {
               const int mid = (lo + hi) >> 1;
               if (lst[mid] >= v) lo = mid + 1; else hi = mid;
@@ -152,8 +155,39 @@ __device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
   int rem = need;
   bool all_in = (need >= C);
   if (need > 0 && !all_in) {
-    for (int a = tid; a < C; a += kThreads) key[a] = order_key(val[a]);
-    for (int shift = 56; shift >= 0; shift -= 8) {
+    // skip the leading key bytes that every candidate shares
+    uint64_t kand = ~0ull, kor = 0ull;
+    for (int a = tid; a < C; a += kThreads) {
+      const uint64_t kv = order_key(val[a]);
+      key[a] = kv;
+      kand &= kv;
+      kor |= kv;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      kand &= __shfl_xor_sync(0xffffffffu, kand, o);
+      kor |= __shfl_xor_sync(0xffffffffu, kor, o);
+    }
+    uint64_t* red = reinterpret_cast<uint64_t*>(hist);   // 2 x kWarps words
+    if (lane == 0) {
+      red[warp] = kand;
+      red[kWarps + warp] = kor;
+    }
+    __syncthreads();
+    kand = ~0ull;
+    kor = 0ull;
+    for (int w = 0; w < kWarps; ++w) {
+      kand &= red[w];
+      kor |= red[kWarps + w];
+    }
+    __syncthreads();
+    const uint64_t diff = kand ^ kor;
+    int start = -8;                      // all keys equal: only the index decides
+    if (diff) start = ((63 - __clzll(static_cast<long long>(diff))) / 8) * 8;
+    pmask = (start + 8 >= 64) ? 0ull : ~((1ull << (start + 8)) - 1ull);
+    prefix = kand & pmask;
+    if (start < 0) pmask = ~0ull, prefix = kand;
+    for (int shift = start; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
       __syncthreads();
       for (int a = tid; a < C; a += kThreads)

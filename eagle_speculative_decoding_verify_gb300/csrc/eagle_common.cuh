@@ -117,6 +117,26 @@ __device__ __forceinline__ uint64_t order_key(double x) {
   return (u >> 63) ? ~u : (u | (1ull << 63));
 }
 
+// ------------------------------------------- exp / log to ~1e-7 relative
+// The fp64 special functions are very slow on this part; these reduce the
+// argument in fp64 and evaluate the remaining small range with the fp32
+// library function.
+//   exp(d) = 2^n * exp(r),  n = round(d / ln 2),  r = d - n ln 2 in [-0.35, 0.35]
+//   log(s) = e ln 2 + log(f_hi) + (f - f_hi) / f_hi,  s = f 2^e, f in [0.5, 1)
+__device__ __forceinline__ double exp_d(double d) {
+  if (d < -745.0) return 0.0;
+  const double n = rint(d * 1.4426950408889634);
+  const double r = fma(-n, 0.6931471805599453, d);   // ln 2 to double precision
+  return ldexp(static_cast<double>(expf(static_cast<float>(r))), static_cast<int>(n));
+}
+__device__ __forceinline__ double log_d(double s) {
+  int e;
+  const double f = frexp(s, &e);
+  const float fh = static_cast<float>(f);
+  return e * 0.6931471805599453 + static_cast<double>(logf(fh)) +
+         (f - static_cast<double>(fh)) / static_cast<double>(fh);
+}
+
 // --------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -1,16 +1,22 @@
 // One HBM pass over rows of fp32 logits, shared by the tree build (draft
 // rows) and the verify walk (target rows).
 //
-// Work split: the rows of all items are cut into 1024-element tiles; the
+// Work split: the rows of all items are cut into 1024-element tiles and the
 // grid (a whole number of CTAs per SM) takes equal contiguous tile ranges.
-// A CTA streams its range through a two-deep shared-memory ring filled by
-// 1-D bulk (TMA) copies and computes, per row segment it owns:
-//   * max and sum of exp((x - max) * scale) (fp32 exps, fp64 combine),
-//   * the exact top-K (value desc, token id asc), K <= 64, by filtering
-//     against a lower bound of the K-th value (the K-th best of a sample of
-//     per-lane maxima, then the running list) and ranking the few survivors,
-//   * optionally (max, sum) per 1024-token tile for inverse-CDF sampling.
-// Each segment is written as a "piece" record.  The CTA whose piece arrives
+// A CTA streams its range through a two-slot shared-memory ring filled by
+// 1-D bulk (TMA) copies; a slot is released through an mbarrier that every
+// thread arrives on once it holds its 32 elements in registers, so no CTA
+// barrier is taken per slot.  Per row segment the CTA computes:
+//   * max and sum of 2^((x - max) * c) per thread (fp32 ex2), combined per
+//     segment with fp32 factors and fp64 accumulation,
+//   * the exact top-K (value desc, token id asc), K <= 64: each warp takes
+//     as survivor threshold the K-th best of the top-2 of every lane in the
+//     segment's first slot (a lower bound of the K-th value of the segment),
+//     keeps elements >= threshold in a warp-private buffer (compacted to its
+//     best K when full, which raises the threshold) and the CTA ranks the
+//     survivors once at the end of the segment,
+//   * optionally per-tile (max, sum) of every warp for inverse-CDF sampling.
+// Each segment is written as a piece record.  The CTA whose piece arrives
 // last for a row merges the row's pieces into a row record; the CTA whose
 // row arrives last for an item runs the item's final step (tree assembly or
 // acceptance walk).  Arrival counters live in the workspace, start at zero
@@ -27,10 +33,11 @@ constexpr int kSub = kTile * kSubTiles;     // 8192 floats = 32 KB per slot
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVec = kSub / kThreads / 4;   // float4 per thread per slot (8)
-constexpr int kCandCap = 1024;              // survivor buffer (entries)
+constexpr int kWarpCap = 128;               // survivors per warp
 constexpr int kKMax = EAGLE_MAX_TOP_K;
 constexpr int kMaxItems = EAGLE_MAX_BATCH;
 constexpr int kMaxPieces = 16;              // CTAs sharing one row (host keeps it)
+constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { kWantSum = 1, kWantTileSums = 2 };
 
@@ -48,12 +55,13 @@ struct RowStream {
   uint32_t* item_cnt;            // [n_items]
   char* pieces;                  // [rows][max_pieces] piece records
   char* rows;                    // [rows] row records
-  float2* tile_sums;             // [rows][tiles_per_row] or null
+  float2* tile_sums;             // [rows][tiles_per_row][kWarps] or null
 };
 
 // Piece record (one row segment of one CTA) and row record share a layout:
 //   double sum; float max; int count; float val[rec_k]; int idx[rec_k]
-// For row records of the draft rows `sum` holds the logsumexp instead.
+// `sum` is sum_x 2^((x - max) * c) with c = exp_scale * log2(e), i.e. the sum
+// of exp((x - max) * exp_scale).
 __host__ __device__ constexpr int rec_bytes(int rec_k) {
   return static_cast<int>(align_up(16 + 8 * static_cast<size_t>(rec_k), 16));
 }
@@ -69,26 +77,31 @@ __device__ __forceinline__ int* rec_idx(char* rec, int rec_k) {
 
 struct StreamSmem {
   float buf[2][kSub];                 // ring (also reused by the item final step)
-  float cand_v[kCandCap];
-  int cand_i[kCandCap];
+  float wv[kWarps][kWarpCap];         // warp survivor buffers
+  int wi[kWarps][kWarpCap];
+  float mv[kMaxPieces * kKMax];       // merge staging (piece lists / all survivors)
+  int mi[kMaxPieces * kKMax];
   float list_v[kKMax];
   int list_i[kKMax];
-  float tmp_v[kKMax];
-  int tmp_i[kKMax];
-  float red_f[kWarps][kSubTiles];
-  float red_g[kWarps][kSubTiles];
+  float red_f[kWarps];
   double red_d[kWarps];
-  int red_i[kWarps];
-  uint64_t bar[2];
-  int cand_n;
-  int list_n;
-  int overflow;
+  int wcnt[kWarps];
+  uint64_t full[2];
+  uint64_t empty[2];
   int is_last;
-  float thr_v;
-  int thr_i;
   int n_done_items;
   int done_items[kMaxItems];
+  int cnt[kMaxPieces];
+  float pmax[kMaxPieces];
+  double psum[kMaxPieces];
 };
+
+// 2^x on the special-function unit (approximate, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ int64_t tile_owner(int64_t t, int64_t T, int G) {
   return ((t + 1) * G - 1) / T;
@@ -102,7 +115,7 @@ __device__ __forceinline__ int64_t next_slot(int64_t t, int64_t t_end, int TR) {
   return e < t_end ? e : t_end;
 }
 
-// Issue the bulk copy of slot starting at tile t into ring buffer b.
+// Issue the bulk copy of the slot starting at tile t into ring buffer b.
 __device__ __forceinline__ void issue_slot(const RowStream& P, StreamSmem& S, int64_t t,
                                            int64_t t_end, int b) {
   const int64_t row = t / P.tiles_per_row;
@@ -115,11 +128,11 @@ __device__ __forceinline__ void issue_slot(const RowStream& P, StreamSmem& S, in
   const int item = static_cast<int>(row / P.rows_per_item);
   const int lrow = static_cast<int>(row - static_cast<int64_t>(item) * P.rows_per_item);
   const float* src = P.base[item] + lrow * P.row_stride + static_cast<int64_t>(tir) * kTile;
-  mbar_arrive_expect_tx(&S.bar[b], bytes);
-  if (bytes) bulk_copy_g2s(S.buf[b], src, bytes, &S.bar[b]);
+  mbar_arrive_expect_tx(&S.full[b], bytes);
+  if (bytes) bulk_copy_g2s(S.buf[b], src, bytes, &S.full[b]);
 }
 
-// best k of n (v, i) entries (all distinct i), sorted into out; all threads.
+// best k of n (v, i) entries (distinct i) from smem, sorted into out; all threads.
 __device__ __forceinline__ void rank_select(const float* v, const int* id, int n, int k,
                                             float* out_v, int* out_i) {
   for (int a = threadIdx.x; a < n; a += blockDim.x) {
@@ -132,6 +145,66 @@ __device__ __forceinline__ void rank_select(const float* v, const int* id, int n
       out_i[rank] = ia;
     }
   }
+}
+
+// Warp bitonic sort of 64 (v, i) pairs held two per lane (position p = lane
+// + 32 r) into (value desc, index asc) order: position 0 holds the best.
+__device__ __forceinline__ void warp_sort64(float (&v)[2], int (&id)[2]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == 32) {  // partner is the other register of the same lane (k == 64)
+        if (before(v[1], id[1], v[0], id[0])) {
+          const float tv = v[0]; v[0] = v[1]; v[1] = tv;
+          const int ti = id[0]; id[0] = id[1]; id[1] = ti;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int p = lane + 32 * r;
+          const float ov = __shfl_xor_sync(0xffffffffu, v[r], j);
+          const int oi = __shfl_xor_sync(0xffffffffu, id[r], j);
+          const bool lower = (p & j) == 0;
+          const bool best_first = (p & k) == 0;   // direction of this block
+          const bool take = (lower == best_first) ? before(ov, oi, v[r], id[r])
+                                                  : before(v[r], id[r], ov, oi);
+          if (take) {
+            v[r] = ov;
+            id[r] = oi;
+          }
+        }
+      }
+    }
+  }
+}
+
+// Keep the best K of a warp's buffer of n entries (in place); returns the count.
+static __device__ int warp_compact(float* bv, int* bi, int n, int K) {
+  const int lane = threadIdx.x & 31;
+  float tv[kWarpCap / 32];
+  int ti[kWarpCap / 32];
+  int rk[kWarpCap / 32];
+#pragma unroll
+  for (int r = 0; r < kWarpCap / 32; ++r) {
+    const int a = lane + 32 * r;
+    tv[r] = a < n ? bv[a] : -INFINITY;
+    ti[r] = a < n ? bi[a] : 0x7fffffff;
+    int rank = 0;
+    if (a < n)
+      for (int b = 0; b < n; ++b) rank += before(bv[b], bi[b], tv[r], ti[r]) ? 1 : 0;
+    rk[r] = a < n ? rank : 0x7fffffff;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < kWarpCap / 32; ++r)
+    if (rk[r] < K) {
+      bv[rk[r]] = tv[r];
+      bi[rk[r]] = ti[r];
+    }
+  __syncwarp();
+  return n < K ? n : K;
 }
 
 // ------------------------------------------------------------ row finalize
@@ -147,42 +220,35 @@ static __device__ void finalize_row(const RowStream& P, StreamSmem& S, int64_t r
   const int np = static_cast<int>(tile_owner(row * TR + TR - 1, T, P.grid) - p0 + 1);
   const int rb = rec_bytes(P.rec_k);
   char* prow = P.pieces + (row * P.max_pieces) * rb;
-  // stage piece lists in the survivor buffer: piece p at offset p * K
-  float* pv = S.cand_v;
-  int* pi = S.cand_i;
-  __shared__ int cnt[kMaxPieces];
-  __shared__ float pmax[kMaxPieces];
-  __shared__ double psum[kMaxPieces];
   for (int p = threadIdx.x; p < np; p += blockDim.x) {
-    char* rec = prow + p * rb;
-    const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rec);
-    cnt[p] = h->count;
-    pmax[p] = h->max;
-    psum[p] = h->sum;
+    const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(prow + p * rb);
+    S.cnt[p] = h->count;
+    S.pmax[p] = h->max;
+    S.psum[p] = h->sum;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < np * K; e += blockDim.x) {
     const int p = e / K, c = e - p * K;
     char* rec = prow + p * rb;
-    if (c < cnt[p]) {
-      pv[e] = __ldcg(rec_val(rec) + c);
-      pi[e] = __ldcg(rec_idx(rec, P.rec_k) + c);
+    if (c < S.cnt[p]) {
+      S.mv[e] = __ldcg(rec_val(rec) + c);
+      S.mi[e] = __ldcg(rec_idx(rec, P.rec_k) + c);
     }
   }
   __syncthreads();
   char* out = P.rows + row * rb;
   for (int e = threadIdx.x; e < np * K; e += blockDim.x) {
     const int p = e / K, c = e - p * K;
-    if (c >= cnt[p]) continue;
-    const float v = pv[e];
-    const int id = pi[e];
+    if (c >= S.cnt[p]) continue;
+    const float v = S.mv[e];
+    const int id = S.mi[e];
     int rank = c;
     for (int q = 0; q < np; ++q) {
       if (q == p) continue;
-      int lo = 0, hi = cnt[q];          // count entries of piece q before (v, id)
+      int lo = 0, hi = S.cnt[q];   // entries of piece q before (v, id)
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (before(pv[q * K + mid], pi[q * K + mid], v, id)) lo = mid + 1; else hi = mid;
+        if (before(S.mv[q * K + mid], S.mi[q * K + mid], v, id)) lo = mid + 1; else hi = mid;
       }
       rank += lo;
     }
@@ -191,22 +257,27 @@ static __device__ void finalize_row(const RowStream& P, StreamSmem& S, int64_t r
       rec_idx(out, P.rec_k)[rank] = id;
     }
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    const float c2 = P.exp_scale[item] * kLog2e;
     float m = -INFINITY;
     int total = 0;
-    for (int p = 0; p < np; ++p) {
-      m = fmaxf(m, pmax[p]);
-      total += cnt[p];
+    for (int p = threadIdx.x; p < np; p += 32) {
+      m = fmaxf(m, S.pmax[p]);
+      total += S.cnt[p];
     }
+    m = warp_max(m);
+    total = warp_sum_i(total);
     double s = 0.0;
-    const double sc = static_cast<double>(P.exp_scale[item]);
-    for (int p = 0; p < np; ++p)
-      if (psum[p] > 0.0) s += psum[p] * exp((static_cast<double>(pmax[p]) - m) * sc);
-    RecHead h;
-    h.sum = s;
-    h.max = m;
-    h.count = total < K ? total : K;
-    *reinterpret_cast<RecHead*>(out) = h;
+    for (int p = threadIdx.x; p < np; p += 32)
+      if (S.psum[p] > 0.0) s += S.psum[p] * static_cast<double>(ex2((S.pmax[p] - m) * c2));
+    s = warp_sum_d(s);
+    if (threadIdx.x == 0) {
+      RecHead h;
+      h.sum = s;
+      h.max = m;
+      h.count = total < K ? total : K;
+      *reinterpret_cast<RecHead*>(out) = h;
+    }
   }
   __syncthreads();
 }
@@ -222,15 +293,17 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
   const int64_t t_end = static_cast<int64_t>(blockIdx.x + 1) * T / P.grid;
 
   if (tid == 0) {
-    mbar_init(&S.bar[0], 1);
-    mbar_init(&S.bar[1], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.full[b], 1);
+      mbar_init(&S.empty[b], kThreads);
+    }
     fence_barrier_init();
     S.n_done_items = 0;
-    S.list_n = 0;
   }
+  if (lane == 0) S.wcnt[warp] = 0;
   __syncthreads();
 
-  int64_t pf = t_begin;  // producer cursor (thread 0 only)
+  int64_t pf = t_begin;  // producer cursor (thread 0)
   if (tid == 0) {
     for (int b = 0; b < 2 && pf < t_end; ++b) {
       issue_slot(P, S, pf, t_end, b);
@@ -241,6 +314,7 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
   float m_run = -INFINITY, s_run = 0.f;       // per-thread running max / sum
   float best_v = -INFINITY;                    // per-thread argmax (K == 1)
   int best_i = 0x7fffffff;
+  float thr_v = INFINITY;                      // warp survivor threshold (K >= 2)
   int64_t cur = t_begin;
   for (int j = 0; cur < t_end; ++j) {
     const int b = j & 1;
@@ -253,11 +327,11 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
     const int item = static_cast<int>(row / P.rows_per_item);
     const int K = P.topk[item];
     const int flags = P.flags[item];
-    const float c2 = P.exp_scale[item] * 1.4426950408889634f;  // scale * log2(e)
+    const float c2 = P.exp_scale[item] * kLog2e;
 
-    if (!mbar_wait(&S.bar[b], (j >> 1) & 1)) {
+    if (!mbar_wait(&S.full[b], (j >> 1) & 1)) {
       record_error(P.err, kDevTimeout, 1);
-      mbar_wait(&S.bar[b], (j >> 1) & 1);  // give an in-flight copy a last chance to land
+      mbar_wait(&S.full[b], (j >> 1) & 1);  // give an in-flight copy a last chance to land
     }
     float x[kVec * 4];
     const int tok0 = tir * kTile;
@@ -281,8 +355,9 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
       x[4 * q + 2] = f.z;
       x[4 * q + 3] = f.w;
     }
-    __syncthreads();  // ring slot b fully read
-    if (tid == 0 && pf < t_end) {
+    mbar_arrive(&S.empty[b]);
+    if (tid == 0 && pf < t_end) {  // refill this slot once every thread has read it
+      if (!mbar_wait(&S.empty[b], (j >> 1) & 1)) record_error(P.err, kDevTimeout, 2);
       fence_proxy_async_smem();
       issue_slot(P, S, pf, t_end, b);
       pf = next_slot(pf, t_end, TR);
@@ -290,234 +365,131 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
 
     const bool seg_first = (cur == t_begin) || (tir == 0);
     const bool seg_last = (nxt == t_end) || (nxt % TR == 0);
-    auto valid = [&](int q, int c) { return (q * kThreads + tid) * 4 + c < nel; };
-    auto token = [&](int q, int c) { return tok0 + (q * kThreads + tid) * 4 + c; };
+    const int tbase = tok0 + tid * 4;   // token of element (q, c) = tbase + q * 1024 + c
 
-    // ---- max / sum of exp
+    float lm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kVec * 4; ++e) lm = fmaxf(lm, x[e]);
+
+    // ---- sum of exp (invalid elements are -inf and contribute 0)
     if (flags & kWantSum) {
-      float lm = -INFINITY;
+      const float mn = fmaxf(m_run, lm);
+      if (mn != -INFINITY) {
+        s_run *= ex2((m_run - mn) * c2);
+        const float off = mn * c2;
+        float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < kVec * 4; ++e) lm = fmaxf(lm, x[e]);
-      if (lm > m_run) {
-        s_run *= exp2f((m_run - lm) * c2);
-        m_run = lm;
+        for (int e = 0; e < kVec * 4; ++e) acc += ex2(fmaf(x[e], c2, -off));
+        s_run += acc;
+        m_run = mn;
       }
-      const float off = m_run * c2;
-#pragma unroll
-      for (int q = 0; q < kVec; ++q)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (valid(q, c)) s_run += exp2f(fmaf(x[4 * q + c], c2, -off));
     }
 
-    // ---- per-tile (max, sum) for inverse-CDF sampling
+    // ---- per-tile (max, sum) of this warp's 128 elements of every tile
     if (flags & kWantTileSums) {
+      const int ntl = static_cast<int>(nxt - cur);
 #pragma unroll
       for (int q = 0; q < kVec; ++q) {
-        float tm = -INFINITY, ts = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tm = fmaxf(tm, x[4 * q + c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (valid(q, c)) ts += exp2f((x[4 * q + c] - tm) * c2);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const float om = __shfl_xor_sync(0xffffffffu, tm, o);
-          const float os = __shfl_xor_sync(0xffffffffu, ts, o);
-          const float nm = fmaxf(tm, om);
-          ts = (nm == -INFINITY) ? 0.f
-                                 : ts * exp2f((tm - nm) * c2) + os * exp2f((om - nm) * c2);
-          tm = nm;
-        }
-        if (lane == 0) {
-          S.red_f[warp][q] = tm;
-          S.red_g[warp][q] = ts;
-        }
-      }
-      __syncthreads();
-      const int ntl = static_cast<int>(nxt - cur);
-      if (tid < ntl) {
-        float tm = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) tm = fmaxf(tm, S.red_f[w][tid]);
+        float tm = fmaxf(fmaxf(x[4 * q], x[4 * q + 1]), fmaxf(x[4 * q + 2], x[4 * q + 3]));
+        tm = warp_max(tm);
         float ts = 0.f;
-        for (int w = 0; w < kWarps; ++w)
-          if (S.red_g[w][tid] > 0.f) ts += S.red_g[w][tid] * exp2f((S.red_f[w][tid] - tm) * c2);
-        P.tile_sums[row * TR + tir + tid] = make_float2(tm, ts);
+        if (tm != -INFINITY) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ts += ex2((x[4 * q + c] - tm) * c2);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, o);
+        if (lane == 0 && q < ntl)
+          P.tile_sums[(row * TR + tir + q) * kWarps + warp] = make_float2(tm, ts);
       }
     }
 
-    // ---- argmax
+    // ---- argmax (each thread sees its tokens in increasing order)
     if (K == 1) {
 #pragma unroll
       for (int q = 0; q < kVec; ++q)
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          if (valid(q, c) && before(x[4 * q + c], token(q, c), best_v, best_i)) {
+          if (x[4 * q + c] > best_v) {
             best_v = x[4 * q + c];
-            best_i = token(q, c);
+            best_i = tbase + q * kTile + c;
           }
     }
 
-    // ---- exact top-K, K >= 2
+    // ---- top-K survivors, K >= 2
     if (K >= 2) {
       if (seg_first) {
-        // lower bound of the K-th value: K-th best of the per-warp top-qn
-        // lane maxima (distinct elements of this row)
-        float lv = -INFINITY;
-        int li = 0x7fffffff;
-#pragma unroll
-        for (int q = 0; q < kVec; ++q)
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (valid(q, c) && before(x[4 * q + c], token(q, c), lv, li)) {
-              lv = x[4 * q + c];
-              li = token(q, c);
-            }
-        const int qn = (K + kWarps - 1) / kWarps;
-        for (int r = 0; r < qn; ++r) {
-          float wv = lv;
-          int wi = li;
-          warp_best(wv, wi);
-          if (lane == 0) {
-            S.tmp_v[warp * qn + r] = wv;
-            S.tmp_i[warp * qn + r] = wi;
-          }
-          if (tid == 0 && r == 0) {
-            S.thr_v = -INFINITY;  // default: every valid element survives
-            S.thr_i = 0x7fffffff;
-          }
-          if (li == wi) {
-            lv = -INFINITY;
-            li = 0x7fffffff;
-          }
-        }
-        __syncthreads();
-        const int ns = qn * kWarps;
-        if (tid < ns) {
-          const float va = S.tmp_v[tid];
-          const int ia = S.tmp_i[tid];
-          int rank = 0;
-          for (int b2 = 0; b2 < ns; ++b2) rank += before(S.tmp_v[b2], S.tmp_i[b2], va, ia) ? 1 : 0;
-          if (rank == K - 1) {
-            S.thr_v = va;
-            S.thr_i = ia;
-          }
-        }
-        if (tid == 0) S.list_n = 0;
-        __syncthreads();
-      } else if (tid == 0) {
-        if (S.list_n >= K) {
-          S.thr_v = S.list_v[K - 1];
-          S.thr_i = S.list_i[K - 1];
-        } else {
-          S.thr_v = -INFINITY;
-          S.thr_i = 0x7fffffff;
-        }
-      }
-      for (int round = 0;; ++round) {
-        if (tid == 0) {
-          S.cand_n = 0;
-          S.overflow = 0;
-        }
-        __syncthreads();
-        const float tv = S.thr_v;
-        const int ti = S.thr_i;
-        int npass = 0;
+        // threshold: K-th best of the lanes' top-2 (distinct elements of the row)
+        float sv[2] = {-INFINITY, -INFINITY};
+        int si[2] = {0x7fffffff, 0x7fffffff};
 #pragma unroll
         for (int q = 0; q < kVec; ++q)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float xv = x[4 * q + c];
-            const int xi = token(q, c);
-            npass += (valid(q, c) && (before(xv, xi, tv, ti) || (xv == tv && xi == ti))) ? 1 : 0;
-          }
-        if (__any_sync(0xffffffffu, npass > 0)) {
-          int incl = npass;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          const int total = __shfl_sync(0xffffffffu, incl, 31);
-          int base = 0;
-          if (lane == 31) base = atomicAdd(&S.cand_n, total);
-          base = __shfl_sync(0xffffffffu, base, 31);
-          int pos = base + incl - npass;
-#pragma unroll
-          for (int q = 0; q < kVec; ++q)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const float xv = x[4 * q + c];
-              const int xi = token(q, c);
-              if (valid(q, c) && (before(xv, xi, tv, ti) || (xv == tv && xi == ti))) {
-                if (pos < kCandCap) {
-                  S.cand_v[pos] = xv;
-                  S.cand_i[pos] = xi;
-                } else {
-                  S.overflow = 1;
-                }
-                ++pos;
+            const int xi = tbase + q * kTile + c;
+            if (xv > sv[1]) {
+              if (xv > sv[0]) {
+                sv[1] = sv[0];
+                si[1] = si[0];
+                sv[0] = xv;
+                si[0] = xi;
+              } else {
+                sv[1] = xv;
+                si[1] = xi;
               }
             }
-        }
-        __syncthreads();
-        // merge running list + survivors -> best K
-        const int nc = S.cand_n < kCandCap ? S.cand_n : kCandCap;
-        const int nl = S.list_n;
-        // append list entries behind the survivors (room kept by the cap check)
-        for (int a = tid; a < nl; a += kThreads) {
-          if (nc + a < kCandCap) {
-            S.cand_v[nc + a] = S.list_v[a];
-            S.cand_i[nc + a] = S.list_i[a];
           }
-        }
-        __syncthreads();
-        const int ntot = (nc + nl) < kCandCap ? (nc + nl) : kCandCap;
-        const bool ovf = S.overflow || (nc + nl) > kCandCap;
-        rank_select(S.cand_v, S.cand_i, ntot, K, S.tmp_v, S.tmp_i);
-        __syncthreads();
-        const int kept = ntot < K ? ntot : K;
-        if (!ovf) {
-          for (int a = tid; a < kept; a += kThreads) {
-            S.list_v[a] = S.tmp_v[a];
-            S.list_i[a] = S.tmp_i[a];
+        warp_sort64(sv, si);
+        const int kk = K - 1;   // the K-th best sits at position K-1
+        thr_v = __shfl_sync(0xffffffffu, kk < 32 ? sv[0] : sv[1], kk & 31);
+        if (lane == 0) S.wcnt[warp] = 0;
+        __syncwarp();
+      }
+      if (__any_sync(0xffffffffu, lm >= thr_v)) {
+        float* bv = S.wv[warp];
+        int* bi = S.wi[warp];
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float xv = x[4 * q + c];
+            bool pass = xv >= thr_v && xv != -INFINITY;
+            unsigned bal = __ballot_sync(0xffffffffu, pass);
+            if (!bal) continue;
+            int n = S.wcnt[warp];
+            if (n + __popc(bal) > kWarpCap) {   // full: keep the best K, raise the bar
+              n = warp_compact(bv, bi, n, K);
+              if (n >= K) thr_v = fmaxf(thr_v, bv[K - 1]);
+              pass = xv >= thr_v && xv != -INFINITY;
+              bal = __ballot_sync(0xffffffffu, pass);
+            }
+            if (pass) {
+              const int pos = n + __popc(bal & ((1u << lane) - 1u));
+              bv[pos] = xv;
+              bi[pos] = tbase + q * kTile + c;
+            }
+            __syncwarp();
+            if (lane == 0) S.wcnt[warp] = n + __popc(bal);
+            __syncwarp();
           }
-          if (tid == 0) S.list_n = kept;
-          __syncthreads();
-          break;
-        }
-        // too many survivors: raise the bound to the K-th of what was seen and
-        // collect this slot again (the running list is unchanged)
-        if (tid == 0) {
-          S.thr_v = S.tmp_v[K - 1];
-          S.thr_i = S.tmp_i[K - 1];
-        }
-        __syncthreads();
-        if (round > 64) {
-          record_error(P.err, kDevAssert, 2);
-          break;
         }
       }
     }
 
-    // ---- end of a row segment: write this CTA's piece record
+    // ---- end of a row segment: piece record, arrival counters, finalize
     if (seg_last) {
       float M = -INFINITY;
       double Ssum = 0.0;
       if (flags & kWantSum) {
         const float wm = warp_max(m_run);
-        double sd = (s_run > 0.f) ? static_cast<double>(s_run) * exp2((static_cast<double>(m_run) - wm) * c2) : 0.0;
+        double sd = (s_run > 0.f)
+                        ? static_cast<double>(s_run) * static_cast<double>(ex2((m_run - wm) * c2))
+                        : 0.0;
         sd = warp_sum_d(sd);
         if (lane == 0) {
-          S.red_f[warp][0] = wm;
+          S.red_f[warp] = wm;
           S.red_d[warp] = sd;
-        }
-        __syncthreads();
-        if (tid == 0) {
-          for (int w = 0; w < kWarps; ++w) M = fmaxf(M, S.red_f[w][0]);
-          for (int w = 0; w < kWarps; ++w)
-            if (S.red_d[w] > 0.0)
-              Ssum += S.red_d[w] * exp2((static_cast<double>(S.red_f[w][0]) - M) * c2);
         }
       }
       if (K == 1) {
@@ -525,37 +497,68 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
         int i = best_i;
         warp_best(v, i);
         if (lane == 0) {
-          S.red_g[warp][0] = v;
-          S.red_i[warp] = i;
+          S.list_v[warp] = v;   // staged per warp
+          S.list_i[warp] = i;
         }
-        __syncthreads();
-        if (tid == 0) {
-          float bv = -INFINITY;
-          int bi = 0x7fffffff;
-          for (int w = 0; w < kWarps; ++w)
-            if (before(S.red_g[w][0], S.red_i[w], bv, bi)) {
-              bv = S.red_g[w][0];
-              bi = S.red_i[w];
-            }
-          S.list_v[0] = bv;
-          S.list_i[0] = bi;
-          S.list_n = 1;
-          if (!(flags & kWantSum)) M = bv;
-        }
-        __syncthreads();
       }
+      __syncthreads();
+      if (tid < 32) {
+        if (flags & kWantSum) {
+          const float fm = lane < kWarps ? S.red_f[lane] : -INFINITY;
+          M = warp_max(fm);
+          double d = 0.0;
+          if (lane < kWarps && S.red_d[lane] > 0.0)
+            d = S.red_d[lane] * static_cast<double>(ex2((S.red_f[lane] - M) * c2));
+          Ssum = warp_sum_d(d);
+        }
+        if (K == 1) {
+          float v = lane < kWarps ? S.list_v[lane] : -INFINITY;
+          int i = lane < kWarps ? S.list_i[lane] : 0x7fffffff;
+          warp_best(v, i);
+          if (!(flags & kWantSum)) M = v;
+          if (lane == 0) {
+            S.mv[0] = v;
+            S.mi[0] = i;
+          }
+        }
+      }
+      int nl = 0;
+      if (K >= 2) {
+        // gather every warp's survivors, rank them once
+        __syncthreads();
+        int off = 0;
+        for (int w = 0; w < kWarps; ++w) {
+          const int n = S.wcnt[w];
+          for (int a = tid; a < n; a += kThreads) {
+            S.mv[off + a] = S.wv[w][a];
+            S.mi[off + a] = S.wi[w][a];
+          }
+          off += n;
+        }
+        __syncthreads();
+        rank_select(S.mv, S.mi, off, K, S.list_v, S.list_i);
+        nl = off < K ? off : K;
+        __syncthreads();
+        for (int a = tid; a < nl; a += kThreads) {
+          S.mv[a] = S.list_v[a];
+          S.mi[a] = S.list_i[a];
+        }
+        if (!(flags & kWantSum) && tid == 0) M = S.list_v[0];
+      } else if (K == 1) {
+        nl = 1;
+      }
+      __syncthreads();
       const int64_t piece = static_cast<int64_t>(blockIdx.x) - tile_owner(row * TR, T, P.grid);
       const int rb = rec_bytes(P.rec_k);
       char* rec = P.pieces + (row * P.max_pieces + piece) * rb;
-      const int nl = (K >= 1) ? S.list_n : 0;
       for (int a = tid; a < nl; a += kThreads) {
-        rec_val(rec)[a] = S.list_v[a];
-        rec_idx(rec, P.rec_k)[a] = S.list_i[a];
+        rec_val(rec)[a] = S.mv[a];
+        rec_idx(rec, P.rec_k)[a] = S.mi[a];
       }
       if (tid == 0) {
         RecHead h;
         h.sum = Ssum;
-        h.max = (K >= 2 && !(flags & kWantSum)) ? S.list_v[0] : M;
+        h.max = M;
         h.count = nl;
         *reinterpret_cast<RecHead*>(rec) = h;
       }
@@ -564,6 +567,8 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
       s_run = 0.f;
       best_v = -INFINITY;
       best_i = 0x7fffffff;
+      thr_v = INFINITY;
+      if (lane == 0) S.wcnt[warp] = 0;
       __threadfence();
       __syncthreads();
       if (tid == 0) {
@@ -571,7 +576,6 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
                                         tile_owner(row * TR, T, P.grid) + 1);
         const uint32_t old = atomicAdd(&P.row_cnt[row], 1u);
         S.is_last = (old == static_cast<uint32_t>(np - 1));
-        S.list_n = 0;
       }
       __syncthreads();
       if (S.is_last) {
@@ -592,6 +596,7 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
     }
     cur = nxt;
   }
+  // every issued copy has been consumed above; the ring is free again
   __syncthreads();
   if (S.n_done_items) __threadfence();
 }

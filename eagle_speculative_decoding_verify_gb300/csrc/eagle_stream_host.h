@@ -36,7 +36,7 @@ inline StreamLayout stream_layout(int n_items, int rows_per_item, int vocab, int
   off += rb * static_cast<size_t>(L.n_rows);
   off = align_up(off, 256);
   L.off_tiles = off;
-  if (tile_sums) off += sizeof(float2) * static_cast<size_t>(L.total_tiles);
+  if (tile_sums) off += sizeof(float2) * kWarps * static_cast<size_t>(L.total_tiles);
   L.total = align_up(off, 256);
   return L;
 }

@@ -57,11 +57,11 @@ __device__ __forceinline__ double warp_incl_scan_d(double v) {
 // p(t) under the full-vocabulary target distribution (lane-local).
 __device__ __forceinline__ double full_prob(const float* lrow, int t, double rowmax, double T,
                                             double zsum) {
-  return exp((static_cast<double>(__ldg(lrow + t)) - rowmax) / T) / zsum;
+  return exp_d((static_cast<double>(__ldg(lrow + t)) - rowmax) / T) / zsum;
 }
 
 // The walk; executed by warp 0 of the CTA.
-__device__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
+static __device__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
   const int lane = threadIdx.x & 31;
   const int m = A.m;
   const int rk = A.rs.rec_k;
@@ -128,7 +128,7 @@ __device__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
         if (e < cnt) {
           z[hh] = static_cast<double>(__ldcg(rec_val(rec) + e)) / T;
           id[hh] = __ldcg(rec_idx(rec, rk) + e);
-          pr[hh] = exp(z[hh] - z0);
+          pr[hh] = exp_d(z[hh] - z0);
         } else {
           pr[hh] = 0.0;
           id[hh] = 0x7fffffff;
@@ -246,7 +246,7 @@ __device__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
       __syncwarp();
     } else {
       // tile masses (tile sums were taken relative to each tile's max)
-      const float2* ts = A.rs.tile_sums + (static_cast<int64_t>(item) * m + node) * TR;
+      const float2* ts = A.rs.tile_sums + (static_cast<int64_t>(item) * m + node) * TR * kWarps;
       const double c2 = static_cast<double>(A.rs.exp_scale[item]) * 1.4426950408889634;
       double cum = 0.0;
       int tile = -1;
@@ -255,8 +255,15 @@ __device__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
         const int t = base + lane;
         double mass = 0.0;
         if (t < TR) {
-          const float2 v = __ldcg(ts + t);
-          if (v.y > 0.f) mass = static_cast<double>(v.y) * exp2((static_cast<double>(v.x) - rowmax) * c2) / zsum;
+          // combine the per-warp partials of tile t (max, sum of 2^((x - max) c2))
+          const float2* tw = ts + static_cast<int64_t>(t) * kWarps;
+          for (int w = 0; w < kWarps; ++w) {
+            const float2 v = __ldcg(tw + w);
+            if (v.y > 0.f)
+              mass += static_cast<double>(v.y) *
+                      static_cast<double>(ex2((v.x - static_cast<float>(rowmax)) * static_cast<float>(c2)));
+          }
+          mass /= zsum;
           for (int r = 0; r < n_rej && r < EAGLE_MAX_TREE; ++r)
             if (rejected[r] / kTile == t) mass -= full_prob(lrow, rejected[r], rowmax, T, zsum);
           if (mass < 0.0) mass = 0.0;
