@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
       }
     } else {
       float* part = P.partials + P.part_start[item] +
-                    (row * splits + split) * static_cast<int64_t>(d + 2);
+                    (row * splits + split) * static_cast<int64_t>(part_stride(d));
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int e = r * 32 + lane;
@@ -136,20 +136,21 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__
   const int splits = P.splits[item];
   if (splits == 1) return;
   const int d = P.head_dim;
-  const float* part = P.partials + P.part_start[item] + row * splits * static_cast<int64_t>(d + 2);
+  const int ps = part_stride(d);
+  const float* part = P.partials + P.part_start[item] + row * splits * static_cast<int64_t>(ps);
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(part + s * (d + 2) + d));
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(part + s * ps + d));
   float L = 0.f;
   for (int s = 0; s < splits; ++s) {
-    const float ms = __ldcg(part + s * (d + 2) + d);
-    if (ms != -INFINITY) L += exp2f(ms - M) * __ldcg(part + s * (d + 2) + d + 1);
+    const float ms = __ldcg(part + s * ps + d);
+    if (ms != -INFINITY) L += exp2f(ms - M) * __ldcg(part + s * ps + d + 1);
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   for (int e = lane; e < d; e += 32) {
     float acc = 0.f;
     for (int s = 0; s < splits; ++s) {
-      const float ms = __ldcg(part + s * (d + 2) + d);
-      if (ms != -INFINITY) acc += exp2f(ms - M) * __ldcg(part + s * (d + 2) + e);
+      const float ms = __ldcg(part + s * ps + d);
+      if (ms != -INFINITY) acc += exp2f(ms - M) * __ldcg(part + s * ps + e);
     }
     it.out[row * d + e] = acc * inv;
   }
@@ -209,7 +210,7 @@ static void plan_simt(AttnPlan& P, const eagle_attn_item* items, int n, int hq, 
     P.part_start[b] = part;
     units += static_cast<int64_t>(hkv) * it.m * splits;
     rows += static_cast<int64_t>(it.m) * hq;
-    if (splits > 1) part += static_cast<int64_t>(it.m) * hq * splits * (d + 2);
+    if (splits > 1) part += static_cast<int64_t>(it.m) * hq * splits * part_stride(d);
     AttnItemDev& di = P.items[b];
     di.q = it.q;
     di.k_cache = it.k_cache;

@@ -14,6 +14,10 @@ constexpr int kAttnMaxItems = 32;  // items per launch (more are chunked)
 // call runs on, so workspace sizes do not depend on the device.
 constexpr int kPlanSMs = 152;
 
+// Floats per (row, split) partial: head_dim outputs, then max (log2 units)
+// and sum, padded to a 16-byte multiple.
+__host__ __device__ constexpr int part_stride(int head_dim) { return head_dim + 4; }
+
 struct AttnItemDev {
   const void* q;
   const void* k_cache;

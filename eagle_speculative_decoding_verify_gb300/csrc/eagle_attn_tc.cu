@@ -165,8 +165,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
     if (valid) {
       const int W = (it.m + 63) >> 6;
-      for (int w = 0; w < W; ++w) mrow[w] = __ldg(it.mask + static_cast<int64_t>(qi) * W + w);
-      for (int w = W; w < 4; ++w) mrow[w] = 0ull;
+      const uint64_t* mr = it.mask + static_cast<int64_t>(qi) * W;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) mrow[w] = w < W ? __ldg(mr + w) : 0ull;
     }
     fence_proxy_async_smem();
   }
@@ -292,36 +293,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     for (int j = 0; j < n_chunks; ++j) {
       if (!bounded_wait(&s_full[t], j & 1, P.err, abort_flag, 40)) { ok = false; break; }
       tc_fence_after();
-      // key validity for this chunk: prefix bound, or the ancestor mask words
+      // key validity: only the last prefix chunk of a split and the tree
+      // chunks need a mask
       const bool pref = j < n_pref;
       const int nvalid = pref ? min(kChunk, split_end - (split_start + j * kChunk)) : 0;
+      const bool masked = !pref || nvalid < kChunk;
       const int t0 = pref ? 0 : (j - n_pref) * kChunk;
       const uint64_t wlo = t0 == 0 ? mrow[0] : mrow[2];
       const uint64_t whi = t0 == 0 ? mrow[1] : mrow[3];
-      auto scaled = [&](float v, int c) {   // c is a compile-time column index
-        bool vis;
-        if (pref) vis = c < nvalid;
-        else vis = (t0 + c < it.m) && (((c < 64 ? wlo : whi) >> (c & 63)) & 1ull);
-        return vis ? v * sl2 : -INFINITY;
-      };
-      // pass 1: row max over the chunk
-      float mx = -INFINITY;
-#pragma unroll
-      for (int cb = 0; cb < kChunk / 32; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + 32 * cb, r);
+      const int nt = pref ? nvalid : it.m - t0;   // keys present in this chunk
+      // load 64 columns of S (two 32-column loads, one wait); mask if needed
+      auto load64 = [&](int half, float (&v)[64]) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(s_addr + 64 * half, ra);
+        tmem_ld32(s_addr + 64 * half + 32, rb);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, scaled(__uint_as_float(r[e]), 32 * cb + e));
+        for (int e = 0; e < 32; ++e) {
+          v[e] = __uint_as_float(ra[e]);
+          v[32 + e] = __uint_as_float(rb[e]);
+        }
+        if (masked) {
+          const uint64_t w = half ? whi : wlo;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int c = 64 * half + e;
+            const bool vis = c < nt && (pref || ((w >> e) & 1ull));
+            if (!vis) v[e] = -INFINITY;
+          }
+        }
+      };
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float v[64];
+        load64(half, v);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
       }
+      mx *= sl2;   // scale > 0: max of the scaled row
       // previous PV of this tile must be done before P is overwritten / O rescaled
       if (fseq > 0 && !bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 41)) { ok = false; break; }
       tc_fence_after();
       const float m_new = fmaxf(m_run, mx);
       const bool grow = (j == 0) || (m_new > m_run + 8.0f);
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        const float f = grow ? exp2f(m_run - m_new) : 1.0f;
-#pragma unroll
+        const float f = grow ? ex2(m_run - m_new) : 1.0f;
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(o_addr + 32 * c, r);
@@ -335,8 +353,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       }
       if (grow) m_run = m_new;
       const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = 2^(s - m) in bf16 -> shared memory (K-major, 128-byte swizzle).
-      // Tree keys (few, possibly dominant) get a second pass with the bf16
+      // P = 2^(s sl2 - m) in bf16 -> shared memory (K-major, 128-byte swizzle).
+      // Tree keys (few, possibly dominant) get a second fill with the bf16
       // rounding residual, so that O accumulates hi + lo ~ P to 2^-17.
       const int nf = pref ? 1 : 2;
 #pragma unroll 1
@@ -347,29 +365,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         float lsum = 0.f;
 #pragma unroll 1
-        for (int cb = 0; cb < kChunk / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld32(s_addr + 32 * cb, r);
-          tmem_wait_ld();
-          const int h = cb >> 1;
+        for (int half = 0; half < 2; ++half) {
+          float v[64];
+          load64(half, v);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {   // four 16-byte chunks of 8 keys
-            uint32_t w[4];
+          for (int e = 0; e < 64; ++e) {
+            float pv = ex2(fmaf(v[e], sl2, -mref));
+            lsum += pv;
+            if (f == 1) pv -= __bfloat162float(__float2bfloat16_rn(pv));
+            v[e] = pv;
+          }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 32 * cb + 8 * q + 2 * e;
-              float p0 = exp2f(scaled(__uint_as_float(r[8 * q + 2 * e]), c) - mref);
-              float p1 = exp2f(scaled(__uint_as_float(r[8 * q + 2 * e + 1]), c + 1) - mref);
-              lsum += p0 + p1;
-              if (f == 1) {   // residual of the bf16 rounding
-                p0 -= __bfloat162float(__float2bfloat16_rn(p0));
-                p1 -= __bfloat162float(__float2bfloat16_rn(p1));
-              }
-              w[e] = pack_bf16x2(p0, p1);
-            }
-            const int cc = ((32 * cb) & 63) / 8 + q;   // chunk index within the 128-byte row
-            *reinterpret_cast<uint4*>(pt + h * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+          for (int cc = 0; cc < 8; ++cc) {   // 16-byte chunks of 8 keys
+            const uint4 w = make_uint4(pack_bf16x2(v[8 * cc + 0], v[8 * cc + 1]),
+                                       pack_bf16x2(v[8 * cc + 2], v[8 * cc + 3]),
+                                       pack_bf16x2(v[8 * cc + 4], v[8 * cc + 5]),
+                                       pack_bf16x2(v[8 * cc + 6], v[8 * cc + 7]));
+            *reinterpret_cast<uint4*>(pt + half * (128 * 128) + row * 128 +
+                                      ((cc ^ (row & 7)) << 4)) = w;
           }
         }
         if (f == 0) l_run += lsum;
@@ -387,23 +400,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       const int qi = valid ? R / g : 0, hl = valid ? R - qi * g : 0;
       const int64_t orow = static_cast<int64_t>(qi) * P.hq + kvh * g + hl;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      float* part = P.partials + it.part_start + (orow * it.splits + split) * (D + 2);
+      float* part = P.partials + it.part_start + (orow * it.splits + split) * part_stride(D);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(o_addr + 32 * c, r);
         tmem_wait_ld();
         if (!valid) continue;
-        if (it.splits == 1) {
-          float4* dst = reinterpret_cast<float4*>(it.out + orow * D + 32 * c);
+        const float sc = it.splits == 1 ? inv : 1.0f;
+        float4* dst = reinterpret_cast<float4*>(it.splits == 1 ? it.out + orow * D + 32 * c
+                                                               : part + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                 __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) part[32 * c + e] = __uint_as_float(r[e]);
-        }
+        for (int e = 0; e < 8; ++e)
+          dst[e] = make_float4(__uint_as_float(r[4 * e]) * sc, __uint_as_float(r[4 * e + 1]) * sc,
+                               __uint_as_float(r[4 * e + 2]) * sc, __uint_as_float(r[4 * e + 3]) * sc);
       }
       if (valid && it.splits > 1) {
         part[D] = m_run;
@@ -489,7 +499,7 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
     const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
     T.splits[b] = std::max(1, (nc + T.span - 1) / T.span);
     units += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
-    if (T.splits[b] > 1) part += static_cast<int64_t>(items[b].m) * hq * T.splits[b] * (d + 2);
+    if (T.splits[b] > 1) part += static_cast<int64_t>(items[b].m) * hq * T.splits[b] * part_stride(d);
   }
   T.units = static_cast<int>(units);
   T.part_floats = part;
@@ -560,7 +570,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       M.row_start[b] = rows;
       M.part_start[b] = part;
       rows += static_cast<int64_t>(x.m) * hq;
-      if (T.splits[b] > 1) part += static_cast<int64_t>(x.m) * hq * T.splits[b] * (D + 2);
+      if (T.splits[b] > 1) part += static_cast<int64_t>(x.m) * hq * T.splits[b] * part_stride(D);
     }
     P.n_items = nb;
     P.hq = hq;

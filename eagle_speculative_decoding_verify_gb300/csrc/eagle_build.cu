@@ -58,39 +58,42 @@ static __device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S
   char* rows = A.rs.rows + static_cast<int64_t>(item) * A.rs.rows_per_item * rb;
   const eagle_tree out = A.out[item];
 
-  // scratch carved from the (now idle) ring buffers: <= 60 KB for C <= 2048
+  // scratch carved from the (now idle) stream state after S.done_items;
+  // every array starts on a 16-byte boundary (<= 78 KB for C <= 2048)
   char* p = reinterpret_cast<char*>(S.buf);
-  double* val = reinterpret_cast<double*>(p);
-  p += sizeof(double) * C;
-  uint64_t* key = reinterpret_cast<uint64_t*>(p);
-  p += sizeof(uint64_t) * C;
-  double* lse = reinterpret_cast<double*>(p);
-  p += sizeof(double) * R;
-  int* tok = reinterpret_cast<int*>(p);
-  p += sizeof(int) * C;
-  int* par = reinterpret_cast<int*>(p);
-  p += sizeof(int) * C;
-  int* node = reinterpret_cast<int*>(p);
-  p += sizeof(int) * C;
-  int* npar = reinterpret_cast<int*>(p);
-  p += sizeof(int) * EAGLE_MAX_TREE;
-  int* fr = reinterpret_cast<int*>(p);
-  p += sizeof(int) * kKMax;
-  int* fr_next = reinterpret_cast<int*>(p);
-  p += sizeof(int) * kKMax;
-  int* hist = reinterpret_cast<int*>(p);
-  p += sizeof(int) * 256;
-  int* misc = reinterpret_cast<int*>(p);  // [0] digit, [1] count above, [2] done flag
-  p += sizeof(int) * 8;
-  int* warp_tot = reinterpret_cast<int*>(p);
+  auto carve = [&p](size_t bytes) {
+    char* q = p;
+    p += align_up(bytes, 16);
+    return q;
+  };
+  double* val = reinterpret_cast<double*>(carve(sizeof(double) * C));
+  uint64_t* key = reinterpret_cast<uint64_t*>(carve(sizeof(uint64_t) * C));
+  double* lse = reinterpret_cast<double*>(carve(sizeof(double) * R));
+  float* rv = reinterpret_cast<float*>(carve(sizeof(float) * R * k));   // row top-k logits
+  int* ri = reinterpret_cast<int*>(carve(sizeof(int) * R * k));         // row top-k tokens
+  int* tok = reinterpret_cast<int*>(carve(sizeof(int) * C));
+  int* par = reinterpret_cast<int*>(carve(sizeof(int) * C));
+  int* node = reinterpret_cast<int*>(carve(sizeof(int) * C));
+  int* npar = reinterpret_cast<int*>(carve(sizeof(int) * EAGLE_MAX_TREE));
+  int* fr = reinterpret_cast<int*>(carve(sizeof(int) * kKMax));
+  int* fr_next = reinterpret_cast<int*>(carve(sizeof(int) * kKMax));
+  int* hist = reinterpret_cast<int*>(carve(sizeof(int) * 256));
+  int* misc = reinterpret_cast<int*>(carve(sizeof(int) * 8));  // [0] digit, [1] count above
+  int* warp_tot = reinterpret_cast<int*>(carve(sizeof(int) * kWarps));
 
+  // every row's statistics in one pass: logsumexp, top-k logits and tokens
   for (int r = tid; r < R; r += kThreads) {
     const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rows + r * rb);
     lse[r] = static_cast<double>(h->max) + log_d(h->sum);
   }
+  for (int e = tid; e < R * k; e += kThreads) {
+    const int r = e / k, c = e - r * k;
+    rv[e] = __ldcg(rec_val(rows + r * rb) + c);
+    ri[e] = __ldcg(rec_idx(rows + r * rb, rk) + c);
+  }
   __syncthreads();
-  auto row_logit = [&](int r, int c) { return __ldcg(rec_val(rows + r * rb) + c); };
-  auto row_token = [&](int r, int c) { return __ldcg(rec_idx(rows + r * rb, rk) + c); };
+  auto row_logit = [&](int r, int c) { return rv[r * k + c]; };
+  auto row_token = [&](int r, int c) { return ri[r * k + c]; };
 
   // depth 1: the root's top_k, rank order
   for (int c = tid; c < k; c += kThreads) {
@@ -295,13 +298,22 @@ static __device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S
   __syncthreads();
   const int W = out.mask_words;
   for (int n = tid; n < m; n += kThreads) {
-    uint64_t w[EAGLE_MAX_TREE / 64] = {0, 0, 0, 0};
+    uint64_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
     int q = n;
     for (int guard = 0; q >= 0 && guard <= EAGLE_MAX_DEPTH + 1; ++guard) {
-      w[q >> 6] |= 1ull << (q & 63);
+      const uint64_t bit = 1ull << (q & 63);
+      const int wi = q >> 6;
+      w0 |= wi == 0 ? bit : 0ull;
+      w1 |= wi == 1 ? bit : 0ull;
+      w2 |= wi == 2 ? bit : 0ull;
+      w3 |= wi == 3 ? bit : 0ull;
       q = npar[q];
     }
-    for (int i = 0; i < W; ++i) out.mask[static_cast<int64_t>(n) * W + i] = w[i];
+    uint64_t* dst = out.mask + static_cast<int64_t>(n) * W;
+    dst[0] = w0;
+    if (W > 1) dst[1] = w1;
+    if (W > 2) dst[2] = w2;
+    if (W > 3) dst[3] = w3;
   }
   __syncthreads();
 }
@@ -316,6 +328,12 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const __grid_constant__
     __syncthreads();
   }
 }
+
+// R = 1 + (depth-1) top_k stays below 256 whenever C <= 2048 and depth <= 16
+static_assert(sizeof(StreamSmem) - offsetof(StreamSmem, buf) >=
+                  (8 + 8 + 4 + 4 + 4 + 4 + 4) * EAGLE_MAX_CANDIDATES + 8 * 256 +
+                      4 * (EAGLE_MAX_TREE + 2 * kKMax + 256 + 8 + kWarps) + 16 * 16,
+              "tree assembly scratch must fit in the stream's shared memory");
 
 static int build_ctas_per_sm() {
   int occ = 0;

@@ -117,6 +117,13 @@ __device__ __forceinline__ uint64_t order_key(double x) {
   return (u >> 63) ? ~u : (u | (1ull << 63));
 }
 
+// 2^x on the special-function unit (approximate, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------- exp / log to ~1e-7 relative
 // The fp64 special functions are very slow on this part; these reduce the
 // argument in fp64 and evaluate the remaining small range with the fp32

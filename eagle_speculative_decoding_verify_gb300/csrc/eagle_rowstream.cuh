@@ -9,12 +9,13 @@
 // barrier is taken per slot.  Per row segment the CTA computes:
 //   * max and sum of 2^((x - max) * c) per thread (fp32 ex2), combined per
 //     segment with fp32 factors and fp64 accumulation,
-//   * the exact top-K (value desc, token id asc), K <= 64: each warp takes
-//     as survivor threshold the K-th best of the top-2 of every lane in the
-//     segment's first slot (a lower bound of the K-th value of the segment),
-//     keeps elements >= threshold in a warp-private buffer (compacted to its
-//     best K when full, which raises the threshold) and the CTA ranks the
-//     survivors once at the end of the segment,
+//   * the exact top-K (value desc, token id asc), K <= 64: the survivor
+//     threshold is the K-th best of the top-2 of every thread in the
+//     segment's first slot (distinct elements, so a lower bound of the K-th
+//     value of the segment); each warp keeps the elements >= threshold in a
+//     private buffer (sorted and cut to its best K when full, which raises
+//     its threshold); at the end of the segment every warp sorts its buffer
+//     and the CTA merges the eight sorted lists by binary-search ranks,
 //   * optionally per-tile (max, sum) of every warp for inverse-CDF sampling.
 // Each segment is written as a piece record.  The CTA whose piece arrives
 // last for a row merges the row's pieces into a row record; the CTA whose
@@ -33,7 +34,7 @@ constexpr int kSub = kTile * kSubTiles;     // 8192 floats = 32 KB per slot
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVec = kSub / kThreads / 4;   // float4 per thread per slot (8)
-constexpr int kWarpCap = 128;               // survivors per warp
+constexpr int kWarpCap = 64;                // survivors per warp
 constexpr int kKMax = EAGLE_MAX_TOP_K;
 constexpr int kMaxItems = EAGLE_MAX_BATCH;
 constexpr int kMaxPieces = 16;              // CTAs sharing one row (host keeps it)
@@ -76,11 +77,15 @@ __device__ __forceinline__ int* rec_idx(char* rec, int rec_k) {
 }
 
 struct StreamSmem {
-  float buf[2][kSub];                 // ring (also reused by the item final step)
+  int n_done_items;                   // items whose final step this CTA runs
+  int done_items[kMaxItems + 31];     // (padded so that the ring starts 16-byte aligned)
+  float buf[2][kSub];                 // ring; from here on reused by the item final step
   float wv[kWarps][kWarpCap];         // warp survivor buffers
   int wi[kWarps][kWarpCap];
-  float mv[kMaxPieces * kKMax];       // merge staging (piece lists / all survivors)
+  float mv[kMaxPieces * kKMax];       // merge staging (piece lists / warp lists)
   int mi[kMaxPieces * kKMax];
+  int lcnt[kWarps];                   // entries of each warp's sorted list
+  float thr;                          // CTA survivor threshold of the segment
   float list_v[kKMax];
   int list_i[kKMax];
   float red_f[kWarps];
@@ -89,19 +94,11 @@ struct StreamSmem {
   uint64_t full[2];
   uint64_t empty[2];
   int is_last;
-  int n_done_items;
-  int done_items[kMaxItems];
   int cnt[kMaxPieces];
   float pmax[kMaxPieces];
   double psum[kMaxPieces];
 };
 
-// 2^x on the special-function unit (approximate, flush-to-zero).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __device__ __forceinline__ int64_t tile_owner(int64_t t, int64_t T, int G) {
   return ((t + 1) * G - 1) / T;
@@ -180,31 +177,47 @@ __device__ __forceinline__ void warp_sort64(float (&v)[2], int (&id)[2]) {
   }
 }
 
-// Keep the best K of a warp's buffer of n entries (in place); returns the count.
-static __device__ int warp_compact(float* bv, int* bi, int n, int K) {
+// Sort a warp's buffer (n <= 64 entries) best first, in place; returns n.
+__device__ __forceinline__ int warp_sort_buffer(float* bv, int* bi, int n) {
   const int lane = threadIdx.x & 31;
-  float tv[kWarpCap / 32];
-  int ti[kWarpCap / 32];
-  int rk[kWarpCap / 32];
+  float v[2];
+  int id[2];
 #pragma unroll
-  for (int r = 0; r < kWarpCap / 32; ++r) {
+  for (int r = 0; r < 2; ++r) {
     const int a = lane + 32 * r;
-    tv[r] = a < n ? bv[a] : -INFINITY;
-    ti[r] = a < n ? bi[a] : 0x7fffffff;
-    int rank = 0;
-    if (a < n)
-      for (int b = 0; b < n; ++b) rank += before(bv[b], bi[b], tv[r], ti[r]) ? 1 : 0;
-    rk[r] = a < n ? rank : 0x7fffffff;
+    v[r] = a < n ? bv[a] : -INFINITY;
+    id[r] = a < n ? bi[a] : 0x7fffffff;
+  }
+  warp_sort64(v, id);
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int a = lane + 32 * r;
+    if (a < n) {
+      bv[a] = v[r];
+      bi[a] = id[r];
+    }
   }
   __syncwarp();
-#pragma unroll
-  for (int r = 0; r < kWarpCap / 32; ++r)
-    if (rk[r] < K) {
-      bv[rk[r]] = tv[r];
-      bi[rk[r]] = ti[r];
+  return n;
+}
+
+// Rank of entry (v, id) of sorted list `self` among the union of `nl` sorted
+// lists stored at stride `stride` (counts in `cnt`): its position plus the
+// number of entries of every other list that come before it.
+__device__ __forceinline__ int merged_rank(const float* lv, const int* li, const int* cnt, int nl,
+                                           int stride, int self, int pos, float v, int id) {
+  int rank = pos;
+  for (int q = 0; q < nl; ++q) {
+    if (q == self) continue;
+    int lo = 0, hi = cnt[q];
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (before(lv[q * stride + mid], li[q * stride + mid], v, id)) lo = mid + 1; else hi = mid;
     }
-  __syncwarp();
-  return n < K ? n : K;
+    rank += lo;
+  }
+  return rank;
 }
 
 // ------------------------------------------------------------ row finalize
@@ -240,21 +253,10 @@ static __device__ void finalize_row(const RowStream& P, StreamSmem& S, int64_t r
   for (int e = threadIdx.x; e < np * K; e += blockDim.x) {
     const int p = e / K, c = e - p * K;
     if (c >= S.cnt[p]) continue;
-    const float v = S.mv[e];
-    const int id = S.mi[e];
-    int rank = c;
-    for (int q = 0; q < np; ++q) {
-      if (q == p) continue;
-      int lo = 0, hi = S.cnt[q];   // entries of piece q before (v, id)
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (before(S.mv[q * K + mid], S.mi[q * K + mid], v, id)) lo = mid + 1; else hi = mid;
-      }
-      rank += lo;
-    }
+    const int rank = merged_rank(S.mv, S.mi, S.cnt, np, K, p, c, S.mv[e], S.mi[e]);
     if (rank < K) {
-      rec_val(out)[rank] = v;
-      rec_idx(out, P.rec_k)[rank] = id;
+      rec_val(out)[rank] = S.mv[e];
+      rec_idx(out, P.rec_k)[rank] = S.mi[e];
     }
   }
   if (threadIdx.x < 32) {
@@ -418,8 +420,10 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
 
     // ---- top-K survivors, K >= 2
     if (K >= 2) {
+      float* bv = S.wv[warp];
+      int* bi = S.wi[warp];
       if (seg_first) {
-        // threshold: K-th best of the lanes' top-2 (distinct elements of the row)
+        // threshold: K-th best of the threads' top-2 over the whole CTA
         float sv[2] = {-INFINITY, -INFINITY};
         int si[2] = {0x7fffffff, 0x7fffffff};
 #pragma unroll
@@ -427,8 +431,8 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float xv = x[4 * q + c];
-            const int xi = tbase + q * kTile + c;
             if (xv > sv[1]) {
+              const int xi = tbase + q * kTile + c;
               if (xv > sv[0]) {
                 sv[1] = sv[0];
                 si[1] = si[0];
@@ -441,39 +445,77 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
             }
           }
         warp_sort64(sv, si);
-        const int kk = K - 1;   // the K-th best sits at position K-1
-        thr_v = __shfl_sync(0xffffffffu, kk < 32 ? sv[0] : sv[1], kk & 31);
-        if (lane == 0) S.wcnt[warp] = 0;
-        __syncwarp();
-      }
-      if (__any_sync(0xffffffffu, lm >= thr_v)) {
-        float* bv = S.wv[warp];
-        int* bi = S.wi[warp];
+        const int keep = K < 64 ? K : 64;
 #pragma unroll
-        for (int q = 0; q < kVec; ++q) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float xv = x[4 * q + c];
-            bool pass = xv >= thr_v && xv != -INFINITY;
-            unsigned bal = __ballot_sync(0xffffffffu, pass);
-            if (!bal) continue;
-            int n = S.wcnt[warp];
-            if (n + __popc(bal) > kWarpCap) {   // full: keep the best K, raise the bar
-              n = warp_compact(bv, bi, n, K);
-              if (n >= K) thr_v = fmaxf(thr_v, bv[K - 1]);
-              pass = xv >= thr_v && xv != -INFINITY;
-              bal = __ballot_sync(0xffffffffu, pass);
-            }
-            if (pass) {
-              const int pos = n + __popc(bal & ((1u << lane) - 1u));
-              bv[pos] = xv;
-              bi[pos] = tbase + q * kTile + c;
-            }
-            __syncwarp();
-            if (lane == 0) S.wcnt[warp] = n + __popc(bal);
-            __syncwarp();
+        for (int r = 0; r < 2; ++r) {
+          const int a = lane + 32 * r;
+          if (a < keep) {
+            S.mv[warp * kKMax + a] = sv[r];
+            S.mi[warp * kKMax + a] = si[r];
           }
         }
+        if (lane == 0) {
+          S.lcnt[warp] = keep;
+          S.wcnt[warp] = 0;
+        }
+        __syncthreads();
+        for (int e = tid; e < kWarps * keep; e += kThreads) {
+          const int w = e / keep, c = e - w * keep;
+          const float v = S.mv[w * kKMax + c];
+          if (merged_rank(S.mv, S.mi, S.lcnt, kWarps, kKMax, w, c, v, S.mi[w * kKMax + c]) == K - 1)
+            S.thr = v;   // -inf when the slot holds fewer than K elements
+        }
+        __syncthreads();
+        thr_v = S.thr;
+      }
+      if (__any_sync(0xffffffffu, lm >= thr_v)) {
+        uint32_t pm = 0;
+#pragma unroll
+        for (int e = 0; e < kVec * 4; ++e) pm |= (x[e] >= thr_v && x[e] != -INFINITY) ? (1u << e) : 0u;
+        int cntp = __popc(pm);
+        int incl = cntp;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int total = __shfl_sync(0xffffffffu, incl, 31);
+        int n = S.wcnt[warp];
+        if (n + total > kWarpCap) {   // full: keep the best K, raise this warp's bar
+          __syncwarp();
+          n = warp_sort_buffer(bv, bi, n);
+          n = n < K ? n : K;
+          if (n >= K) thr_v = fmaxf(thr_v, bv[K - 1]);
+          pm = 0;
+#pragma unroll
+          for (int e = 0; e < kVec * 4; ++e) pm |= (x[e] >= thr_v && x[e] != -INFINITY) ? (1u << e) : 0u;
+          cntp = __popc(pm);
+          incl = cntp;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          total = __shfl_sync(0xffffffffu, incl, 31);
+          if (n + total > kWarpCap) {   // cannot happen for distinct values; keep the bound
+            record_error(P.err, kDevAssert, 3);
+            total = 0;
+            pm = 0;
+          }
+        }
+        int pos = n + incl - cntp;
+        if (pm) {
+#pragma unroll
+          for (int e = 0; e < kVec * 4; ++e)   // static indices keep x in registers
+            if ((pm >> e) & 1u) {
+              bv[pos] = x[e];
+              bi[pos] = tbase + (e >> 2) * kTile + (e & 3);
+              ++pos;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) S.wcnt[warp] = n + total;
+        __syncwarp();
       }
     }
 
@@ -524,20 +566,33 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
       }
       int nl = 0;
       if (K >= 2) {
-        // gather every warp's survivors, rank them once
-        __syncthreads();
-        int off = 0;
-        for (int w = 0; w < kWarps; ++w) {
-          const int n = S.wcnt[w];
-          for (int a = tid; a < n; a += kThreads) {
-            S.mv[off + a] = S.wv[w][a];
-            S.mi[off + a] = S.wi[w][a];
+        // every warp sorts its survivors; the CTA merges the sorted lists
+        {
+          float* bv = S.wv[warp];
+          int* bi = S.wi[warp];
+          const int n = warp_sort_buffer(bv, bi, S.wcnt[warp]);
+          const int keep = n < K ? n : K;
+          for (int a = lane; a < keep; a += 32) {
+            S.mv[warp * kKMax + a] = bv[a];
+            S.mi[warp * kKMax + a] = bi[a];
           }
-          off += n;
+          if (lane == 0) S.lcnt[warp] = keep;
         }
         __syncthreads();
-        rank_select(S.mv, S.mi, off, K, S.list_v, S.list_i);
-        nl = off < K ? off : K;
+        int total = 0;
+        for (int w = 0; w < kWarps; ++w) total += S.lcnt[w];
+        for (int e = tid; e < kWarps * kKMax; e += kThreads) {
+          const int w = e / kKMax, c = e - w * kKMax;
+          if (c >= S.lcnt[w]) continue;
+          const float v = S.mv[e];
+          const int id = S.mi[e];
+          const int rank = merged_rank(S.mv, S.mi, S.lcnt, kWarps, kKMax, w, c, v, id);
+          if (rank < K) {
+            S.list_v[rank] = v;
+            S.list_i[rank] = id;
+          }
+        }
+        nl = total < K ? total : K;
         __syncthreads();
         for (int a = tid; a < nl; a += kThreads) {
           S.mv[a] = S.list_v[a];
