@@ -328,8 +328,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       for (int half = 0; half < 2; ++half) {
         float v[64];
         load64(half, v);
+        float m8[8];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
+        for (int a = 0; a < 8; ++a) m8[a] = v[a];
+#pragma unroll
+        for (int e = 8; e < 64; ++e) m8[e & 7] = fmaxf(m8[e & 7], v[e]);
+        mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
       }
       mx *= sl2;   // scale > 0: max of the scaled row
       // previous PV of this tile must be done before P is overwritten / O rescaled
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           if (!bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 43)) { ok = false; break; }
           tc_fence_after();
         }
-        float lsum = 0.f;
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           float v[64];
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
             float pv = ex2(fmaf(v[e], sl2, -mref));
-            lsum += pv;
+            ls[e & 7] += pv;
             if (f == 1) pv -= __bfloat162float(__float2bfloat16_rn(pv));
             v[e] = pv;
           }
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                                       ((cc ^ (row & 7)) << 4)) = w;
           }
         }
-        if (f == 0) l_run += lsum;
+        if (f == 0) l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[t]);

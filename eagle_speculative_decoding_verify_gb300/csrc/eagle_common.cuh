@@ -112,8 +112,8 @@ __device__ __forceinline__ bool before_d(double va, int ia, double vb, int ib) {
 
 // Monotone map of a double to uint64 (larger value -> larger key); -0 == +0.
 __device__ __forceinline__ uint64_t order_key(double x) {
-  x = x + 0.0;
-  const uint64_t u = static_cast<uint64_t>(__double_as_longlong(x));
+  uint64_t u = static_cast<uint64_t>(__double_as_longlong(x));
+  if (u == (1ull << 63)) u = 0;   // -0 -> +0
   return (u >> 63) ? ~u : (u | (1ull << 63));
 }
 

@@ -34,7 +34,7 @@ constexpr int kSub = kTile * kSubTiles;     // 8192 floats = 32 KB per slot
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVec = kSub / kThreads / 4;   // float4 per thread per slot (8)
-constexpr int kWarpCap = 64;                // survivors per warp
+constexpr int kWarpCap = 128;               // survivors per warp (> K, so merges progress)
 constexpr int kKMax = EAGLE_MAX_TOP_K;
 constexpr int kMaxItems = EAGLE_MAX_BATCH;
 constexpr int kMaxPieces = 16;              // CTAs sharing one row (host keeps it)
@@ -144,22 +144,32 @@ __device__ __forceinline__ void rank_select(const float* v, const int* id, int n
   }
 }
 
-// Warp bitonic sort of 64 (v, i) pairs held two per lane (position p = lane
+// Warp bitonic sort of 32E (v, i) pairs held E per lane (position p = lane
 // + 32 r) into (value desc, index asc) order: position 0 holds the best.
-__device__ __forceinline__ void warp_sort64(float (&v)[2], int (&id)[2]) {
+template <int E>
+__device__ __forceinline__ void warp_sort(float (&v)[E], int (&id)[E]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int k = 2; k <= 64; k <<= 1) {
+  for (int k = 2; k <= 32 * E; k <<= 1) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j == 32) {  // partner is the other register of the same lane (k == 64)
-        if (before(v[1], id[1], v[0], id[0])) {
-          const float tv = v[0]; v[0] = v[1]; v[1] = tv;
-          const int ti = id[0]; id[0] = id[1]; id[1] = ti;
+      if (j >= 32) {  // partner is another register of the same lane
+        const int dr = j >> 5;
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          if (r & dr) continue;   // r is the lower position of the pair (r, r + dr)
+          const int p = lane + 32 * r;
+          const bool best_first = (p & k) == 0;
+          const bool swap = best_first ? before(v[r + dr], id[r + dr], v[r], id[r])
+                                       : before(v[r], id[r], v[r + dr], id[r + dr]);
+          if (swap) {
+            const float tv = v[r]; v[r] = v[r + dr]; v[r + dr] = tv;
+            const int ti = id[r]; id[r] = id[r + dr]; id[r + dr] = ti;
+          }
         }
       } else {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
+        for (int r = 0; r < E; ++r) {
           const int p = lane + 32 * r;
           const float ov = __shfl_xor_sync(0xffffffffu, v[r], j);
           const int oi = __shfl_xor_sync(0xffffffffu, id[r], j);
@@ -177,21 +187,24 @@ __device__ __forceinline__ void warp_sort64(float (&v)[2], int (&id)[2]) {
   }
 }
 
-// Sort a warp's buffer (n <= 64 entries) best first, in place; returns n.
+__device__ __forceinline__ void warp_sort64(float (&v)[2], int (&id)[2]) { warp_sort<2>(v, id); }
+
+// Sort a warp's buffer (n <= kWarpCap entries) best first, in place; returns n.
 __device__ __forceinline__ int warp_sort_buffer(float* bv, int* bi, int n) {
   const int lane = threadIdx.x & 31;
-  float v[2];
-  int id[2];
+  constexpr int E = kWarpCap / 32;
+  float v[E];
+  int id[E];
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
+  for (int r = 0; r < E; ++r) {
     const int a = lane + 32 * r;
     v[r] = a < n ? bv[a] : -INFINITY;
     id[r] = a < n ? bi[a] : 0x7fffffff;
   }
-  warp_sort64(v, id);
+  warp_sort<E>(v, id);
   __syncwarp();
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
+  for (int r = 0; r < E; ++r) {
     const int a = lane + 32 * r;
     if (a < n) {
       bv[a] = v[r];
@@ -316,7 +329,8 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
   float m_run = -INFINITY, s_run = 0.f;       // per-thread running max / sum
   float best_v = -INFINITY;                    // per-thread argmax (K == 1)
   int best_i = 0x7fffffff;
-  float thr_v = INFINITY;                      // warp survivor threshold (K >= 2)
+  float thr_v = INFINITY;                      // warp survivor threshold (K >= 2):
+  int thr_i = 0x7fffffff;                      // survivors come at or before (thr_v, thr_i)
   int64_t cur = t_begin;
   for (int j = 0; cur < t_end; ++j) {
     const int b = j & 1;
@@ -369,9 +383,16 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
     const bool seg_last = (nxt == t_end) || (nxt % TR == 0);
     const int tbase = tok0 + tid * 4;   // token of element (q, c) = tbase + q * 1024 + c
 
-    float lm = -INFINITY;
+    float lm;
+    {
+      float m4[4];
 #pragma unroll
-    for (int e = 0; e < kVec * 4; ++e) lm = fmaxf(lm, x[e]);
+      for (int a = 0; a < 4; ++a) m4[a] = fmaxf(fmaxf(x[a], x[4 + a]), fmaxf(x[8 + a], x[12 + a]));
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        m4[a] = fmaxf(m4[a], fmaxf(fmaxf(x[16 + a], x[20 + a]), fmaxf(x[24 + a], x[28 + a])));
+      lm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    }
 
     // ---- sum of exp (invalid elements are -inf and contribute 0)
     if (flags & kWantSum) {
@@ -379,10 +400,12 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
       if (mn != -INFINITY) {
         s_run *= ex2((m_run - mn) * c2);
         const float off = mn * c2;
-        float acc = 0.f;
+        float acc[8];
 #pragma unroll
-        for (int e = 0; e < kVec * 4; ++e) acc += ex2(fmaf(x[e], c2, -off));
-        s_run += acc;
+        for (int a = 0; a < 8; ++a) acc[a] = ex2(fmaf(x[a], c2, -off));
+#pragma unroll
+        for (int e = 8; e < kVec * 4; ++e) acc[e & 7] += ex2(fmaf(x[e], c2, -off));
+        s_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         m_run = mn;
       }
     }
@@ -467,55 +490,64 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
         }
         __syncthreads();
         thr_v = S.thr;
+        thr_i = 0x7fffffff;
       }
       if (__any_sync(0xffffffffu, lm >= thr_v)) {
+        auto survives = [&](int e) {
+          const float xv = x[e];
+          const int xi = tbase + (e >> 2) * kTile + (e & 3);
+          return xv != -INFINITY && (xv > thr_v || (xv == thr_v && xi <= thr_i));
+        };
         uint32_t pm = 0;
 #pragma unroll
-        for (int e = 0; e < kVec * 4; ++e) pm |= (x[e] >= thr_v && x[e] != -INFINITY) ? (1u << e) : 0u;
-        int cntp = __popc(pm);
-        int incl = cntp;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        int total = __shfl_sync(0xffffffffu, incl, 31);
-        int n = S.wcnt[warp];
-        if (n + total > kWarpCap) {   // full: keep the best K, raise this warp's bar
-          __syncwarp();
-          n = warp_sort_buffer(bv, bi, n);
-          n = n < K ? n : K;
-          if (n >= K) thr_v = fmaxf(thr_v, bv[K - 1]);
-          pm = 0;
-#pragma unroll
-          for (int e = 0; e < kVec * 4; ++e) pm |= (x[e] >= thr_v && x[e] != -INFINITY) ? (1u << e) : 0u;
-          cntp = __popc(pm);
-          incl = cntp;
+        for (int e = 0; e < kVec * 4; ++e) pm |= survives(e) ? (1u << e) : 0u;
+        for (;;) {
+          const int cntp = __popc(pm);
+          int incl = cntp;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
           }
-          total = __shfl_sync(0xffffffffu, incl, 31);
-          if (n + total > kWarpCap) {   // cannot happen for distinct values; keep the bound
-            record_error(P.err, kDevAssert, 3);
-            total = 0;
-            pm = 0;
-          }
-        }
-        int pos = n + incl - cntp;
-        if (pm) {
+          const int total = __shfl_sync(0xffffffffu, incl, 31);
+          const int n = S.wcnt[warp];
+          const bool fits = n + total <= kWarpCap;
+          // append (all, or the first kWarpCap - n in lane order)
+          int take = cntp;
+          if (!fits) take = max(0, min(cntp, kWarpCap - n - (incl - cntp)));
+          int pos = n + incl - cntp;
+          if (take) {
+            int taken = 0;
 #pragma unroll
-          for (int e = 0; e < kVec * 4; ++e)   // static indices keep x in registers
-            if ((pm >> e) & 1u) {
-              bv[pos] = x[e];
-              bi[pos] = tbase + (e >> 2) * kTile + (e & 3);
-              ++pos;
-            }
+            for (int e = 0; e < kVec * 4; ++e)   // static indices keep x in registers
+              if (((pm >> e) & 1u) && taken < take) {
+                bv[pos++] = x[e];
+                bi[pos - 1] = tbase + (e >> 2) * kTile + (e & 3);
+                pm &= ~(1u << e);
+                ++taken;
+              }
+          }
+          __syncwarp();
+          if (fits) {
+            if (lane == 0) S.wcnt[warp] = n + total;
+            __syncwarp();
+            break;
+          }
+          // buffer full: keep the best K, raise this warp's bar, drop what no
+          // longer survives, and go on with the rest of this slot
+          const int kept = min(warp_sort_buffer(bv, bi, kWarpCap), K);
+          if (kept >= K && before(bv[K - 1], bi[K - 1], thr_v, thr_i)) {
+            thr_v = bv[K - 1];
+            thr_i = bi[K - 1];
+          }
+          uint32_t keep = 0;
+#pragma unroll
+          for (int e = 0; e < kVec * 4; ++e) keep |= survives(e) ? (1u << e) : 0u;
+          pm &= keep;
+          if (lane == 0) S.wcnt[warp] = kept;
+          __syncwarp();
+          if (!__any_sync(0xffffffffu, pm != 0u)) break;
         }
-        __syncwarp();
-        if (lane == 0) S.wcnt[warp] = n + total;
-        __syncwarp();
       }
     }
 
@@ -623,6 +655,7 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
       best_v = -INFINITY;
       best_i = 0x7fffffff;
       thr_v = INFINITY;
+      thr_i = 0x7fffffff;
       if (lane == 0) S.wcnt[warp] = 0;
       __threadfence();
       __syncthreads();
