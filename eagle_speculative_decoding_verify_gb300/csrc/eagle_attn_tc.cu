@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   uint64_t* p_full = s_full + 2;        // [2]
   uint64_t* o_done = p_full + 2;        // [2]
   uint64_t* drain = o_done + 2;         // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* q_ready = drain + 1;        // [1] Q tiles written (8 softmax warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -127,10 +128,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&p_full[t], 4);   // one arrival per softmax warp
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(q_ready, 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -145,7 +147,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     tma_prefetch_map(&P.tvmap[item]);
   }
 
-  // ---- Q tiles -> shared memory (128-byte swizzle), mask rows -> registers
+  tc_fence_before();
+  __syncthreads();   // barriers initialised, tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_S = tmem;               // S_t at column 128 t
+  const uint32_t tmem_O = tmem + 256;         // O_t at column 256 + D t
+
+  // ---- Q tiles -> shared memory (128-byte swizzle), mask rows -> registers;
+  // the producer is already streaming K/V meanwhile
   const int wg = warp >= 4 ? (warp - 4) >> 2 : -1;   // softmax warpgroup = query tile
   const int row = (warp & 3) * 32 + lane;            // row within the tile = TMEM lane
   const int R = 256 * tp + 128 * (wg < 0 ? 0 : wg) + row;
@@ -157,26 +167,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const int hl = valid ? R - qi * g : 0;
     const int4* src = reinterpret_cast<const int4*>(
         it.q + (static_cast<int64_t>(qi) * P.hq + kvh * g + hl) * D);
+    int4 qv[D / 8];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {   // 16-byte chunks of the row
-      const int4 v = valid ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-      const int half = c >> 3, cc = c & 7;
-      *reinterpret_cast<int4*>(qt + half * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
-    }
+    for (int c = 0; c < D / 8; ++c) qv[c] = valid ? __ldg(src + c) : make_int4(0, 0, 0, 0);
     if (valid) {
       const int W = (it.m + 63) >> 6;
       const uint64_t* mr = it.mask + static_cast<int64_t>(qi) * W;
 #pragma unroll
       for (int w = 0; w < 4; ++w) mrow[w] = w < W ? __ldg(mr + w) : 0ull;
     }
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {   // 16-byte chunks of the row
+      const int half = c >> 3, cc = c & 7;
+      *reinterpret_cast<int4*>(qt + half * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = qv[c];
+    }
     fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_ready);
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_S = tmem;               // S_t at column 128 t
-  const uint32_t tmem_O = tmem + 256;         // O_t at column 256 + D t
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -236,7 +244,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                    smem_desc_sw128(vb + boff, 128 * 128, 1024), idesc_o, (acc || kk > 0));
         }
       };
-      bool ok = n_chunks > 0 && bounded_wait(&full[0], 0, P.err, abort_flag, 30);
+      bool ok = n_chunks > 0 && bounded_wait(q_ready, 0, P.err, abort_flag, 29) &&
+                bounded_wait(&full[0], 0, P.err, abort_flag, 30);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < n_tiles; ++t) {
@@ -393,7 +402,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (f == 0) l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&p_full[t]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
         ++fseq;
       }
       if (!ok) break;
@@ -405,24 +415,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       const int qi = valid ? R / g : 0, hl = valid ? R - qi * g : 0;
       const int64_t orow = static_cast<int64_t>(qi) * P.hq + kvh * g + hl;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      float* part = P.partials + it.part_start + (orow * it.splits + split) * part_stride(D);
+      const int Mpad = it.tile_pairs * 256;
+      float* part = P.partials + it.part_start +
+                    static_cast<int64_t>(kvh * it.splits + split) * (D + 2) * Mpad + R;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(o_addr + 32 * c, r);
         tmem_wait_ld();
-        if (!valid) continue;
-        const float sc = it.splits == 1 ? inv : 1.0f;
-        float4* dst = reinterpret_cast<float4*>(it.splits == 1 ? it.out + orow * D + 32 * c
-                                                               : part + 32 * c);
+        if (it.splits == 1) {
+          if (!valid) continue;
+          float4* dst = reinterpret_cast<float4*>(it.out + orow * D + 32 * c);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          dst[e] = make_float4(__uint_as_float(r[4 * e]) * sc, __uint_as_float(r[4 * e + 1]) * sc,
-                               __uint_as_float(r[4 * e + 2]) * sc, __uint_as_float(r[4 * e + 3]) * sc);
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                 __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
+        } else {
+          // lanes hold consecutive rows: every store covers 128 contiguous bytes
+#pragma unroll
+          for (int e = 0; e < 32; ++e) part[static_cast<int64_t>(32 * c + e) * Mpad] = __uint_as_float(r[e]);
+        }
       }
-      if (valid && it.splits > 1) {
-        part[D] = m_run;
-        part[D + 1] = l_run;
+      if (it.splits > 1) {
+        part[static_cast<int64_t>(D) * Mpad] = m_run;
+        part[static_cast<int64_t>(D + 1) * Mpad] = l_run;
       }
     }
   }
@@ -432,6 +448,67 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Split merge for the tensor-core partial layout [kvh][split][D + 2][Mpad]:
+// one warp per 32 consecutive query rows R of one (item, kv head); lanes are
+// rows, so every partial load is a coalesced 128-byte line; outputs go out
+// row by row through a shared-memory transpose.
+struct TcMergeParams {
+  TcItem items[kTcMaxItems];
+  int block_start[kTcMaxItems + 1];   // first block of each item
+  int n_items, hq, hkv, g;
+  const float* partials;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_tc_merge_kernel(const __grid_constant__ TcMergeParams P) {
+  __shared__ float tr[4][32][33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int item = 0;
+  while (item + 1 < P.n_items && static_cast<int>(blockIdx.x) >= P.block_start[item + 1]) ++item;
+  const TcItem& it = P.items[item];
+  const int Mpad = it.tile_pairs * 256;
+  const int wpk = Mpad / 32;                      // warps per kv head
+  const int w = (blockIdx.x - P.block_start[item]) * 4 + warp;
+  if (it.splits == 1 || w >= P.hkv * wpk) return;
+  const int kvh = w / wpk;
+  const int R0 = (w - kvh * wpk) * 32;
+  const int R = R0 + lane;
+  const int M = it.m * P.g;
+  const int S = it.splits;
+  const float* base = P.partials + it.part_start + static_cast<int64_t>(kvh) * S * (D + 2) * Mpad + R;
+  float mmax = -INFINITY;
+  for (int s = 0; s < S; ++s) mmax = fmaxf(mmax, __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad));
+  float L = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float ms = __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad);
+    if (ms != -INFINITY) L += ex2(ms - mmax) * __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D + 1) * Mpad);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float ms = __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad);
+      const float ws = ms == -INFINITY ? 0.f : ex2(ms - mmax) * inv;
+      const float* src = base + (static_cast<int64_t>(s) * (D + 2) + c0) * Mpad;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) acc[e] = fmaf(ws, __ldcg(src + static_cast<int64_t>(e) * Mpad), acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) tr[warp][lane][e] = acc[e];
+    __syncwarp();
+    for (int r = 0; r < 32; ++r) {   // row R0 + r: lanes write 32 consecutive columns
+      const int Rr = R0 + r;
+      if (Rr < M) {
+        const int qi = Rr / P.g, hl = Rr - qi * P.g;
+        it.out[(static_cast<int64_t>(qi) * P.hq + kvh * P.g + hl) * D + c0 + lane] = tr[warp][r][lane];
+      }
+    }
+    __syncwarp();
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -504,7 +581,8 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
     const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
     T.splits[b] = std::max(1, (nc + T.span - 1) / T.span);
     units += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
-    if (T.splits[b] > 1) part += static_cast<int64_t>(items[b].m) * hq * T.splits[b] * part_stride(d);
+    if (T.splits[b] > 1)
+      part += static_cast<int64_t>(hkv) * T.splits[b] * (d + 2) * T.tile_pairs[b] * 256;
   }
   T.units = static_cast<int>(units);
   T.part_floats = part;
@@ -543,9 +621,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       return EAGLE_ERR_WORKSPACE_TOO_SMALL;
     TcParams P;
     memset(&P, 0, sizeof(P));
-    AttnPlan M;   // plan of the merge kernel (same partial layout as the CUDA-core path)
-    memset(&M, 0, sizeof(M));
-    int64_t units = 0, part = 0, rows = 0;
+    int64_t units = 0, part = 0;
     for (int b = 0; b < nb; ++b) {
       const eagle_attn_item& x = its[b];
       const uint64_t S = static_cast<uint64_t>(x.prefix_len);
@@ -568,14 +644,8 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       ti.unit_start = static_cast<int>(units);
       ti.part_start = part;
       units += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
-      // merge plan
-      M.items[b].out = x.out;
-      M.items[b].m = x.m;
-      M.splits[b] = T.splits[b];
-      M.row_start[b] = rows;
-      M.part_start[b] = part;
-      rows += static_cast<int64_t>(x.m) * hq;
-      if (T.splits[b] > 1) part += static_cast<int64_t>(x.m) * hq * T.splits[b] * part_stride(D);
+      if (T.splits[b] > 1)
+        part += static_cast<int64_t>(hkv) * T.splits[b] * (D + 2) * T.tile_pairs[b] * 256;
     }
     P.n_items = nb;
     P.hq = hq;
@@ -593,15 +663,23 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     eagle_status st = launch_status();
     if (st != EAGLE_OK) return st;
     if (part > 0) {
-      M.n_items = nb;
-      M.n_q_heads = hq;
-      M.n_kv_heads = hkv;
-      M.head_dim = D;
-      M.row_start[nb] = rows;
-      M.part_floats = part;
-      M.err = P.err;
-      M.partials = P.partials;
-      if ((st = launch_attn_merge(M, stream)) != EAGLE_OK) return st;
+      TcMergeParams MP;
+      memset(&MP, 0, sizeof(MP));
+      int blocks = 0;
+      for (int b = 0; b < nb; ++b) {
+        MP.items[b] = P.items[b];
+        MP.block_start[b] = blocks;
+        const int warps = hkv * P.items[b].tile_pairs * 8;   // 32 rows per warp
+        blocks += (warps + 3) / 4;
+      }
+      MP.block_start[nb] = blocks;
+      MP.n_items = nb;
+      MP.hq = hq;
+      MP.hkv = hkv;
+      MP.g = hq / hkv;
+      MP.partials = P.partials;
+      attn_tc_merge_kernel<D><<<blocks, 128, 0, stream>>>(MP);
+      if ((st = launch_status()) != EAGLE_OK) return st;
     }
   }
   return EAGLE_OK;

@@ -310,7 +310,7 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.full[b], 1);
-      mbar_init(&S.empty[b], kThreads);
+      mbar_init(&S.empty[b], kWarps);
     }
     fence_barrier_init();
     S.n_done_items = 0;
@@ -371,8 +371,9 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
       x[4 * q + 2] = f.z;
       x[4 * q + 3] = f.w;
     }
-    mbar_arrive(&S.empty[b]);
-    if (tid == 0 && pf < t_end) {  // refill this slot once every thread has read it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[b]);   // one arrival per warp
+    if (tid == 0 && pf < t_end) {  // refill this slot once every warp has read it
       if (!mbar_wait(&S.empty[b], (j >> 1) & 1)) record_error(P.err, kDevTimeout, 2);
       fence_proxy_async_smem();
       issue_slot(P, S, pf, t_end, b);
