@@ -450,10 +450,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Split merge for the tensor-core partial layout [kvh][split][D + 2][Mpad]:
-// one warp per 32 consecutive query rows R of one (item, kv head); lanes are
-// rows, so every partial load is a coalesced 128-byte line; outputs go out
-// row by row through a shared-memory transpose.
+// Split merge for the tensor-core partial layout [kvh][split][D + 2][Mpad].
+// One CTA (4 warps) per (item, kv head, 32 query rows, 32 output columns):
+// lanes are rows, so every partial load is a coalesced 128-byte line; warp w
+// accumulates columns 8w..8w+7 of the group over all splits; the 32 x 32
+// result goes out row by row through a shared-memory transpose.
 struct TcMergeParams {
   TcItem items[kTcMaxItems];
   int block_start[kTcMaxItems + 1];   // first block of each item
@@ -463,51 +464,51 @@ struct TcMergeParams {
 
 template <int D>
 __global__ void __launch_bounds__(128) attn_tc_merge_kernel(const __grid_constant__ TcMergeParams P) {
-  __shared__ float tr[4][32][33];
+  __shared__ float tr[32][33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int item = 0;
   while (item + 1 < P.n_items && static_cast<int>(blockIdx.x) >= P.block_start[item + 1]) ++item;
   const TcItem& it = P.items[item];
+  if (it.splits == 1) return;
   const int Mpad = it.tile_pairs * 256;
-  const int wpk = Mpad / 32;                      // warps per kv head
-  const int w = (blockIdx.x - P.block_start[item]) * 4 + warp;
-  if (it.splits == 1 || w >= P.hkv * wpk) return;
-  const int kvh = w / wpk;
-  const int R0 = (w - kvh * wpk) * 32;
-  const int R = R0 + lane;
+  const int rgroups = Mpad / 32;
+  int b = blockIdx.x - P.block_start[item];
+  const int cg = b % (D / 32);
+  b /= D / 32;
+  const int rg = b % rgroups;
+  const int kvh = b / rgroups;
+  const int R0 = rg * 32, R = R0 + lane;
+  const int c0 = cg * 32 + warp * 8;
   const int M = it.m * P.g;
   const int S = it.splits;
   const float* base = P.partials + it.part_start + static_cast<int64_t>(kvh) * S * (D + 2) * Mpad + R;
   float mmax = -INFINITY;
-  for (int s = 0; s < S; ++s) mmax = fmaxf(mmax, __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad));
+  for (int s = 0; s < S; ++s)
+    mmax = fmaxf(mmax, __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad));
   float L = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int s = 0; s < S; ++s) {
-    const float ms = __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad);
-    if (ms != -INFINITY) L += ex2(ms - mmax) * __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D + 1) * Mpad);
+    const float* ps = base + static_cast<int64_t>(s) * (D + 2) * Mpad;
+    const float ms = __ldcg(ps + static_cast<int64_t>(D) * Mpad);
+    const float ls = __ldcg(ps + static_cast<int64_t>(D + 1) * Mpad);
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = __ldcg(ps + static_cast<int64_t>(c0 + e) * Mpad);
+    const float ws = ms == -INFINITY ? 0.f : ex2(ms - mmax);
+    L = fmaf(ws, ls, L);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws, o[e], acc[e]);
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  for (int c0 = 0; c0 < D; c0 += 32) {
-    float acc[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float ms = __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad);
-      const float ws = ms == -INFINITY ? 0.f : ex2(ms - mmax) * inv;
-      const float* src = base + (static_cast<int64_t>(s) * (D + 2) + c0) * Mpad;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = fmaf(ws, __ldcg(src + static_cast<int64_t>(e) * Mpad), acc[e]);
+  for (int e = 0; e < 8; ++e) tr[lane][warp * 8 + e] = acc[e] * inv;
+  __syncthreads();
+  for (int r = warp; r < 32; r += 4) {   // row R0 + r: lanes write 32 consecutive columns
+    const int Rr = R0 + r;
+    if (Rr < M) {
+      const int qi = Rr / P.g, hl = Rr - qi * P.g;
+      it.out[(static_cast<int64_t>(qi) * P.hq + kvh * P.g + hl) * D + cg * 32 + lane] = tr[r][lane];
     }
-#pragma unroll
-    for (int e = 0; e < 32; ++e) tr[warp][lane][e] = acc[e];
-    __syncwarp();
-    for (int r = 0; r < 32; ++r) {   // row R0 + r: lanes write 32 consecutive columns
-      const int Rr = R0 + r;
-      if (Rr < M) {
-        const int qi = Rr / P.g, hl = Rr - qi * P.g;
-        it.out[(static_cast<int64_t>(qi) * P.hq + kvh * P.g + hl) * D + c0 + lane] = tr[warp][r][lane];
-      }
-    }
-    __syncwarp();
   }
 }
 
@@ -669,8 +670,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       for (int b = 0; b < nb; ++b) {
         MP.items[b] = P.items[b];
         MP.block_start[b] = blocks;
-        const int warps = hkv * P.items[b].tile_pairs * 8;   // 32 rows per warp
-        blocks += (warps + 3) / 4;
+        blocks += hkv * P.items[b].tile_pairs * 8 * (D / 32);   // 32 rows x 32 columns each
       }
       MP.block_start[nb] = blocks;
       MP.n_items = nb;

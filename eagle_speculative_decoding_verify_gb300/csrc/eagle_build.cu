@@ -29,7 +29,7 @@ struct BuildArgs {
 __device__ __forceinline__ int cand_depth(int a, int k) { return a < k ? 1 : 2 + (a - k) / (k * k); }
 
 // Block-wide exclusive scan of per-thread counts (blockDim == kThreads).
-static __device__ int block_excl_scan(int v, int* warp_tot, int& total) {
+static __device__ __noinline__ int block_excl_scan(int v, int* warp_tot, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
 #pragma unroll
@@ -49,7 +49,7 @@ static __device__ int block_excl_scan(int v, int* warp_tot, int& total) {
   return off + incl - v;
 }
 
-static __device__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
+static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = A.top_k, D = A.depth, m = A.total_tokens, C = A.n_cand;
   const int R = 1 + (D - 1) * k;

@@ -149,22 +149,28 @@ __device__ __forceinline__ void rank_select(const float* v, const int* id, int n
 template <int E>
 __device__ __forceinline__ void warp_sort(float (&v)[E], int (&id)[E]) {
   const int lane = threadIdx.x & 31;
-#pragma unroll
+#pragma unroll 1
   for (int k = 2; k <= 32 * E; k <<= 1) {
-#pragma unroll
+#pragma unroll 1
     for (int j = k >> 1; j > 0; j >>= 1) {
       if (j >= 32) {  // partner is another register of the same lane
-        const int dr = j >> 5;
-#pragma unroll
-        for (int r = 0; r < E; ++r) {
-          if (r & dr) continue;   // r is the lower position of the pair (r, r + dr)
-          const int p = lane + 32 * r;
+        auto cx = [&](float& va, int& ia, float& vb, int& ib, int p) {   // (a lower, b upper)
           const bool best_first = (p & k) == 0;
-          const bool swap = best_first ? before(v[r + dr], id[r + dr], v[r], id[r])
-                                       : before(v[r], id[r], v[r + dr], id[r + dr]);
+          const bool swap = best_first ? before(vb, ib, va, ia) : before(va, ia, vb, ib);
           if (swap) {
-            const float tv = v[r]; v[r] = v[r + dr]; v[r + dr] = tv;
-            const int ti = id[r]; id[r] = id[r + dr]; id[r + dr] = ti;
+            const float tv = va; va = vb; vb = tv;
+            const int ti = ia; ia = ib; ib = ti;
+          }
+        };
+        if constexpr (E == 2) {
+          cx(v[0], id[0], v[1], id[1], lane);
+        } else if constexpr (E == 4) {
+          if (j == 64) {
+            cx(v[0], id[0], v[2], id[2], lane);
+            cx(v[1], id[1], v[3], id[3], lane + 32);
+          } else {
+            cx(v[0], id[0], v[1], id[1], lane);
+            cx(v[2], id[2], v[3], id[3], lane + 64);
           }
         }
       } else {
@@ -190,7 +196,7 @@ __device__ __forceinline__ void warp_sort(float (&v)[E], int (&id)[E]) {
 __device__ __forceinline__ void warp_sort64(float (&v)[2], int (&id)[2]) { warp_sort<2>(v, id); }
 
 // Sort a warp's buffer (n <= kWarpCap entries) best first, in place; returns n.
-__device__ __forceinline__ int warp_sort_buffer(float* bv, int* bi, int n) {
+static __device__ __noinline__ int warp_sort_buffer(float* bv, int* bi, int n) {
   const int lane = threadIdx.x & 31;
   constexpr int E = kWarpCap / 32;
   float v[E];
@@ -218,7 +224,7 @@ __device__ __forceinline__ int warp_sort_buffer(float* bv, int* bi, int n) {
 // Rank of entry (v, id) of sorted list `self` among the union of `nl` sorted
 // lists stored at stride `stride` (counts in `cnt`): its position plus the
 // number of entries of every other list that come before it.
-__device__ __forceinline__ int merged_rank(const float* lv, const int* li, const int* cnt, int nl,
+static __device__ __noinline__ int merged_rank(const float* lv, const int* li, const int* cnt, int nl,
                                            int stride, int self, int pos, float v, int id) {
   int rank = pos;
   for (int q = 0; q < nl; ++q) {
@@ -233,11 +239,42 @@ __device__ __forceinline__ int merged_rank(const float* lv, const int* li, const
   return rank;
 }
 
+// K-th best of every thread's top-2 (sv, si) over the CTA: each warp sorts
+// its 64 samples, the CTA ranks the warps' best K by binary search.  Every
+// thread of the CTA calls this (two CTA barriers).
+static __device__ __noinline__ float cta_threshold(StreamSmem& S, float (&sv)[2], int (&si)[2],
+                                                   int K) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_sort64(sv, si);
+  const int keep = K < 64 ? K : 64;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int a = lane + 32 * r;
+    if (a < keep) {
+      S.mv[warp * kKMax + a] = sv[r];
+      S.mi[warp * kKMax + a] = si[r];
+    }
+  }
+  if (lane == 0) {
+    S.lcnt[warp] = keep;
+    S.wcnt[warp] = 0;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kWarps * keep; e += kThreads) {
+    const int w = e / keep, c = e - w * keep;
+    const float v = S.mv[w * kKMax + c];
+    if (merged_rank(S.mv, S.mi, S.lcnt, kWarps, kKMax, w, c, v, S.mi[w * kKMax + c]) == K - 1)
+      S.thr = v;   // -inf when the slot holds fewer than K elements
+  }
+  __syncthreads();
+  return S.thr;
+}
+
 // ------------------------------------------------------------ row finalize
 // Merge the pieces of `row` into its row record.  Piece lists are sorted, so
 // an entry's rank is its position plus, for every other piece, the number of
 // that piece's entries that come before it (binary search).
-static __device__ void finalize_row(const RowStream& P, StreamSmem& S, int64_t row) {
+static __device__ __noinline__ void finalize_row(const RowStream& P, StreamSmem& S, int64_t row) {
   const int TR = P.tiles_per_row;
   const int64_t T = P.total_tiles;
   const int item = static_cast<int>(row / P.rows_per_item);
@@ -468,29 +505,7 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
               }
             }
           }
-        warp_sort64(sv, si);
-        const int keep = K < 64 ? K : 64;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int a = lane + 32 * r;
-          if (a < keep) {
-            S.mv[warp * kKMax + a] = sv[r];
-            S.mi[warp * kKMax + a] = si[r];
-          }
-        }
-        if (lane == 0) {
-          S.lcnt[warp] = keep;
-          S.wcnt[warp] = 0;
-        }
-        __syncthreads();
-        for (int e = tid; e < kWarps * keep; e += kThreads) {
-          const int w = e / keep, c = e - w * keep;
-          const float v = S.mv[w * kKMax + c];
-          if (merged_rank(S.mv, S.mi, S.lcnt, kWarps, kKMax, w, c, v, S.mi[w * kKMax + c]) == K - 1)
-            S.thr = v;   // -inf when the slot holds fewer than K elements
-        }
-        __syncthreads();
-        thr_v = S.thr;
+        thr_v = cta_threshold(S, sv, si, K);
         thr_i = 0x7fffffff;
       }
       if (__any_sync(0xffffffffu, lm >= thr_v)) {

@@ -61,7 +61,7 @@ __device__ __forceinline__ double full_prob(const float* lrow, int t, double row
 }
 
 // The walk; executed by warp 0 of the CTA.
-static __device__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
+static __device__ __noinline__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
   const int lane = threadIdx.x & 31;
   const int m = A.m;
   const int rk = A.rs.rec_k;
