@@ -103,11 +103,9 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 
 // --------------------------------------------------------- ordering / keys
 // (value desc, index asc): does (va, ia) come before (vb, ib)?
+// Written with bitwise operators so that it compiles to predicates, not branches.
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-__device__ __forceinline__ bool before_d(double va, int ia, double vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+  return (va > vb) | ((va == vb) & (ia < ib));
 }
 
 // Monotone map of a double to uint64 (larger value -> larger key); -0 == +0.
@@ -169,10 +167,9 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
   for (int o = 16; o; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, v, o);
     const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (before(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
+    const bool t = before(ov, oi, v, i);
+    v = t ? ov : v;
+    i = t ? oi : i;
   }
 }
 

@@ -156,11 +156,11 @@ __device__ __forceinline__ void warp_sort(float (&v)[E], int (&id)[E]) {
       if (j >= 32) {  // partner is another register of the same lane
         auto cx = [&](float& va, int& ia, float& vb, int& ib, int p) {   // (a lower, b upper)
           const bool best_first = (p & k) == 0;
-          const bool swap = best_first ? before(vb, ib, va, ia) : before(va, ia, vb, ib);
-          if (swap) {
-            const float tv = va; va = vb; vb = tv;
-            const int ti = ia; ia = ib; ib = ti;
-          }
+          const bool b_first = before(vb, ib, va, ia);
+          const bool swap = best_first == b_first;
+          const float tv = swap ? vb : va, tw = swap ? va : vb;
+          const int ti = swap ? ib : ia, tj = swap ? ia : ib;
+          va = tv; vb = tw; ia = ti; ib = tj;
         };
         if constexpr (E == 2) {
           cx(v[0], id[0], v[1], id[1], lane);
@@ -181,12 +181,11 @@ __device__ __forceinline__ void warp_sort(float (&v)[E], int (&id)[E]) {
           const int oi = __shfl_xor_sync(0xffffffffu, id[r], j);
           const bool lower = (p & j) == 0;
           const bool best_first = (p & k) == 0;   // direction of this block
-          const bool take = (lower == best_first) ? before(ov, oi, v[r], id[r])
-                                                  : before(v[r], id[r], ov, oi);
-          if (take) {
-            v[r] = ov;
-            id[r] = oi;
-          }
+          const bool other_first = before(ov, oi, v[r], id[r]);
+          // keep the better one at (lower == best_first), the worse one otherwise
+          const bool take = (lower == best_first) == other_first;
+          v[r] = take ? ov : v[r];
+          id[r] = take ? oi : id[r];
         }
       }
     }
@@ -225,16 +224,20 @@ static __device__ __noinline__ int warp_sort_buffer(float* bv, int* bi, int n) {
 // lists stored at stride `stride` (counts in `cnt`): its position plus the
 // number of entries of every other list that come before it.
 static __device__ __noinline__ int merged_rank(const float* lv, const int* li, const int* cnt, int nl,
-                                           int stride, int self, int pos, float v, int id) {
+                                               int stride, int self, int pos, float v, int id) {
   int rank = pos;
   for (int q = 0; q < nl; ++q) {
-    if (q == self) continue;
+    // entries of list q before (v, id): fixed 7 halving steps (lists <= 64)
     int lo = 0, hi = cnt[q];
-    while (lo < hi) {
+#pragma unroll
+    for (int step = 0; step < 7; ++step) {
       const int mid = (lo + hi) >> 1;
-      if (before(lv[q * stride + mid], li[q * stride + mid], v, id)) lo = mid + 1; else hi = mid;
+      const bool go = (lo < hi) & before(lv[q * stride + mid], li[q * stride + mid], v, id);
+      const bool stay = (lo < hi) & !go;
+      lo = go ? mid + 1 : lo;
+      hi = stay ? mid : hi;
     }
-    rank += lo;
+    rank += (q == self) ? 0 : lo;
   }
   return rank;
 }
@@ -472,11 +475,11 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
 #pragma unroll
       for (int q = 0; q < kVec; ++q)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (x[4 * q + c] > best_v) {
-            best_v = x[4 * q + c];
-            best_i = tbase + q * kTile + c;
-          }
+        for (int c = 0; c < 4; ++c) {
+          const bool t = x[4 * q + c] > best_v;
+          best_v = t ? x[4 * q + c] : best_v;
+          best_i = t ? tbase + q * kTile + c : best_i;
+        }
     }
 
     // ---- top-K survivors, K >= 2
@@ -492,18 +495,12 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const float xv = x[4 * q + c];
-            if (xv > sv[1]) {
-              const int xi = tbase + q * kTile + c;
-              if (xv > sv[0]) {
-                sv[1] = sv[0];
-                si[1] = si[0];
-                sv[0] = xv;
-                si[0] = xi;
-              } else {
-                sv[1] = xv;
-                si[1] = xi;
-              }
-            }
+            const int xi = tbase + q * kTile + c;
+            const bool gt1 = xv > sv[1], gt0 = xv > sv[0];
+            sv[1] = gt0 ? sv[0] : (gt1 ? xv : sv[1]);
+            si[1] = gt0 ? si[0] : (gt1 ? xi : si[1]);
+            sv[0] = gt0 ? xv : sv[0];
+            si[0] = gt0 ? xi : si[0];
           }
         thr_v = cta_threshold(S, sv, si, K);
         thr_i = 0x7fffffff;
@@ -512,7 +509,7 @@ static __device__ void run_stream(const RowStream& P, StreamSmem& S) {
         auto survives = [&](int e) {
           const float xv = x[e];
           const int xi = tbase + (e >> 2) * kTile + (e & 3);
-          return xv != -INFINITY && (xv > thr_v || (xv == thr_v && xi <= thr_i));
+          return (xv != -INFINITY) & ((xv > thr_v) | ((xv == thr_v) & (xi <= thr_i)));
         };
         uint32_t pm = 0;
 #pragma unroll
