@@ -15,11 +15,13 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle.so")
 
 EAGLE_OK = 0
+EAGLE_ERR_WORKSPACE_TOO_SMALL = 3
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape",
                 3: "workspace too small", 4: "CUDA error", 5: "device wait timed out",
                 6: "device invariant violated"}
 EAGLE_F32 = 0
 EAGLE_BF16 = 1
+EAGLE_NOALLOC_SCRATCH_BYTES = 256 * 1024   # include/eagle.h
 MAX_TOP_K = 64
 MAX_DEPTH = 16
 MAX_CANDIDATES = 2048
@@ -69,6 +71,8 @@ EXPORTS = {
     "eagle_tree_build": (_I32, [_P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, CTree, _P, _SZ, _P]),
     "eagle_tree_build_batched": (_I32, [_I32, _P, _I64, _I32, _I32, _I32, _I32, _I32, _P, _P,
                                         _P, _SZ, _P]),
+    "eagle_tree_build_noalloc": (_I32, [_P, _I64, _I32, _I32, _I32, _I32, _I32, _I32, CTree,
+                                        _P]),
     "eagle_tree_attn_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "eagle_tree_attn": (_I32, [_P, _P, _P, _I64, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32,
                                _F, _P, _P, _SZ, _P]),
@@ -180,6 +184,18 @@ def eagle_tree_build(draft_logits, top_k, depth, total_tokens, root_token, out=N
     _check(lib().eagle_tree_build(_ptr(draft_logits), draft_logits.stride(0), n_rows, vocab,
                                   top_k, depth, total_tokens, int(root_token), out.c(), _ptr(ws),
                                   ws.numel(), _stream(stream)), "eagle_tree_build")
+    return out
+
+
+def eagle_tree_build_noalloc(draft_logits, top_k, depth, total_tokens, root_token, out=None,
+                             stream=None):
+    """eagle_tree_build on the library's fixed static scratch (no workspace);
+    calls on one device must not overlap on the GPU."""
+    n_rows, vocab = draft_logits.shape
+    out = out or Tree(total_tokens, draft_logits.device)
+    _check(lib().eagle_tree_build_noalloc(_ptr(draft_logits), draft_logits.stride(0), n_rows,
+                                          vocab, top_k, depth, total_tokens, int(root_token),
+                                          out.c(), _stream(stream)), "eagle_tree_build_noalloc")
     return out
 
 

@@ -15,6 +15,8 @@
 // final best m-1 by an MSB radix select on order-preserving 64-bit keys
 // (ties -> lower candidate index); node ids by a block scan; ancestor mask
 // by walking parent pointers (depth <= 16).
+#include <mutex>
+
 #include "eagle_stream_host.h"
 
 namespace eagle {
@@ -394,6 +396,31 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
   return launch_status();
 }
 
+// Scratch of the allocation-free entry point: fixed size, static device
+// memory of this library, shared by every call on a device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[EAGLE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+static eagle_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  EAGLE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return EAGLE_ERR_UNSUPPORTED_SHAPE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    EAGLE_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    if (!p || !aligned16(p)) return EAGLE_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return EAGLE_OK;
+}
+
 }  // namespace eagle
 
 using namespace eagle;
@@ -428,4 +455,35 @@ extern "C" eagle_status eagle_tree_build_batched(int32_t n_items,
   return build_impl(n_items, draft_logits, row_stride, n_rows, vocab, top_k, depth,
                     total_tokens, root_tokens, outs, ws, ws_bytes,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" eagle_status eagle_tree_build_noalloc(const float* draft_logits, int64_t row_stride,
+                                                 int32_t n_rows, int32_t vocab, int32_t top_k,
+                                                 int32_t depth, int32_t total_tokens,
+                                                 int32_t root_token, eagle_tree out,
+                                                 eagle_stream stream) {
+  // the checks build_impl makes, made here first so that a bad argument
+  // enqueues nothing (not even the scratch clear)
+  EAGLE_CHECK_ARG(draft_logits && aligned16(draft_logits));
+  EAGLE_CHECK_ARG(vocab >= 1 && n_rows >= 1 && top_k >= 1 && depth >= 1 && total_tokens >= 1);
+  EAGLE_CHECK_SHAPE(top_k <= kKMax && top_k <= vocab && depth <= EAGLE_MAX_DEPTH);
+  const int64_t C = top_k + static_cast<int64_t>(depth - 1) * top_k * top_k;
+  EAGLE_CHECK_SHAPE(C <= EAGLE_MAX_CANDIDATES);
+  EAGLE_CHECK_SHAPE(total_tokens <= EAGLE_MAX_TREE && total_tokens <= 1 + C);
+  const int R = 1 + (depth - 1) * top_k;
+  EAGLE_CHECK_ARG(n_rows >= R);
+  EAGLE_CHECK_ARG(row_stride >= vocab && row_stride % 4 == 0);
+  EAGLE_CHECK_ARG(out.parents && out.tokens && out.depth && out.pos && out.mask);
+  EAGLE_CHECK_ARG(out.m == total_tokens && out.mask_words == (total_tokens + 63) / 64);
+  const StreamLayout L = stream_layout(1, R, vocab, top_k, false);
+  if (L.total > EAGLE_NOALLOC_SCRATCH_BYTES) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  const eagle_status st = noalloc_scratch(&ws);
+  if (st != EAGLE_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // header (error word) and the per-row / per-item arrival counters must
+  // start at zero; the records behind them are written before they are read
+  EAGLE_CUDA(cudaMemsetAsync(ws, 0, L.off_pieces, s));
+  return build_impl(1, &draft_logits, row_stride, n_rows, vocab, top_k, depth, total_tokens,
+                    &root_token, &out, ws, EAGLE_NOALLOC_SCRATCH_BYTES, s);
 }

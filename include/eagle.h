@@ -22,7 +22,8 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers unless marked "host".  The
  *     caller owns every buffer, including the workspace `ws`; the library
- *     allocates nothing and keeps no global state.
+ *     allocates nothing and keeps no global state (one exception: the
+ *     fixed static scratch of eagle_tree_build_noalloc).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream); nothing synchronises with the host.  Calls on one stream run
  *     in order; two calls that share a workspace must not overlap.
@@ -157,6 +158,38 @@ eagle_status eagle_tree_build_batched(int32_t n_items, const float* const* draft
                                       int32_t top_k, int32_t depth, int32_t total_tokens,
                                       const int32_t* root_tokens, const eagle_tree* outs,
                                       void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_build_noalloc -- the paper has no counterpart: this is a
+ * deployment variant of eagle_tree_build for callers that cannot hand the
+ * library device memory (no allocator reachable at the call site, or a
+ * runtime that forbids allocation while it runs).  Same computation, same
+ * arguments and same output as eagle_tree_build, without `ws`.
+ *
+ * Scratch: a fixed array of EAGLE_NOALLOC_SCRATCH_BYTES in the library's own
+ * static device memory (one per device, located once per device on first
+ * use) -- the one piece of global state in the library.  The call allocates
+ * nothing (no cudaMalloc / cudaFree / allocating library routine); it clears
+ * the scratch's header and counters on `stream` before its launch, so stale
+ * contents from an earlier call (even one that recorded a device error) do
+ * not matter.  Every call on a device shares that array: calls that overlap
+ * on the GPU (different streams without ordering, or concurrent host
+ * threads) race and give undefined results.  Device-side errors are recorded
+ * in the shared scratch and are not reported.
+ * Limit: the stream workspace of the shape,
+ *   eagle_tree_build_workspace_size(1, n_rows, vocab, top_k, depth, m),
+ *   must fit in EAGLE_NOALLOC_SCRATCH_BYTES; larger shapes return
+ *   EAGLE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The size
+ *   grows with R = 1 + (depth-1)*top_k rows and with top_k (about
+ *   17 * R * (16 + 8*top_k) bytes): every shape with top_k <= 10 fits;
+ *   e.g. top_k 12, depth 13 does not (277,248 bytes).
+ * ------------------------------------------------------------------------ */
+#define EAGLE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+
+eagle_status eagle_tree_build_noalloc(const float* draft_logits, int64_t row_stride,
+                                      int32_t n_rows, int32_t vocab, int32_t top_k,
+                                      int32_t depth, int32_t total_tokens, int32_t root_token,
+                                      eagle_tree out, eagle_stream stream);
 
 /* ------------------------------------------------------------------------
  * eagle_tree_attn -- [blog] "Single-Pass Tree Verification" (a tree token
