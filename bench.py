@@ -300,6 +300,17 @@ def _time_e2e(torch, step, s, flush, K):
     return times, d2h
 
 
+def max_over_ranks(x, world, device):
+    """Slowest replica's value: the job's step time is set by the last rank
+    to finish (all ranks run the same workload on their own GPU)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # known ncu DRAM traffic per launch (bytes), keyed by kernel and source hash;
 # entries whose hash no longer matches the sources are reported as null
 TRAFFIC = {}
@@ -351,11 +362,7 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.1)
     sampler.stop()
 
-    us = statistics.mean(times)
-    if world > 1:
-        t = torch.tensor([us], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        us = float(t.item())
+    us = max_over_ranks(statistics.mean(times), world, dev)
     hbm, tf, tf_sus, peak_src = _peaks()
     k_us = {k: statistics.mean(v) for k, v in per.items()}
     attn_gbs = step.bytes_attn() / (k_us["attn"] * 1e-6) / 1e9
