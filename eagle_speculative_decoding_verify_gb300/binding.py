@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape",
                 6: "device invariant violated"}
 EAGLE_F32 = 0
 EAGLE_BF16 = 1
-EAGLE_NOALLOC_SCRATCH_BYTES = 256 * 1024   # include/eagle.h
+EAGLE_NOALLOC_SCRATCH_BYTES = 16 * 1024   # include/eagle.h
 MAX_TOP_K = 64
 MAX_DEPTH = 16
 MAX_CANDIDATES = 2048

@@ -7,21 +7,31 @@
 // The m tree queries of one KV head times its g query heads form the M
 // dimension (row R = i*g + head-in-group), so the g heads that share a KV
 // head share every K/V byte.  One CTA = (item, kv head, pair of 128-row
-// query tiles, KV split) and runs warp-specialised:
-//   warp 0      TMA producer: K and V chunks of 128 keys (prefix from the
-//               cache tensor map, then the tree keys) into a 3-slot ring of
+// query tiles, split).  Splits 0..n-2 each take a contiguous span of prefix
+// chunks (128 keys); the last split takes the tree keys only (a CTA of its
+// own, so the masked chunk with its two P fills is off the prefix critical
+// path).  Warp-specialised:
+//   warp 0      TMA producer: K and V chunks into a 5-slot ring of
 //               128-byte-swizzled shared-memory tiles.
 //   warp 1      tensor-memory owner and MMA issuer: S_t = Q_t K^T (M 128,
-//               N 128, K = head_dim) and O_t += P_t V (M 128, N = head_dim,
-//               K 128) with tcgen05.mma kind::f16, fp32 accumulators in
-//               tensor memory (S_0, S_1, O_0, O_1 = 512 columns).
+//               N 128, K = head_dim, A and B from shared memory) and
+//               O_t += P_t V (M 128, N = head_dim, K 128, A = P from tensor
+//               memory) with tcgen05.mma kind::f16, fp32 accumulators in
+//               tensor memory (S_0, S_1, O_0, O_1 = 512 columns).  The MMAs
+//               of a thread run in issue order, so PV_t(j) has read P_t(j)
+//               before S_t(j+1) overwrites those columns, and the completion
+//               of S_t(j+1) implies that of PV_t(j).
 //   warps 4-7   softmax for tile 0, warps 8-11 for tile 1: one thread per
 //   / 8-11      query row reads its S row from tensor memory, applies scale,
 //               the prefix bound and the ancestor mask, updates the running
 //               max / sum (O rescaled in tensor memory only when the max
-//               grows by more than 2^8), writes P in bf16 to shared memory.
+//               grows by more than 2^8) and writes P as bf16 over the S
+//               columns it has read (32 keys -> 16 columns); for tree keys
+//               (few, possibly dominant) the bf16 rounding residual goes to
+//               the next 16 columns and a second MMA adds it, so that O
+//               accumulates P to ~2^-17.
 // The epilogue writes the normalised row (one split) or an unnormalised
-// partial (o, max, sum) that attn_merge_kernel combines.  Every mbarrier
+// partial (o, max, sum) that attn_tc_merge_kernel combines.  Every mbarrier
 // wait is bounded; on a timeout the CTA records the error, drains its own
 // copies and MMAs, frees tensor memory and returns.
 #include <cuda.h>
@@ -40,7 +50,7 @@ namespace eagle {
 constexpr int kTcMaxItems = 16;     // items per launch (tensor maps live in the params)
 constexpr int kTcThreads = 384;     // 12 warps
 constexpr int kChunk = 128;         // keys per K/V chunk
-constexpr int kSlots = 3;           // K/V ring depth
+constexpr int kSlots = 5;           // K/V ring depth
 constexpr uint32_t kTmemCols = 512;
 
 struct TcItem {
@@ -48,7 +58,7 @@ struct TcItem {
   float* out;
   const uint64_t* mask;
   int m, prefix_len, splits, tile_pairs, unit_start;
-  int64_t part_start;
+  int64_t part_start;   // first partial unit of the item (units of 256 rows)
 };
 
 struct TcParams {
@@ -59,21 +69,21 @@ struct TcParams {
   TcItem items[kTcMaxItems];
   int n_items, hq, hkv, g, span_chunks, total_units;
   float scale_log2;
-  float* partials;
+  float* part_o;     // [unit][256 rows][D]
+  float2* part_ml;   // [unit][256 rows] (max in log2 units, sum)
   int32_t* err;
 };
 
 template <int D>
 struct TcSmem {
   static constexpr int kTileBytes = 128 * D * 2;      // one 128-row bf16 tile of width D
-  static constexpr int kPBytes = 128 * kChunk * 2;    // P tile: 128 rows x 128 keys
   static constexpr int kQ = 0;
-  static constexpr int kP = kQ + 2 * kTileBytes;
-  static constexpr int kRing = kP + 2 * kPBytes;
+  static constexpr int kRing = kQ + 2 * kTileBytes;
   static constexpr int kBars = kRing + kSlots * kTileBytes;
   static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
 };
+static_assert(TcSmem<128>::kAlloc <= 232448, "shared memory of the tensor-core kernel");
 
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* err,
                                              volatile int* abort_flag, int where) {
@@ -115,11 +125,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const int g = P.g;
   const int M = it.m * g;
   const int n_tiles = (M - 256 * tp) > 128 ? 2 : 1;
+  const bool tree_split = split == it.splits - 1;
   const int split_start = split * P.span_chunks * kChunk;
-  const int split_end = min(it.prefix_len, split_start + P.span_chunks * kChunk);
+  const int split_end = tree_split ? 0 : min(it.prefix_len, split_start + P.span_chunks * kChunk);
   const int n_pref = split_end > split_start ? (split_end - split_start + kChunk - 1) / kChunk : 0;
-  const bool last_split = split == it.splits - 1;
-  const int n_chunks = n_pref + (last_split ? (it.m + kChunk - 1) / kChunk : 0);
+  const int n_chunks = n_pref + (tree_split ? (it.m + kChunk - 1) / kChunk : 0);
 
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   __syncthreads();   // barriers initialised, tensor memory allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_S = tmem;               // S_t at column 128 t
+  const uint32_t tmem_S = tmem;               // S_t at column 128 t (P_t aliases it)
   const uint32_t tmem_O = tmem + 256;         // O_t at column 256 + D t
 
   // ---- Q tiles -> shared memory (128-byte swizzle), mask rows -> registers;
@@ -159,7 +169,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   const int wg = warp >= 4 ? (warp - 4) >> 2 : -1;   // softmax warpgroup = query tile
   const int row = (warp & 3) * 32 + lane;            // row within the tile = TMEM lane
   const int R = 256 * tp + 128 * (wg < 0 ? 0 : wg) + row;
-  uint64_t mrow[4] = {~0ull, ~0ull, ~0ull, ~0ull};
   if (wg >= 0) {
     uint8_t* qt = smem + L::kQ + wg * L::kTileBytes;
     const bool valid = R < M;
@@ -170,12 +179,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     int4 qv[D / 8];
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) qv[c] = valid ? __ldg(src + c) : make_int4(0, 0, 0, 0);
-    if (valid) {
-      const int W = (it.m + 63) >> 6;
-      const uint64_t* mr = it.mask + static_cast<int64_t>(qi) * W;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) mrow[w] = w < W ? __ldg(mr + w) : 0ull;
-    }
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {   // 16-byte chunks of the row
       const int half = c >> 3, cc = c & 7;
@@ -221,7 +224,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kChunk, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       const uint32_t q_base = smem_addr(smem + L::kQ);
-      const uint32_t p_base = smem_addr(smem + L::kP);
       const uint32_t ring_base = smem_addr(smem + L::kRing);
       auto issue_s = [&](int t, int slot) {   // S_t = Q_t K^T
         const uint32_t qa = q_base + t * L::kTileBytes;
@@ -233,16 +235,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                    smem_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int slot, bool acc) {   // O_t += P_t V
-        const uint32_t pa = p_base + t * L::kPBytes;
+      auto issue_pv = [&](int t, int slot, int fill, bool acc) {   // O_t += P_t V
+        // keys 16kk.. : columns 32 (kk/2) + 16 fill + 8 (kk%2) of S_t (bf16 pairs)
+        const uint32_t pa = tmem_S + 128 * t + 16 * fill;
         const uint32_t vb = ring_base + slot * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          const uint32_t boff = kk * 2048;   // 16 keys = two 8-row groups
-          mma_bf16(tmem_O + D * t, smem_desc_sw128(pa + aoff, 16, 1024),
-                   smem_desc_sw128(vb + boff, 128 * 128, 1024), idesc_o, (acc || kk > 0));
-        }
+        for (int kk = 0; kk < kChunk / 16; ++kk)
+          mma_bf16_ta(tmem_O + D * t, pa + 32 * (kk >> 1) + 8 * (kk & 1),
+                      smem_desc_sw128(vb + kk * 2048, 128 * 128, 1024), idesc_o, (acc || kk > 0));
       };
       bool ok = n_chunks > 0 && bounded_wait(q_ready, 0, P.err, abort_flag, 29) &&
                 bounded_wait(&full[0], 0, P.err, abort_flag, 30);
@@ -254,7 +254,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         }
         mma_commit(&empty[0]);
       }
-      int fseq = 0;   // P fills consumed so far (per tile; every tile has the same schedule)
       for (int j = 0; ok && j < n_chunks; ++j) {
         const int nv = 2 * j + 1, nk = 2 * j + 2;
         const int vslot = nv % kSlots, kslot = nk % kSlots;
@@ -262,14 +261,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         if (!bounded_wait(&full[vslot], (nv / kSlots) & 1, P.err, abort_flag, 31)) break;
         tc_fence_after();
         const bool more = j + 1 < n_chunks;
-        for (int t = 0; t < n_tiles && ok; ++t) {
-          for (int f = 0; f < nf; ++f) {
-            if (!bounded_wait(&p_full[t], (fseq + f) & 1, P.err, abort_flag, 32)) { ok = false; break; }
-            tc_fence_after();
-            issue_pv(t, vslot, j > 0 || f > 0);
-            mma_commit(&o_done[t]);
-          }
-          if (!ok) break;
+        for (int t = 0; t < n_tiles; ++t) {
+          if (!bounded_wait(&p_full[t], j & 1, P.err, abort_flag, 32)) { ok = false; break; }
+          tc_fence_after();
+          for (int f = 0; f < nf; ++f) issue_pv(t, vslot, f, j > 0 || f > 0);
+          mma_commit(&o_done[t]);
           if (more) {
             if (t == 0) {
               if (!bounded_wait(&full[kslot], (nk / kSlots) & 1, P.err, abort_flag, 33)) { ok = false; break; }
@@ -280,7 +276,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           }
         }
         if (!ok) break;
-        fseq += nf;
         if (more) mma_commit(&empty[kslot]);
         mma_commit(&empty[vslot]);
       }
@@ -294,12 +289,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem_S + 128 * t + lane_off;
     const uint32_t o_addr = tmem_O + D * t + lane_off;
-    uint8_t* pt = smem + L::kP + t * L::kPBytes;
     const float sl2 = P.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    int fseq = 0;   // P fills produced so far
     for (int j = 0; j < n_chunks; ++j) {
+      // S_t(j) done implies PV_t(j-1) done: P and O may be touched
       if (!bounded_wait(&s_full[t], j & 1, P.err, abort_flag, 40)) { ok = false; break; }
       tc_fence_after();
       // key validity: only the last prefix chunk of a split and the tree
@@ -308,8 +302,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       const int nvalid = pref ? min(kChunk, split_end - (split_start + j * kChunk)) : 0;
       const bool masked = !pref || nvalid < kChunk;
       const int t0 = pref ? 0 : (j - n_pref) * kChunk;
-      const uint64_t wlo = t0 == 0 ? mrow[0] : mrow[2];
-      const uint64_t whi = t0 == 0 ? mrow[1] : mrow[3];
+      // ancestor mask words of this row for the chunk's 128 tree keys
+      uint64_t wlo = ~0ull, whi = ~0ull;
+      if (!pref) {
+        wlo = whi = 0ull;
+        if (R < M) {
+          const int W = (it.m + 63) >> 6;
+          const uint64_t* mr = it.mask + static_cast<int64_t>(R / g) * W + (t0 >> 6);
+          wlo = __ldg(mr);
+          if ((t0 >> 6) + 1 < W) whi = __ldg(mr + 1);
+        }
+      }
       const int nt = pref ? nvalid : it.m - t0;   // keys present in this chunk
       // load 64 columns of S (two 32-column loads, one wait); mask if needed
       auto load64 = [&](int half, float (&v)[64]) {
@@ -346,9 +349,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
       }
       mx *= sl2;   // scale > 0: max of the scaled row
-      // previous PV of this tile must be done before P is overwritten / O rescaled
-      if (fseq > 0 && !bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 41)) { ok = false; break; }
-      tc_fence_after();
       const float m_new = fmaxf(m_run, mx);
       const bool grow = (j == 0) || (m_new > m_run + 8.0f);
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
@@ -362,84 +362,99 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
           tmem_st32(o_addr + 32 * c, r);
         }
-        tmem_wait_st();
         if (grow) l_run *= f;
       }
       if (grow) m_run = m_new;
       const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-      // P = 2^(s sl2 - m) in bf16 -> shared memory (K-major, 128-byte swizzle).
-      // Tree keys (few, possibly dominant) get a second fill with the bf16
-      // rounding residual, so that O accumulates hi + lo ~ P to 2^-17.
-      const int nf = pref ? 1 : 2;
-#pragma unroll 1
-      for (int f = 0; f < nf; ++f) {
-        if (f == 1) {
-          if (!bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 43)) { ok = false; break; }
-          tc_fence_after();
-        }
-        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float v[64];
-          load64(half, v);
+      // P = 2^(s sl2 - m) in bf16 over the S columns just read: keys
+      // 32q..32q+31 -> columns 32q..32q+15 (key pairs per column); tree
+      // chunks write the rounding residual to columns 32q+16..32q+31.
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!masked) {
+        // full prefix chunk: the next quarter's S load is in flight while
+        // this one is computed
+        auto fill = [&](int q, const uint32_t (&ra)[32]) {
+          uint32_t hi[16];
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            float pv = ex2(fmaf(v[e], sl2, -mref));
-            ls[e & 7] += pv;
-            if (f == 1) pv -= __bfloat162float(__float2bfloat16_rn(pv));
-            v[e] = pv;
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(__uint_as_float(ra[2 * e]), sl2, -mref));
+            const float p1 = ex2(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -mref));
+            ls[e & 3] += p0 + p1;
+            hi[e] = pack_bf16x2(p0, p1);
           }
+          tmem_st16(s_addr + 32 * q, hi);
+        };
+        uint32_t qa[32], qb[32];
+        tmem_ld32(s_addr, qa);
+        tmem_wait_ld();
+        tmem_ld32(s_addr + 32, qb);
+        fill(0, qa);
+        tmem_wait_ld();
+        tmem_ld32(s_addr + 64, qa);
+        fill(1, qb);
+        tmem_wait_ld();
+        tmem_ld32(s_addr + 96, qb);
+        fill(2, qa);
+        tmem_wait_ld();
+        fill(3, qb);
+      } else {
+        // masked chunk (tree keys, or the ragged end of a split): invisible
+        // keys get P = 0; tree keys also get the bf16 rounding residual
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          uint32_t ra[32];
+          tmem_ld32(s_addr + 32 * q, ra);
+          tmem_wait_ld();
+          const uint64_t w = q < 2 ? wlo : whi;
+          uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {   // 16-byte chunks of 8 keys
-            const uint4 w = make_uint4(pack_bf16x2(v[8 * cc + 0], v[8 * cc + 1]),
-                                       pack_bf16x2(v[8 * cc + 2], v[8 * cc + 3]),
-                                       pack_bf16x2(v[8 * cc + 4], v[8 * cc + 5]),
-                                       pack_bf16x2(v[8 * cc + 6], v[8 * cc + 7]));
-            *reinterpret_cast<uint4*>(pt + half * (128 * 128) + row * 128 +
-                                      ((cc ^ (row & 7)) << 4)) = w;
+          for (int e = 0; e < 16; ++e) {
+            float s0 = __uint_as_float(ra[2 * e]), s1 = __uint_as_float(ra[2 * e + 1]);
+            const int c0 = 32 * q + 2 * e;
+            const int b0 = (32 * (q & 1)) + 2 * e;   // bit of key c0 in its mask word
+            if (!(c0 < nt && (pref || ((w >> b0) & 1ull)))) s0 = -INFINITY;
+            if (!(c0 + 1 < nt && (pref || ((w >> (b0 + 1)) & 1ull)))) s1 = -INFINITY;
+            const float p0 = ex2(fmaf(s0, sl2, -mref));
+            const float p1 = ex2(fmaf(s1, sl2, -mref));
+            ls[e & 3] += p0 + p1;
+            hi[e] = pack_bf16x2(p0, p1);
+            const float r0 = p0 - __uint_as_float(hi[e] << 16);
+            const float r1 = p1 - __uint_as_float(hi[e] & 0xffff0000u);
+            lo[e] = pack_bf16x2(r0, r1);
           }
+          tmem_st16(s_addr + 32 * q, hi);
+          if (!pref) tmem_st16(s_addr + 32 * q + 16, lo);
         }
-        if (f == 0) l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[t]);
-        ++fseq;
       }
-      if (!ok) break;
+      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    // ---- epilogue
-    if (ok && fseq > 0 && bounded_wait(&o_done[t], (fseq - 1) & 1, P.err, abort_flag, 42)) {
+    // ---- epilogue: the last PV of this tile
+    if (ok && n_chunks > 0 && bounded_wait(&o_done[t], (n_chunks - 1) & 1, P.err, abort_flag, 42)) {
       tc_fence_after();
       const bool valid = R < M;
       const int qi = valid ? R / g : 0, hl = valid ? R - qi * g : 0;
       const int64_t orow = static_cast<int64_t>(qi) * P.hq + kvh * g + hl;
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const int Mpad = it.tile_pairs * 256;
-      float* part = P.partials + it.part_start +
-                    static_cast<int64_t>(kvh * it.splits + split) * (D + 2) * Mpad + R;
-#pragma unroll
+      const int64_t punit = it.part_start + static_cast<int64_t>(kvh * it.tile_pairs + tp) * it.splits + split;
+      float* po = P.part_o + (punit * 256 + (R - 256 * tp)) * D;
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(o_addr + 32 * c, r);
         tmem_wait_ld();
-        if (it.splits == 1) {
-          if (!valid) continue;
-          float4* dst = reinterpret_cast<float4*>(it.out + orow * D + 32 * c);
+        if (!valid) continue;
+        float4* dst = reinterpret_cast<float4*>((it.splits == 1 ? it.out + orow * D : po) + 32 * c);
+        const float sc = it.splits == 1 ? inv : 1.f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                                 __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
-        } else {
-          // lanes hold consecutive rows: every store covers 128 contiguous bytes
-#pragma unroll
-          for (int e = 0; e < 32; ++e) part[static_cast<int64_t>(32 * c + e) * Mpad] = __uint_as_float(r[e]);
-        }
+        for (int e = 0; e < 8; ++e)
+          dst[e] = make_float4(__uint_as_float(r[4 * e]) * sc, __uint_as_float(r[4 * e + 1]) * sc,
+                               __uint_as_float(r[4 * e + 2]) * sc, __uint_as_float(r[4 * e + 3]) * sc);
       }
-      if (it.splits > 1) {
-        part[static_cast<int64_t>(D) * Mpad] = m_run;
-        part[static_cast<int64_t>(D + 1) * Mpad] = l_run;
-      }
+      if (valid && it.splits > 1) P.part_ml[punit * 256 + (R - 256 * tp)] = make_float2(m_run, l_run);
     }
   }
 
@@ -450,66 +465,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Split merge for the tensor-core partial layout [kvh][split][D + 2][Mpad].
-// One CTA (4 warps) per (item, kv head, 32 query rows, 32 output columns):
-// lanes are rows, so every partial load is a coalesced 128-byte line; warp w
-// accumulates columns 8w..8w+7 of the group over all splits; the 32 x 32
-// result goes out row by row through a shared-memory transpose.
+// Split merge: one thread per (row, 4 output columns) of every 256-row tile
+// pair of every kv head, online over the splits (running max in log2 units);
+// partial and output rows are read and written as contiguous float4 runs.
 struct TcMergeParams {
   TcItem items[kTcMaxItems];
   int block_start[kTcMaxItems + 1];   // first block of each item
   int n_items, hq, hkv, g;
-  const float* partials;
+  const float* part_o;
+  const float2* part_ml;
 };
 
 template <int D>
-__global__ void __launch_bounds__(128) attn_tc_merge_kernel(const __grid_constant__ TcMergeParams P) {
-  __shared__ float tr[32][33];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcMergeParams P) {
+  constexpr int kCols4 = D / 4;                 // threads per row
+  constexpr int kRows = 256 / kCols4;           // rows per block
   int item = 0;
   while (item + 1 < P.n_items && static_cast<int>(blockIdx.x) >= P.block_start[item + 1]) ++item;
   const TcItem& it = P.items[item];
-  if (it.splits == 1) return;
-  const int Mpad = it.tile_pairs * 256;
-  const int rgroups = Mpad / 32;
-  int b = blockIdx.x - P.block_start[item];
-  const int cg = b % (D / 32);
-  b /= D / 32;
-  const int rg = b % rgroups;
-  const int kvh = b / rgroups;
-  const int R0 = rg * 32, R = R0 + lane;
-  const int c0 = cg * 32 + warp * 8;
-  const int M = it.m * P.g;
   const int S = it.splits;
-  const float* base = P.partials + it.part_start + static_cast<int64_t>(kvh) * S * (D + 2) * Mpad + R;
-  float mmax = -INFINITY;
-  for (int s = 0; s < S; ++s)
-    mmax = fmaxf(mmax, __ldcg(base + (static_cast<int64_t>(s) * (D + 2) + D) * Mpad));
-  float L = 0.f;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int b = blockIdx.x - P.block_start[item];
+  const int blocks_per_pair = 256 / kRows;
+  const int pair = b / blocks_per_pair;         // kvh * tile_pairs + tp
+  const int kvh = pair / it.tile_pairs, tp = pair - kvh * it.tile_pairs;
+  const int r = (b - pair * blocks_per_pair) * kRows + threadIdx.x / kCols4;   // row in the pair
+  const int c4 = threadIdx.x % kCols4;
+  const int Rg = 256 * tp + r;
+  if (Rg >= it.m * P.g) return;
+  const int64_t u0 = it.part_start + static_cast<int64_t>(pair) * S;
+  float mx = -INFINITY, l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
   for (int s = 0; s < S; ++s) {
-    const float* ps = base + static_cast<int64_t>(s) * (D + 2) * Mpad;
-    const float ms = __ldcg(ps + static_cast<int64_t>(D) * Mpad);
-    const float ls = __ldcg(ps + static_cast<int64_t>(D + 1) * Mpad);
-    float o[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = __ldcg(ps + static_cast<int64_t>(c0 + e) * Mpad);
-    const float ws = ms == -INFINITY ? 0.f : ex2(ms - mmax);
-    L = fmaf(ws, ls, L);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws, o[e], acc[e]);
+    const float2 ml = __ldcg(P.part_ml + (u0 + s) * 256 + r);
+    const float4 o = __ldcg(reinterpret_cast<const float4*>(P.part_o + ((u0 + s) * 256 + r) * D) + c4);
+    const float mn = fmaxf(mx, ml.x);
+    const float a = mx == -INFINITY ? 0.f : ex2(mx - mn);
+    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - mn);
+    acc = make_float4(acc.x * a + w * o.x, acc.y * a + w * o.y, acc.z * a + w * o.z,
+                      acc.w * a + w * o.w);
+    l = l * a + w * ml.y;
+    mx = mn;
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) tr[lane][warp * 8 + e] = acc[e] * inv;
-  __syncthreads();
-  for (int r = warp; r < 32; r += 4) {   // row R0 + r: lanes write 32 consecutive columns
-    const int Rr = R0 + r;
-    if (Rr < M) {
-      const int qi = Rr / P.g, hl = Rr - qi * P.g;
-      it.out[(static_cast<int64_t>(qi) * P.hq + kvh * P.g + hl) * D + cg * 32 + lane] = tr[r][lane];
-    }
-  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int qi = Rg / P.g, hl = Rg - qi * P.g;
+  reinterpret_cast<float4*>(it.out + (static_cast<int64_t>(qi) * P.hq + kvh * P.g + hl) * D)[c4] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 // ------------------------------------------------------------------ host
@@ -549,11 +550,13 @@ struct TcPlan {
   int splits[kTcMaxItems];
   int tile_pairs[kTcMaxItems];
   int units;
-  int64_t part_floats;
+  int64_t part_units;   // 256-row partial blocks
 };
 
-// Choose the KV span (chunks per CTA) that minimises waves x (span + 2),
-// the +2 standing for the per-CTA fixed work (Q tiles, tree chunk, epilogue).
+// Splits per (kv head, tile pair): ceil(prefix chunks / span) prefix splits
+// plus one tree split.  The span minimises waves x (span + 2) -- the +2 for a
+// CTA's fixed work (Q tiles, epilogue) -- plus a small charge per CTA for its
+// partial's write and read.
 static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int d) {
   TcPlan T;
   memset(&T, 0, sizeof(T));
@@ -563,16 +566,16 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
     T.tile_pairs[b] = (items[b].m * g + 255) / 256;
     max_nc = std::max(max_nc, (items[b].prefix_len + kChunk - 1) / kChunk);
   }
-  int64_t best_cost = -1;
+  double best_cost = -1.0;
   for (int span = 1; span <= max_nc; ++span) {
     int64_t total = 0;
     for (int b = 0; b < n; ++b) {
       const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
-      total += static_cast<int64_t>(hkv) * T.tile_pairs[b] * std::max(1, (nc + span - 1) / span);
+      total += static_cast<int64_t>(hkv) * T.tile_pairs[b] * ((nc + span - 1) / span + 1);
     }
     const int64_t waves = (total + kPlanSMs - 1) / kPlanSMs;
-    const int64_t cost = waves * (span + 2);
-    if (best_cost < 0 || cost <= best_cost) {
+    const double cost = static_cast<double>(waves * (span + 2)) + 0.05 * static_cast<double>(total);
+    if (best_cost < 0.0 || cost <= best_cost) {
       best_cost = cost;
       T.span = span;
     }
@@ -580,14 +583,19 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
   int64_t units = 0, part = 0;
   for (int b = 0; b < n; ++b) {
     const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
-    T.splits[b] = std::max(1, (nc + T.span - 1) / T.span);
+    T.splits[b] = (nc + T.span - 1) / T.span + 1;
     units += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
-    if (T.splits[b] > 1)
-      part += static_cast<int64_t>(hkv) * T.splits[b] * (d + 2) * T.tile_pairs[b] * 256;
+    if (T.splits[b] > 1) part += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
   }
   T.units = static_cast<int>(units);
-  T.part_floats = part;
+  T.part_units = part;
+  (void)d;
   return T;
+}
+
+static size_t part_bytes(const TcPlan& T, int d) {
+  return align_up(sizeof(float) * static_cast<size_t>(T.part_units) * 256 * d, 256) +
+         align_up(sizeof(float2) * static_cast<size_t>(T.part_units) * 256, 256);
 }
 
 int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d) {
@@ -595,7 +603,7 @@ int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, i
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
     const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d);
-    count += 1 + (T.part_floats > 0 ? 1 : 0);
+    count += 1 + (T.part_units > 0 ? 1 : 0);
   }
   return count;
 }
@@ -605,7 +613,7 @@ size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
     const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d);
-    need = std::max(need, align_up(kWsHeader + sizeof(float) * static_cast<size_t>(T.part_floats), 256));
+    need = std::max(need, kWsHeader + part_bytes(T, d));
   }
   return need;
 }
@@ -618,8 +626,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     const int nb = std::min(kTcMaxItems, n - b0);
     const eagle_attn_item* its = items + b0;
     const TcPlan T = plan_tc(its, nb, hq, hkv, D);
-    if (ws_bytes < align_up(kWsHeader + sizeof(float) * static_cast<size_t>(T.part_floats), 256))
-      return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < kWsHeader + part_bytes(T, D)) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
     TcParams P;
     memset(&P, 0, sizeof(P));
     int64_t units = 0, part = 0;
@@ -645,8 +652,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       ti.unit_start = static_cast<int>(units);
       ti.part_start = part;
       units += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
-      if (T.splits[b] > 1)
-        part += static_cast<int64_t>(hkv) * T.splits[b] * (D + 2) * T.tile_pairs[b] * 256;
+      if (T.splits[b] > 1) part += static_cast<int64_t>(hkv) * T.tile_pairs[b] * T.splits[b];
     }
     P.n_items = nb;
     P.hq = hq;
@@ -656,7 +662,10 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     P.total_units = static_cast<int>(units);
     P.scale_log2 = (scale != 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D))) * 1.4426950408889634f;
     P.err = static_cast<int32_t*>(ws);
-    P.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+    char* pbase = static_cast<char*>(ws) + kWsHeader;
+    P.part_o = reinterpret_cast<float*>(pbase);
+    P.part_ml = reinterpret_cast<float2*>(
+        pbase + align_up(sizeof(float) * static_cast<size_t>(T.part_units) * 256 * D, 256));
     const size_t smem = TcSmem<D>::kAlloc;
     EAGLE_CUDA(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem)));
@@ -666,19 +675,21 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     if (part > 0) {
       TcMergeParams MP;
       memset(&MP, 0, sizeof(MP));
+      constexpr int kRows = 256 / (D / 4);
       int blocks = 0;
       for (int b = 0; b < nb; ++b) {
         MP.items[b] = P.items[b];
         MP.block_start[b] = blocks;
-        blocks += hkv * P.items[b].tile_pairs * 8 * (D / 32);   // 32 rows x 32 columns each
+        if (P.items[b].splits > 1) blocks += hkv * P.items[b].tile_pairs * (256 / kRows);
       }
       MP.block_start[nb] = blocks;
       MP.n_items = nb;
       MP.hq = hq;
       MP.hkv = hkv;
       MP.g = hq / hkv;
-      MP.partials = P.partials;
-      attn_tc_merge_kernel<D><<<blocks, 128, 0, stream>>>(MP);
+      MP.part_o = P.part_o;
+      MP.part_ml = P.part_ml;
+      attn_tc_merge_kernel<D><<<blocks, 256, 0, stream>>>(MP);
       if ((st = launch_status()) != EAGLE_OK) return st;
     }
   }

@@ -7,14 +7,14 @@
 // Decoding in llama.cpp", reply on the dynamic tree (node value = draft
 // confidence, tree grown per drafting step and pruned at the end).
 //
-// Phase 1 (all CTAs, eagle_rowstream.cuh): one HBM pass over the R draft
-// rows -> per row the top_k (value desc, token id asc) and logsumexp.
-// Phase 2 (the CTA that finalizes an item's last row): candidate values
+// Phase 1 (one cluster per row, eagle_rowstream.cuh): one HBM pass over the
+// R draft rows -> per row the top_k (value desc, token id asc) and logsumexp.
+// Phase 2 (the CTA whose row of an item arrives last): candidate values
 // value = parent value + (logit - logsumexp), in fp64; per depth the top_k
-// frontier (ranks by binary search over the per-slot sorted child lists);
-// final best m-1 by an MSB radix select on order-preserving 64-bit keys
-// (ties -> lower candidate index); node ids by a block scan; ancestor mask
-// by walking parent pointers (depth <= 16).
+// frontier; the final best m-1 -- both by ranks across the sorted child lists
+// (binary search on order-preserving 64-bit keys, ties -> lower candidate
+// index); node ids by a block scan; ancestor mask by walking parent pointers
+// (depth <= 16).
 #include <mutex>
 
 #include "eagle_stream_host.h"
@@ -52,35 +52,34 @@ static __device__ __noinline__ int block_excl_scan(int v, int* warp_tot, int& to
 }
 
 static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int k = A.top_k, D = A.depth, m = A.total_tokens, C = A.n_cand;
   const int R = 1 + (D - 1) * k;
+  const int kk = k * k;
   const int rk = A.rs.rec_k;
   const int rb = rec_bytes(rk);
   char* rows = A.rs.rows + static_cast<int64_t>(item) * A.rs.rows_per_item * rb;
   const eagle_tree out = A.out[item];
 
-  // scratch carved from the (now idle) stream state after S.done_items;
-  // every array starts on a 16-byte boundary (<= 78 KB for C <= 2048)
-  char* p = reinterpret_cast<char*>(S.buf);
+  // scratch carved from the (now idle) ring and warp buffers; every array
+  // starts on a 16-byte boundary (<= 77 KB for C <= 2048; R k = C)
+  char* p = reinterpret_cast<char*>(S.ring);
   auto carve = [&p](size_t bytes) {
     char* q = p;
     p += align_up(bytes, 16);
     return q;
   };
-  double* val = reinterpret_cast<double*>(carve(sizeof(double) * C));
-  uint64_t* key = reinterpret_cast<uint64_t*>(carve(sizeof(uint64_t) * C));
+  uint64_t* key = reinterpret_cast<uint64_t*>(carve(sizeof(uint64_t) * C));  // value as order key
   double* lse = reinterpret_cast<double*>(carve(sizeof(double) * R));
-  float* rv = reinterpret_cast<float*>(carve(sizeof(float) * R * k));   // row top-k logits
-  int* ri = reinterpret_cast<int*>(carve(sizeof(int) * R * k));         // row top-k tokens
+  float* rv = reinterpret_cast<float*>(carve(sizeof(float) * C));   // row top-k logits
+  int* ri = reinterpret_cast<int*>(carve(sizeof(int) * C));         // row top-k tokens
   int* tok = reinterpret_cast<int*>(carve(sizeof(int) * C));
   int* par = reinterpret_cast<int*>(carve(sizeof(int) * C));
+  int* srt = reinterpret_cast<int*>(carve(sizeof(int) * C));    // candidates of each level, best first
+  int* lrank = reinterpret_cast<int*>(carve(sizeof(int) * C));  // rank of a candidate in its level
   int* node = reinterpret_cast<int*>(carve(sizeof(int) * C));
   int* npar = reinterpret_cast<int*>(carve(sizeof(int) * EAGLE_MAX_TREE));
-  int* fr = reinterpret_cast<int*>(carve(sizeof(int) * kKMax));
-  int* fr_next = reinterpret_cast<int*>(carve(sizeof(int) * kKMax));
-  int* hist = reinterpret_cast<int*>(carve(sizeof(int) * 256));
-  int* misc = reinterpret_cast<int*>(carve(sizeof(int) * 8));  // [0] digit, [1] count above
+  int* fr = reinterpret_cast<int*>(carve(sizeof(int) * 2 * kKMax));  // frontiers, by depth parity
   int* warp_tot = reinterpret_cast<int*>(carve(sizeof(int) * kWarps));
 
   // every row's statistics in one pass: logsumexp, top-k logits and tokens
@@ -88,178 +87,116 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
     const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rows + r * rb);
     lse[r] = static_cast<double>(h->max) + log_d(h->sum);
   }
-  for (int e = tid; e < R * k; e += kThreads) {
+  for (int e = tid; e < C; e += kThreads) {
     const int r = e / k, c = e - r * k;
     rv[e] = __ldcg(rec_val(rows + r * rb) + c);
     ri[e] = __ldcg(rec_idx(rows + r * rb, rk) + c);
   }
   __syncthreads();
-  auto row_logit = [&](int r, int c) { return rv[r * k + c]; };
-  auto row_token = [&](int r, int c) { return ri[r * k + c]; };
 
-  // depth 1: the root's top_k, rank order
+  // Candidates are compared on (value desc, candidate index asc), values as
+  // order-preserving integer keys.  Level 1 = candidates 0..k-1 (the root's
+  // top_k, already in order); level j >= 2 = candidates k + (j-2) k^2 ..
+  // + k^2 - 1, ranked by counting with every thread of a warp reading the
+  // same keys (broadcast, no bank conflicts).
   for (int c = tid; c < k; c += kThreads) {
-    val[c] = static_cast<double>(row_logit(0, c)) - lse[0];
-    tok[c] = row_token(0, c);
+    key[c] = order_key(static_cast<double>(rv[c]) - lse[0]);
+    tok[c] = ri[c];
     par[c] = -1;
     fr[c] = c;
+    srt[c] = c;
+    lrank[c] = c;
   }
   __syncthreads();
 
-  int level_base = 0;
+  // threads per candidate for the level ranks: a power of two <= 8
+  int tpc = kThreads / kk;
+  tpc = tpc >= 8 ? 8 : tpc >= 4 ? 4 : tpc >= 2 ? 2 : 1;
+  const int sub = tid & (tpc - 1);
+  const int stride = kThreads / tpc;
+  int base = k;   // first candidate of the level being built
   for (int l = 1; l < D; ++l) {
-    const int child_base = (l == 1) ? k : level_base + k * k;
-    for (int e = tid; e < k * k; e += kThreads) {
+    const int* fcur = fr + ((l - 1) & 1) * kKMax;
+    int* fnext = fr + (l & 1) * kKMax;
+    for (int e = tid; e < kk; e += kThreads) {
       const int s = e / k, c = e - s * k;
       const int r = 1 + (l - 1) * k + s;
-      const int a = child_base + e;
-      const int pa = fr[s];
-      val[a] = val[pa] + (static_cast<double>(row_logit(r, c)) - lse[r]);
-      tok[a] = row_token(r, c);
+      const int a = base + e;
+      const int pa = fcur[s];
+      key[a] = order_key(key_value(key[pa]) + (static_cast<double>(rv[r * k + c]) - lse[r]));
+      tok[a] = ri[r * k + c];
       par[a] = pa;
     }
     __syncthreads();
-    level_base = child_base;
-    if (l + 1 < D) {
-      // frontier of depth l+1: best k of the k sorted child lists, compared on
-      // order-preserving integer keys (ties -> lower candidate index)
-      for (int e = tid; e < k * k; e += kThreads) key[level_base + e] = order_key(val[level_base + e]);
-      __syncthreads();
-      for (int e = tid; e < k * k; e += kThreads) {
-        const int s = e / k, c = e - s * k;
-        const uint64_t v = key[level_base + e];
-        int rank = c;
-        for (int s2 = 0; s2 < k && rank < k; ++s2) {
-          if (s2 == s) continue;
-          const uint64_t* lst = key + level_base + s2 * k;
-          int lo = 0, hi = k;
-          if (s2 < s) {  // lower indices: entries with key >= v come first
-            while (lo < hi) {
-              const int mid = (lo + hi) >> 1;
-              if (lst[mid] >= v) lo = mid + 1; else hi = mid;
-            }
-          } else {
-            while (lo < hi) {
-              const int mid = (lo + hi) >> 1;
-              if (lst[mid] > v) lo = mid + 1; else hi = mid;
-            }
+    // full rank of every candidate within the level (tpc threads each)
+    const uint64_t* lk = key + base;
+    for (int e0 = 0; e0 < kk; e0 += stride) {
+      const int e = e0 + tid / tpc;
+      int cnt = 0;
+      if (e < kk) {
+        const uint64_t kv = lk[e];
+#pragma unroll 4
+        for (int f = sub; f < kk; f += tpc) {
+          const uint64_t o = lk[f];
+          cnt += ((o > kv) | ((o == kv) & (f < e))) ? 1 : 0;
+        }
+      }
+      for (int o = tpc >> 1; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if (e < kk && sub == 0) {
+        srt[base + cnt] = base + e;
+        lrank[base + e] = cnt;
+        if (cnt < k && l + 1 < D) fnext[cnt] = base + e;
+      }
+    }
+    __syncthreads();
+    base += kk;
+  }
+
+  // final rerank: the best need = m-1 of the C candidates.  Global rank =
+  // rank within the own level + entries of every other level before it
+  // (binary search in that level's sorted list).
+  const int need = m - 1;
+  for (int a = tid; a < C; a += kThreads) {
+    bool sel;
+    if (need <= 0) {
+      sel = false;
+    } else if (need >= C) {
+      sel = true;
+    } else {
+      int rank = lrank[a];
+      if (rank < need) {
+        const uint64_t kv = key[a];
+        const int la = a < k ? 0 : 1 + (a - k) / kk;
+        for (int j = 0; j < D && rank < need; ++j) {
+          if (j == la) continue;
+          const int lb = j == 0 ? 0 : k + (j - 1) * kk;
+          const int len = j == 0 ? k : kk;
+          const int* ls = srt + lb;
+          int lo = 0, hi = len;
+          const int steps = 32 - __clz(len);
+          for (int t = 0; t < steps; ++t) {
+            const bool act = lo < hi;
+            const int mid = (lo + hi) >> 1;
+            const int b = ls[act ? mid : 0];
+            const uint64_t o = key[b];
+            const bool go = act & ((o > kv) | ((o == kv) & (b < a)));
+            lo = go ? mid + 1 : lo;
+            hi = (act & !go) ? mid : hi;
           }
           rank += lo;
         }
-        if (rank < k) fr_next[rank] = level_base + e;
       }
-      __syncthreads();
-      for (int c = tid; c < k; c += kThreads) fr[c] = fr_next[c];
-      __syncthreads();
+      sel = rank < need;
     }
+    node[a] = sel ? 1 : 0;
   }
-
-  // final rerank: best need = m-1 of C candidates
-  const int need = m - 1;
-  uint64_t prefix = 0, pmask = 0;
-  int rem = need;
-  bool all_in = (need >= C);
-  if (need > 0 && !all_in) {
-    // skip the leading key bytes that every candidate shares
-    uint64_t kand = ~0ull, kor = 0ull;
-    for (int a = tid; a < C; a += kThreads) {
-      const uint64_t kv = order_key(val[a]);
-      key[a] = kv;
-      kand &= kv;
-      kor |= kv;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      kand &= __shfl_xor_sync(0xffffffffu, kand, o);
-      kor |= __shfl_xor_sync(0xffffffffu, kor, o);
-    }
-    uint64_t* red = reinterpret_cast<uint64_t*>(hist);   // 2 x kWarps words
-    if (lane == 0) {
-      red[warp] = kand;
-      red[kWarps + warp] = kor;
-    }
-    __syncthreads();
-    kand = ~0ull;
-    kor = 0ull;
-    for (int w = 0; w < kWarps; ++w) {
-      kand &= red[w];
-      kor |= red[kWarps + w];
-    }
-    __syncthreads();
-    const uint64_t diff = kand ^ kor;
-    int start = -8;                      // all keys equal: only the index decides
-    if (diff) start = ((63 - __clzll(static_cast<long long>(diff))) / 8) * 8;
-    pmask = (start + 8 >= 64) ? 0ull : ~((1ull << (start + 8)) - 1ull);
-    prefix = kand & pmask;
-    if (start < 0) pmask = ~0ull, prefix = kand;
-    for (int shift = start; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (int a = tid; a < C; a += kThreads)
-        if ((key[a] & pmask) == prefix) atomicAdd(&hist[(key[a] >> shift) & 255], 1);
-      __syncthreads();
-      if (warp == 0) {
-        // lane l owns digits 255-8l .. 248-8l (descending)
-        int cnt[8];
-        int lsum = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          cnt[j] = hist[255 - 8 * lane - j];
-          lsum += cnt[j];
-        }
-        int incl = lsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        int above = incl - lsum;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (above < rem && rem <= above + cnt[j]) {
-            misc[0] = 255 - 8 * lane - j;
-            misc[1] = above;
-          }
-          above += cnt[j];
-        }
-      }
-      __syncthreads();
-      const int d = misc[0];
-      rem -= misc[1];
-      prefix |= static_cast<uint64_t>(d) << shift;
-      pmask |= 0xFFull << shift;
-      const bool done = (hist[d] == rem);
-      __syncthreads();
-      if (done) {
-        all_in = true;
-        break;
-      }
-    }
-  }
-
-  // selection flags in candidate order -> node ids (1 + exclusive count)
+  __syncthreads();
   const int per = (C + kThreads - 1) / kThreads;
   const int a0 = tid * per, a1 = min(C, a0 + per);
   int cnt_local = 0;
-  for (int a = a0; a < a1; ++a) {
-    bool sel;
-    if (need <= 0) sel = false;
-    else if (need >= C) sel = true;
-    else {
-      const uint64_t top = key[a] & pmask;
-      sel = top > prefix;
-      if (top == prefix) {
-        if (all_in) sel = true;
-        else {  // fully equal keys: lowest candidate indices first
-          int before_cnt = 0;
-          for (int b = 0; b < a; ++b) before_cnt += (key[b] == prefix) ? 1 : 0;
-          sel = before_cnt < rem;
-        }
-      }
-    }
-    node[a] = sel ? 1 : 0;
-    cnt_local += sel ? 1 : 0;
-  }
+  for (int a = a0; a < a1; ++a) cnt_local += node[a];
+
+  // selection flags in candidate order -> node ids (1 + exclusive count)
   int total = 0;
   int off = block_excl_scan(cnt_local, warp_tot, total);
   for (int a = a0; a < a1; ++a) {
@@ -268,6 +205,7 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
   }
   __syncthreads();
   if (tid == 0 && total != (need > 0 ? min(need, C) : 0)) record_error(A.rs.err, kDevAssert, 10);
+  (void)lane;
 
   // node arrays
   if (tid == 0) {
@@ -294,7 +232,7 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
     out.tokens[n] = tok[a];
     out.depth[n] = dep;
     out.pos[n] = dep;
-    if (out.values) out.values[n] = val[a];
+    if (out.values) out.values[n] = key_value(key[a]);
     npar[n] = pn;
   }
   __syncthreads();
@@ -320,34 +258,18 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) build_kernel(const __grid_constant__ BuildArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) build_kernel(const __grid_constant__ BuildArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
-  run_stream(A.rs, S);
-  const int n_done = S.n_done_items;
-  for (int d = 0; d < n_done; ++d) {
-    assemble_tree(A, S.done_items[d], S);
-    __syncthreads();
-  }
+  const RowCtx cx = stream_row(A.rs, S);
+  if (!cx.leader) return;
+  if (item_arrive(A.rs, S, cx.item)) assemble_tree(A, cx.item, S);
 }
 
-// R = 1 + (depth-1) top_k stays below 256 whenever C <= 2048 and depth <= 16
-static_assert(sizeof(StreamSmem) - offsetof(StreamSmem, buf) >=
-                  (8 + 8 + 4 + 4 + 4 + 4 + 4) * EAGLE_MAX_CANDIDATES + 8 * 256 +
-                      4 * (EAGLE_MAX_TREE + 2 * kKMax + 256 + 8 + kWarps) + 16 * 16,
+// tree assembly scratch (R = 1 + (depth-1) top_k <= 256 whenever C <= 2048)
+static_assert(kScratchBytes >= (8 + 4 * 7) * EAGLE_MAX_CANDIDATES + 8 * 256 +
+                                   4 * (EAGLE_MAX_TREE + 2 * kKMax + kWarps) + 16 * 16,
               "tree assembly scratch must fit in the stream's shared memory");
-
-static int build_ctas_per_sm() {
-  int occ = 0;
-  const size_t smem = sizeof(StreamSmem);
-  if (cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, build_kernel, kThreads, smem) !=
-      cudaSuccess)
-    return 0;
-  return occ;
-}
 
 static eagle_status build_impl(int32_t n_items, const float* const* logits, int64_t row_stride,
                                int32_t n_rows, int32_t vocab, int32_t top_k, int32_t depth,
@@ -371,15 +293,16 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
     EAGLE_CHECK_ARG(t.parents && t.tokens && t.depth && t.pos && t.mask);
     EAGLE_CHECK_ARG(t.m == total_tokens && t.mask_words == (total_tokens + 63) / 64);
   }
-  const StreamLayout L = stream_layout(n_items, R, vocab, top_k, false);
+  const StreamLayout L = stream_layout(n_items, R, vocab, top_k, false, false);
   if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
 
   BuildArgs A;
   memset(&A, 0, sizeof(A));
-  const int occ = build_ctas_per_sm();
+  const int occ = stream_ctas_per_sm(build_kernel);
   if (occ <= 0) return EAGLE_ERR_CUDA;
-  const int grid = stream_grid(L, occ);
-  fill_stream(A.rs, L, static_cast<char*>(ws), n_items, R, vocab, row_stride, grid, false);
+  const int ctas = stream_ctas_per_row(build_kernel, L, occ);
+  if (ctas <= 0) return EAGLE_ERR_CUDA;
+  fill_stream(A.rs, L, static_cast<char*>(ws), n_items, R, vocab, row_stride, ctas, false);
   for (int i = 0; i < n_items; ++i) {
     A.rs.base[i] = logits[i];
     A.rs.exp_scale[i] = 1.0f;
@@ -392,8 +315,7 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
   A.depth = depth;
   A.total_tokens = total_tokens;
   A.n_cand = static_cast<int>(C);
-  build_kernel<<<grid, kThreads, sizeof(StreamSmem), stream>>>(A);
-  return launch_status();
+  return launch_stream(build_kernel, A, L.n_rows, ctas, stream);
 }
 
 // Scratch of the allocation-free entry point: fixed size, static device
@@ -432,7 +354,7 @@ extern "C" size_t eagle_tree_build_workspace_size(int32_t n_items, int32_t n_row
   (void)total_tokens;
   if (n_items < 1 || vocab < 1 || top_k < 1 || depth < 1) return 0;
   const int R = 1 + (depth - 1) * top_k;
-  return stream_layout(n_items, R, vocab, top_k, false).total;
+  return stream_layout(n_items, R, vocab, top_k, false, false).total;
 }
 
 extern "C" eagle_status eagle_tree_build(const float* draft_logits, int64_t row_stride,
@@ -475,15 +397,15 @@ extern "C" eagle_status eagle_tree_build_noalloc(const float* draft_logits, int6
   EAGLE_CHECK_ARG(row_stride >= vocab && row_stride % 4 == 0);
   EAGLE_CHECK_ARG(out.parents && out.tokens && out.depth && out.pos && out.mask);
   EAGLE_CHECK_ARG(out.m == total_tokens && out.mask_words == (total_tokens + 63) / 64);
-  const StreamLayout L = stream_layout(1, R, vocab, top_k, false);
+  const StreamLayout L = stream_layout(1, R, vocab, top_k, false, false);
   if (L.total > EAGLE_NOALLOC_SCRATCH_BYTES) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   const eagle_status st = noalloc_scratch(&ws);
   if (st != EAGLE_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // header (error word) and the per-row / per-item arrival counters must
-  // start at zero; the records behind them are written before they are read
-  EAGLE_CUDA(cudaMemsetAsync(ws, 0, L.off_pieces, s));
+  // header (error word) and the per-item arrival counters must start at
+  // zero; the row records behind them are written before they are read
+  EAGLE_CUDA(cudaMemsetAsync(ws, 0, L.off_rows, s));
   return build_impl(1, &draft_logits, row_stride, n_rows, vocab, top_k, depth, total_tokens,
                     &root_token, &out, ws, EAGLE_NOALLOC_SCRATCH_BYTES, s);
 }

@@ -115,6 +115,12 @@ __device__ __forceinline__ uint64_t order_key(double x) {
   return (u >> 63) ? ~u : (u | (1ull << 63));
 }
 
+// Inverse of order_key.
+__device__ __forceinline__ double key_value(uint64_t k) {
+  const uint64_t u = (k >> 63) ? (k & ~(1ull << 63)) : ~k;
+  return __longlong_as_double(static_cast<long long>(u));
+}
+
 // 2^x on the special-function unit (approximate, flush-to-zero).
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -1,5 +1,6 @@
 // sm_100-family tensor-core helpers written as inline PTX: tensor-memory
-// allocation, tcgen05.mma (bf16 x bf16 -> fp32, A and B from shared memory),
+// allocation, tcgen05.mma (bf16 x bf16 -> fp32, A from shared or tensor
+// memory, B from shared memory),
 // tcgen05 commit / fences, tensor-memory loads and stores, tiled TMA loads,
 // and the shared-memory matrix / instruction descriptors.
 #pragma once
@@ -43,6 +44,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// Same with the A operand read from tensor memory (M rows = lanes, K packed
+// along the columns, two bf16 per 32-bit column, lower element in the low
+// half); B from shared memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -71,6 +85,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       EAGLE_W8(0), EAGLE_W8(8), EAGLE_W8(16), EAGLE_W8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      EAGLE_W8(0), EAGLE_W8(8)
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {

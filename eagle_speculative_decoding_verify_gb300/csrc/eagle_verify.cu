@@ -10,11 +10,14 @@
 // Support for llama.cpp - Phase 1", "Performance Notes" (temperature + top_k
 // + top_p).
 //
-// Phase 1 (all CTAs, eagle_rowstream.cuh): one HBM pass over the m target
-// rows of every item -> per row the argmax (greedy), the top_k logits
-// (sampling with top_k) or the max, sum of exp((x-max)/T) and per-tile sums
-// (sampling over the full vocabulary).
-// Phase 2 (the CTA that finalizes an item's last row, one warp): the walk.
+// Phase 1 (one cluster per row, eagle_rowstream.cuh): one HBM pass over the
+// m target rows of every item -> per row the argmax (greedy), the top_k
+// logits (sampling with top_k) or the max, sum of exp((x-max)/T) and
+// per-tile sums (sampling over the full vocabulary).
+// Phase 2 (the row's leader CTA, one warp): the walk's decision at that
+// node -- the accepted child, or the bonus token if the walk stops there.
+// Phase 3 (the CTA whose row of an item arrives last): follow the decisions
+// from the root.
 // Sampling follows recursive speculative sampling with one-hot draft
 // distributions (tree children are deterministic top-k picks): accept child j
 // iff u_j (1 - rho) < p(token_j), else rho += p(token_j); on rejection of all
@@ -42,6 +45,7 @@ struct VerifyArgs {
   uint64_t step;
   int32_t* n_accepted;
   int32_t* bonus;
+  int2* dec;                      // [rows] per-node decision: (accepted child or -1, bonus)
 };
 
 __device__ __forceinline__ double warp_incl_scan_d(double v) {
@@ -60,78 +64,86 @@ __device__ __forceinline__ double full_prob(const float* lrow, int t, double row
   return exp_d((static_cast<double>(__ldg(lrow + t)) - rowmax) / T) / zsum;
 }
 
-// The walk; executed by warp 0 of the CTA.
-static __device__ __noinline__ void walk(const VerifyArgs& A, int item, StreamSmem& S) {
+// Decision of the walk at one node (warp 0 of the node's row leader): the
+// child accepted there (-1 if none) and the token emitted when the walk stops
+// there.  It depends only on the node's own row, its children and the
+// uniforms keyed by (seed, step, node, j), so every node decides on its own,
+// in parallel, and the item's final step follows the decisions from the root.
+static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t row, int item,
+                                                  StreamSmem& S) {
   const int lane = threadIdx.x & 31;
   const int m = A.m;
-  const int rk = A.rs.rec_k;
-  const int rb = rec_bytes(rk);
-  const int TR = A.rs.tiles_per_row;
-  char* rows = A.rs.rows + static_cast<int64_t>(item) * m * rb;
+  const int node = static_cast<int>(row - static_cast<int64_t>(item) * m);
   const int mode = A.mode[item];
   const double T = static_cast<double>(A.temperature[item]);
   const double top_p = static_cast<double>(A.top_p[item]);
   const int K = A.top_k[item];
   const uint64_t seed = A.seed[item];
-  int32_t* acc = A.accepted[item];
+  const int32_t* parents = A.parents[item];
+  const int32_t* tokens = A.tokens[item];
+  const int TR = A.rs.tiles_per_row;
 
-  int* par = reinterpret_cast<int*>(S.buf[0]);
-  int* tok = par + EAGLE_MAX_TREE;
-  int* rejected = tok + EAGLE_MAX_TREE;        // tokens rejected at the current node
-  double* kp = reinterpret_cast<double*>(S.buf[1]);  // kept probabilities (top-k mode)
-  int* kid = reinterpret_cast<int*>(kp + kKMax);     // kept ids
-  double* sp = reinterpret_cast<double*>(kid + kKMax);  // kept probs sorted by id
+  int* kn = reinterpret_cast<int*>(S.ring[0]);          // children (node ids), node order
+  int* kt = kn + EAGLE_MAX_TREE;                         // their tokens
+  double* kp = reinterpret_cast<double*>(S.ring[1]);     // kept probabilities, by rank
+  int* kid = reinterpret_cast<int*>(kp + kKMax);         // kept ids, by rank
+  double* sp = reinterpret_cast<double*>(kid + kKMax);   // kept probabilities sorted by id
   int* sid = reinterpret_cast<int*>(sp + kKMax);
-  for (int i = lane; i < m; i += 32) {
-    par[i] = A.parents[item][i];
-    tok[i] = A.tokens[item][i];
+
+  // ---- the children of this node, in node order
+  int nk = 0;
+  {
+    int pv[EAGLE_MAX_TREE / 32];
+#pragma unroll
+    for (int r = 0; r < EAGLE_MAX_TREE / 32; ++r) {
+      const int i = lane + 32 * r;
+      pv[r] = (i > node && i < m) ? __ldg(parents + i) : -2;
+    }
+#pragma unroll
+    for (int r = 0; r < EAGLE_MAX_TREE / 32; ++r) {
+      const int i = lane + 32 * r;
+      const bool is = pv[r] == node;
+      const unsigned bal = __ballot_sync(0xffffffffu, is);
+      if (is) {
+        const int pos = nk + __popc(bal & ((1u << lane) - 1u));
+        kn[pos] = i;
+        kt[pos] = __ldg(tokens + i);
+      }
+      nk += __popc(bal);
+    }
   }
   __syncwarp();
 
-  int node = 0, n_acc = 0, bonus = -1;
-  if (lane == 0) acc[0] = 0;
-  for (int guard = 0; guard < m; ++guard) {
-    char* rec = rows + static_cast<int64_t>(node) * rb;
-    const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rec);
-    if (mode == kModeGreedy) {
-      const int a = __ldcg(rec_idx(rec, rk));
-      int child = -1;
-      for (int base = node + 1; base < m && child < 0; base += 32) {
-        const int i = base + lane;
-        const bool hit = i < m && par[i] == node && tok[i] == a;
-        const unsigned bal = __ballot_sync(0xffffffffu, hit);
-        if (bal) child = base + __ffs(bal) - 1;
-      }
-      if (child < 0) {
-        bonus = a;
-        break;
-      }
-      node = child;
-      ++n_acc;
-      if (lane == 0) acc[n_acc] = node;
-      continue;
+  int child = -1, bonus = -1;
+  if (mode == kModeGreedy) {
+    const int a = key_i(S.rlist[0]);   // argmax
+    for (int b = 0; b < nk && child < 0; b += 32) {
+      const bool hit = b + lane < nk && kt[b + lane] == a;
+      const unsigned bal = __ballot_sync(0xffffffffu, hit);
+      if (bal) child = kn[b + __ffs(bal) - 1];
     }
-
+    bonus = a;
+  } else {
     // ---- the warped target distribution at this node
     const float* lrow = A.rs.base[item] + static_cast<int64_t>(node) * A.rs.row_stride;
     double rowmax = 0.0, zsum = 1.0;
     int nkeep = 0;
     if (mode == kModeTopK) {
-      int cnt = h->count;
+      int cnt = S.rcount;
       if (cnt > K) cnt = K;
       double z[2], pr[2];
       int id[2];
-      const double z0 = static_cast<double>(__ldcg(rec_val(rec))) / T;
+      const double z0 = static_cast<double>(key_v(S.rlist[0])) / T;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int e = lane + 32 * hh;
         if (e < cnt) {
-          z[hh] = static_cast<double>(__ldcg(rec_val(rec) + e)) / T;
-          id[hh] = __ldcg(rec_idx(rec, rk) + e);
+          z[hh] = static_cast<double>(key_v(S.rlist[e])) / T;
+          id[hh] = key_i(S.rlist[e]);
           pr[hh] = exp_d(z[hh] - z0);
         } else {
           pr[hh] = 0.0;
-          id[hh] = 0x7fffffff;
+          id[hh] = kNoIndex;
         }
       }
       const double tot = warp_sum_d(pr[0] + pr[1]);
@@ -157,203 +169,203 @@ static __device__ __noinline__ void walk(const VerifyArgs& A, int item, StreamSm
         pr[1] /= tot2;
       }
       kp[lane] = pr[0];
-      kid[lane] = lane < nkeep ? id[0] : 0x7fffffff;
+      kid[lane] = lane < nkeep ? id[0] : kNoIndex;
       kp[lane + 32] = pr[1];
-      kid[lane + 32] = lane + 32 < nkeep ? id[1] : 0x7fffffff;
+      kid[lane + 32] = lane + 32 < nkeep ? id[1] : kNoIndex;
       __syncwarp();
     } else {  // full vocabulary
-      rowmax = static_cast<double>(h->max);
-      zsum = h->sum;
+      rowmax = static_cast<double>(S.rmax);
+      zsum = S.rsum;
     }
-    auto prob_of = [&](int t) -> double {  // warp-uniform result
+    auto prob_of = [&](int t) -> double {  // lane-local
       if (mode == kModeTopK) {
         double v = 0.0;
-        if (kid[lane] == t) v = kp[lane];
-        if (kid[lane + 32] == t) v = kp[lane + 32];
-        return warp_sum_d(v);
+        for (int e = 0; e < nkeep; ++e)
+          if (kid[e] == t) v = kp[e];
+        return v;
       }
       return full_prob(lrow, t, rowmax, T, zsum);
     };
 
-    // ---- children in node order: recursive speculative sampling
-    double rho = 0.0;
-    int n_rej = 0, child = -1, j = 0;
-    for (int base = node + 1; base < m && child < 0; base += 32) {
-      const int i = base + lane;
-      unsigned bal = __ballot_sync(0xffffffffu, i < m && par[i] == node);
-      while (bal && child < 0) {
-        const int c = base + __ffs(bal) - 1;
-        bal &= bal - 1;
-        const int t = tok[c];
-        const double pt = prob_of(t);
-        const double u = philox_uniform(seed, A.step, static_cast<uint32_t>(node),
-                                        static_cast<uint32_t>(j));
-        if (u * (1.0 - rho) < pt) {
-          child = c;
-        } else {
-          rho += pt;
-          if (lane == 0 && n_rej < EAGLE_MAX_TREE) rejected[n_rej] = t;
-          ++n_rej;
-        }
-        ++j;
-      }
-    }
-    __syncwarp();
-    if (child >= 0) {
-      node = child;
-      ++n_acc;
-      if (lane == 0) acc[n_acc] = node;
-      continue;
+    // ---- children in node order, 32 at a time: child j is accepted iff
+    // u_j (1 - rho_j) < p(token_j), rho_j = mass of the children before it
+    // (all of them rejected when j is reached)
+    double rho_all = 0.0;
+    for (int b = 0; b < nk && child < 0; b += 32) {
+      const int j = b + lane;
+      const bool valid = j < nk;
+      const double pt = valid ? prob_of(kt[j]) : 0.0;
+      const double incl = warp_incl_scan_d(pt);
+      const double rho = rho_all + (incl - pt);
+      const double u = valid ? philox_uniform(seed, A.step, static_cast<uint32_t>(node),
+                                              static_cast<uint32_t>(j))
+                             : 1.0;
+      const unsigned bal = __ballot_sync(0xffffffffu, valid && (u * (1.0 - rho) < pt));
+      if (bal) child = kn[b + __ffs(bal) - 1];
+      rho_all += __shfl_sync(0xffffffffu, incl, 31);
     }
 
-    // ---- residual / bonus draw: inverse CDF over ids ascending
-    const double thr =
-        philox_uniform(seed, A.step, static_cast<uint32_t>(node), kResidualChild) * (1.0 - rho);
-    auto is_rejected = [&](int t) {
-      for (int r = 0; r < n_rej && r < EAGLE_MAX_TREE; ++r)
-        if (rejected[r] == t) return true;
-      return false;
-    };
-    if (mode == kModeTopK) {
-      // sort the kept entries by token id (rank by counting)
+    if (child < 0) {
+      // ---- every child rejected (or a leaf): residual draw by inverse CDF
+      // over ids ascending, the children's tokens removed
+      const double thr =
+          philox_uniform(seed, A.step, static_cast<uint32_t>(node), kResidualChild) *
+          (1.0 - rho_all);
+      auto is_rejected = [&](int t) {
+        for (int r = 0; r < nk; ++r)
+          if (kt[r] == t) return true;
+        return false;
+      };
+      if (mode == kModeTopK) {
+        // kept entries sorted by token id (rank by counting)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int e = lane + 32 * hh;
-        if (e < nkeep) {
-          int r = 0;
-          for (int f = 0; f < nkeep; ++f) r += kid[f] < kid[e] ? 1 : 0;
-          sid[r] = kid[e];
-          sp[r] = is_rejected(kid[e]) ? 0.0 : kp[e];
+        for (int hh = 0; hh < 2; ++hh) {
+          const int e = lane + 32 * hh;
+          if (e < nkeep) {
+            int r = 0;
+            for (int f = 0; f < nkeep; ++f) r += kid[f] < kid[e] ? 1 : 0;
+            sid[r] = kid[e];
+            sp[r] = is_rejected(kid[e]) ? 0.0 : kp[e];
+          }
         }
-      }
-      __syncwarp();
-      int pick_id = 0;
-      if (lane == 0) {
+        __syncwarp();
+        int pick = -1, last = -1;
         double cum = 0.0;
-        int pick = -1, last_pos = -1;
-        for (int r = 0; r < nkeep; ++r) {
-          cum += sp[r];
-          if (sp[r] > 0.0) last_pos = r;
-          if (cum > thr) {
-            pick = r;
-            break;
-          }
+        for (int hh = 0; hh < 2 && pick < 0; ++hh) {
+          const int r = lane + 32 * hh;
+          const double mass = r < nkeep ? sp[r] : 0.0;
+          const double incl = warp_incl_scan_d(mass) + cum;
+          const unsigned bal = __ballot_sync(0xffffffffu, r < nkeep && incl > thr);
+          if (bal) pick = 32 * hh + __ffs(bal) - 1;
+          const unsigned nz = __ballot_sync(0xffffffffu, r < nkeep && mass > 0.0);
+          if (nz) last = 32 * hh + 31 - __clz(nz);
+          cum = __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (pick < 0) pick = last_pos >= 0 ? last_pos : nkeep - 1;
-        pick_id = sid[pick];
-      }
-      bonus = __shfl_sync(0xffffffffu, pick_id, 0);
-      __syncwarp();
-    } else {
-      // tile masses (tile sums were taken relative to each tile's max)
-      const float2* ts = A.rs.tile_sums + (static_cast<int64_t>(item) * m + node) * TR * kWarps;
-      const double c2 = static_cast<double>(A.rs.exp_scale[item]) * 1.4426950408889634;
-      double cum = 0.0;
-      int tile = -1;
-      double before_tile = 0.0;
-      for (int base = 0; base < TR && tile < 0; base += 32) {
-        const int t = base + lane;
-        double mass = 0.0;
-        if (t < TR) {
-          // combine the per-warp partials of tile t (max, sum of 2^((x - max) c2))
-          const float2* tw = ts + static_cast<int64_t>(t) * kWarps;
-          for (int w = 0; w < kWarps; ++w) {
-            const float2 v = __ldcg(tw + w);
-            if (v.y > 0.f)
-              mass += static_cast<double>(v.y) *
-                      static_cast<double>(ex2((v.x - static_cast<float>(rowmax)) * static_cast<float>(c2)));
+        if (pick < 0) pick = last >= 0 ? last : nkeep - 1;
+        bonus = sid[pick];
+      } else {
+        // tile masses (tile sums were taken relative to each tile's max)
+        const float2* ts = A.rs.tile_sums + row * TR * kWarps;
+        const double c2 = static_cast<double>(A.rs.exp_scale[item]) * 1.4426950408889634;
+        double cum = 0.0;
+        int tile = -1;
+        double before_tile = 0.0;
+        for (int base = 0; base < TR && tile < 0; base += 32) {
+          const int t = base + lane;
+          double mass = 0.0;
+          if (t < TR) {
+            // combine the per-warp partials of tile t (max, sum of 2^((x - max) c2))
+            const float2* tw = ts + static_cast<int64_t>(t) * kWarps;
+            for (int w = 0; w < kWarps; ++w) {
+              const float2 v = __ldcg(tw + w);
+              if (v.y > 0.f)
+                mass += static_cast<double>(v.y) *
+                        static_cast<double>(ex2((v.x - static_cast<float>(rowmax)) * static_cast<float>(c2)));
+            }
+            mass /= zsum;
+            for (int r = 0; r < nk; ++r) {   // rejected tokens of this tile, each once
+              const int rt = kt[r];
+              if (rt / kTile != t) continue;
+              bool first = true;
+              for (int r2 = 0; r2 < r; ++r2) first &= kt[r2] != rt;
+              if (first) mass -= full_prob(lrow, rt, rowmax, T, zsum);
+            }
+            if (mass < 0.0) mass = 0.0;
           }
-          mass /= zsum;
-          for (int r = 0; r < n_rej && r < EAGLE_MAX_TREE; ++r)
-            if (rejected[r] / kTile == t) mass -= full_prob(lrow, rejected[r], rowmax, T, zsum);
-          if (mass < 0.0) mass = 0.0;
+          const double incl = warp_incl_scan_d(mass) + cum;
+          const unsigned bal = __ballot_sync(0xffffffffu, t < TR && incl > thr);
+          if (bal) {
+            const int l = __ffs(bal) - 1;
+            tile = base + l;
+            before_tile = __shfl_sync(0xffffffffu, incl - mass, l);
+          }
+          cum = __shfl_sync(0xffffffffu, incl, 31);
         }
-        const double incl = warp_incl_scan_d(mass) + cum;
-        const unsigned bal = __ballot_sync(0xffffffffu, t < TR && incl > thr);
+        if (tile < 0) tile = TR - 1, before_tile = cum;  // rounding: take the last tile
+        // scan inside the tile: lane owns 32 consecutive tokens
+        const int v0 = tile * kTile + lane * 32;
+        double lm[32];
+        double lsum = 0.0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int t = v0 + q;
+          double mass = 0.0;
+          if (t < A.rs.vocab && !is_rejected(t)) {
+            const float x = __ldg(lrow + t);
+            mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) / zsum;
+          }
+          lm[q] = mass;
+          lsum += mass;
+        }
+        const double incl = warp_incl_scan_d(lsum) + before_tile;
+        const unsigned bal = __ballot_sync(0xffffffffu, incl > thr);
+        int pick = -1;
         if (bal) {
           const int l = __ffs(bal) - 1;
-          tile = base + l;
-          before_tile = __shfl_sync(0xffffffffu, incl - mass, l);
-        }
-        cum = __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (tile < 0) tile = TR - 1, before_tile = cum;  // rounding: take the last tile
-      // scan inside the tile: lane owns 32 consecutive tokens
-      const int v0 = tile * kTile + lane * 32;
-      double lm[32];
-      double lsum = 0.0;
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int t = v0 + q;
-        double mass = 0.0;
-        if (t < A.rs.vocab && !is_rejected(t)) {
-          const float x = __ldg(lrow + t);
-          mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) / zsum;
-        }
-        lm[q] = mass;
-        lsum += mass;
-      }
-      const double incl = warp_incl_scan_d(lsum) + before_tile;
-      const unsigned bal = __ballot_sync(0xffffffffu, incl > thr);
-      int pick = -1;
-      if (bal) {
-        const int l = __ffs(bal) - 1;
-        if (lane == l) {
-          double c = incl - lsum;
-          for (int q = 0; q < 32; ++q) {
-            c += lm[q];
-            if (lm[q] > 0.0 && c > thr) {
-              pick = v0 + q;
+          if (lane == l) {
+            double c = incl - lsum;
+            for (int q = 0; q < 32; ++q) {
+              c += lm[q];
+              if (lm[q] > 0.0 && c > thr) {
+                pick = v0 + q;
+                break;
+              }
+            }
+            if (pick < 0) pick = v0 + 31;
+          }
+          pick = __shfl_sync(0xffffffffu, pick, l);
+        } else {  // rounding: last token of the tile with mass
+          int last = -1;
+          for (int q = 31; q >= 0; --q)
+            if (lm[q] > 0.0) {
+              last = v0 + q;
               break;
             }
-          }
-          if (pick < 0) pick = v0 + 31;
+          const unsigned b2 = __ballot_sync(0xffffffffu, last >= 0);
+          const int l = b2 ? 31 - __clz(b2) : 0;
+          pick = __shfl_sync(0xffffffffu, last, l);
+          if (pick < 0) pick = tile * kTile;
         }
-        pick = __shfl_sync(0xffffffffu, pick, l);
-      } else {  // rounding: last token of the tile with mass
-        int last = -1;
-        for (int q = 31; q >= 0; --q)
-          if (lm[q] > 0.0) {
-            last = v0 + q;
-            break;
-          }
-        const unsigned b2 = __ballot_sync(0xffffffffu, last >= 0);
-        const int l = b2 ? 31 - __clz(b2) : 0;
-        pick = __shfl_sync(0xffffffffu, last, l);
-        if (pick < 0) pick = tile * kTile;
+        bonus = pick;
       }
-      bonus = pick;
     }
-    break;
   }
+  if (lane == 0) A.dec[row] = make_int2(child, bonus);
+  __syncwarp();
+}
+
+// The item's final step (warp 0 of the CTA whose row arrived last): follow
+// the decisions from the root.
+static __device__ __noinline__ void follow_path(const VerifyArgs& A, int item, StreamSmem& S) {
+  const int lane = threadIdx.x & 31;
+  const int m = A.m;
+  int2* dec = reinterpret_cast<int2*>(S.ring[0]);
+  const int2* src = A.dec + static_cast<int64_t>(item) * m;
+  for (int i = lane; i < m; i += 32) dec[i] = __ldcg(src + i);
+  __syncwarp();
   if (lane == 0) {
-    A.n_accepted[item] = n_acc;
-    A.bonus[item] = bonus;
+    int32_t* acc = A.accepted[item];
+    int node = 0, n = 0;
+    acc[0] = 0;
+    for (int guard = 0; guard < m; ++guard) {
+      const int c = dec[node].x;
+      if (c <= node || c >= m) break;   // -1: the walk stops here
+      node = c;
+      acc[++n] = node;
+    }
+    A.n_accepted[item] = n;
+    A.bonus[item] = dec[node].y;
   }
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(kThreads) verify_kernel(const __grid_constant__ VerifyArgs A) {
+__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_constant__ VerifyArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
-  run_stream(A.rs, S);
-  const int n_done = S.n_done_items;
-  for (int d = 0; d < n_done; ++d) {
-    if (threadIdx.x < 32) walk(A, S.done_items[d], S);
-    __syncthreads();
-  }
-}
-
-static int verify_ctas_per_sm() {
-  int occ = 0;
-  const size_t smem = sizeof(StreamSmem);
-  if (cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, verify_kernel, kThreads, smem) !=
-      cudaSuccess)
-    return 0;
-  return occ;
+  const RowCtx cx = stream_row(A.rs, S);
+  if (!cx.leader) return;
+  if (threadIdx.x < 32) node_decision(A, cx.row, cx.item, S);
+  if (item_arrive(A.rs, S, cx.item) && threadIdx.x < 32) follow_path(A, cx.item, S);
 }
 
 static eagle_status verify_impl(int32_t n_items, const float* const* logits, int64_t row_stride,
@@ -404,18 +416,19 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
     any_full |= mode == kModeFull;
   }
   (void)any_full;
-  const StreamLayout L = stream_layout(n_items, m, vocab, kKMax, true);
+  const StreamLayout L = stream_layout(n_items, m, vocab, kKMax, true, true);
   if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
-  const int occ = verify_ctas_per_sm();
+  const int occ = stream_ctas_per_sm(verify_kernel);
   if (occ <= 0) return EAGLE_ERR_CUDA;
-  const int grid = stream_grid(L, occ);
-  fill_stream(A.rs, L, static_cast<char*>(ws), n_items, m, vocab, row_stride, grid, true);
+  const int ctas = stream_ctas_per_row(verify_kernel, L, occ);
+  if (ctas <= 0) return EAGLE_ERR_CUDA;
+  fill_stream(A.rs, L, static_cast<char*>(ws), n_items, m, vocab, row_stride, ctas, true);
   A.m = m;
   A.step = step;
   A.n_accepted = n_accepted;
   A.bonus = bonus;
-  verify_kernel<<<grid, kThreads, sizeof(StreamSmem), stream>>>(A);
-  return launch_status();
+  A.dec = reinterpret_cast<int2*>(static_cast<char*>(ws) + L.off_dec);
+  return launch_stream(verify_kernel, A, L.n_rows, ctas, stream);
 }
 
 }  // namespace eagle
@@ -424,7 +437,7 @@ using namespace eagle;
 
 extern "C" size_t eagle_tree_verify_workspace_size(int32_t n_items, int32_t m, int32_t vocab) {
   if (n_items < 1 || m < 1 || vocab < 1) return 0;
-  return stream_layout(n_items, m, vocab, kKMax, true).total;
+  return stream_layout(n_items, m, vocab, kKMax, true, true).total;
 }
 
 extern "C" eagle_status eagle_tree_verify(const float* target_logits, int64_t row_stride,

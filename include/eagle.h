@@ -176,15 +176,15 @@ eagle_status eagle_tree_build_batched(int32_t n_items, const float* const* draft
  * on the GPU (different streams without ordering, or concurrent host
  * threads) race and give undefined results.  Device-side errors are recorded
  * in the shared scratch and are not reported.
- * Limit: the stream workspace of the shape,
+ * Limit: the workspace of the shape,
  *   eagle_tree_build_workspace_size(1, n_rows, vocab, top_k, depth, m),
  *   must fit in EAGLE_NOALLOC_SCRATCH_BYTES; larger shapes return
  *   EAGLE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The size
- *   grows with R = 1 + (depth-1)*top_k rows and with top_k (about
- *   17 * R * (16 + 8*top_k) bytes): every shape with top_k <= 10 fits;
- *   e.g. top_k 12, depth 13 does not (277,248 bytes).
+ *   is about 512 + R * (16 + 8*top_k) bytes, R = 1 + (depth-1)*top_k rows:
+ *   every shape with top_k <= 10 fits; e.g. top_k 12, depth 13 does not
+ *   (16,896 bytes).
  * ------------------------------------------------------------------------ */
-#define EAGLE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+#define EAGLE_NOALLOC_SCRATCH_BYTES (16u * 1024u)
 
 eagle_status eagle_tree_build_noalloc(const float* draft_logits, int64_t row_stride,
                                       int32_t n_rows, int32_t vocab, int32_t top_k,
