@@ -206,6 +206,52 @@ class Step:
                     for n in ("q", "tree_k", "tree_v")))
 
 
+def attn_long(eb, wl, dev, reps=5):
+    """Tree attention at long context: 32 independent layers of a
+    llama-3-8b-shaped KV cache (8 kv heads, d 128, bf16 prefix 32768; 4.3 GB,
+    far above L2) for one 60-token tree, all layers in one batched call.
+    Returns achieved GB/s (algorithmic bytes / device time) and TFLOP/s."""
+    import torch
+    w = wl.WORKLOADS["c3"]
+    draft = wl.draft_logits(w).to(dev)
+    tree = eb.eagle_tree_build(draft, w.top_k, w.depth, w.total_tokens, wl.root_token(w))
+    layers = [wl.attention_inputs(w, layer=l, device=dev) for l in range(w.layers)]
+    outs = [torch.empty(w.total_tokens, w.n_q_heads, w.head_dim, device=dev)
+            for _ in range(w.layers)]
+    items = [eb.attn_item(a["q"], a["k_cache"], a["v_cache"], a["tree_k"], a["tree_v"],
+                          tree.mask, o) for a, o in zip(layers, outs)]
+    dt = eb.EAGLE_BF16
+    ws = eb.workspace(eb.eagle_tree_attn_batched_workspace_size(
+        items, w.n_q_heads, w.n_kv_heads, w.head_dim, dt), dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def run():
+        eb.eagle_tree_attn_batched(items, w.n_q_heads, w.n_kv_heads, w.head_dim, dt, ws=ws,
+                                   stream=s, device=dev)
+
+    for _ in range(2):
+        run()
+    s.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        run()
+        e1.record(s)
+        s.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(times)
+    m, hq, hkv, d, S, L = w.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.prefix, w.layers
+    nbytes = L * (2 * S * hkv * d * 2 + m * hq * d * 2 + 2 * m * hkv * d * 2 + m * hq * d * 4)
+    flops = L * 4.0 * m * hq * (S + m) * d
+    del layers, outs, items, ws
+    torch.cuda.empty_cache()
+    return {"workload": "c3: 32 layers x bf16 prefix 32768, 32/8 heads d128, 60-token tree, "
+                        "one batched call", "us": round(t * 1e6, 1),
+            "achieved_gbs": round(nbytes / t / 1e9, 1), "achieved_tflops": round(flops / t / 1e12, 1),
+            "bytes": nbytes}
+
+
 class L2Flush:
     """Evicts the step's inputs from L2 before every step: writes 512 MB (4x
     L2), then reads 256 MB so that the lines left behind are clean and the
@@ -313,7 +359,12 @@ def max_over_ranks(x, world, device):
 
 # known ncu DRAM traffic per launch (bytes), keyed by kernel and source hash;
 # entries whose hash no longer matches the sources are reported as null
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/verify_kernel_c2.md: dram__bytes_read.sum + dram__bytes_write.sum
+    "verify:c2": ("8009c80761b6", 36609280),
+    "build:c2": ("8009c80761b6", 31124224),
+    "attn:c2": ("8009c80761b6", 17394944),
+}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -404,6 +455,12 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": step.launches * args.steps,
         "clocks": sampler.summary(),
     }
+    if not args.no_long_attn:
+        la = attn_long(eb, wl, dev)
+        la["frac_hbm"] = round(la["achieved_gbs"] / hbm, 4)
+        la["frac_tensor"] = round(la["achieved_tflops"] / tf, 4)
+        la["peak_source"] = peak_src
+        line["tree_attn_long"] = la
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, samples=1)
     return line
@@ -494,6 +551,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c2", choices=["c0", "c1", "c2"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long-attn", action="store_true",
+                    help="skip the 32-layer x 32K-context attention measurement")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

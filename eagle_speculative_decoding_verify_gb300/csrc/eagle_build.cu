@@ -80,7 +80,7 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
   int* node = reinterpret_cast<int*>(carve(sizeof(int) * C));
   int* npar = reinterpret_cast<int*>(carve(sizeof(int) * EAGLE_MAX_TREE));
   int* fr = reinterpret_cast<int*>(carve(sizeof(int) * 2 * kKMax));  // frontiers, by depth parity
-  int* warp_tot = reinterpret_cast<int*>(carve(sizeof(int) * kWarps));
+  int* warp_tot = reinterpret_cast<int*>(carve(sizeof(int) * EAGLE_MAX_DEPTH));
 
   // every row's statistics in one pass: logsumexp, top-k logits and tokens
   for (int r = tid; r < R; r += kThreads) {
@@ -152,43 +152,54 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
     base += kk;
   }
 
-  // final rerank: the best need = m-1 of the C candidates.  Global rank =
-  // rank within the own level + entries of every other level before it
-  // (binary search in that level's sorted list).
+  // final rerank: the best need = m-1 of the C candidates.  Every level's
+  // list is sorted, so the kept set is a prefix of each level: warp w finds
+  // the cut of level w (and w+8, ...) by binary search over its positions,
+  // the global rank of a probe being its position plus, over the other
+  // levels (one lane each), the entries before it (binary search over that
+  // level's keys in sorted order, materialised over the row top-k scratch,
+  // which is no longer needed).
+  uint64_t* skey = reinterpret_cast<uint64_t*>(rv);   // rv and ri are contiguous: 8 C bytes
+  for (int i = tid; i < C; i += kThreads) skey[i] = key[srt[i]];
+  int* cut = warp_tot;                                 // [D] kept entries per level (D <= 16)
+  __syncthreads();
   const int need = m - 1;
-  for (int a = tid; a < C; a += kThreads) {
-    bool sel;
-    if (need <= 0) {
-      sel = false;
-    } else if (need >= C) {
-      sel = true;
-    } else {
-      int rank = lrank[a];
-      if (rank < need) {
-        const uint64_t kv = key[a];
-        const int la = a < k ? 0 : 1 + (a - k) / kk;
-        for (int j = 0; j < D && rank < need; ++j) {
-          if (j == la) continue;
-          const int lb = j == 0 ? 0 : k + (j - 1) * kk;
-          const int len = j == 0 ? k : kk;
-          const int* ls = srt + lb;
-          int lo = 0, hi = len;
-          const int steps = 32 - __clz(len);
-          for (int t = 0; t < steps; ++t) {
-            const bool act = lo < hi;
-            const int mid = (lo + hi) >> 1;
-            const int b = ls[act ? mid : 0];
-            const uint64_t o = key[b];
-            const bool go = act & ((o > kv) | ((o == kv) & (b < a)));
-            lo = go ? mid + 1 : lo;
-            hi = (act & !go) ? mid : hi;
+  {
+    const int lane = tid & 31, warp = tid >> 5;
+    auto lbase = [&](int l) { return l == 0 ? 0 : k + (l - 1) * kk; };
+    auto llen = [&](int l) { return l == 0 ? k : kk; };
+    for (int l = warp; l < D; l += kWarps) {
+      int lo = 0, hi = llen(l);   // first position whose global rank reaches need
+      if (need <= 0) hi = 0;
+      else if (need >= C) lo = hi;
+      while (lo < hi) {
+        const int p = (lo + hi) >> 1;
+        const int ap = srt[lbase(l) + p];
+        const uint64_t kv = key[ap];
+        int cnt = 0;
+        if (lane < D && lane != l) {   // entries of level `lane` before (kv, ap)
+          const int lb = lbase(lane);
+          int a = 0, b = llen(lane);
+          while (a < b) {
+            const int mid = (a + b) >> 1;
+            const uint64_t o = skey[lb + mid];
+            const bool go = (o > kv) | ((o == kv) & (srt[lb + mid] < ap));
+            if (go) a = mid + 1;
+            else b = mid;
           }
-          rank += lo;
+          cnt = a;
         }
+        const int rank = p + warp_sum_i(cnt);
+        if (rank < need) lo = p + 1;
+        else hi = p;
       }
-      sel = rank < need;
+      if (lane == 0) cut[l] = lo;
     }
-    node[a] = sel ? 1 : 0;
+  }
+  __syncthreads();
+  for (int a = tid; a < C; a += kThreads) {
+    const int la = a < k ? 0 : 1 + (a - k) / kk;
+    node[a] = lrank[a] < cut[la] ? 1 : 0;
   }
   __syncthreads();
   const int per = (C + kThreads - 1) / kThreads;

@@ -101,6 +101,18 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy (completes per thread).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // --------------------------------------------------------- ordering / keys
 // (value desc, index asc): does (va, ia) come before (vb, ib)?
 // Written with bitwise operators so that it compiles to predicates, not branches.
@@ -133,12 +145,16 @@ __device__ __forceinline__ float ex2(float x) {
 // argument in fp64 and evaluate the remaining small range with the fp32
 // library function.
 //   exp(d) = 2^n * exp(r),  n = round(d / ln 2),  r = d - n ln 2 in [-0.35, 0.35]
+//   (0 below e^-708, where a probability no longer matters)
 //   log(s) = e ln 2 + log(f_hi) + (f - f_hi) / f_hi,  s = f 2^e, f in [0.5, 1)
 __device__ __forceinline__ double exp_d(double d) {
-  if (d < -745.0) return 0.0;
+  if (d < -708.0) return 0.0;   // below the normal range: negligible as a probability
+  if (d > 709.0) d = 709.0;
   const double n = rint(d * 1.4426950408889634);
   const double r = fma(-n, 0.6931471805599453, d);   // ln 2 to double precision
-  return ldexp(static_cast<double>(expf(static_cast<float>(r))), static_cast<int>(n));
+  // 2^n from its exponent bits (n in [-1022, 1023])
+  const double two_n = __longlong_as_double(static_cast<long long>(static_cast<int>(n) + 1023) << 52);
+  return static_cast<double>(expf(static_cast<float>(r))) * two_n;
 }
 __device__ __forceinline__ double log_d(double s) {
   int e;

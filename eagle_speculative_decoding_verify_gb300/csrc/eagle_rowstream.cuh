@@ -11,12 +11,13 @@
 //   * max and sum of 2^((x - max) c) per thread (fp32 ex2), combined with
 //     fp32 factors and fp64 accumulation;
 //   * the exact top-K (value desc, token id asc), K <= 64.  Each warp keeps
-//     the elements at or before its threshold in a private buffer.  The first
-//     threshold is the K-th best of the lanes' best element (K <= 32) or best
-//     two (K > 32) in the first slot: K distinct elements reach it, so it is
-//     a lower bound of the warp's K-th best.  After the first slot, and
-//     whenever the buffer is full, the buffer is cut to its best K, which
-//     raises the threshold to the exact K-th best seen so far;
+//     the elements at or before its bound in a private buffer.  The first
+//     bound is CTA-wide: the smallest of the warps' ceil(K/8)-th best lane
+//     maxima of the first slot (K distinct elements reach it).  A warp whose
+//     buffer grows past max(2K, 64) entries cuts it to its best K, which
+//     raises its bound to its exact K-th best; that entry is also published
+//     as the CTA's running bound (shared-memory atomicMax on the 64-bit
+//     key), which every warp reads once per slot;
 //   * the argmax (K = 1);
 //   * optionally per-tile (max, sum) of every warp for inverse-CDF sampling.
 // Row end: every warp ranks its survivors by counting into a sorted list of at
@@ -128,6 +129,7 @@ struct StreamSmem {
   int rcount;
   int flag;
   Key cta_bound;                       // K-th best of the CTA's first slot
+  int aux[2 * EAGLE_MAX_TREE];         // callers' own data (never touched by the stream)
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
 };
@@ -218,15 +220,28 @@ __device__ __forceinline__ int union_rank(const Key* L, const int* cnt, int nl, 
   return r;
 }
 
-// Before a merge (one warp, nl <= 32 sorted lists at `stride`): an entry
-// strictly after the best of the lists' K-th entries has K entries before it
-// in that list, so it cannot be among the union's best K.  Cuts every list's
-// count to its entries at or before that bound.
+// Before a merge (one warp, nl <= 32 sorted lists at `stride`): a bound with
+// K entries of the union at or before it, below which nothing can be among
+// the union's best K -- the best of the lists' K-th entries (K entries in
+// that list), and, when every list has q = ceil(K / nl) entries, the worst of
+// the lists' q-th entries (nl q >= K entries).  Cuts every list's count to
+// its entries at or before the better bound.
 __device__ __forceinline__ void prune_lists(const Key* L, int* cnt, int nl, int K, int stride) {
   const int lane = threadIdx.x & 31;
-  const bool full = lane < nl && cnt[lane] == K;
-  const Key tau = warp_max_key(full ? L[lane * stride + K - 1] : 0ull);
-  if (!__any_sync(0xffffffffu, full)) return;
+  const int q = (K + nl - 1) / nl;
+  const int n = lane < nl ? cnt[lane] : 0;
+  const bool full = n == K;
+  Key tau = warp_max_key(full ? L[lane * stride + K - 1] : 0ull);
+  if (__all_sync(0xffffffffu, lane >= nl || n >= q)) {
+    Key t2 = lane < nl ? L[lane * stride + q - 1] : ~0ull;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const Key y = __shfl_xor_sync(0xffffffffu, t2, o);
+      t2 = y < t2 ? y : t2;
+    }
+    tau = t2 > tau ? t2 : tau;
+  }
+  if (tau == 0ull) return;
   if (lane < nl) {
     const Key* lq = L + lane * stride;
     int lo = 0, hi = cnt[lane];   // entries at or before tau form a prefix
@@ -411,45 +426,38 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
     // ---- top-K survivors, K >= 2
     if (K >= 2) {
       if (j == 0) {
-        // first bound: K-th best of the lanes' best one (K <= 32) or two
-        // (K > 32) elements of this slot
-        float v0 = -INFINITY, v1 = -INFINITY;
-        int i0 = kNoIndex, i1 = kNoIndex;
+        // First bound, CTA-wide: every warp takes the q-th best of its lanes'
+        // maxima, q = ceil(K / 8); the smallest of the eight has 8 q >= K
+        // distinct elements at or before it (0: fewer valid lanes, no bound).
+        const int q = (K + kWarps - 1) / kWarps;
+        float v0 = -INFINITY;
+        int i0 = kNoIndex;
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {   // each lane sees its tokens in increasing order
-          const float xv = x[e];
-          const int xi = tbase + (e >> 2) * kTile + (e & 3);
-          const bool b0 = xv > v0, b1 = xv > v1;
-          v1 = b0 ? v0 : (b1 ? xv : v1);
-          i1 = b0 ? i0 : (b1 ? xi : i1);
-          v0 = b0 ? xv : v0;
-          i0 = b0 ? xi : i0;
+        for (int e = 0; e < kPer; ++e) {   // tokens ascend along the lane: first maximum kept
+          const bool t = x[e] > v0;
+          v0 = t ? x[e] : v0;
+          i0 = t ? tbase + (e >> 2) * kTile + (e & 3) : i0;
         }
         const Key c0 = mkkey(v0, i0);
-        const Key c1 = K > 32 ? mkkey(v1, i1) : 0ull;
-        int r0 = 0, r1 = 0;
-        if (K <= 32) {
+        int r0 = 0;
 #pragma unroll 8
-          for (int s = 0; s < 32; ++s) r0 += __shfl_sync(0xffffffffu, c0, s) > c0 ? 1 : 0;
-        } else {
-#pragma unroll 8
-          for (int s = 0; s < 32; ++s) {
-            const Key o0 = __shfl_sync(0xffffffffu, c0, s), o1 = __shfl_sync(0xffffffffu, c1, s);
-            r0 += (o0 > c0 ? 1 : 0) + (o1 > c0 ? 1 : 0);
-            r1 += (o0 > c1 ? 1 : 0) + (o1 > c1 ? 1 : 0);
-          }
-        }
-        const bool h0 = (r0 == K - 1) & (c0 != 0ull);
-        const bool h1 = (K > 32) & (r1 == K - 1) & (c1 != 0ull);
-        const unsigned bal = __ballot_sync(0xffffffffu, h0 | h1);
-        // K distinct elements reach the K-th candidate; with fewer than K
-        // valid candidates every valid element survives
-        thr_v = -INFINITY;
-        thr_i = kNoIndex;
-        if (bal) {
-          const Key t = __shfl_sync(0xffffffffu, h0 ? c0 : c1, __ffs(bal) - 1);
-          thr_v = key_v(t);
-          thr_i = key_i(t);
+        for (int s = 0; s < 32; ++s) r0 += __shfl_sync(0xffffffffu, c0, s) > c0 ? 1 : 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, (r0 == q - 1) & (c0 != 0ull));
+        const Key wbound = bal ? __shfl_sync(0xffffffffu, c0, __ffs(bal) - 1) : 0ull;
+        if (lane == 0) S.red_best[warp] = wbound;
+        if (tid == 0) S.cta_bound = 0ull;
+        __syncthreads();
+        Key cb = S.red_best[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) cb = S.red_best[w] < cb ? S.red_best[w] : cb;
+        thr_v = cb ? key_v(cb) : -INFINITY;
+        thr_i = cb ? key_i(cb) : kNoIndex;
+      } else {
+        // the running bound: the best K-th entry any warp has cut to so far
+        const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
+        if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
+          thr_v = key_v(cb);
+          thr_i = key_i(cb);
         }
       }
       if (__any_sync(0xffffffffu, lm >= thr_v)) {
@@ -463,7 +471,21 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
 #pragma unroll
           for (int e = 0; e < kPer; ++e) pm |= survives(e) ? (1u << e) : 0u;
         }
-        for (;;) {
+        // common case: no lane holds more than one survivor.  A lone survivor
+        // has the lane maximum's value (any survivor of a lane whose maximum
+        // is above the bound is that maximum; at the bound all share its
+        // value); its token follows from its bit; positions from a ballot.
+        const unsigned one = __ballot_sync(0xffffffffu, pm != 0u);
+        if (__all_sync(0xffffffffu, (pm & (pm - 1u)) == 0u) && wn + __popc(one) <= kWarpCap) {
+          if (pm) {
+            const int e = __ffs(pm) - 1;
+            wb[wn + __popc(one & ((1u << lane) - 1u))] = mkkey(lm, tbase + (e >> 2) * kTile + (e & 3));
+          }
+          wn += __popc(one);
+          __syncwarp();
+          pm = 0u;
+        }
+        while (__any_sync(0xffffffffu, pm != 0u)) {
           const int cntp = __popc(pm);
           int incl = cntp;
 #pragma unroll
@@ -498,6 +520,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
           if (wn >= K && before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
             thr_v = key_v(wb[K - 1]);
             thr_i = key_i(wb[K - 1]);
+            if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
           }
           uint32_t keep = 0;
 #pragma unroll
@@ -506,33 +529,16 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
           if (!__any_sync(0xffffffffu, pm != 0u)) break;
         }
       }
-      if (j == 0) {
-        // Cut the first slot's survivors to each warp's best K (sorted), then
-        // take the exact K-th best of the whole CTA's first slot from the
-        // union of the warp lists as every warp's bound from here on.
-        if (wn > 0) wn = warp_select(wb, wn, K, wb);
-        if (lane == 0) S.lcnt[warp] = wn;
-        if (tid == 0) S.cta_bound = 0ull;
-        __syncthreads();
-        if (warp == 0) prune_lists(&S.wbuf[0][0], S.lcnt, kWarps, K, kWarpCap);
-        __syncthreads();
-        for (int e = tid; e < kWarps * K; e += kThreads) {
-          const int w = e / K, c = e - w * K;
-          if (c >= S.lcnt[w]) continue;
-          const Key ent = S.wbuf[w][c];
-          if (union_rank(&S.wbuf[0][0], S.lcnt, kWarps, kWarpCap, ent) == K - 1) S.cta_bound = ent;
+      // keep the buffer short: past max(2K, 64) entries cut it to the best K,
+      // which raises this warp's bound and, through the shared running bound,
+      // every other warp's
+      if (wn > (2 * K > 64 ? 2 * K : 64)) {
+        wn = warp_select(wb, wn, K, wb);
+        if (before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
+          thr_v = key_v(wb[K - 1]);
+          thr_i = key_i(wb[K - 1]);
+          if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
         }
-        __syncthreads();
-        const Key cb = S.cta_bound;
-        if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
-          thr_v = key_v(cb);
-          thr_i = key_i(cb);
-        }
-        // the warp's sorted list keeps only what reaches the bound
-        int keep = 0;
-        for (int c = lane; c < wn; c += 32)
-          keep += !before(thr_v, thr_i, key_v(wb[c]), key_i(wb[c])) ? 1 : 0;
-        wn = warp_sum_i(keep);
       }
     }
   }

@@ -35,7 +35,7 @@ struct VerifyArgs {
   RowStream rs;
   int m;
   int mode[kMaxItems];
-  float temperature[kMaxItems];
+  double inv_temperature[kMaxItems];   // 1 / T
   float top_p[kMaxItems];
   int top_k[kMaxItems];
   const int32_t* parents[kMaxItems];
@@ -59,9 +59,9 @@ __device__ __forceinline__ double warp_incl_scan_d(double v) {
 }
 
 // p(t) under the full-vocabulary target distribution (lane-local).
-__device__ __forceinline__ double full_prob(const float* lrow, int t, double rowmax, double T,
-                                            double zsum) {
-  return exp_d((static_cast<double>(__ldg(lrow + t)) - rowmax) / T) / zsum;
+__device__ __forceinline__ double full_prob(const float* lrow, int t, double rowmax, double invT,
+                                            double inv_zsum) {
+  return exp_d((static_cast<double>(__ldg(lrow + t)) - rowmax) * invT) * inv_zsum;
 }
 
 // Decision of the walk at one node (warp 0 of the node's row leader): the
@@ -75,12 +75,12 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
   const int m = A.m;
   const int node = static_cast<int>(row - static_cast<int64_t>(item) * m);
   const int mode = A.mode[item];
-  const double T = static_cast<double>(A.temperature[item]);
+  const double invT = A.inv_temperature[item];
   const double top_p = static_cast<double>(A.top_p[item]);
   const int K = A.top_k[item];
   const uint64_t seed = A.seed[item];
-  const int32_t* parents = A.parents[item];
-  const int32_t* tokens = A.tokens[item];
+  const int* parents = S.aux;                   // prefetched at kernel start
+  const int* tokens = S.aux + EAGLE_MAX_TREE;
   const int TR = A.rs.tiles_per_row;
 
   int* kn = reinterpret_cast<int*>(S.ring[0]);          // children (node ids), node order
@@ -97,7 +97,7 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
 #pragma unroll
     for (int r = 0; r < EAGLE_MAX_TREE / 32; ++r) {
       const int i = lane + 32 * r;
-      pv[r] = (i > node && i < m) ? __ldg(parents + i) : -2;
+      pv[r] = (i > node && i < m) ? parents[i] : -2;
     }
 #pragma unroll
     for (int r = 0; r < EAGLE_MAX_TREE / 32; ++r) {
@@ -107,7 +107,7 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
       if (is) {
         const int pos = nk + __popc(bal & ((1u << lane) - 1u));
         kn[pos] = i;
-        kt[pos] = __ldg(tokens + i);
+        kt[pos] = tokens[i];
       }
       nk += __popc(bal);
     }
@@ -126,19 +126,19 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
   } else {
     // ---- the warped target distribution at this node
     const float* lrow = A.rs.base[item] + static_cast<int64_t>(node) * A.rs.row_stride;
-    double rowmax = 0.0, zsum = 1.0;
+    double rowmax = 0.0, zsum = 1.0, izsum = 1.0;
     int nkeep = 0;
     if (mode == kModeTopK) {
       int cnt = S.rcount;
       if (cnt > K) cnt = K;
       double z[2], pr[2];
       int id[2];
-      const double z0 = static_cast<double>(key_v(S.rlist[0])) / T;
+      const double z0 = static_cast<double>(key_v(S.rlist[0])) * invT;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int e = lane + 32 * hh;
         if (e < cnt) {
-          z[hh] = static_cast<double>(key_v(S.rlist[e])) / T;
+          z[hh] = static_cast<double>(key_v(S.rlist[e])) * invT;
           id[hh] = key_i(S.rlist[e]);
           pr[hh] = exp_d(z[hh] - z0);
         } else {
@@ -146,9 +146,9 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
           id[hh] = kNoIndex;
         }
       }
-      const double tot = warp_sum_d(pr[0] + pr[1]);
-      pr[0] /= tot;
-      pr[1] /= tot;
+      const double itot = 1.0 / warp_sum_d(pr[0] + pr[1]);
+      pr[0] *= itot;
+      pr[1] *= itot;
       nkeep = cnt;
       if (top_p < 1.0) {
         // entries are in probability order; keep the shortest prefix whose
@@ -164,9 +164,9 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
         nkeep = last + 1;
         if (lane > last) pr[0] = 0.0;
         if (lane + 32 > last) pr[1] = 0.0;
-        const double tot2 = warp_sum_d(pr[0] + pr[1]);
-        pr[0] /= tot2;
-        pr[1] /= tot2;
+        const double itot2 = 1.0 / warp_sum_d(pr[0] + pr[1]);
+        pr[0] *= itot2;
+        pr[1] *= itot2;
       }
       kp[lane] = pr[0];
       kid[lane] = lane < nkeep ? id[0] : kNoIndex;
@@ -176,6 +176,7 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
     } else {  // full vocabulary
       rowmax = static_cast<double>(S.rmax);
       zsum = S.rsum;
+      izsum = 1.0 / zsum;
     }
     auto prob_of = [&](int t) -> double {  // lane-local
       if (mode == kModeTopK) {
@@ -184,7 +185,7 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
           if (kid[e] == t) v = kp[e];
         return v;
       }
-      return full_prob(lrow, t, rowmax, T, zsum);
+      return full_prob(lrow, t, rowmax, invT, izsum);
     };
 
     // ---- children in node order, 32 at a time: child j is accepted iff
@@ -262,13 +263,13 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
                 mass += static_cast<double>(v.y) *
                         static_cast<double>(ex2((v.x - static_cast<float>(rowmax)) * static_cast<float>(c2)));
             }
-            mass /= zsum;
+            mass *= izsum;
             for (int r = 0; r < nk; ++r) {   // rejected tokens of this tile, each once
               const int rt = kt[r];
               if (rt / kTile != t) continue;
               bool first = true;
               for (int r2 = 0; r2 < r; ++r2) first &= kt[r2] != rt;
-              if (first) mass -= full_prob(lrow, rt, rowmax, T, zsum);
+              if (first) mass -= full_prob(lrow, rt, rowmax, invT, izsum);
             }
             if (mass < 0.0) mass = 0.0;
           }
@@ -292,7 +293,7 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
           double mass = 0.0;
           if (t < A.rs.vocab && !is_rejected(t)) {
             const float x = __ldg(lrow + t);
-            mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) / zsum;
+            mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) * izsum;
           }
           lm[q] = mass;
           lsum += mass;
@@ -362,9 +363,24 @@ static __device__ __noinline__ void follow_path(const VerifyArgs& A, int item, S
 __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_constant__ VerifyArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
+  // the row leader's warp 0 prefetches its item's tree (parents, tokens)
+  // while the stream runs
+  const int PC = A.rs.ctas_per_row;
+  if (blockIdx.x % PC == 0 && threadIdx.x < 32) {
+    const int item = static_cast<int>((blockIdx.x / PC) / A.m);
+    for (int i = threadIdx.x; i < A.m; i += 32) {
+      cp_async4(S.aux + i, A.parents[item] + i);
+      cp_async4(S.aux + EAGLE_MAX_TREE + i, A.tokens[item] + i);
+    }
+    cp_async_commit();
+  }
   const RowCtx cx = stream_row(A.rs, S);
   if (!cx.leader) return;
-  if (threadIdx.x < 32) node_decision(A, cx.row, cx.item, S);
+  if (threadIdx.x < 32) {
+    cp_async_wait_all();
+    __syncwarp();
+    node_decision(A, cx.row, cx.item, S);
+  }
   if (item_arrive(A.rs, S, cx.item) && threadIdx.x < 32) follow_path(A, cx.item, S);
 }
 
@@ -402,7 +418,7 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
     }
     A.mode[i] = mode;
     A.top_k[i] = k;
-    A.temperature[i] = p.greedy ? 1.f : p.temperature;
+    A.inv_temperature[i] = p.greedy ? 1.0 : 1.0 / static_cast<double>(p.temperature);
     A.top_p[i] = p.greedy ? 1.f : p.top_p;
     A.parents[i] = trees[i].parents;
     A.tokens[i] = trees[i].tokens;
