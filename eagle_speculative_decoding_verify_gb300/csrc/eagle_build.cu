@@ -152,54 +152,34 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
     base += kk;
   }
 
-  // final rerank: the best need = m-1 of the C candidates.  Every level's
-  // list is sorted, so the kept set is a prefix of each level: warp w finds
-  // the cut of level w (and w+8, ...) by binary search over its positions,
-  // the global rank of a probe being its position plus, over the other
-  // levels (one lane each), the entries before it (binary search over that
+  // final rerank: the best need = m-1 of the C candidates.  The global rank
+  // of a candidate is its rank in its own level plus, for every other level,
+  // the number of that level's entries before it (a binary search over the
   // level's keys in sorted order, materialised over the row top-k scratch,
-  // which is no longer needed).
+  // which is no longer needed); it is kept if that rank is below need.
+  // Every candidate is ranked independently, all in parallel.
   uint64_t* skey = reinterpret_cast<uint64_t*>(rv);   // rv and ri are contiguous: 8 C bytes
   for (int i = tid; i < C; i += kThreads) skey[i] = key[srt[i]];
-  int* cut = warp_tot;                                 // [D] kept entries per level (D <= 16)
   __syncthreads();
   const int need = m - 1;
-  {
-    const int lane = tid & 31, warp = tid >> 5;
-    auto lbase = [&](int l) { return l == 0 ? 0 : k + (l - 1) * kk; };
-    auto llen = [&](int l) { return l == 0 ? k : kk; };
-    for (int l = warp; l < D; l += kWarps) {
-      int lo = 0, hi = llen(l);   // first position whose global rank reaches need
-      if (need <= 0) hi = 0;
-      else if (need >= C) lo = hi;
-      while (lo < hi) {
-        const int p = (lo + hi) >> 1;
-        const int ap = srt[lbase(l) + p];
-        const uint64_t kv = key[ap];
-        int cnt = 0;
-        if (lane < D && lane != l) {   // entries of level `lane` before (kv, ap)
-          const int lb = lbase(lane);
-          int a = 0, b = llen(lane);
-          while (a < b) {
-            const int mid = (a + b) >> 1;
-            const uint64_t o = skey[lb + mid];
-            const bool go = (o > kv) | ((o == kv) & (srt[lb + mid] < ap));
-            if (go) a = mid + 1;
-            else b = mid;
-          }
-          cnt = a;
-        }
-        const int rank = p + warp_sum_i(cnt);
-        if (rank < need) lo = p + 1;
-        else hi = p;
-      }
-      if (lane == 0) cut[l] = lo;
-    }
-  }
-  __syncthreads();
   for (int a = tid; a < C; a += kThreads) {
     const int la = a < k ? 0 : 1 + (a - k) / kk;
-    node[a] = lrank[a] < cut[la] ? 1 : 0;
+    int rank = lrank[a];
+    const uint64_t kv = key[a];
+    for (int l = 0; l < D && rank < need; ++l) {
+      if (l == la) continue;
+      const int lb = l == 0 ? 0 : k + (l - 1) * kk;
+      int lo = 0, hi = l == 0 ? k : kk;   // entries of level l before (kv, a)
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const uint64_t o = skey[lb + mid];
+        const bool go = (o > kv) | ((o == kv) & (srt[lb + mid] < a));
+        lo = go ? mid + 1 : lo;
+        hi = go ? hi : mid;
+      }
+      rank += lo;
+    }
+    node[a] = rank < need ? 1 : 0;
   }
   __syncthreads();
   const int per = (C + kThreads - 1) / kThreads;

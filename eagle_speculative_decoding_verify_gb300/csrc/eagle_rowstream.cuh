@@ -111,6 +111,8 @@ __device__ __forceinline__ Key warp_max_key(Key k) {
   return k;
 }
 
+static_assert(kWarps * kKMax >= kThreads, "the warp lists hold one key per thread (first-slot bound)");
+
 struct StreamSmem {
   float ring[kSlots][kSlotElems];      // 64 KB; with wbuf reused by the final steps
   Key wbuf[kWarps][kWarpCap];          // 16 KB warp survivor buffers
@@ -128,7 +130,8 @@ struct StreamSmem {
   float rmax;
   int rcount;
   int flag;
-  Key cta_bound;                       // K-th best of the CTA's first slot
+  int ncand;                           // first-slot bound: candidate lane maxima
+  Key cta_bound;                       // running bound: K-th best of the CTA so far
   int aux[2 * EAGLE_MAX_TREE];         // callers' own data (never touched by the stream)
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
@@ -301,6 +304,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
       mbar_init(&S.empty[s], kWarps);
     }
     fence_barrier_init();
+    S.ncand = 0;
   }
   __syncthreads();
   if (tid == 0)
@@ -452,6 +456,27 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
         for (int w = 1; w < kWarps; ++w) cb = S.red_best[w] < cb ? S.red_best[w] : cb;
         thr_v = cb ? key_v(cb) : -INFINITY;
         thr_i = cb ? key_i(cb) : kNoIndex;
+        // Refinement for the following slots: the exact K-th best lane
+        // maximum of the CTA (K distinct elements reach it).  The lane maxima
+        // at or before cb are the candidates (at least K of them); each counts
+        // the candidates before it, and the one with K - 1 before it raises
+        // the running bound.  cb is the same in every thread.
+        if (cb != 0ull) {
+          const bool cand = c0 >= cb;
+          const unsigned bm = __ballot_sync(0xffffffffu, cand);
+          int off = 0;
+          if (lane == 0 && bm) off = atomicAdd(&S.ncand, __popc(bm));
+          off = __shfl_sync(0xffffffffu, off, 0);
+          Key* ck = S.wlist;   // the warp lists are filled only after the stream
+          if (cand) ck[off + __popc(bm & ((1u << lane) - 1u))] = c0;
+          __syncthreads();
+          if (cand) {
+            const int n = S.ncand;
+            int r = 0;
+            for (int i = 0; i < n; ++i) r += ck[i] > c0 ? 1 : 0;
+            if (r == K - 1) atomicMax(&S.cta_bound, c0);
+          }
+        }
       } else {
         // the running bound: the best K-th entry any warp has cut to so far
         const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
