@@ -360,10 +360,10 @@ def max_over_ranks(x, world, device):
 # known ncu DRAM traffic per launch (bytes), keyed by kernel and source hash;
 # entries whose hash no longer matches the sources are reported as null
 TRAFFIC = {
-    # profiles/verify_kernel_c2.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "verify:c2": ("8009c80761b6", 36609280),
-    "build:c2": ("8009c80761b6", 31124224),
-    "attn:c2": ("8009c80761b6", 17394944),
+    # profiles/*_c2.md: dram__bytes_read.sum + dram__bytes_write.sum of one launch
+    "build:c2": ("02a24cf56b48", 31122688),
+    "verify:c2": ("02a24cf56b48", 36601600),
+    "attn:c2": ("02a24cf56b48", 17389824),
 }
 
 
