@@ -206,18 +206,21 @@ class Step:
                     for n in ("q", "tree_k", "tree_v")))
 
 
-def attn_long(eb, wl, dev, reps=5):
+def attn_long(eb, wl, dev, reps=5, n_layers=None):
     """Tree attention at long context: 32 independent layers of a
     llama-3-8b-shaped KV cache (8 kv heads, d 128, bf16 prefix 32768; 4.3 GB,
-    far above L2) for one 60-token tree, all layers in one batched call.
-    Returns achieved GB/s (algorithmic bytes / device time) and TFLOP/s."""
+    far above L2) for one 60-token tree, all layers in one batched call
+    (n_layers of them when given: a smaller case of the same kernel, for
+    profiling).  Returns achieved GB/s (algorithmic bytes / device time) and
+    TFLOP/s."""
     import torch
     w = wl.WORKLOADS["c3"]
+    nl = w.layers if n_layers is None else n_layers
     draft = wl.draft_logits(w).to(dev)
     tree = eb.eagle_tree_build(draft, w.top_k, w.depth, w.total_tokens, wl.root_token(w))
-    layers = [wl.attention_inputs(w, layer=l, device=dev) for l in range(w.layers)]
+    layers = [wl.attention_inputs(w, layer=l, device=dev) for l in range(nl)]
     outs = [torch.empty(w.total_tokens, w.n_q_heads, w.head_dim, device=dev)
-            for _ in range(w.layers)]
+            for _ in range(nl)]
     items = [eb.attn_item(a["q"], a["k_cache"], a["v_cache"], a["tree_k"], a["tree_v"],
                           tree.mask, o) for a, o in zip(layers, outs)]
     dt = eb.EAGLE_BF16
@@ -241,12 +244,12 @@ def attn_long(eb, wl, dev, reps=5):
         s.synchronize()
         times.append(e0.elapsed_time(e1) * 1e-3)
     t = statistics.median(times)
-    m, hq, hkv, d, S, L = w.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.prefix, w.layers
+    m, hq, hkv, d, S, L = w.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.prefix, nl
     nbytes = L * (2 * S * hkv * d * 2 + m * hq * d * 2 + 2 * m * hkv * d * 2 + m * hq * d * 4)
     flops = L * 4.0 * m * hq * (S + m) * d
     del layers, outs, items, ws
     torch.cuda.empty_cache()
-    return {"workload": "c3: 32 layers x bf16 prefix 32768, 32/8 heads d128, 60-token tree, "
+    return {"workload": f"c3: {nl} layers x bf16 prefix 32768, 32/8 heads d128, 60-token tree, "
                         "one batched call", "us": round(t * 1e6, 1),
             "achieved_gbs": round(nbytes / t / 1e9, 1), "achieved_tflops": round(flops / t / 1e12, 1),
             "bytes": nbytes}
@@ -553,7 +556,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long-attn", action="store_true",
                     help="skip the 32-layer x 32K-context attention measurement")
+    ap.add_argument("--long-attn-only", type=int, default=0, metavar="LAYERS",
+                    help="only time the long-context attention, on LAYERS layers "
+                         "(a profiling case; prints its own JSON line)")
     args = ap.parse_args()
+    if args.long_attn_only:
+        import torch
+        from eagle_speculative_decoding_verify_gb300 import binding as eb, workloads as wl
+        res = attn_long(eb, wl, torch.device("cuda"), reps=max(args.steps, 1),
+                        n_layers=args.long_attn_only)
+        print(json.dumps(res), flush=True)
+        return 0
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
