@@ -13,7 +13,10 @@
 //   * the exact top-K (value desc, token id asc), K <= 64.  Each warp keeps
 //     the elements at or before its bound in a private buffer.  The first
 //     bound is CTA-wide: the smallest of the warps' ceil(K/8)-th best lane
-//     maxima of the first slot (K distinct elements reach it).  A warp whose
+//     maxima of the first slot (K distinct elements reach it) for that slot,
+//     then the exact K-th best of the CTA's lane maxima (found by counting
+//     among the lane maxima at or before the first bound) as the running
+//     bound for the following slots.  A warp whose
 //     buffer grows past max(2K, 64) entries cuts it to its best K, which
 //     raises its bound to its exact K-th best; that entry is also published
 //     as the CTA's running bound (shared-memory atomicMax on the 64-bit
