@@ -328,29 +328,44 @@ def _time_kernels(torch, step, s, flush, K):
 
 def _time_e2e(torch, step, s, flush, K):
     """Same step with per-step inputs from pinned host memory and the result
-    read back; device-timed around copies + calls."""
+    read back; device-timed around copies + calls.  The target logits, which
+    only the verify call reads, are copied on a second stream once the draft
+    logits are in, so that their transfer overlaps the tree build and the
+    attention."""
     pin = {n: step.attn_h[n].pin_memory() for n in ("q", "tree_k", "tree_v")}
     draft_p = step.draft_h.pin_memory()
     target_p = step.target_h.pin_memory()
     out_acc = torch.empty(step.acc.numel() + 2, dtype=torch.int32).pin_memory()
+    s2 = torch.cuda.Stream(device=s.device)
     times = []
     evs = []
-    with torch.cuda.stream(s):
-        for _ in range(K):
+    for _ in range(K):
+        with torch.cuda.stream(s):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            drafted = torch.cuda.Event()
             e0.record(s)
             step.draft.copy_(draft_p, non_blocking=True)
+            drafted.record(s)
+        s2.wait_event(drafted)
+        with torch.cuda.stream(s2):
+            step.target.copy_(target_p, non_blocking=True)
+            targeted = torch.cuda.Event()
+            targeted.record(s2)
+        with torch.cuda.stream(s):
             for n in ("q", "tree_k", "tree_v"):
                 step.attn[n].copy_(pin[n], non_blocking=True)
-            step.target.copy_(target_p, non_blocking=True)
-            step.run(s)
+            step.build(s)
+            step.attention(s)
+            s.wait_event(targeted)
+            step.verify(s)
             out_acc[: step.acc.numel()].copy_(step.acc, non_blocking=True)
             out_acc[-2:-1].copy_(step.n_acc, non_blocking=True)
             out_acc[-1:].copy_(step.bonus, non_blocking=True)
             e1.record(s)
             evs.append((e0, e1))
     s.synchronize()
+    s2.synchronize()
     for e0, e1 in evs:
         times.append(e0.elapsed_time(e1) * 1e3)
     d2h = (step.acc.numel() + 2) * 4
