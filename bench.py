@@ -263,6 +263,73 @@ def attn_long(eb, wl, dev, reps=5, n_layers=None):
             "bytes": nbytes}
 
 
+def kv_commit_bench(eb, wl, dev, step, s, reps=200):
+    """The KV commit after acceptance (append the accepted path's keys and
+    values to the prefix cache): device time of one call for the c2 layer and
+    of one batched call over the 32 layers of the c3 shape (32K prefix each),
+    for the path to a deepest node of the step's tree (root + one node per depth), each
+    call replayed from a CUDA graph.  Tens of KB to 1 MB move per call, so
+    the figure is a latency, reported with its bytes (read + written)."""
+    import torch
+    w = step.w
+    parents = step.tree.parents.cpu().tolist()
+    depth = step.tree.depth.cpu().tolist()
+    node = max(range(len(depth)), key=lambda i: (depth[i], -i))   # a deepest node
+    path = []
+    while node >= 0:   # its ancestors, root first
+        path.append(node)
+        node = parents[node]
+    path = path[::-1]
+    acc = torch.zeros(w.total_tokens, dtype=torch.int32, device=dev)
+    acc[: len(path)] = torch.tensor(path, dtype=torch.int32, device=dev)
+    n_acc = torch.tensor([len(path) - 1], dtype=torch.int32, device=dev)
+    rows = len(path)
+    m, hkv, d = w.total_tokens, w.n_kv_heads, w.head_dim
+    el = 2 if w.dtype == "bf16" else 4
+    kc = torch.empty(hkv, w.prefix + m, d, dtype=step.attn["k_cache"].dtype, device=dev)
+    vc = torch.empty_like(kc)
+    ws = eb.workspace(eb.eagle_kv_commit_workspace_size(), dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(s)
+        s.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    c2_us = timed(lambda: eb.eagle_kv_commit(kc, vc, step.attn["tree_k"], step.attn["tree_v"],
+                                             acc, n_acc, w.prefix, ws=ws, stream=s))
+    w3 = wl.WORKLOADS["c3"]
+    L3, S3 = w3.layers, w3.prefix
+    g = torch.Generator(device=dev).manual_seed(7)
+    items, keep = [], []
+    for _ in range(L3):
+        k3 = torch.empty(w3.n_kv_heads, S3 + m, w3.head_dim, dtype=torch.bfloat16, device=dev)
+        v3 = torch.empty_like(k3)
+        tk = torch.randn(m, w3.n_kv_heads, w3.head_dim, generator=g, device=dev).to(torch.bfloat16)
+        tv = torch.randn(m, w3.n_kv_heads, w3.head_dim, generator=g, device=dev).to(torch.bfloat16)
+        keep.append((k3, v3, tk, tv))
+        items.append(eb.kv_item(k3, v3, tk, tv, acc, n_acc, S3))
+    c3_us = timed(lambda: eb.eagle_kv_commit_batched(items, w3.n_kv_heads, w3.head_dim,
+                                                     eb.EAGLE_BF16, ws=ws, stream=s))
+    st, _ = eb.workspace_error(ws, s)
+    assert st == 0, f"kv commit device error {st}"
+    b2 = 2 * 2 * rows * hkv * d * el
+    b3 = L3 * 2 * 2 * rows * w3.n_kv_heads * w3.head_dim * 2
+    del keep, items
+    return {"rows": rows, "c2_us": round(c2_us, 2), "c2_bytes": b2,
+            "c3_32layers_us": round(c3_us, 2), "c3_bytes": b3,
+            "c3_achieved_gbs": round(b3 / (c3_us * 1e-6) / 1e9, 1)}
+
+
 class L2Flush:
     """Evicts the step's inputs from L2 before every step: writes 512 MB (4x
     L2), then reads 256 MB so that the lines left behind are clean and the
@@ -481,6 +548,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": step.launches * args.steps,
         "clocks": sampler.summary(),
     }
+    with torch.cuda.stream(s):
+        line["kv_commit"] = kv_commit_bench(eb, wl, dev, step, s)
     if not args.no_long_attn:
         la = attn_long(eb, wl, dev)
         la["frac_hbm"] = round(la["achieved_gbs"] / hbm, 4)

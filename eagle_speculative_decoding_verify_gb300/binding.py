@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle.so
 
 EAGLE_OK = 0
 EAGLE_ERR_WORKSPACE_TOO_SMALL = 3
+EAGLE_ERR_DEVICE_ASSERT = 6
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape",
                 3: "workspace too small", 4: "CUDA error", 5: "device wait timed out",
                 6: "device invariant violated"}
@@ -55,6 +56,14 @@ class CAttnItem(ctypes.Structure):
                 ("prefix_len", ctypes.c_int32), ("m", ctypes.c_int32)]
 
 
+class CKvItem(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("tree_k", ctypes.c_void_p), ("tree_v", ctypes.c_void_p),
+                ("accepted", ctypes.c_void_p), ("n_accepted", ctypes.c_void_p),
+                ("cache_head_stride", ctypes.c_int64), ("prefix_len", ctypes.c_int32),
+                ("m", ctypes.c_int32)]
+
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -84,6 +93,10 @@ EXPORTS = {
                                  _P, _P, _P, _P, _SZ, _P]),
     "eagle_tree_verify_batched": (_I32, [_I32, _P, _I64, _I32, _P, _P, _P, _U64, _P, _P, _P,
                                          _P, _SZ, _P]),
+    "eagle_kv_commit_workspace_size": (_SZ, []),
+    "eagle_kv_commit": (_I32, [_P, _P, _I64, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P,
+                               _SZ, _P]),
+    "eagle_kv_commit_batched": (_I32, [_P, _I32, _I32, _I32, _I32, _P, _SZ, _P]),
 }
 
 _lib = None
@@ -335,3 +348,38 @@ def eagle_tree_verify_batched(target_logits, trees, params, seeds, step=0, accep
                                            _ptr(ws), ws.numel(), _stream(stream)),
            "eagle_tree_verify_batched")
     return accepted, n_accepted, bonus_tokens
+
+
+# ----------------------------------------------------------------- KV commit
+def eagle_kv_commit_workspace_size():
+    return lib().eagle_kv_commit_workspace_size()
+
+
+def kv_item(k_cache, v_cache, tree_k, tree_v, accepted, n_accepted, prefix_len):
+    """C item for one commit (k/v cache [Hkv, cap, d], rows contiguous)."""
+    return CKvItem(k_cache.data_ptr(), v_cache.data_ptr(), tree_k.data_ptr(), tree_v.data_ptr(),
+                   accepted.data_ptr(), n_accepted.data_ptr(), k_cache.stride(0),
+                   int(prefix_len), tree_k.shape[0])
+
+
+def eagle_kv_commit(k_cache, v_cache, tree_k, tree_v, accepted, n_accepted, prefix_len, ws=None,
+                    stream=None):
+    """Append the accepted path (node ids ``accepted``, *n_accepted + 1 of them,
+    both device int32) of tree_k/v [m, Hkv, d] to k/v_cache [Hkv, cap, d] at
+    rows prefix_len ..; returns nothing (the caches are updated in place)."""
+    hkv, _, d = k_cache.shape
+    if ws is None:
+        ws = workspace(eagle_kv_commit_workspace_size(), k_cache.device)
+    _check(lib().eagle_kv_commit(_ptr(k_cache), _ptr(v_cache), k_cache.stride(0), int(prefix_len),
+                                 _ptr(tree_k), _ptr(tree_v), tree_k.shape[0], hkv, d,
+                                 _dtype_code(k_cache), _ptr(accepted), _ptr(n_accepted), _ptr(ws),
+                                 ws.numel(), _stream(stream)), "eagle_kv_commit")
+
+
+def eagle_kv_commit_batched(items, n_kv_heads, head_dim, dtype, ws=None, stream=None, device=None):
+    """items: list of CKvItem (see kv_item)."""
+    arr = (CKvItem * len(items))(*items)
+    if ws is None:
+        ws = workspace(eagle_kv_commit_workspace_size(), device)
+    _check(lib().eagle_kv_commit_batched(arr, len(items), n_kv_heads, head_dim, dtype, _ptr(ws),
+                                         ws.numel(), _stream(stream)), "eagle_kv_commit_batched")

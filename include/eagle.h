@@ -303,6 +303,63 @@ eagle_status eagle_tree_verify_batched(int32_t n_items, const float* const* targ
                                        int32_t* bonus_tokens,
                                        void* ws, size_t ws_bytes, eagle_stream stream);
 
+/* ------------------------------------------------------------------------
+ * eagle_kv_commit -- [disc] reply on KV caches (the target model keeps the
+ * KV cache of accepted tokens only) and [blog] "Single-Pass Tree
+ * Verification" (the tree's keys / values come from one target pass; the
+ * accepted tokens form a root-to-node path).  Appends the accepted path to
+ * the prefix cache, for every kv head h and i = 0 .. *n_accepted:
+ *
+ *   k_cache[h][prefix_len + i][:] = tree_k[accepted[i]][h][:]   (same for v)
+ *
+ * The root is node 0 of the tree and has keys / values like every tree
+ * token, so *n_accepted + 1 rows are written and the new prefix length is
+ * prefix_len + *n_accepted + 1.  No other cache row is touched.
+ *
+ * k_cache,
+ * v_cache:   [n_kv_heads][cache_head_stride] as for eagle_tree_attn; the
+ *            head stride is also the capacity (cache_head_stride / head_dim
+ *            rows), a multiple of head_dim; 16-byte aligned.
+ * tree_k,
+ * tree_v:    [m][n_kv_heads][head_dim] (16-byte aligned).
+ * accepted:  device int32, node ids of the accepted path starting with the
+ *            root; n_accepted: device int32 scalar (both as written by
+ *            eagle_tree_verify; read on the device, no host synchronisation).
+ * dtype:     EAGLE_BF16 or EAGLE_F32; head_dim * element size a multiple of
+ *            16 bytes.
+ * ws:        at least eagle_kv_commit_workspace_size() bytes (its error word).
+ * Errors: bad arguments -> EAGLE_ERR_INVALID_ARG / UNSUPPORTED_SHAPE before
+ * any launch.  A device value out of range (*n_accepted outside [0, m), the
+ * committed rows past the capacity, an accepted id outside [0, m)) is
+ * recorded as EAGLE_ERR_DEVICE_ASSERT in the workspace error word and the
+ * affected rows are not written.
+ * ------------------------------------------------------------------------ */
+size_t eagle_kv_commit_workspace_size(void);
+
+eagle_status eagle_kv_commit(void* k_cache, void* v_cache, int64_t cache_head_stride,
+                             int32_t prefix_len, const void* tree_k, const void* tree_v,
+                             int32_t m, int32_t n_kv_heads, int32_t head_dim, eagle_dtype dtype,
+                             const int32_t* accepted, const int32_t* n_accepted,
+                             void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* One commit per item (a layer of the target, or a sequence of a batch), all
+ * in one launch per 64 items; same head count, head_dim and dtype. */
+typedef struct {
+  void*          k_cache;
+  void*          v_cache;
+  const void*    tree_k;
+  const void*    tree_v;
+  const int32_t* accepted;
+  const int32_t* n_accepted;
+  int64_t        cache_head_stride;
+  int32_t        prefix_len;
+  int32_t        m;
+} eagle_kv_item;
+
+eagle_status eagle_kv_commit_batched(const eagle_kv_item* items, int32_t n_items,
+                                     int32_t n_kv_heads, int32_t head_dim, eagle_dtype dtype,
+                                     void* ws, size_t ws_bytes, eagle_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
