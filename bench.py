@@ -108,20 +108,38 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
-def _kernel_source_hash():
-    """sha1 of the kernel sources with comments and blank lines removed, so
-    that editing a comment does not void the recorded traffic figures."""
+# the sources each timed kernel is compiled from (its .cu and every header
+# it includes, directly or not)
+KERNEL_SOURCES = {
+    "build": ["eagle_build.cu", "eagle_stream_host.h", "eagle_rowstream.cuh", "eagle_host.h",
+              "eagle_common.cuh"],
+    "verify": ["eagle_verify.cu", "eagle_philox.cuh", "eagle_stream_host.h", "eagle_rowstream.cuh",
+               "eagle_host.h", "eagle_common.cuh"],
+    "attn": ["eagle_attn_tc.cu", "eagle_attn.cu", "eagle_attn.h", "eagle_tc.cuh", "eagle_host.h",
+             "eagle_common.cuh"],
+}
+
+
+def _kernel_source_hash(kernel):
+    """sha1 of one kernel's sources with comments and blank lines removed, so
+    that editing a comment, or another kernel, does not void its recorded
+    traffic figures."""
     import re
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "eagle_speculative_decoding_verify_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.normpath(os.path.join(csrc, name)), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
-        h.update(name.encode())
+        h.update(os.path.basename(name).encode())
         h.update("\n".join(lines).encode())
+    # of the public header, the constants the kernels use (limits, status codes)
+    with open(os.path.join(ROOT, "include", "eagle.h"), encoding="utf-8") as f:
+        consts = [ln.split("/*")[0].rstrip() for ln in f
+                  if re.match(r"\s*(#define\s+EAGLE_|EAGLE_[A-Z0-9_]+\s*=)", ln)]
+    h.update("\n".join(consts).encode())
     return h.hexdigest()[:12]
 
 
@@ -453,10 +471,11 @@ def max_over_ranks(x, world, device):
 # known ncu DRAM traffic per launch (bytes), keyed by kernel and source hash;
 # entries whose hash no longer matches the sources are reported as null
 TRAFFIC = {
-    # profiles/*_c2.md: dram__bytes_read.sum + dram__bytes_write.sum of one launch
-    "build:c2": ("41feb340df67", 31122688),
-    "verify:c2": ("41feb340df67", 36601600),
-    "attn:c2": ("41feb340df67", 17389824),
+    # profiles/*_c2.md: dram__bytes_read.sum + dram__bytes_write.sum of one launch,
+    # keyed by the kernel's source hash (_kernel_source_hash)
+    "build:c2": ("03f5a85d6f51", 31122688),
+    "verify:c2": ("7efcb1250654", 36601600),
+    "attn:c2": ("f0bf516efb78", 17389824),
 }
 
 
@@ -512,7 +531,6 @@ def run_ours(args, rank, world, local_rank):
     attn_gbs = step.bytes_attn() / (k_us["attn"] * 1e-6) / 1e9
     attn_tflops = step.flops_attn() / (k_us["attn"] * 1e-6) / 1e12
     dominant = max(k_us, key=k_us.get)
-    src_hash = _kernel_source_hash()
     if dominant == "attn" and step.flops_attn() / step.bytes_attn() > tf * 1e12 / (hbm * 1e9):
         roof = {"bound": "tensor", "achieved": attn_tflops, "peak": tf, "unit": "TFLOP/s",
                 "frac": attn_tflops / tf}
@@ -523,7 +541,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
     tr = TRAFFIC.get(f"{dominant}:{args.workload}")
     roof.update({"kernel": dominant, "peak_source": peak_src,
-                 "traffic": tr[1] if tr and tr[0] == src_hash else None})
+                 "traffic": tr[1] if tr and tr[0] == _kernel_source_hash(dominant) else None})
     step_roof_us = (step.bytes_build() / (hbm * 1e3) + step.bytes_verify() / (hbm * 1e3) +
                     max(step.bytes_attn() / (hbm * 1e3), step.flops_attn() / (tf * 1e6)))
     line = {
