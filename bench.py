@@ -348,6 +348,47 @@ def kv_commit_bench(eb, wl, dev, step, s, reps=200):
             "c3_achieved_gbs": round(b3 / (c3_us * 1e-6) / 1e9, 1)}
 
 
+def tree_expand_bench(eb, wl, dev, step, s, flush, reps=50):
+    """The per-depth tree build of a drafting round (one eagle_tree_expand
+    call per depth on that depth's draft rows, then eagle_tree_finalize) on
+    the step's draft logits, replayed from a CUDA graph with L2 flushed before
+    every round; the tree must equal the one-shot build's."""
+    import torch
+    w = step.w
+    k, D, m, V = w.top_k, w.depth, w.total_tokens, w.vocab
+    g = eb.TreeGrowth(k, D, V, dev)
+    out = eb.Tree(m, dev)
+    rows = [step.draft[0:1]] + [step.draft[1 + (l - 1) * k: 1 + l * k] for l in range(1, D)]
+
+    def round_():
+        for level in range(D):
+            g.expand(rows[level], level, stream=s)
+        g.finalize(m, step.root, out=out, stream=s)
+
+    for _ in range(3):
+        round_()
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        round_()
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        graph.replay()
+        e1.record(s)
+        s.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    st, _ = eb.workspace_error(g.ws, s)
+    same = (st == 0 and torch.equal(out.parents, step.tree.parents) and
+            torch.equal(out.mask, step.tree.mask))
+    assert same, "per-depth build differs from the one-shot build"
+    return {"us_per_round": round(statistics.median(times), 2), "launches": D + 1,
+            "bytes": (1 + (D - 1) * k) * V * 4,
+            "note": "L2 flushed before each round; rows of every depth from HBM"}
+
+
 class L2Flush:
     """Evicts the step's inputs from L2 before every step: writes 512 MB (4x
     L2), then reads 256 MB so that the lines left behind are clean and the
@@ -568,6 +609,7 @@ def run_ours(args, rank, world, local_rank):
     }
     with torch.cuda.stream(s):
         line["kv_commit"] = kv_commit_bench(eb, wl, dev, step, s)
+        line["tree_expand"] = tree_expand_bench(eb, wl, dev, step, s, flush)
     if not args.no_long_attn:
         la = attn_long(eb, wl, dev)
         la["frac_hbm"] = round(la["achieved_gbs"] / hbm, 4)

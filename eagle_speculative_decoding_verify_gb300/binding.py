@@ -93,6 +93,10 @@ EXPORTS = {
                                  _P, _P, _P, _P, _SZ, _P]),
     "eagle_tree_verify_batched": (_I32, [_I32, _P, _I64, _I32, _P, _P, _P, _U64, _P, _P, _P,
                                          _P, _SZ, _P]),
+    "eagle_tree_state_bytes": (_SZ, [_I32, _I32]),
+    "eagle_tree_expand_workspace_size": (_SZ, [_I32, _I32]),
+    "eagle_tree_expand": (_I32, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "eagle_tree_finalize": (_I32, [_P, _I32, _I32, _I32, _I32, CTree, _P, _SZ, _P]),
     "eagle_kv_commit_workspace_size": (_SZ, []),
     "eagle_kv_commit": (_I32, [_P, _P, _I64, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P,
                                _SZ, _P]),
@@ -383,3 +387,33 @@ def eagle_kv_commit_batched(items, n_kv_heads, head_dim, dtype, ws=None, stream=
         ws = workspace(eagle_kv_commit_workspace_size(), device)
     _check(lib().eagle_kv_commit_batched(arr, len(items), n_kv_heads, head_dim, dtype, _ptr(ws),
                                          ws.numel(), _stream(stream)), "eagle_kv_commit_batched")
+
+
+# ----------------------------------------------------------- incremental build
+class TreeGrowth:
+    """Device state of one drafting round of eagle_tree_expand calls."""
+
+    def __init__(self, top_k, depth, vocab, device=None):
+        dev = device or torch.device("cuda")
+        self.top_k, self.depth, self.vocab = int(top_k), int(depth), int(vocab)
+        self.state = torch.zeros(max(int(lib().eagle_tree_state_bytes(top_k, depth)), 16),
+                                 dtype=torch.uint8, device=dev)
+        self.ws = workspace(lib().eagle_tree_expand_workspace_size(top_k, vocab), dev)
+        self.frontier = torch.zeros(2, top_k, dtype=torch.int32, device=dev)
+
+    def expand(self, rows, level, stream=None):
+        """rows: fp32 [1 or top_k, V] with a row stride that is a multiple of 4.
+        Returns the new frontier (device int32 [2, top_k]: tokens, parent slots)."""
+        _check(lib().eagle_tree_expand(_ptr(rows), rows.stride(0), rows.shape[1], self.top_k,
+                                       self.depth, int(level), _ptr(self.state),
+                                       _ptr(self.frontier), _ptr(self.ws), self.ws.numel(),
+                                       _stream(stream)), "eagle_tree_expand")
+        return self.frontier
+
+    def finalize(self, total_tokens, root_token, out=None, stream=None):
+        out = out or Tree(total_tokens, self.state.device)
+        _check(lib().eagle_tree_finalize(_ptr(self.state), self.top_k, self.depth,
+                                         int(total_tokens), int(root_token), out.c(),
+                                         _ptr(self.ws), self.ws.numel(), _stream(stream)),
+               "eagle_tree_finalize")
+        return out

@@ -304,6 +304,50 @@ eagle_status eagle_tree_verify_batched(int32_t n_items, const float* const* targ
                                        void* ws, size_t ws_bytes, eagle_stream stream);
 
 /* ------------------------------------------------------------------------
+ * eagle_tree_expand / eagle_tree_finalize -- the tree of eagle_tree_build,
+ * grown one depth per call as the drafting loop produces the draft rows
+ * ([blog] "The Recurrent Feature Drafting Step": the draft model runs on the
+ * tokens just drafted, so the rows of depth l + 1 exist only once the
+ * frontier of depth l is known; [disc] reply on the dynamic tree: expanded
+ * step by step, pruned at the end of drafting).
+ *
+ * Call eagle_tree_expand for level = 0, 1, .., depth - 1 in order, then
+ * eagle_tree_finalize; the result equals eagle_tree_build on the same rows
+ * (level 0: the root's row; level l: row j = the draft row of frontier slot
+ * j of depth l, j = 0 .. top_k - 1, i.e. draft rows 1 + (l-1) top_k + j of
+ * the one-shot build).
+ *
+ * rows:         fp32 [1 or top_k][row_stride] (16-byte aligned, row_stride
+ *               % 4 == 0).
+ * state:        caller-owned device buffer of eagle_tree_state_bytes(top_k,
+ *               depth) bytes (16-byte aligned) holding the growing tree
+ *               between the calls of one drafting round (no host copy).
+ * frontier_out: device int32 [2][top_k] or null: the new frontier (the
+ *               top_k candidates of depth level + 1, best first): their
+ *               tokens, then the frontier slot of their parent at depth level
+ *               (0 at level 0) -- what the drafting loop feeds to its next
+ *               draft-model pass.
+ * ws:           eagle_tree_expand_workspace_size(top_k, vocab) bytes for the
+ *               expand calls; at least 256 bytes (its error word) for
+ *               finalize.
+ * Errors: as eagle_tree_build; calls out of order (a level before the
+ * previous one, finalize before depth levels) are recorded as
+ * EAGLE_ERR_DEVICE_ASSERT in the workspace error word and write nothing.
+ * ------------------------------------------------------------------------ */
+size_t eagle_tree_state_bytes(int32_t top_k, int32_t depth);
+
+size_t eagle_tree_expand_workspace_size(int32_t top_k, int32_t vocab);
+
+eagle_status eagle_tree_expand(const float* rows, int64_t row_stride, int32_t vocab,
+                               int32_t top_k, int32_t depth, int32_t level, void* state,
+                               int32_t* frontier_out, void* ws, size_t ws_bytes,
+                               eagle_stream stream);
+
+eagle_status eagle_tree_finalize(const void* state, int32_t top_k, int32_t depth,
+                                 int32_t total_tokens, int32_t root_token, eagle_tree out,
+                                 void* ws, size_t ws_bytes, eagle_stream stream);
+
+/* ------------------------------------------------------------------------
  * eagle_kv_commit -- [disc] reply on KV caches (the target model keeps the
  * KV cache of accepted tokens only) and [blog] "Single-Pass Tree
  * Verification" (the tree's keys / values come from one target pass; the
