@@ -82,3 +82,29 @@ def tree_attention_rows(q, k_cache, v_cache, tree_k, tree_v, mask, prefix_len,
         w = np.exp(s)
         out[n] = (w / w.sum()) @ vals
     return out
+
+
+def gather_pages(pool, block_table, prefix_len, page=128):
+    """A paged KV cache back to the contiguous layout: pool [Hkv, rows, d],
+    page j of the sequence (prefix tokens page*j .. page*j + page - 1) at pool
+    rows block_table[j]*page .. +page.  Returns [Hkv, prefix_len, d].
+
+    Source: "EAGLE-2: Feature-Level Speculative Decoding Guide", production
+    section (serving engines keep the KV cache in a shared pool for high
+    concurrency).  Reading: fixed pages of `page` tokens, one block table of
+    page ids per sequence (the pages give no layout)."""
+    pool = np.asarray(pool)
+    n_pages = (prefix_len + page - 1) // page
+    parts = [pool[:, int(block_table[j]) * page: int(block_table[j]) * page + page]
+             for j in range(n_pages)]
+    if not parts:
+        return pool[:, :0]
+    return np.concatenate(parts, axis=1)[:, :prefix_len]
+
+
+def tree_attention_paged(q, k_pool, v_pool, block_table, tree_k, tree_v, mask, prefix_len,
+                         scale=None, heads=None, page=128):
+    """tree_attention over a paged prefix cache (gather, then the definition)."""
+    return tree_attention(q, gather_pages(k_pool, block_table, prefix_len, page),
+                          gather_pages(v_pool, block_table, prefix_len, page),
+                          tree_k, tree_v, mask, prefix_len, scale=scale, heads=heads)

@@ -90,3 +90,27 @@ def test_identical_keys_average_visible_values():
         anc = [j for j in range(m) if (int(t["mask"][i, j // 64]) >> (j % 64)) & 1]
         vals = torch.cat([vc[0, :S], tv[anc, 0]])
         np.testing.assert_allclose(out[i, 0], vals.mean(0).numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_paged_prefix_equals_the_contiguous_cache():
+    """A contiguous cache scattered into shuffled pages of a larger pool (by
+    hand, page by page) and gathered back gives the same attention; the pool's
+    unused rows hold values that would change the result if read."""
+    from oracle.tree_attn import gather_pages, tree_attention_paged
+    t = _tree(9)
+    m, Hq, Hkv, d, S, page = t["m"], 4, 2, 16, 300, 128
+    q, kc, vc, tk, tv = _inputs(3, m, Hq, Hkv, d, S)
+    n_pages = (S + page - 1) // page
+    rng = np.random.default_rng(1)
+    table = rng.permutation(7)[:n_pages]                 # pages anywhere in a 7-page pool
+    kpool = np.full((Hkv, 7 * page, d), 1e3)
+    vpool = np.full((Hkv, 7 * page, d), -1e3)
+    for j in range(n_pages):
+        lo, hi = j * page, min(S, (j + 1) * page)
+        kpool[:, table[j] * page: table[j] * page + hi - lo] = kc[:, lo:hi].numpy()
+        vpool[:, table[j] * page: table[j] * page + hi - lo] = vc[:, lo:hi].numpy()
+    assert np.array_equal(gather_pages(kpool, table, S, page), kc[:, :S].numpy())
+    ref = tree_attention(q.numpy(), kc.numpy(), vc.numpy(), tk.numpy(), tv.numpy(), t["mask"], S)
+    got = tree_attention_paged(q.numpy(), kpool, vpool, table, tk.numpy(), tv.numpy(), t["mask"],
+                               S, page=page)
+    assert np.array_equal(got, ref)
