@@ -232,7 +232,7 @@ class Step:
                     for n in ("q", "tree_k", "tree_v")))
 
 
-def attn_long(eb, wl, dev, reps=5, n_layers=None):
+def attn_long(eb, wl, dev, reps=5, n_layers=None, paged=True):
     """Tree attention at long context: 32 independent layers of a
     llama-3-8b-shaped KV cache (8 kv heads, d 128, bf16 prefix 32768; 4.3 GB,
     far above L2) for one 60-token tree, all layers in one batched call
@@ -273,12 +273,47 @@ def attn_long(eb, wl, dev, reps=5, n_layers=None):
     m, hq, hkv, d, S, L = w.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim, w.prefix, nl
     nbytes = L * (2 * S * hkv * d * 2 + m * hq * d * 2 + 2 * m * hkv * d * 2 + m * hq * d * 4)
     flops = L * 4.0 * m * hq * (S + m) * d
+    res = {"workload": f"c3: {nl} layers x bf16 prefix 32768, 32/8 heads d128, 60-token tree, "
+                       "one batched call", "us": round(t * 1e6, 1),
+           "achieved_gbs": round(nbytes / t / 1e9, 1),
+           "achieved_tflops": round(flops / t / 1e12, 1), "bytes": nbytes}
+    if paged:   # the same keys / values in 128-token pages, shuffled within each layer's pool
+        page = eb.EAGLE_KV_PAGE_TOKENS
+        n_pages = S // page
+        gen = torch.Generator().manual_seed(5)
+        pitems, keep = [], []
+        for a, o in zip(layers, outs):
+            perm = torch.randperm(n_pages, generator=gen)
+            table = torch.argsort(perm).to(torch.int32).to(dev)   # page j at pool page table[j]
+            kp = a["k_cache"].view(hkv, n_pages, page, d)[:, perm].reshape(hkv, S, d).contiguous()
+            vp = a["v_cache"].view(hkv, n_pages, page, d)[:, perm].reshape(hkv, S, d).contiguous()
+            keep.append((kp, vp, table))
+            pitems.append(eb.attn_paged_item(a["q"], kp, vp, table, a["tree_k"], a["tree_v"],
+                                             tree.mask, o, S))
+        pws = eb.workspace(eb.lib().eagle_tree_attn_paged_workspace_size(
+            (eb.CAttnPagedItem * nl)(*pitems), nl, hq, hkv, d), dev)
+
+        def run_paged():
+            eb.eagle_tree_attn_paged_batched(pitems, hq, hkv, d, ws=pws, stream=s)
+
+        for _ in range(2):
+            run_paged()
+        s.synchronize()
+        ptimes = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            run_paged()
+            e1.record(s)
+            s.synchronize()
+            ptimes.append(e0.elapsed_time(e1) * 1e-3)
+        pt = statistics.median(ptimes)
+        res["paged"] = {"us": round(pt * 1e6, 1), "achieved_gbs": round(nbytes / pt / 1e9, 1),
+                        "page_tokens": page, "pages_shuffled": True}
+        del keep, pitems, pws
     del layers, outs, items, ws
     torch.cuda.empty_cache()
-    return {"workload": f"c3: {nl} layers x bf16 prefix 32768, 32/8 heads d128, 60-token tree, "
-                        "one batched call", "us": round(t * 1e6, 1),
-            "achieved_gbs": round(nbytes / t / 1e9, 1), "achieved_tflops": round(flops / t / 1e12, 1),
-            "bytes": nbytes}
+    return res
 
 
 def kv_commit_bench(eb, wl, dev, step, s, reps=200):
@@ -716,7 +751,7 @@ def main():
         import torch
         from eagle_speculative_decoding_verify_gb300 import binding as eb, workloads as wl
         res = attn_long(eb, wl, torch.device("cuda"), reps=max(args.steps, 1),
-                        n_layers=args.long_attn_only)
+                        n_layers=args.long_attn_only, paged=False)
         print(json.dumps(res), flush=True)
         return 0
     rank = int(os.environ.get("RANK", "0"))

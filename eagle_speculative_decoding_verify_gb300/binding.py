@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape",
 EAGLE_F32 = 0
 EAGLE_BF16 = 1
 EAGLE_NOALLOC_SCRATCH_BYTES = 16 * 1024   # include/eagle.h
+EAGLE_KV_PAGE_TOKENS = 128
 MAX_TOP_K = 64
 MAX_DEPTH = 16
 MAX_CANDIDATES = 2048
@@ -54,6 +55,14 @@ class CAttnItem(ctypes.Structure):
                 ("tree_v", ctypes.c_void_p), ("mask", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("cache_head_stride", ctypes.c_int64),
                 ("prefix_len", ctypes.c_int32), ("m", ctypes.c_int32)]
+
+
+class CAttnPagedItem(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("tree_k", ctypes.c_void_p),
+                ("tree_v", ctypes.c_void_p), ("mask", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("pool_head_stride", ctypes.c_int64), ("prefix_len", ctypes.c_int32),
+                ("m", ctypes.c_int32)]
 
 
 class CKvItem(ctypes.Structure):
@@ -93,6 +102,8 @@ EXPORTS = {
                                  _P, _P, _P, _P, _SZ, _P]),
     "eagle_tree_verify_batched": (_I32, [_I32, _P, _I64, _I32, _P, _P, _P, _U64, _P, _P, _P,
                                          _P, _SZ, _P]),
+    "eagle_tree_attn_paged_workspace_size": (_SZ, [_P, _I32, _I32, _I32, _I32]),
+    "eagle_tree_attn_paged_batched": (_I32, [_P, _I32, _I32, _I32, _I32, _F, _P, _SZ, _P]),
     "eagle_tree_state_bytes": (_SZ, [_I32, _I32]),
     "eagle_tree_expand_workspace_size": (_SZ, [_I32, _I32]),
     "eagle_tree_expand": (_I32, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
@@ -417,3 +428,26 @@ class TreeGrowth:
                                          _ptr(self.ws), self.ws.numel(), _stream(stream)),
                "eagle_tree_finalize")
         return out
+
+
+# ----------------------------------------------------------- paged prefix
+def attn_paged_item(q, k_pool, v_pool, block_table, tree_k, tree_v, mask, out, prefix_len):
+    """C item for one attention problem over a paged prefix (pools [Hkv, rows, d],
+    block_table device int32 page ids of the prefix's 128-token pages)."""
+    return CAttnPagedItem(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                          block_table.data_ptr(), tree_k.data_ptr(), tree_v.data_ptr(),
+                          mask.data_ptr(), out.data_ptr(), k_pool.stride(0), int(prefix_len),
+                          q.shape[0])
+
+
+def eagle_tree_attn_paged_batched(items, n_q_heads, n_kv_heads, head_dim, scale=0.0, ws=None,
+                                  stream=None, device=None):
+    """items: list of CAttnPagedItem (see attn_paged_item)."""
+    arr = (CAttnPagedItem * len(items))(*items)
+    if ws is None:
+        ws = workspace(lib().eagle_tree_attn_paged_workspace_size(arr, len(items), n_q_heads,
+                                                                  n_kv_heads, head_dim), device)
+    _check(lib().eagle_tree_attn_paged_batched(arr, len(items), n_q_heads, n_kv_heads, head_dim,
+                                               float(scale), _ptr(ws), ws.numel(),
+                                               _stream(stream)), "eagle_tree_attn_paged_batched")
+    return ws

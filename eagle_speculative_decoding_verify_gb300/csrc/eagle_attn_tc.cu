@@ -49,6 +49,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "eagle_attn.h"
 #include "eagle_host.h"
@@ -68,6 +69,8 @@ struct TcItem {
   const uint64_t* mask;
   int m, prefix_len, splits, tiles, pairs, unit_start;
   int64_t part_start;   // first partial unit of the item (units of 128 rows)
+  const int32_t* table; // paged prefix: pool page of every 128-token page (null: contiguous)
+  int pool_pages;       // pages in the pool (the table's entries must lie below)
 };
 
 struct TcParams {
@@ -155,7 +158,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(L::kKvBytes));
     if (j < n_pref) {
       const CUtensorMap* map = is_v ? &P.vmap[item] : &P.kmap[item];
-      const int y = split_start + j * kChunk;
+      int y = split_start + j * kChunk;
+      if (it.table) {   // paged prefix: a chunk is one page (a bad id reads page 0, reported)
+        int page = __ldg(it.table + split_start / kChunk + j);
+        if (page < 0 || page >= it.pool_pages) {
+          record_error(P.err, kDevAssert, 60);
+          page = 0;
+        }
+        y = page * kChunk;
+      }
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * L::kBoxBytes, map, 64 * h, y, kvh, &full[slot]);
     } else {
@@ -631,9 +642,13 @@ size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int
   return need;
 }
 
+// tables / pool_rows: per item, the block table and the pool's rows per head
+// of a paged prefix (null arrays: every item contiguous)
 template <int D>
 static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hkv, float scale,
-                             void* ws, size_t ws_bytes, cudaStream_t stream) {
+                             void* ws, size_t ws_bytes, cudaStream_t stream,
+                             const int32_t* const* tables = nullptr,
+                             const int64_t* pool_rows = nullptr) {
   static_assert(sizeof(TcParams) < 32000, "kernel parameter block too large");
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
@@ -645,7 +660,10 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     int64_t units = 0, part = 0;
     for (int b = 0; b < nb; ++b) {
       const eagle_attn_item& x = its[b];
-      const uint64_t S = static_cast<uint64_t>(x.prefix_len);
+      // rows the prefix maps cover: the prefix, or the whole pool of a paged item
+      const bool paged = tables && tables[b0 + b] && x.prefix_len > 0;
+      const uint64_t S = paged ? static_cast<uint64_t>(pool_rows[b0 + b])
+                               : static_cast<uint64_t>(x.prefix_len);
       const void* kbase = x.prefix_len ? x.k_cache : x.tree_k;
       const void* vbase = x.prefix_len ? x.v_cache : x.tree_v;
       const uint64_t hs = static_cast<uint64_t>(x.cache_head_stride) * 2;
@@ -656,6 +674,8 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
         return EAGLE_ERR_CUDA;
       TcItem& ti = P.items[b];
       ti.q = static_cast<const __nv_bfloat16*>(x.q);
+      ti.table = paged ? tables[b0 + b] : nullptr;
+      ti.pool_pages = paged ? static_cast<int>(pool_rows[b0 + b] / kChunk) : 0;
       ti.out = x.out;
       ti.mask = x.mask;
       ti.m = x.m;
@@ -716,4 +736,75 @@ eagle_status attn_tc_launch(const eagle_attn_item* items, int n, int hq, int hkv
   return EAGLE_ERR_UNSUPPORTED_SHAPE;
 }
 
+// ------------------------------------------------------------- paged prefix
+static eagle_status paged_items(const eagle_attn_paged_item* items, int n, int hq, int hkv, int d,
+                                eagle_attn_item* flat, const int32_t** tables, int64_t* rows) {
+  EAGLE_CHECK_ARG(items && n >= 1 && hq >= 1 && hkv >= 1 && hq % hkv == 0);
+  EAGLE_CHECK_SHAPE(tc_supported(d));
+  static_assert(EAGLE_KV_PAGE_TOKENS == kChunk, "a page is one K/V chunk of the kernel");
+  for (int b = 0; b < n; ++b) {
+    const eagle_attn_paged_item& x = items[b];
+    EAGLE_CHECK_ARG(x.m >= 1 && x.prefix_len >= 0);
+    EAGLE_CHECK_SHAPE(x.m <= EAGLE_MAX_TREE);
+    EAGLE_CHECK_ARG(x.q && x.tree_k && x.tree_v && x.mask && x.out);
+    EAGLE_CHECK_ARG(aligned16(x.q) && aligned16(x.tree_k) && aligned16(x.tree_v) &&
+                    aligned16(x.out));
+    if (x.prefix_len > 0) {
+      EAGLE_CHECK_ARG(x.k_pool && x.v_pool && x.block_table && aligned16(x.k_pool) &&
+                      aligned16(x.v_pool));
+      EAGLE_CHECK_ARG(x.pool_head_stride % d == 0 && x.pool_head_stride % 8 == 0 &&
+                      x.pool_head_stride >= static_cast<int64_t>(kChunk) * d);
+    }
+    eagle_attn_item& f = flat[b];
+    f.q = x.q;
+    f.k_cache = x.k_pool;
+    f.v_cache = x.v_pool;
+    f.tree_k = x.tree_k;
+    f.tree_v = x.tree_v;
+    f.mask = x.mask;
+    f.out = x.out;
+    f.cache_head_stride = x.pool_head_stride;
+    f.prefix_len = x.prefix_len;
+    f.m = x.m;
+    tables[b] = x.block_table;
+    rows[b] = x.prefix_len > 0 ? x.pool_head_stride / d : 0;
+  }
+  return EAGLE_OK;
+}
+
 }  // namespace eagle
+
+using namespace eagle;
+
+extern "C" size_t eagle_tree_attn_paged_workspace_size(const eagle_attn_paged_item* items,
+                                                       int32_t n_items, int32_t n_q_heads,
+                                                       int32_t n_kv_heads, int32_t head_dim) {
+  if (!items || n_items < 1 || n_items > (1 << 20)) return 0;
+  std::vector<eagle_attn_item> flat(n_items);
+  std::vector<const int32_t*> tables(n_items);
+  std::vector<int64_t> rows(n_items);
+  if (paged_items(items, n_items, n_q_heads, n_kv_heads, head_dim, flat.data(), tables.data(),
+                  rows.data()) != EAGLE_OK)
+    return 0;
+  return attn_tc_ws_size(flat.data(), n_items, n_q_heads, n_kv_heads, head_dim, kPlanSMs);
+}
+
+extern "C" eagle_status eagle_tree_attn_paged_batched(const eagle_attn_paged_item* items,
+                                                      int32_t n_items, int32_t n_q_heads,
+                                                      int32_t n_kv_heads, int32_t head_dim,
+                                                      float scale, void* ws, size_t ws_bytes,
+                                                      eagle_stream stream) {
+  EAGLE_CHECK_ARG(ws != nullptr && n_items >= 1 && n_items <= (1 << 20));
+  std::vector<eagle_attn_item> flat(n_items);
+  std::vector<const int32_t*> tables(n_items);
+  std::vector<int64_t> rows(n_items);
+  eagle_status st = paged_items(items, n_items, n_q_heads, n_kv_heads, head_dim, flat.data(),
+                                tables.data(), rows.data());
+  if (st != EAGLE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return head_dim == 128
+             ? launch_d<128>(flat.data(), n_items, n_q_heads, n_kv_heads, scale, ws, ws_bytes, s,
+                             tables.data(), rows.data())
+             : launch_d<64>(flat.data(), n_items, n_q_heads, n_kv_heads, scale, ws, ws_bytes, s,
+                            tables.data(), rows.data());
+}

@@ -261,6 +261,45 @@ eagle_status eagle_tree_attn_batched(const eagle_attn_item* items, int32_t n_ite
                                      eagle_dtype dtype, float scale,
                                      void* ws, size_t ws_bytes, eagle_stream stream);
 
+/* Paged prefix cache (serving: the cache lives in a shared pool; [blog]
+ * production section).  Fixed pages of EAGLE_KV_PAGE_TOKENS tokens: page j
+ * of an item (its prefix tokens 128 j .. 128 j + 127) is pool rows
+ * block_table[j] * 128 .. + 127 of every kv head.
+ *
+ * k_pool,
+ * v_pool:          [n_kv_heads][pool_head_stride]; each head's rows (head_dim
+ *                  elements each) are contiguous; pool_head_stride a multiple
+ *                  of head_dim and of 8, at least one page; 16-byte aligned.
+ * block_table:     device int32 [ceil(prefix_len / 128)] page ids; an id
+ *                  outside the pool is recorded as EAGLE_ERR_DEVICE_ASSERT in
+ *                  the workspace error word (page 0 is read instead).
+ * Everything else as for eagle_tree_attn_batched; bf16 only, head_dim 64 or
+ * 128 (the tensor-core path). */
+#define EAGLE_KV_PAGE_TOKENS 128
+
+typedef struct {
+  const void*     q;
+  const void*     k_pool;
+  const void*     v_pool;
+  const int32_t*  block_table;
+  const void*     tree_k;
+  const void*     tree_v;
+  const uint64_t* mask;
+  float*          out;
+  int64_t         pool_head_stride;
+  int32_t         prefix_len;
+  int32_t         m;
+} eagle_attn_paged_item;
+
+size_t eagle_tree_attn_paged_workspace_size(const eagle_attn_paged_item* items,
+                                            int32_t n_items, int32_t n_q_heads,
+                                            int32_t n_kv_heads, int32_t head_dim);
+
+eagle_status eagle_tree_attn_paged_batched(const eagle_attn_paged_item* items, int32_t n_items,
+                                           int32_t n_q_heads, int32_t n_kv_heads,
+                                           int32_t head_dim, float scale, void* ws,
+                                           size_t ws_bytes, eagle_stream stream);
+
 /* ------------------------------------------------------------------------
  * eagle_tree_verify -- [blog] "Single-Pass Tree Verification" (walk from the
  * root, accept matching tokens until the first discrepancy; lossless) and
