@@ -127,19 +127,24 @@ def _kernel_source_hash(kernel):
     import re
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "eagle_speculative_decoding_verify_gb300", "csrc")
+    used = set()
     for name in KERNEL_SOURCES[kernel]:
         with open(os.path.normpath(os.path.join(csrc, name)), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        used |= set(re.findall(r"\bEAGLE_[A-Z0-9_]+\b", text))
         h.update(os.path.basename(name).encode())
         h.update("\n".join(lines).encode())
-    # of the public header, the constants the kernels use (limits, status codes)
+    # of the public header, the constants these sources use (limits, status codes)
     with open(os.path.join(ROOT, "include", "eagle.h"), encoding="utf-8") as f:
-        consts = [ln.split("/*")[0].rstrip() for ln in f
-                  if re.match(r"\s*(#define\s+EAGLE_|EAGLE_[A-Z0-9_]+\s*=)", ln)]
-    h.update("\n".join(consts).encode())
+        consts = []
+        for ln in f:
+            mt = re.match(r"\s*(?:#define\s+)?(EAGLE_[A-Z0-9_]+)(?:\s+|\s*=)", ln)
+            if mt and mt.group(1) in used and ("#define" in ln or "=" in ln):
+                consts.append(ln.split("/*")[0].strip())
+    h.update("\n".join(sorted(consts)).encode())
     return h.hexdigest()[:12]
 
 
@@ -549,9 +554,9 @@ def max_over_ranks(x, world, device):
 TRAFFIC = {
     # profiles/*_c2.md: dram__bytes_read.sum + dram__bytes_write.sum of one launch,
     # keyed by the kernel's source hash (_kernel_source_hash)
-    "build:c2": ("03f5a85d6f51", 31122688),
-    "verify:c2": ("7efcb1250654", 36601600),
-    "attn:c2": ("f0bf516efb78", 17389824),
+    "build:c2": ("79251290ef33", 31122688),
+    "verify:c2": ("f97b7e0e9036", 36601600),
+    "attn:c2": ("d4abccd751ad", 17386496),
 }
 
 
