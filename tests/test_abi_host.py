@@ -97,3 +97,121 @@ def test_attn_rejects_bad_arguments(lib):
                                  a["hkv"], a["d"], a["S"], a["dtype"], 0.0, fake,
                                  ctypes.c_void_p(1 << 21), 1 << 30, None)
         assert st == status, over
+
+
+def test_new_workspace_and_state_sizes_are_host_only(lib):
+    assert lib.eagle_kv_commit_workspace_size() >= 16
+    a = lib.eagle_tree_state_bytes(10, 6)
+    assert a > 0 and a % 16 == 0
+    assert lib.eagle_tree_state_bytes(10, 7) > a        # more candidates, more state
+    assert lib.eagle_tree_state_bytes(0, 6) == 0
+    # the row stream keeps per-CTA candidate buffers: the size grows with top_k, not the vocabulary
+    assert lib.eagle_tree_expand_workspace_size(10, 128256) >= 256
+    assert lib.eagle_tree_expand_workspace_size(64, 128256) > lib.eagle_tree_expand_workspace_size(4, 128256)
+
+
+_FAKE = 1 << 20
+_FAKE_WS = 1 << 21
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(k_cache=0), 1),                        # null cache
+    (dict(k_cache=_FAKE + 8), 1),                # cache not 16-byte aligned
+    (dict(m=0), 1),
+    (dict(prefix_len=-1), 1),
+    (dict(stride=100), 1),                       # head stride not a multiple of d
+    (dict(stride=32), 1),                        # head stride below one row
+    (dict(d=4), 2),                              # a row of 8 bytes cannot be copied in 16-byte units
+    (dict(dtype=7), 1),
+    (dict(ws_bytes=8), 1),
+])
+def test_kv_commit_rejects_bad_arguments(lib, over, status):
+    a = dict(k_cache=_FAKE, stride=64 * 64, prefix_len=5, m=9, hkv=2, d=64, dtype=eb.EAGLE_BF16,
+             ws_bytes=1 << 12)
+    a.update(over)
+    st = lib.eagle_kv_commit(ctypes.c_void_p(a["k_cache"]), ctypes.c_void_p(_FAKE), a["stride"],
+                             a["prefix_len"], ctypes.c_void_p(_FAKE), ctypes.c_void_p(_FAKE), a["m"],
+                             a["hkv"], a["d"], a["dtype"], ctypes.c_void_p(_FAKE),
+                             ctypes.c_void_p(_FAKE), ctypes.c_void_p(_FAKE_WS), a["ws_bytes"], None)
+    assert st == status, over
+
+
+def test_kv_commit_batched_checks_every_item(lib):
+    good = eb.CKvItem(_FAKE, _FAKE, _FAKE, _FAKE, _FAKE, _FAKE, 64 * 64, 5, 9)
+    bad = eb.CKvItem(_FAKE, _FAKE, _FAKE, 0, _FAKE, _FAKE, 64 * 64, 5, 9)   # null tree_v
+    arr = (eb.CKvItem * 3)(good, good, bad)
+    st = lib.eagle_kv_commit_batched(arr, 3, 2, 64, eb.EAGLE_BF16, ctypes.c_void_p(_FAKE_WS), 1 << 12,
+                                     None)
+    assert st == 1
+    assert lib.eagle_kv_commit_batched(arr, 0, 2, 64, eb.EAGLE_BF16, ctypes.c_void_p(_FAKE_WS),
+                                       1 << 12, None) == 1
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(rows=0), 1),
+    (dict(level=3), 1),                          # level must be below depth
+    (dict(level=-1), 1),
+    (dict(top_k=65), 2),
+    (dict(top_k=1001), 2),                       # more children than the vocabulary
+    (dict(depth=17), 2),
+    (dict(row_stride=1002), 1),                  # not a multiple of 4
+    (dict(row_stride=996), 1),                   # shorter than a row
+    (dict(ws_bytes=64), 3),
+])
+def test_tree_expand_rejects_bad_arguments(lib, over, status):
+    a = dict(rows=_FAKE, row_stride=1000, vocab=1000, top_k=4, depth=3, level=0, ws_bytes=1 << 30)
+    a.update(over)
+    st = lib.eagle_tree_expand(ctypes.c_void_p(a["rows"]), a["row_stride"], a["vocab"], a["top_k"],
+                               a["depth"], a["level"], ctypes.c_void_p(_FAKE), None,
+                               ctypes.c_void_p(_FAKE_WS), a["ws_bytes"], None)
+    assert st == status, over
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(state=0), 1),
+    (dict(top_k=0), 1),
+    (dict(total_tokens=38), 2),                  # above 1 + the 4 + 2*16 candidates of top_k 4, depth 3
+    (dict(total_tokens=300), 2),                 # above the tree limit
+    (dict(out_m=8), 1),                          # output arrays sized for another tree
+    (dict(ws_bytes=4), 1),
+])
+def test_tree_finalize_rejects_bad_arguments(lib, over, status):
+    a = dict(state=_FAKE, top_k=4, depth=3, total_tokens=10, out_m=None, ws_bytes=1 << 12)
+    a.update(over)
+    out = _fake_tree(a["out_m"] or a["total_tokens"])
+    st = lib.eagle_tree_finalize(ctypes.c_void_p(a["state"]), a["top_k"], a["depth"],
+                                 a["total_tokens"], 7, out, ctypes.c_void_p(_FAKE_WS), a["ws_bytes"],
+                                 None)
+    assert st == status, over
+
+
+def _paged(**over):
+    f = dict(q=_FAKE, k_pool=_FAKE, v_pool=_FAKE, block_table=_FAKE, tree_k=_FAKE, tree_v=_FAKE,
+             mask=_FAKE, out=_FAKE, pool_head_stride=4 * 128 * 64, prefix_len=300, m=16)
+    f.update(over)
+    return eb.CAttnPagedItem(**f)
+
+
+@pytest.mark.parametrize("item,shape,status", [
+    (dict(m=0), {}, 1),
+    (dict(m=300), {}, 2),
+    (dict(block_table=0), {}, 1),                # a prefix needs a page table
+    (dict(k_pool=_FAKE + 4), {}, 1),             # pool not 16-byte aligned
+    (dict(pool_head_stride=100 * 64), {}, 1),    # fewer rows per head than one page
+    (dict(q=0), {}, 1),
+    (dict(), dict(hq=5), 1),                     # query heads not a multiple of KV heads
+    (dict(), dict(d=96), 2),                     # head size the kernel does not take
+])
+def test_attn_paged_rejects_bad_arguments(lib, item, shape, status):
+    s = dict(hq=4, hkv=2, d=64)
+    s.update(shape)
+    arr = (eb.CAttnPagedItem * 2)(_paged(), _paged(**item))
+    st = lib.eagle_tree_attn_paged_batched(arr, 2, s["hq"], s["hkv"], s["d"], 0.125,
+                                           ctypes.c_void_p(_FAKE_WS), 1 << 30, None)
+    assert st == status, (item, shape)
+    assert lib.eagle_tree_attn_paged_workspace_size(arr, 2, s["hq"], s["hkv"], s["d"]) == 0
+
+
+def test_attn_paged_without_prefix_needs_no_pool(lib):
+    arr = (eb.CAttnPagedItem * 1)(_paged(k_pool=0, v_pool=0, block_table=0, prefix_len=0))
+    assert lib.eagle_tree_attn_paged_workspace_size(arr, 1, 4, 2, 64) >= 256
