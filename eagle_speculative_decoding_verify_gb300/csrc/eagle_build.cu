@@ -26,7 +26,22 @@ struct BuildArgs {
   int top_k, depth, total_tokens, n_cand;
   int root_token[kMaxItems];
   eagle_tree out[kMaxItems];
+  char* warm;   // kWarmBytes of workspace for the code warm-up's own tree
 };
+
+// One tree assembly: the item's R row records and its outputs.
+struct TreeJob {
+  char* rows;        // R records of rec_bytes(rec_k) bytes
+  eagle_tree out;
+  int32_t* err;
+  int rec_k, top_k, depth, total_tokens, n_cand, root_token;
+};
+
+// Workspace of the code warm-up: error word, 3 records of a top-2 row,
+// parents / tokens / depth / pos of 4 nodes, 4 mask words.
+constexpr int kWarmK = 2;
+constexpr size_t kWarmBytes = 256;
+static_assert(16 + 3 * rec_bytes(kWarmK) + 4 * 16 + 8 * 4 <= kWarmBytes, "warm-up workspace");
 
 __device__ __forceinline__ int cand_depth(int a, int k) { return a < k ? 1 : 2 + (a - k) / (k * k); }
 
@@ -51,15 +66,15 @@ static __device__ __noinline__ int block_excl_scan(int v, int* warp_tot, int& to
   return off + incl - v;
 }
 
-static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, StreamSmem& S) {
+static __device__ __noinline__ void assemble_tree(const TreeJob J, StreamSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31;
-  const int k = A.top_k, D = A.depth, m = A.total_tokens, C = A.n_cand;
+  const int k = J.top_k, D = J.depth, m = J.total_tokens, C = J.n_cand;
   const int R = 1 + (D - 1) * k;
   const int kk = k * k;
-  const int rk = A.rs.rec_k;
+  const int rk = J.rec_k;
   const int rb = rec_bytes(rk);
-  char* rows = A.rs.rows + static_cast<int64_t>(item) * A.rs.rows_per_item * rb;
-  const eagle_tree out = A.out[item];
+  char* rows = J.rows;
+  const eagle_tree out = J.out;
 
   // scratch carved from the (now idle) ring and warp buffers; every array
   // starts on a 16-byte boundary (<= 77 KB for C <= 2048; R k = C)
@@ -195,13 +210,13 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
     else node[a] = 0;
   }
   __syncthreads();
-  if (tid == 0 && total != (need > 0 ? min(need, C) : 0)) record_error(A.rs.err, kDevAssert, 10);
+  if (tid == 0 && total != (need > 0 ? min(need, C) : 0)) record_error(J.err, kDevAssert, 10);
   (void)lane;
 
   // node arrays
   if (tid == 0) {
     out.parents[0] = -1;
-    out.tokens[0] = A.root_token[item];
+    out.tokens[0] = J.root_token;
     out.depth[0] = 0;
     out.pos[0] = 0;
     if (out.values) out.values[0] = 0.0;
@@ -214,7 +229,7 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
     if (par[a] >= 0) {
       pn = node[par[a]];
       if (pn == 0) {
-        record_error(A.rs.err, kDevAssert, 11);  // kept set not ancestor-closed
+        record_error(J.err, kDevAssert, 11);  // kept set not ancestor-closed
         pn = 0;
       }
     }
@@ -249,12 +264,78 @@ static __device__ __noinline__ void assemble_tree(const BuildArgs& A, int item, 
   __syncthreads();
 }
 
+// Code warm-up.  The tree assembly runs once per item, in one CTA, after the
+// item's last row; when the L2 holds other data (as it does between decode
+// steps, after the target model's forward pass) each first use of a stretch
+// of its code is an instruction fetch from HBM, several microseconds in all.
+// The first CTA of one extra cluster runs the same function at launch, on a
+// tree of its own (three top-2 rows, depth 2, four nodes) in kWarmBytes of
+// workspace, so that the code is in L2 when the real assembly needs it.  It
+// reads and writes nothing else and has its own error word.
+static __device__ __noinline__ void warm_assembly(char* warm, StreamSmem& S) {
+  const int rb = rec_bytes(kWarmK);
+  char* rows = warm + 16;
+  int32_t* ints = reinterpret_cast<int32_t*>(rows + 3 * rb);
+  const int t = threadIdx.x;
+  if (t == 0) *reinterpret_cast<int32_t*>(warm) = 0;
+  if (t < 3) {
+    char* rec = rows + t * rb;
+    RecHead* h = reinterpret_cast<RecHead*>(rec);
+    h->sum = 2.0;
+    h->max = 0.f;
+    h->count = kWarmK;
+    rec_val(rec)[0] = 0.f;
+    rec_val(rec)[1] = -1.f;
+    rec_idx(rec, kWarmK)[0] = 2 * t;
+    rec_idx(rec, kWarmK)[1] = 2 * t + 1;
+  }
+  __threadfence();
+  __syncthreads();
+  TreeJob J;
+  J.rows = rows;
+  J.out.parents = ints;
+  J.out.tokens = ints + 4;
+  J.out.depth = ints + 8;
+  J.out.pos = ints + 12;
+  J.out.mask = reinterpret_cast<uint64_t*>(ints + 16);
+  J.out.values = nullptr;
+  J.out.m = 4;
+  J.out.mask_words = 1;
+  J.err = reinterpret_cast<int32_t*>(warm);
+  J.rec_k = kWarmK;
+  J.top_k = kWarmK;
+  J.depth = 2;
+  J.total_tokens = 4;
+  J.n_cand = kWarmK + kWarmK * kWarmK;
+  J.root_token = 0;
+  assemble_tree(J, S);
+}
+
+// Grid: the rows' clusters, then one more cluster for the code warm-up.
 __global__ void __launch_bounds__(kThreads, 2) build_kernel(const __grid_constant__ BuildArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
+  const int64_t row_ctas =
+      static_cast<int64_t>(A.rs.n_items) * A.rs.rows_per_item * A.rs.ctas_per_row;
+  if (blockIdx.x >= row_ctas) {
+    if (blockIdx.x == row_ctas) warm_assembly(A.warm, S);
+    return;
+  }
   const RowCtx cx = stream_row(A.rs, S);
   if (!cx.leader) return;
-  if (item_arrive(A.rs, S, cx.item)) assemble_tree(A, cx.item, S);
+  if (!item_arrive(A.rs, S, cx.item)) return;
+  const int rb = rec_bytes(A.rs.rec_k);
+  TreeJob J;
+  J.rows = A.rs.rows + static_cast<int64_t>(cx.item) * A.rs.rows_per_item * rb;
+  J.out = A.out[cx.item];
+  J.err = A.rs.err;
+  J.rec_k = A.rs.rec_k;
+  J.top_k = A.top_k;
+  J.depth = A.depth;
+  J.total_tokens = A.total_tokens;
+  J.n_cand = A.n_cand;
+  J.root_token = A.root_token[cx.item];
+  assemble_tree(J, S);
 }
 
 // tree assembly scratch (R = 1 + (depth-1) top_k <= 256 whenever C <= 2048)
@@ -285,7 +366,7 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
     EAGLE_CHECK_ARG(t.m == total_tokens && t.mask_words == (total_tokens + 63) / 64);
   }
   const StreamLayout L = stream_layout(n_items, R, vocab, top_k, false, false);
-  if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < L.total + kWarmBytes) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
 
   BuildArgs A;
   memset(&A, 0, sizeof(A));
@@ -306,7 +387,8 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
   A.depth = depth;
   A.total_tokens = total_tokens;
   A.n_cand = static_cast<int>(C);
-  return launch_stream(build_kernel, A, L.n_rows, ctas, stream);
+  A.warm = static_cast<char*>(ws) + L.total;
+  return launch_stream(build_kernel, A, L.n_rows + 1, ctas, stream);
 }
 
 // Scratch of the allocation-free entry point: fixed size, static device
@@ -345,7 +427,7 @@ extern "C" size_t eagle_tree_build_workspace_size(int32_t n_items, int32_t n_row
   (void)total_tokens;
   if (n_items < 1 || vocab < 1 || top_k < 1 || depth < 1) return 0;
   const int R = 1 + (depth - 1) * top_k;
-  return stream_layout(n_items, R, vocab, top_k, false, false).total;
+  return stream_layout(n_items, R, vocab, top_k, false, false).total + kWarmBytes;
 }
 
 extern "C" eagle_status eagle_tree_build(const float* draft_logits, int64_t row_stride,
@@ -389,7 +471,7 @@ extern "C" eagle_status eagle_tree_build_noalloc(const float* draft_logits, int6
   EAGLE_CHECK_ARG(out.parents && out.tokens && out.depth && out.pos && out.mask);
   EAGLE_CHECK_ARG(out.m == total_tokens && out.mask_words == (total_tokens + 63) / 64);
   const StreamLayout L = stream_layout(1, R, vocab, top_k, false, false);
-  if (L.total > EAGLE_NOALLOC_SCRATCH_BYTES) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  if (L.total + kWarmBytes > EAGLE_NOALLOC_SCRATCH_BYTES) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   const eagle_status st = noalloc_scratch(&ws);
   if (st != EAGLE_OK) return st;
