@@ -10,13 +10,15 @@
 // is taken per slot.  Per CTA:
 //   * max and sum of 2^((x - max) c) per thread (fp32 ex2), combined with
 //     fp32 factors and fp64 accumulation;
-//   * the exact top-K (value desc, token id asc), K <= 64.  Each warp keeps
-//     the elements at or before its bound in a private buffer.  The first
-//     bound is CTA-wide: the smallest of the warps' ceil(K/8)-th best lane
-//     maxima of the first slot (K distinct elements reach it) for that slot,
-//     then the exact K-th best of the CTA's lane maxima (found by counting
-//     among the lane maxima at or before the first bound) as the running
-//     bound for the following slots.  A warp whose
+//   * the exact top-K (value desc, token id asc), K <= 64, in two passes
+//     over the CTA's share.  The first (the stream itself) keeps each
+//     thread's maximum and each warp's maximum of every slot; at its end the
+//     K-th largest of the CTA's 256 thread maxima (K distinct elements reach
+//     it) becomes the bound.  The second revisits only the warp-slots whose
+//     maximum reaches the bound (about K of them), reloading their elements
+//     from L2, and each warp keeps the elements at or above the bound in a
+//     private buffer: about K per CTA, where a one-pass running bound lets
+//     some K ln(n / K) through, nearly one per warp and slot.  A warp whose
 //     buffer grows past max(2K, 64) entries cuts it to its best K, which
 //     raises its bound to its exact K-th best; that entry is also published
 //     as the CTA's running bound (shared-memory atomicMax on the 64-bit
@@ -50,6 +52,7 @@ constexpr int kWarpCap = 256;                 // survivors per warp (> K, so cut
 constexpr int kKMax = EAGLE_MAX_TOP_K;
 constexpr int kMaxItems = EAGLE_MAX_BATCH;
 constexpr int kMaxCluster = 8;                // CTAs per row
+constexpr int kTrackSlots = 64;               // slots per CTA with a recorded warp maximum
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { kWantSum = 1, kWantTileSums = 2 };
@@ -102,6 +105,9 @@ __device__ __forceinline__ float key_v(Key k) {
   const uint32_t h = static_cast<uint32_t>(k >> 32);
   return k ? __uint_as_float((h & 0x80000000u) ? (h & 0x7fffffffu) : ~h) : -INFINITY;
 }
+__device__ __forceinline__ float fkey_value(uint32_t h) {   // inverse of fkey
+  return __uint_as_float((h & 0x80000000u) ? (h & 0x7fffffffu) : ~h);
+}
 __device__ __forceinline__ int key_i(Key k) {
   return k ? static_cast<int>(~static_cast<uint32_t>(k)) : kNoIndex;
 }
@@ -133,7 +139,10 @@ struct StreamSmem {
   float rmax;
   int rcount;
   int flag;
-  int ncand;                           // first-slot bound: candidate lane maxima
+  int ncand;                           // second-pass bound: candidate thread maxima
+  uint32_t wbound[kWarps];             // second-pass bound: per-warp bounds (value keys)
+  uint32_t tkey;                       // second-pass bound (value key; 0: none)
+  float wsmax[kWarps][kTrackSlots];    // first pass: every warp's maximum of every slot
   Key cta_bound;                       // running bound: K-th best of the CTA so far
   int aux[2 * EAGLE_MAX_TREE];         // callers' own data (never touched by the stream)
   uint64_t full[kSlots];
@@ -308,6 +317,8 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
     }
     fence_barrier_init();
     S.ncand = 0;
+    S.tkey = 0u;
+    S.cta_bound = 0ull;
   }
   __syncthreads();
   if (tid == 0)
@@ -316,6 +327,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
   cluster_arrive_relaxed();   // every CTA of the cluster has started (waited on at row end)
 
   float m_run = -INFINITY, s_run = 0.f;       // per-thread running max / sum
+  float tmax = -INFINITY;                      // per-thread maximum (K >= 2, first pass)
   float best_v = -INFINITY;                    // per-thread argmax (K == 1)
   int best_i = kNoIndex;
   float thr_v = INFINITY;                      // warp survivor bound (K >= 2): elements
@@ -430,143 +442,178 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
         }
     }
 
-    // ---- top-K survivors, K >= 2
+    // ---- end of the first pass (K >= 2): the second pass's bound.  The
+    // K-th largest of the CTA's thread maxima has K distinct elements at or
+    // above it, so the CTA's best K are all at or above it as well.  First a
+    // per-warp bound, the largest lane maximum that q = ceil(K / 8) lanes
+    // reach; the smallest of the eight is reached by 8 q >= K lanes (0: fewer
+    // valid lanes, no bound).  Then the exact K-th largest among the lane
+    // maxima at or above it, by counting.  Values only: an element equal to
+    // the bound survives whatever its token, which keeps a superset.
     if (K >= 2) {
-      if (j == 0) {
-        // First bound, CTA-wide: every warp takes the q-th best of its lanes'
-        // maxima, q = ceil(K / 8); the smallest of the eight has 8 q >= K
-        // distinct elements at or before it (0: fewer valid lanes, no bound).
+      tmax = fmaxf(tmax, lm);
+      const float wm = warp_max(lm);
+      if (lane == 0 && j < kTrackSlots) S.wsmax[warp][j] = wm;
+      if (j == n_slots - 1) {
+        const uint32_t c0 = tmax == -INFINITY ? 0u : fkey(tmax);
         const int q = (K + kWarps - 1) / kWarps;
-        float v0 = -INFINITY;
-        int i0 = kNoIndex;
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) {   // tokens ascend along the lane: first maximum kept
-          const bool t = x[e] > v0;
-          v0 = t ? x[e] : v0;
-          i0 = t ? tbase + (e >> 2) * kTile + (e & 3) : i0;
-        }
-        const Key c0 = mkkey(v0, i0);
-        int r0 = 0;
+        int ge = 0;
 #pragma unroll 8
-        for (int s = 0; s < 32; ++s) r0 += __shfl_sync(0xffffffffu, c0, s) > c0 ? 1 : 0;
-        const unsigned bal = __ballot_sync(0xffffffffu, (r0 == q - 1) & (c0 != 0ull));
-        const Key wbound = bal ? __shfl_sync(0xffffffffu, c0, __ffs(bal) - 1) : 0ull;
-        if (lane == 0) S.red_best[warp] = wbound;
-        if (tid == 0) S.cta_bound = 0ull;
+        for (int s = 0; s < 32; ++s) ge += __shfl_sync(0xffffffffu, c0, s) >= c0 ? 1 : 0;
+        const uint32_t wq = __reduce_max_sync(0xffffffffu, (ge >= q && c0 != 0u) ? c0 : 0u);
+        if (lane == 0) S.wbound[warp] = wq;
         __syncthreads();
-        Key cb = S.red_best[0];
+        uint32_t cb = S.wbound[0];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) cb = S.red_best[w] < cb ? S.red_best[w] : cb;
-        thr_v = cb ? key_v(cb) : -INFINITY;
-        thr_i = cb ? key_i(cb) : kNoIndex;
-        // Refinement for the following slots: the exact K-th best lane
-        // maximum of the CTA (K distinct elements reach it).  The lane maxima
-        // at or before cb are the candidates (at least K of them); each counts
-        // the candidates before it, and the one with K - 1 before it raises
-        // the running bound.  cb is the same in every thread.
-        if (cb != 0ull) {
+        for (int w = 1; w < kWarps; ++w) cb = S.wbound[w] < cb ? S.wbound[w] : cb;
+        if (cb != 0u) {   // the same in every thread
           const bool cand = c0 >= cb;
           const unsigned bm = __ballot_sync(0xffffffffu, cand);
-          int off = 0;
-          if (lane == 0 && bm) off = atomicAdd(&S.ncand, __popc(bm));
-          off = __shfl_sync(0xffffffffu, off, 0);
-          Key* ck = S.wlist;   // the warp lists are filled only after the stream
-          if (cand) ck[off + __popc(bm & ((1u << lane) - 1u))] = c0;
+          int o = 0;
+          if (lane == 0 && bm) o = atomicAdd(&S.ncand, __popc(bm));
+          o = __shfl_sync(0xffffffffu, o, 0);
+          uint32_t* ck = reinterpret_cast<uint32_t*>(S.wlist);  // filled only after the stream
+          if (cand) ck[o + __popc(bm & ((1u << lane) - 1u))] = c0;
           __syncthreads();
           if (cand) {
             const int n = S.ncand;
-            int r = 0;
-            for (int i = 0; i < n; ++i) r += ck[i] > c0 ? 1 : 0;
-            if (r == K - 1) atomicMax(&S.cta_bound, c0);
+            int g = 0;   // thread maxima at or above this one, itself included
+            for (int i = 0; i < n; ++i) g += ck[i] >= c0 ? 1 : 0;
+            if (g >= K) atomicMax(&S.tkey, c0);
           }
+          __syncthreads();
         }
-      } else {
-        // the running bound: the best K-th entry any warp has cut to so far
-        const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
-        if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
-          thr_v = key_v(cb);
-          thr_i = key_i(cb);
-        }
+        const uint32_t t = S.tkey;
+        thr_v = t ? fkey_value(t) : -INFINITY;   // -inf: every valid element survives
+        thr_i = kNoIndex;
       }
-      if (__any_sync(0xffffffffu, lm >= thr_v)) {
-        auto survives = [&](int e) {
-          const float xv = x[e];
-          const int xi = tbase + (e >> 2) * kTile + (e & 3);
-          return (xv != -INFINITY) & ((xv > thr_v) | ((xv == thr_v) & (xi <= thr_i)));
-        };
-        uint32_t pm = 0;
-        if (lm >= thr_v) {
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) pm |= survives(e) ? (1u << e) : 0u;
-        }
-        // common case: no lane holds more than one survivor.  A lone survivor
-        // has the lane maximum's value (any survivor of a lane whose maximum
-        // is above the bound is that maximum; at the bound all share its
-        // value); its token follows from its bit; positions from a ballot.
-        const unsigned one = __ballot_sync(0xffffffffu, pm != 0u);
-        if (__all_sync(0xffffffffu, (pm & (pm - 1u)) == 0u) && wn + __popc(one) <= kWarpCap) {
-          if (pm) {
-            const int e = __ffs(pm) - 1;
-            wb[wn + __popc(one & ((1u << lane) - 1u))] = mkkey(lm, tbase + (e >> 2) * kTile + (e & 3));
-          }
-          wn += __popc(one);
-          __syncwarp();
-          pm = 0u;
-        }
-        while (__any_sync(0xffffffffu, pm != 0u)) {
-          const int cntp = __popc(pm);
-          int incl = cntp;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          const int total = __shfl_sync(0xffffffffu, incl, 31);
-          const bool fits = wn + total <= kWarpCap;
-          // append (all, or the first kWarpCap - wn in lane order)
-          int take = cntp;
-          if (!fits) take = max(0, min(cntp, kWarpCap - wn - (incl - cntp)));
-          int pos = wn + incl - cntp;
-          if (take) {
-            int taken = 0;
-#pragma unroll
-            for (int e = 0; e < kPer; ++e)   // static indices keep x in registers
-              if (((pm >> e) & 1u) && taken < take) {
-                wb[pos++] = mkkey(x[e], tbase + (e >> 2) * kTile + (e & 3));
-                pm &= ~(1u << e);
-                ++taken;
-              }
-          }
-          __syncwarp();
-          if (fits) {
-            wn += total;
-            break;
-          }
-          // buffer full: keep the best K, raise this warp's bound, drop what no
-          // longer survives, and go on with the rest of this slot
-          wn = warp_select(wb, kWarpCap, K, wb);
-          if (wn >= K && before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
-            thr_v = key_v(wb[K - 1]);
-            thr_i = key_i(wb[K - 1]);
-            if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
-          }
-          uint32_t keep = 0;
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) keep |= survives(e) ? (1u << e) : 0u;
-          pm &= keep;
-          if (!__any_sync(0xffffffffu, pm != 0u)) break;
-        }
+    }
+  }
+
+  // ---- second pass (K >= 2): only the warp-slots whose maximum reaches the
+  // bound can hold survivors (about K of the CTA's 8 x n_slots); each of
+  // those warps reloads its 512 elements of the slot, now from L2, with
+  // plain 16-byte loads in the ring's layout (slots past kTrackSlots have
+  // no recorded maximum and are always reloaded)
+  for (int j = 0; K >= 2 && j < n_slots; ++j) {
+    {
+      // the running bound: the best K-th entry any warp has cut to so far
+      const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
+      if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
+        thr_v = key_v(cb);
+        thr_i = key_i(cb);
       }
-      // keep the buffer short: past max(2K, 64) entries cut it to the best K,
-      // which raises this warp's bound and, through the shared running bound,
-      // every other warp's
-      if (wn > (2 * K > 64 ? 2 * K : 64)) {
-        wn = warp_select(wb, wn, K, wb);
-        if (before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
+    }
+    const float wmax = j < kTrackSlots ? S.wsmax[warp][j] : INFINITY;
+    if (!(wmax >= thr_v)) continue;   // the same in every lane of the warp
+    const int off = j * kSlotElems;
+    int nel = n_el - off;
+    if (nel > kSlotElems) nel = kSlotElems;
+    const float* g0 = src + e_begin + off;
+    float x[kPer];
+#pragma unroll
+    for (int q = 0; q < kVec; ++q) {
+      const int e = (q * kThreads + tid) * 4;
+      float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (e + 4 <= nel) {
+        f = __ldcg(reinterpret_cast<const float4*>(g0 + e));
+      } else if (e < nel) {
+        const int avail = nel - e;
+        f.x = __ldcg(g0 + e);
+        if (avail > 1) f.y = __ldcg(g0 + e + 1);
+        if (avail > 2) f.z = __ldcg(g0 + e + 2);
+      }
+      x[4 * q + 0] = f.x;
+      x[4 * q + 1] = f.y;
+      x[4 * q + 2] = f.z;
+      x[4 * q + 3] = f.w;
+    }
+    const int tbase = e_begin + off + tid * 4;
+    float lm;
+    {
+      float m4[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) m4[a] = fmaxf(fmaxf(x[a], x[4 + a]), fmaxf(x[8 + a], x[12 + a]));
+      lm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    }
+    if (__any_sync(0xffffffffu, lm >= thr_v)) {
+      auto survives = [&](int e) {
+        const float xv = x[e];
+        const int xi = tbase + (e >> 2) * kTile + (e & 3);
+        return (xv != -INFINITY) & ((xv > thr_v) | ((xv == thr_v) & (xi <= thr_i)));
+      };
+      uint32_t pm = 0;
+      if (lm >= thr_v) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) pm |= survives(e) ? (1u << e) : 0u;
+      }
+      // common case: no lane holds more than one survivor.  A lone survivor
+      // has the lane maximum's value (any survivor of a lane whose maximum
+      // is above the bound is that maximum; at the bound all share its
+      // value); its token follows from its bit; positions from a ballot.
+      const unsigned one = __ballot_sync(0xffffffffu, pm != 0u);
+      if (__all_sync(0xffffffffu, (pm & (pm - 1u)) == 0u) && wn + __popc(one) <= kWarpCap) {
+        if (pm) {
+          const int e = __ffs(pm) - 1;
+          wb[wn + __popc(one & ((1u << lane) - 1u))] = mkkey(lm, tbase + (e >> 2) * kTile + (e & 3));
+        }
+        wn += __popc(one);
+        __syncwarp();
+        pm = 0u;
+      }
+      while (__any_sync(0xffffffffu, pm != 0u)) {
+        const int cntp = __popc(pm);
+        int incl = cntp;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        const bool fits = wn + total <= kWarpCap;
+        // append (all, or the first kWarpCap - wn in lane order)
+        int take = cntp;
+        if (!fits) take = max(0, min(cntp, kWarpCap - wn - (incl - cntp)));
+        int pos = wn + incl - cntp;
+        if (take) {
+          int taken = 0;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e)   // static indices keep x in registers
+            if (((pm >> e) & 1u) && taken < take) {
+              wb[pos++] = mkkey(x[e], tbase + (e >> 2) * kTile + (e & 3));
+              pm &= ~(1u << e);
+              ++taken;
+            }
+        }
+        __syncwarp();
+        if (fits) {
+          wn += total;
+          break;
+        }
+        // buffer full: keep the best K, raise this warp's bound, drop what no
+        // longer survives, and go on with the rest of this slot
+        wn = warp_select(wb, kWarpCap, K, wb);
+        if (wn >= K && before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
           thr_v = key_v(wb[K - 1]);
           thr_i = key_i(wb[K - 1]);
           if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
         }
+        uint32_t keep = 0;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) keep |= survives(e) ? (1u << e) : 0u;
+        pm &= keep;
+        if (!__any_sync(0xffffffffu, pm != 0u)) break;
+      }
+    }
+    // keep the buffer short: past max(2K, 64) entries cut it to the best K,
+    // which raises this warp's bound and, through the shared running bound,
+    // every other warp's
+    if (wn > (2 * K > 64 ? 2 * K : 64)) {
+      wn = warp_select(wb, wn, K, wb);
+      if (before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
+        thr_v = key_v(wb[K - 1]);
+        thr_i = key_i(wb[K - 1]);
+        if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
       }
     }
   }
