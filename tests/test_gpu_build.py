@@ -112,3 +112,51 @@ def test_repeated_calls_reuse_workspace():
     torch.cuda.synchronize()
     assert torch.equal(p1, t2.parents) and torch.equal(m1, t2.mask)
     assert eb.workspace_error(ws) == (0, 0)
+
+
+def _adversarial(kind, R, V, k, seed):
+    """Rows that stress the two-pass top-K bound of the row stream."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(R, V, generator=g)
+    if kind == "one_lane":
+        # every row's best k in the 16 elements one thread reads from its
+        # first slot (positions q * 1024 + c): a single lane holds them all
+        pos = [q * 1024 + c for q in range(4) for c in range(4)][:k]
+        x[:, pos] = 100.0 + torch.rand(R, len(pos), generator=g)
+    elif kind == "duplicates":
+        # 100 copies of each row's maximum at random places: lowest ids win
+        for r in range(R):
+            idx = torch.randperm(V, generator=g)[:100]
+            x[r, idx] = 50.0
+    elif kind == "tail":
+        # the best k in the last elements of a row whose length is no
+        # multiple of 4 (read element-wise by the stream)
+        x[:, V - k:] = 100.0 + torch.rand(R, k, generator=g)
+    elif kind == "negative":
+        x = x - 1000.0
+    return x
+
+
+@pytest.mark.parametrize("kind,V,k,D,m", [
+    ("one_lane", 40000, 10, 3, 40),
+    ("one_lane", 152064, 16, 2, 60),
+    ("duplicates", 30000, 10, 3, 40),
+    ("duplicates", 152064, 50, 1, 51),
+    ("tail", 5003, 10, 3, 40),
+    ("tail", 152063, 64, 1, 65),
+    ("negative", 20000, 8, 3, 30),
+    ("plain", 100, 64, 1, 65),       # fewer valid lanes than the bound needs: no bound
+])
+def test_adversarial_top_k_rows(kind, V, k, D, m):
+    R, _ = tree_sizes(k, D)
+    x = _adversarial(kind, R, V, k, 31)
+    ref = build_draft_tree(x.numpy(), k, D, m, 5)
+    t = _run(x, k, D, m, 5)
+    if kind == "duplicates":
+        # exact ties (the oracle reports them): the lowest token ids and
+        # candidate indices decide, so the tree is still unique
+        np.testing.assert_array_equal(t.parents.cpu().numpy(), ref["parents"])
+        np.testing.assert_array_equal(t.tokens.cpu().numpy(), ref["tokens"])
+        np.testing.assert_array_equal(t.mask_u64(), ref["mask"])
+    else:
+        tree_matches(t, ref, f"{kind} V{V} k{k}")
