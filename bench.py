@@ -429,6 +429,51 @@ def tree_expand_bench(eb, wl, dev, step, s, flush, reps=50):
             "note": "L2 flushed before each round; rows of every depth from HBM"}
 
 
+def tree_policy_bench(eb, wl, dev, step, s, flush, reps=50):
+    """The tree-shape policies on the step's draft logits (51 rows of the
+    vocabulary): the confidence-ratio tree (tau 2, up to 4 branches, depth <= 7,
+    at most 52 nodes: one row per possible inner node) and 10 batched chains
+    of depth 6 (61 nodes, the 51 rows exactly); one call each, replayed from a
+    CUDA graph with L2 flushed before every call."""
+    import torch
+    V = step.w.vocab
+    n_rows = step.draft.shape[0]
+    cases = {"confidence": (eb.tree_policy(eb.EAGLE_POLICY_CONFIDENCE, 4, 7, 2.0), n_rows + 1),
+             "chains_10x6": (eb.tree_policy(eb.EAGLE_POLICY_CHAINS, 10, 6), 61)}
+    res = {}
+    for name, (pol, m) in cases.items():
+        ws = eb.workspace(eb.eagle_tree_policy_workspace_size(V, pol, m), dev)
+        out = eb.Tree(m, dev, with_values=False)
+        nn = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def call():
+            eb.eagle_tree_build_policy(step.draft, pol, m, step.root, out=out, n_nodes=nn, ws=ws,
+                                       stream=s)
+
+        for _ in range(3):
+            call()
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            call()
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            graph.replay()
+            e1.record(s)
+            s.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        assert eb.workspace_error(ws, s)[0] == 0, "policy build recorded a device error"
+        rows = min(n_rows, m - 1)
+        us = statistics.median(times)
+        res[name] = {"us": round(us, 2), "nodes": int(nn.item()), "rows": rows,
+                     "bytes": rows * V * 4, "achieved_gbs": round(rows * V * 4 / us / 1e3, 1)}
+    res["note"] = "L2 flushed before each call; one launch per call"
+    return res
+
+
 class L2Flush:
     """Evicts the step's inputs from L2 before every step: writes 512 MB (4x
     L2), then reads 256 MB so that the lines left behind are clean and the
@@ -650,6 +695,7 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(s):
         line["kv_commit"] = kv_commit_bench(eb, wl, dev, step, s)
         line["tree_expand"] = tree_expand_bench(eb, wl, dev, step, s, flush)
+        line["tree_policy"] = tree_policy_bench(eb, wl, dev, step, s, flush)
     if not args.no_long_attn:
         la = attn_long(eb, wl, dev)
         la["frac_hbm"] = round(la["achieved_gbs"] / hbm, 4)

@@ -65,6 +65,14 @@ class CAttnPagedItem(ctypes.Structure):
                 ("m", ctypes.c_int32)]
 
 
+class CTreePolicy(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("width", ctypes.c_int32), ("depth", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("tau", ctypes.c_double)]
+
+
+EAGLE_POLICY_STATIC, EAGLE_POLICY_CHAINS, EAGLE_POLICY_CONFIDENCE = 0, 1, 2
+
+
 class CKvItem(ctypes.Structure):
     _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
                 ("tree_k", ctypes.c_void_p), ("tree_v", ctypes.c_void_p),
@@ -108,6 +116,9 @@ EXPORTS = {
     "eagle_tree_expand_workspace_size": (_SZ, [_I32, _I32]),
     "eagle_tree_expand": (_I32, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "eagle_tree_finalize": (_I32, [_P, _I32, _I32, _I32, _I32, CTree, _P, _SZ, _P]),
+    "eagle_tree_policy_workspace_size": (_SZ, [_I32, ctypes.POINTER(CTreePolicy), _I32]),
+    "eagle_tree_build_policy": (_I32, [_P, _I64, _I32, _I32, ctypes.POINTER(CTreePolicy), _I32,
+                                       _I32, CTree, _P, _P, _SZ, _P]),
     "eagle_kv_commit_workspace_size": (_SZ, []),
     "eagle_kv_commit": (_I32, [_P, _P, _I64, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _P,
                                _SZ, _P]),
@@ -213,6 +224,32 @@ def eagle_tree_build(draft_logits, top_k, depth, total_tokens, root_token, out=N
                                   top_k, depth, total_tokens, int(root_token), out.c(), _ptr(ws),
                                   ws.numel(), _stream(stream)), "eagle_tree_build")
     return out
+
+
+def tree_policy(kind, width, depth, tau=2.0):
+    return CTreePolicy(int(kind), int(width), int(depth), 0, float(tau))
+
+
+def eagle_tree_policy_workspace_size(vocab, policy, total_tokens):
+    return lib().eagle_tree_policy_workspace_size(int(vocab), ctypes.byref(policy),
+                                                  int(total_tokens))
+
+
+def eagle_tree_build_policy(draft_logits, policy, total_tokens, root_token, out=None,
+                            n_nodes=None, ws=None, stream=None):
+    """draft_logits: fp32 CUDA tensor [n_rows, vocab]; policy: tree_policy(...).
+    Returns (tree with total_tokens node slots, device int32 [1] tree size)."""
+    n_rows, vocab = draft_logits.shape
+    dev = draft_logits.device
+    out = out or Tree(total_tokens, dev, with_values=False)
+    n_nodes = n_nodes if n_nodes is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(eagle_tree_policy_workspace_size(vocab, policy, total_tokens), dev)
+    _check(lib().eagle_tree_build_policy(_ptr(draft_logits), draft_logits.stride(0), n_rows,
+                                         vocab, ctypes.byref(policy), total_tokens,
+                                         int(root_token), out.c(), _ptr(n_nodes), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "eagle_tree_build_policy")
+    return out, n_nodes
 
 
 def eagle_tree_build_noalloc(draft_logits, top_k, depth, total_tokens, root_token, out=None,

@@ -160,7 +160,7 @@ eagle_status eagle_tree_build_batched(int32_t n_items, const float* const* draft
                                       void* ws, size_t ws_bytes, eagle_stream stream);
 
 /* ------------------------------------------------------------------------
- * eagle_tree_build_noalloc -- the paper has no counterpart: this is a
+ * eagle_tree_build_noalloc -- the pages have no counterpart: this is a
  * deployment variant of eagle_tree_build for callers that cannot hand the
  * library device memory (no allocator reachable at the call site, or a
  * runtime that forbids allocation while it runs).  Same computation, same
@@ -190,6 +190,71 @@ eagle_status eagle_tree_build_noalloc(const float* draft_logits, int64_t row_str
                                       int32_t n_rows, int32_t vocab, int32_t top_k,
                                       int32_t depth, int32_t total_tokens, int32_t root_token,
                                       eagle_tree out, eagle_stream stream);
+
+/* ------------------------------------------------------------------------
+ * eagle_tree_build_policy -- tree shapes other than the dynamic top-k tree:
+ *   [disc] reply on PR #3624 (a static tree: n candidate tokens taken at
+ *   every decoding step) and the proposal of batched candidate sequences;
+ *   [blog] "Context-Aware Dynamic Tree Construction in EAGLE-2" (confidence
+ *   C = P(y1) / P(y2); above tau a linear chain, otherwise 2 to 4 branches).
+ *
+ * Nodes are numbered breadth-first (by depth, then parent, then the child's
+ * rank in its parent's row), node 0 = the root (token root_token), pos =
+ * depth, and draft row i (row i of draft_logits) is node i's draft output.
+ *   EAGLE_POLICY_STATIC      every node above depth `depth` gets the `width`
+ *                            best tokens of its row (a full width-ary tree);
+ *                            total_tokens must be 1 + width + ... + width^depth;
+ *                            rows read: the 1 + ... + width^(depth-1) inner nodes.
+ *   EAGLE_POLICY_CHAINS      the root gets row 0's `width` best tokens; every
+ *                            chain then grows by its last node's best token
+ *                            to depth `depth` (>= 1); total_tokens must be
+ *                            1 + width*depth; rows read: 1 + width*(depth-1)
+ *                            (chain j's node at depth d is node 1+(d-1)*width+j).
+ *   EAGLE_POLICY_CONFIDENCE  breadth-first; a node above depth `depth` whose
+ *                            row has l1 - l2 > ln(tau) gets one child (its best
+ *                            token), otherwise the b best tokens, b = the count
+ *                            of tokens with l1 - l <= ln(tau) (2 <= b <= width,
+ *                            width 2..8); children are added while the tree
+ *                            has fewer than total_tokens nodes, so the tree
+ *                            may come out smaller; rows read: total_tokens - 1.
+ * Ties go to the lower token id; the logit gaps and ln(tau) are compared in
+ * double precision (the gap of two float logits is exact there).
+ *
+ * draft_logits: float [n_rows][row_stride], 16-byte aligned, row_stride >= vocab,
+ *               a multiple of 4; n_rows >= the rows the policy reads.
+ * policy:       host pointer.
+ * out:          out.m == total_tokens (the node slots); slots past the tree's
+ *               size get parent -1, token -1, depth 0, pos 0 and no mask bits;
+ *               out.values is not written.
+ * n_nodes:      optional device int32: the tree's size (<= total_tokens).
+ * ws:           eagle_tree_policy_workspace_size(vocab, policy, total_tokens)
+ *               bytes (0 = the policy or the sizes are rejected).
+ * Errors: EAGLE_ERR_INVALID_ARG for a bad pointer, stride, policy field or a
+ * total_tokens that does not match a static / chains shape;
+ * EAGLE_ERR_UNSUPPORTED_SHAPE past EAGLE_MAX_TREE nodes, a width above
+ * EAGLE_MAX_TOP_K (8 for the confidence policy) or above vocab.
+ * ------------------------------------------------------------------------ */
+#define EAGLE_POLICY_STATIC 0
+#define EAGLE_POLICY_CHAINS 1
+#define EAGLE_POLICY_CONFIDENCE 2
+
+typedef struct {
+  int32_t kind;    /* EAGLE_POLICY_*                                         */
+  int32_t width;   /* static: children per node; chains: number of chains;   */
+                   /* confidence: most branches per node (2..8)             */
+  int32_t depth;   /* static / chains: depth; confidence: maximum depth      */
+  int32_t reserved;
+  double  tau;     /* confidence threshold (> 0); ignored by the others      */
+} eagle_tree_policy;
+
+size_t eagle_tree_policy_workspace_size(int32_t vocab, const eagle_tree_policy* policy,
+                                        int32_t total_tokens);
+
+eagle_status eagle_tree_build_policy(const float* draft_logits, int64_t row_stride,
+                                     int32_t n_rows, int32_t vocab,
+                                     const eagle_tree_policy* policy, int32_t total_tokens,
+                                     int32_t root_token, eagle_tree out, int32_t* n_nodes,
+                                     void* ws, size_t ws_bytes, eagle_stream stream);
 
 /* ------------------------------------------------------------------------
  * eagle_tree_attn -- [blog] "Single-Pass Tree Verification" (a tree token

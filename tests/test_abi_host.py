@@ -215,3 +215,34 @@ def test_attn_paged_rejects_bad_arguments(lib, item, shape, status):
 def test_attn_paged_without_prefix_needs_no_pool(lib):
     arr = (eb.CAttnPagedItem * 1)(_paged(k_pool=0, v_pool=0, block_table=0, prefix_len=0))
     assert lib.eagle_tree_attn_paged_workspace_size(arr, 1, 4, 2, 64) >= 256
+
+
+@pytest.mark.parametrize("pol,m,n_rows,status", [
+    (dict(kind=0, width=2, depth=3), 14, 7, 1),        # static tree of 15 nodes, not 14
+    (dict(kind=0, width=2, depth=3), 15, 6, 1),        # 7 inner nodes need 7 rows
+    (dict(kind=0, width=2, depth=8), 511, 255, 2),     # past the tree limit
+    (dict(kind=0, width=65, depth=1), 66, 1, 2),       # width above the top-k limit
+    (dict(kind=1, width=3, depth=0), 1, 1, 1),         # chains need depth >= 1
+    (dict(kind=1, width=3, depth=4), 12, 10, 1),       # chains of 13 nodes, not 12
+    (dict(kind=1, width=3, depth=4), 13, 9, 1),        # 10 rows needed
+    (dict(kind=2, width=1, depth=7, tau=2.0), 20, 19, 1),   # confidence width >= 2
+    (dict(kind=2, width=9, depth=7, tau=2.0), 20, 19, 2),   # ... and <= 8
+    (dict(kind=2, width=4, depth=7, tau=0.0), 20, 19, 1),   # tau > 0
+    (dict(kind=2, width=4, depth=7, tau=float("inf")), 20, 19, 1),
+    (dict(kind=2, width=4, depth=7, tau=2.0), 20, 18, 1),   # m - 1 rows needed
+    (dict(kind=3, width=4, depth=7, tau=2.0), 20, 19, 1),   # unknown policy
+])
+def test_policy_build_rejects_bad_arguments(lib, pol, m, n_rows, status):
+    p = eb.tree_policy(pol["kind"], pol["width"], pol["depth"], pol.get("tau", 2.0))
+    st = lib.eagle_tree_build_policy(ctypes.c_void_p(_FAKE), 1000, n_rows, 1000, ctypes.byref(p),
+                                     m, 0, _fake_tree(m), None, ctypes.c_void_p(_FAKE_WS), 1 << 30,
+                                     None)
+    assert st == status, (pol, m, n_rows)
+
+
+def test_policy_workspace_sizes(lib):
+    ok = eb.tree_policy(eb.EAGLE_POLICY_CONFIDENCE, 4, 7, 2.0)
+    assert eb.eagle_tree_policy_workspace_size(152064, ok, 60) > 0
+    bad = eb.tree_policy(eb.EAGLE_POLICY_STATIC, 2, 3)
+    assert eb.eagle_tree_policy_workspace_size(1000, bad, 14) == 0
+    assert eb.eagle_tree_policy_workspace_size(1000, bad, 15) > 0
