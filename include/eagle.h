@@ -227,6 +227,11 @@ eagle_status eagle_tree_build_noalloc(const float* draft_logits, int64_t row_str
  *               size get parent -1, token -1, depth 0, pos 0 and no mask bits;
  *               out.values is not written.
  * n_nodes:      optional device int32: the tree's size (<= total_tokens).
+ *               The tree can go to eagle_tree_attn / eagle_tree_verify with
+ *               all total_tokens slots: a padded slot is nobody's child, so
+ *               the walk never accepts it, and it sees no tree keys, so its
+ *               attention output is unspecified (it has no keys at all when
+ *               prefix_len is 0).
  * ws:           eagle_tree_policy_workspace_size(vocab, policy, total_tokens)
  *               bytes (0 = the policy or the sizes are rejected).
  * Errors: EAGLE_ERR_INVALID_ARG for a bad pointer, stride, policy field or a
