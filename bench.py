@@ -583,6 +583,18 @@ def _time_e2e(torch, step, s, flush, K):
     return times, d2h
 
 
+def spread(times):
+    """p10 / median / p90 of per-step times (nearest-rank percentiles)."""
+    xs = sorted(float(t) for t in times)
+    if not xs:
+        return None
+
+    def rank(q):
+        return round(xs[min(len(xs) - 1, max(0, -(-q * len(xs) // 100) - 1))], 3)
+
+    return {"p10": rank(10), "median": round(statistics.median(xs), 3), "p90": rank(90)}
+
+
 def max_over_ranks(x, world, device):
     """Slowest replica's value: the job's step time is set by the last rank
     to finish (all ranks run the same workload on their own GPU)."""
@@ -673,6 +685,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(us, 3), "unit": "us", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "spread_us": spread(times),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 logits + bf16 attention (fp32 accumulate)" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded generators; no dataset or weights)",
