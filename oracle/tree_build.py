@@ -18,7 +18,7 @@ Sources:
 * "EAGLE-2: Feature-Level Speculative Decoding Guide", "Single-Pass Tree
   Verification": a token attends to its ancestors (and itself) only.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * depth D = deepest drafted level; root has depth 0; rows R = 1 + (D-1)k,
   candidates C = k + (D-1)k^2.
 * row map: row 0 is the root; the j-th frontier slot at depth l (frontier

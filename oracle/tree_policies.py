@@ -17,7 +17,7 @@ Sources:
   Drafting Step": the draft distribution is the softmax of the logits, so
   P(y_(1)) / P(y_(j)) = exp(l_(1) - l_(j)) and every ranking is by raw logit.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * Nodes are numbered breadth-first (by depth; within a depth by parent, then
   by the child's rank in its parent's row); node 0 is the root, pos = depth.
 * Draft row i is node i's draft output: the rows a policy reads are those of

@@ -17,7 +17,7 @@ Sources:
 * "EAGLE-2 Speculative Decoding Support for llama.cpp - Phase 1",
   "Performance Notes": mixed sampling = temperature + top_k + top_p.
 
-Readings (listed in DESIGN.md):
+Readings where the pages are silent or ambiguous:
 * row i of the target logits predicts the token after node i.
 * warped target distribution: logits / T; keep the top_k largest (ties ->
   lower id; top_k = 0 keeps all); softmax over the kept set; if top_p < 1 keep
