@@ -25,3 +25,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    try:
+        from tests.parity import ATTN_ERRORS
+    except Exception:
+        return
+    if ATTN_ERRORS:
+        terminalreporter.write_line("attention max abs error vs the oracle (bound 2e-3):")
+        for what, err in sorted(ATTN_ERRORS.items()):
+            terminalreporter.write_line(f"  {what}: {err:.3e}")

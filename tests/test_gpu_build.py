@@ -8,7 +8,7 @@ import torch
 from eagle_speculative_decoding_verify_gb300 import binding as eb
 from eagle_speculative_decoding_verify_gb300 import workloads as wl
 from oracle.tree_build import build_draft_tree, tree_sizes
-from tests.parity import to_device_rows, tree_matches
+from tests.parity import PAD, to_device_rows, tree_matches
 
 pytestmark = pytest.mark.gpu
 
@@ -18,7 +18,7 @@ def _rows(R, V, seed, stride=None):
     sig = torch.tensor([1.0, 3.0, 6.0])[torch.randint(0, 3, (R,), generator=g)]
     x = torch.randn(R, V, generator=g) * sig[:, None]
     if stride is not None and stride > V:
-        big = torch.full((R, stride), -1e30)
+        big = torch.full((R, stride), PAD)
         big[:, :V] = x
         return big[:, :V]
     return x
@@ -33,7 +33,7 @@ def _run(x, k, D, m, root=3):
     return t
 
 
-@pytest.mark.parametrize("key", ["c0", "c1", "c2"])
+@pytest.mark.parametrize("key", ["c0", "c1", "c2", "c3"])
 def test_workload_trees(key):
     w = wl.WORKLOADS[key]
     x = wl.draft_logits(w)

@@ -39,7 +39,8 @@ def test_full_step(key):
     assert max_abs(out.cpu().numpy(), o_ref) <= ATTN_TOL
     v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=bool(gr),
                     temperature=T, top_k=k, top_p=p, seed=42, step=0)
-    path_matches(acc.cpu().numpy(), int(n.item()), int(bonus.item()), v, key)
+    path_matches(acc.cpu().numpy(), int(n.item()), int(bonus.item()), v, key, ref["parents"],
+                 ref["tokens"], target.numpy(), (gr, T, k, p))
 
 
 def test_smoke_entry():

@@ -35,7 +35,8 @@ def test_greedy_workloads(key):
     w, ref, target = _case(key)
     v = verify_tree(target.numpy(), ref["parents"], ref["tokens"])
     acc, n, bonus = _verify(target, ref)
-    path_matches(acc, n, bonus, v, key)
+    path_matches(acc, n, bonus, v, key, ref["parents"], ref["tokens"], target.numpy(),
+                 (1, 1.0, 0, 1.0))
 
 
 def test_greedy_forced_full_chain():
@@ -56,7 +57,8 @@ def test_greedy_forced_full_chain():
         node = kids[node][0]
         chain += 1
     assert n == chain
-    path_matches(acc, n, bonus, v, "forced chain")
+    path_matches(acc, n, bonus, v, "forced chain", ref["parents"], ref["tokens"], target.numpy(),
+                 (1, 1.0, 0, 1.0))
 
 
 @pytest.mark.parametrize("seed", range(8))
@@ -66,7 +68,8 @@ def test_sampling_topk_topp_qwen7b(seed):
     v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False, temperature=T,
                     top_k=k, top_p=p, seed=seed, step=seed * 7)
     acc, n, bonus = _verify(target, ref, False, T, k, p, seed, seed * 7)
-    path_matches(acc, n, bonus, v, f"seed{seed}")
+    path_matches(acc, n, bonus, v, f"seed{seed}", ref["parents"], ref["tokens"], target.numpy(),
+                 (0, T, k, p))
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -75,7 +78,8 @@ def test_sampling_full_vocab(seed):
     v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False, temperature=1.0,
                     seed=seed, step=3)
     acc, n, bonus = _verify(target, ref, False, 1.0, 0, 1.0, seed, 3)
-    path_matches(acc, n, bonus, v, f"full seed{seed}")
+    path_matches(acc, n, bonus, v, f"full seed{seed}", ref["parents"], ref["tokens"],
+                 target.numpy(), (0, 1.0, 0, 1.0))
 
 
 @pytest.mark.parametrize("T,k,p", [(0.5, 1, 1.0), (1.3, 64, 1.0), (0.9, 7, 0.5), (2.0, 0, 1.0)])
@@ -89,7 +93,8 @@ def test_sampling_variants_rejections(T, k, p):
         v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False,
                         temperature=T, top_k=k, top_p=p, seed=seed, step=1)
         acc, n, bonus = _verify(target, ref, False, T, k, p, seed, 1)
-        path_matches(acc, n, bonus, v, f"T{T} k{k} p{p} seed{seed}")
+        path_matches(acc, n, bonus, v, f"T{T} k{k} p{p} seed{seed}", ref["parents"],
+                     ref["tokens"], target.numpy(), (0, T, k, p))
 
 
 def test_batched_ragged16_mixed_modes():
@@ -110,7 +115,8 @@ def test_batched_ragged16_mixed_modes():
         gr, T, k, p = w.sampling_of(b)
         v = verify_tree(targets[b].numpy(), refs[b]["parents"], refs[b]["tokens"], greedy=bool(gr),
                         temperature=T, top_k=k, top_p=p, seed=seeds[b], step=5)
-        path_matches(acc[b].cpu().numpy(), int(n[b]), int(bonus[b]), v, f"item{b}")
+        path_matches(acc[b].cpu().numpy(), int(n[b]), int(bonus[b]), v, f"item{b}",
+                     refs[b]["parents"], refs[b]["tokens"], targets[b].numpy(), (gr, T, k, p))
 
 
 def test_single_node_tree():
