@@ -609,8 +609,9 @@ def max_over_ranks(x, world, device):
 # known ncu DRAM traffic per launch (bytes), keyed by kernel and source hash;
 # entries whose hash no longer matches the sources are reported as null
 TRAFFIC = {
-    # profiles/*_c2.md: dram__bytes_read.sum + dram__bytes_write.sum of one launch,
-    # keyed by the kernel's source hash (_kernel_source_hash)
+    # dram__bytes_read.sum + dram__bytes_write.sum of one launch on the c2
+    # workload from one ncu capture, keyed by the kernel's source hash
+    # (_kernel_source_hash)
     "build:c2": ("780fe5897637", 31123456),
     "verify:c2": ("122e946b2dc0", 36598528),
     "attn:c2": ("d4abccd751ad", 17386496),

@@ -1,11 +1,14 @@
 """Compile the CUDA sources into the in-tree C-ABI library ``libeagle.so``.
 
 nvcc, sm_103a only; translation units are compiled in parallel and linked
-with the CUDA runtime statically.  Re-runs only when a source is newer than
-the library.
+with the CUDA runtime statically.  The library embeds a hash of its sources
+and build flags (``eagle_build_id()``); a build is reused only when that hash
+equals the hash of the sources on disk, and the binding refuses a library
+whose hash differs.
 """
 
 import glob
+import hashlib
 import os
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -38,11 +41,28 @@ def _deps():
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
+def source_hash():
+    """sha256 (16 hex digits) of every source and header, by relative path and
+    content, and of the compiler flags."""
+    h = hashlib.sha256()
+    for p in sorted(_deps()):
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + FLAGS[:-4]).encode())
+    return h.hexdigest()[:16]
+
+
+BUILD_ID_FILE = LIB + ".buildid"
+
+
 def up_to_date():
-    if not os.path.exists(LIB):
+    """True when libeagle.so was built from the sources on disk (its recorded
+    build id equals their hash)."""
+    if not os.path.exists(LIB) or not os.path.exists(BUILD_ID_FILE):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    with open(BUILD_ID_FILE) as f:
+        return f.read().strip() == source_hash()
 
 
 def build(force=False, verbose=False, extra_flags=()):
@@ -51,10 +71,12 @@ def build(force=False, verbose=False, extra_flags=()):
         return LIB
     os.makedirs(OBJ, exist_ok=True)
     nvcc = _nvcc()
+    build_id = source_hash()
 
     def compile_one(src):
         obj = os.path.join(OBJ, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, f"-DEAGLE_BUILD_ID=\"{build_id}\"", "-c", src,
+               "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stderr[-4000:]}")
@@ -70,6 +92,8 @@ def build(force=False, verbose=False, extra_flags=()):
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr[-4000:])
     os.replace(tmp, LIB)
+    with open(BUILD_ID_FILE, "w") as f:
+        f.write(build_id + "\n")
     return LIB
 
 

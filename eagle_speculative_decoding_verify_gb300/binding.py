@@ -91,6 +91,8 @@ _F = ctypes.c_float
 EXPORTS = {
     "eagle_status_string": (ctypes.c_char_p, [_I32]),
     "eagle_version": (_I32, []),
+    "eagle_build_id": (ctypes.c_char_p, []),
+    "eagle_tree_build_noalloc_error": (_I32, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "eagle_workspace_init": (_I32, [_P, _SZ, _P]),
     "eagle_workspace_error": (_I32, [_P, _P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "eagle_tree_build_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
@@ -140,8 +142,19 @@ def lib():
             fn = getattr(handle, name)
             fn.restype = res
             fn.argtypes = args
+        from . import _build
+        built = handle.eagle_build_id().decode()
+        if os.path.isdir(_build.CSRC) and built != _build.source_hash():
+            raise RuntimeError(f"{LIB_PATH} was built from other sources (build id {built}, "
+                               f"sources {_build.source_hash()}): rebuild it "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
         _lib = handle
     return _lib
+
+
+def build_id():
+    """Hash of the sources the loaded library was built from."""
+    return lib().eagle_build_id().decode()
 
 
 def _check(status, what):
@@ -153,6 +166,12 @@ def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on(t):
+    """Make t's device current for the call (the library works on the current
+    device, and its default stream is that device's current stream)."""
+    return torch.cuda.device(t.device if isinstance(t, torch.Tensor) else t)
 
 
 def _ptr(t):
@@ -220,9 +239,10 @@ def eagle_tree_build(draft_logits, top_k, depth, total_tokens, root_token, out=N
     if ws is None:
         ws = workspace(eagle_tree_build_workspace_size(1, n_rows, vocab, top_k, depth,
                                                        total_tokens), draft_logits.device)
-    _check(lib().eagle_tree_build(_ptr(draft_logits), draft_logits.stride(0), n_rows, vocab,
-                                  top_k, depth, total_tokens, int(root_token), out.c(), _ptr(ws),
-                                  ws.numel(), _stream(stream)), "eagle_tree_build")
+    with _on(draft_logits):
+        _check(lib().eagle_tree_build(_ptr(draft_logits), draft_logits.stride(0), n_rows, vocab,
+                                      top_k, depth, total_tokens, int(root_token), out.c(), _ptr(ws),
+                                      ws.numel(), _stream(stream)), "eagle_tree_build")
     return out
 
 
@@ -245,10 +265,11 @@ def eagle_tree_build_policy(draft_logits, policy, total_tokens, root_token, out=
     n_nodes = n_nodes if n_nodes is not None else torch.zeros(1, dtype=torch.int32, device=dev)
     if ws is None:
         ws = workspace(eagle_tree_policy_workspace_size(vocab, policy, total_tokens), dev)
-    _check(lib().eagle_tree_build_policy(_ptr(draft_logits), draft_logits.stride(0), n_rows,
-                                         vocab, ctypes.byref(policy), total_tokens,
-                                         int(root_token), out.c(), _ptr(n_nodes), _ptr(ws),
-                                         ws.numel(), _stream(stream)), "eagle_tree_build_policy")
+    with _on(draft_logits):
+        _check(lib().eagle_tree_build_policy(_ptr(draft_logits), draft_logits.stride(0), n_rows,
+                                             vocab, ctypes.byref(policy), total_tokens,
+                                             int(root_token), out.c(), _ptr(n_nodes), _ptr(ws),
+                                             ws.numel(), _stream(stream)), "eagle_tree_build_policy")
     return out, n_nodes
 
 
@@ -258,10 +279,21 @@ def eagle_tree_build_noalloc(draft_logits, top_k, depth, total_tokens, root_toke
     calls on one device must not overlap on the GPU."""
     n_rows, vocab = draft_logits.shape
     out = out or Tree(total_tokens, draft_logits.device)
-    _check(lib().eagle_tree_build_noalloc(_ptr(draft_logits), draft_logits.stride(0), n_rows,
-                                          vocab, top_k, depth, total_tokens, int(root_token),
-                                          out.c(), _stream(stream)), "eagle_tree_build_noalloc")
+    with _on(draft_logits):
+        _check(lib().eagle_tree_build_noalloc(_ptr(draft_logits), draft_logits.stride(0), n_rows,
+                                              vocab, top_k, depth, total_tokens, int(root_token),
+                                              out.c(), _stream(stream)), "eagle_tree_build_noalloc")
     return out
+
+
+def eagle_tree_build_noalloc_error(stream=None):
+    """(status, detail) of the static scratch's error word after the last
+    eagle_tree_build_noalloc call on the current device (synchronises)."""
+    st, detail = _I32(0), _I32(0)
+    _check(lib().eagle_tree_build_noalloc_error(_stream(stream), ctypes.byref(st),
+                                                ctypes.byref(detail)),
+           "eagle_tree_build_noalloc_error")
+    return st.value, detail.value
 
 
 def eagle_tree_build_batched(draft_logits, top_k, depth, total_tokens, root_tokens, outs=None,
@@ -276,10 +308,11 @@ def eagle_tree_build_batched(draft_logits, top_k, depth, total_tokens, root_toke
     ptrs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in draft_logits])
     roots = (ctypes.c_int32 * n)(*[int(r) for r in root_tokens])
     trees = (CTree * n)(*[o.c() for o in outs])
-    _check(lib().eagle_tree_build_batched(n, ptrs, draft_logits[0].stride(0), n_rows, vocab,
-                                          top_k, depth, total_tokens, roots, trees, _ptr(ws),
-                                          ws.numel(), _stream(stream)),
-           "eagle_tree_build_batched")
+    with _on(draft_logits[0]):
+        _check(lib().eagle_tree_build_batched(n, ptrs, draft_logits[0].stride(0), n_rows, vocab,
+                                              top_k, depth, total_tokens, roots, trees, _ptr(ws),
+                                              ws.numel(), _stream(stream)),
+               "eagle_tree_build_batched")
     return outs
 
 
@@ -316,10 +349,11 @@ def eagle_tree_attn(q, k_cache, v_cache, tree_k, tree_v, mask, prefix_len=None, 
     out = out if out is not None else torch.empty(m, hq, d, dtype=torch.float32, device=q.device)
     if ws is None:
         ws = workspace(eagle_tree_attn_workspace_size(m, hq, hkv, d, S, dt), q.device)
-    _check(lib().eagle_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0),
-                                 _ptr(tree_k), _ptr(tree_v), _ptr(mask), m, hq, hkv, d, S, dt,
-                                 float(scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
-           "eagle_tree_attn")
+    with _on(q):
+        _check(lib().eagle_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0),
+                                     _ptr(tree_k), _ptr(tree_v), _ptr(mask), m, hq, hkv, d, S, dt,
+                                     float(scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+               "eagle_tree_attn")
     return out
 
 
@@ -371,10 +405,11 @@ def eagle_tree_verify(target_logits, tree, params=None, seed=0, step=0, accepted
                                                                           device=dev)
     if ws is None:
         ws = workspace(eagle_tree_verify_workspace_size(1, m, vocab), dev)
-    _check(lib().eagle_tree_verify(_ptr(target_logits), target_logits.stride(0), vocab, tree.c(),
-                                   ctypes.byref(params), seed, step, _ptr(accepted),
-                                   _ptr(n_accepted), _ptr(bonus_token), _ptr(ws), ws.numel(),
-                                   _stream(stream)), "eagle_tree_verify")
+    with _on(target_logits):
+        _check(lib().eagle_tree_verify(_ptr(target_logits), target_logits.stride(0), vocab, tree.c(),
+                                       ctypes.byref(params), seed, step, _ptr(accepted),
+                                       _ptr(n_accepted), _ptr(bonus_token), _ptr(ws), ws.numel(),
+                                       _stream(stream)), "eagle_tree_verify")
     return accepted, n_accepted, bonus_token
 
 
@@ -395,10 +430,11 @@ def eagle_tree_verify_batched(target_logits, trees, params, seeds, step=0, accep
     pa = (CSampling * n)(*params)
     sd = (ctypes.c_uint64 * n)(*[int(s) for s in seeds])
     ac = (ctypes.c_void_p * n)(*[a.data_ptr() for a in accepted])
-    _check(lib().eagle_tree_verify_batched(n, lp, target_logits[0].stride(0), vocab, tr, pa, sd,
-                                           step, ac, _ptr(n_accepted), _ptr(bonus_tokens),
-                                           _ptr(ws), ws.numel(), _stream(stream)),
-           "eagle_tree_verify_batched")
+    with _on(target_logits[0]):
+        _check(lib().eagle_tree_verify_batched(n, lp, target_logits[0].stride(0), vocab, tr, pa, sd,
+                                               step, ac, _ptr(n_accepted), _ptr(bonus_tokens),
+                                               _ptr(ws), ws.numel(), _stream(stream)),
+               "eagle_tree_verify_batched")
     return accepted, n_accepted, bonus_tokens
 
 
@@ -422,10 +458,11 @@ def eagle_kv_commit(k_cache, v_cache, tree_k, tree_v, accepted, n_accepted, pref
     hkv, _, d = k_cache.shape
     if ws is None:
         ws = workspace(eagle_kv_commit_workspace_size(), k_cache.device)
-    _check(lib().eagle_kv_commit(_ptr(k_cache), _ptr(v_cache), k_cache.stride(0), int(prefix_len),
-                                 _ptr(tree_k), _ptr(tree_v), tree_k.shape[0], hkv, d,
-                                 _dtype_code(k_cache), _ptr(accepted), _ptr(n_accepted), _ptr(ws),
-                                 ws.numel(), _stream(stream)), "eagle_kv_commit")
+    with _on(k_cache):
+        _check(lib().eagle_kv_commit(_ptr(k_cache), _ptr(v_cache), k_cache.stride(0), int(prefix_len),
+                                     _ptr(tree_k), _ptr(tree_v), tree_k.shape[0], hkv, d,
+                                     _dtype_code(k_cache), _ptr(accepted), _ptr(n_accepted), _ptr(ws),
+                                     ws.numel(), _stream(stream)), "eagle_kv_commit")
 
 
 def eagle_kv_commit_batched(items, n_kv_heads, head_dim, dtype, ws=None, stream=None, device=None):
@@ -452,18 +489,20 @@ class TreeGrowth:
     def expand(self, rows, level, stream=None):
         """rows: fp32 [1 or top_k, V] with a row stride that is a multiple of 4.
         Returns the new frontier (device int32 [2, top_k]: tokens, parent slots)."""
-        _check(lib().eagle_tree_expand(_ptr(rows), rows.stride(0), rows.shape[1], self.top_k,
-                                       self.depth, int(level), _ptr(self.state),
-                                       _ptr(self.frontier), _ptr(self.ws), self.ws.numel(),
-                                       _stream(stream)), "eagle_tree_expand")
+        with _on(rows):
+            _check(lib().eagle_tree_expand(_ptr(rows), rows.stride(0), rows.shape[1], self.top_k,
+                                           self.depth, int(level), _ptr(self.state),
+                                           _ptr(self.frontier), _ptr(self.ws), self.ws.numel(),
+                                           _stream(stream)), "eagle_tree_expand")
         return self.frontier
 
     def finalize(self, total_tokens, root_token, out=None, stream=None):
         out = out or Tree(total_tokens, self.state.device)
-        _check(lib().eagle_tree_finalize(_ptr(self.state), self.top_k, self.depth,
-                                         int(total_tokens), int(root_token), out.c(),
-                                         _ptr(self.ws), self.ws.numel(), _stream(stream)),
-               "eagle_tree_finalize")
+        with _on(self.state):
+            _check(lib().eagle_tree_finalize(_ptr(self.state), self.top_k, self.depth,
+                                             int(total_tokens), int(root_token), out.c(),
+                                             _ptr(self.ws), self.ws.numel(), _stream(stream)),
+                   "eagle_tree_finalize")
         return out
 
 

@@ -17,7 +17,15 @@ extern "C" const char* eagle_status_string(eagle_status s) {
   return "unknown status";
 }
 
-extern "C" int32_t eagle_version(void) { return 1; }
+extern "C" int32_t eagle_version(void) { return 2; }
+
+#ifndef EAGLE_BUILD_ID
+#define EAGLE_BUILD_ID "unknown"
+#endif
+
+// Hash of the sources and flags this library was compiled from (set by the
+// build script), so that a caller can tell a stale binary from a current one.
+extern "C" const char* eagle_build_id(void) { return EAGLE_BUILD_ID; }
 
 extern "C" eagle_status eagle_workspace_init(void* ws, size_t ws_bytes, eagle_stream stream) {
   EAGLE_CHECK_ARG(ws != nullptr && ws_bytes >= kWsHeader);

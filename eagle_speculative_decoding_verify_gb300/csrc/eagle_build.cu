@@ -15,6 +15,9 @@
 // (binary search on order-preserving 64-bit keys, ties -> lower candidate
 // index); node ids by a block scan; ancestor mask by walking parent pointers
 // (depth <= 16).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "eagle_stream_host.h"
@@ -397,22 +400,60 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[EAGLE_NOALLOC_S
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
+// through the runtime's driver entry-point query, so the library does not
+// link the driver library itself); 0 when there is no current context yet or
+// the query is unavailable.  The id is never reused within a process, so a
+// context created after cudaDeviceReset, or a separate driver-API context on
+// the same device, gets a new one.
+static unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch in the current context.  The symbol's
+// address belongs to the library's module as loaded in one context, so it is
+// looked up with cudaGetSymbolAddress once per (device, context) -- on the
+// first call in a context, with that device current -- and cached under the
+// context's id; when the id cannot be read, it is looked up on every call.
 static eagle_status noalloc_scratch(void** out) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = 0;
   EAGLE_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kMaxDevices) return EAGLE_ERR_UNSUPPORTED_SHAPE;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    EAGLE_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
-    if (!p || !aligned16(p)) return EAGLE_ERR_CUDA;
-    addr[dev] = p;
+  unsigned long long ctx = current_context_id();
+  if (ctx != 0 && ctx_of[dev] == ctx && addr[dev]) {
+    *out = addr[dev];
+    return EAGLE_OK;
   }
-  *out = addr[dev];
+  void* p = nullptr;
+  EAGLE_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+  if (!p || !aligned16(p)) return EAGLE_ERR_CUDA;
+  ctx = current_context_id();   // the lookup made the device's context current
+  addr[dev] = p;
+  ctx_of[dev] = ctx;
+  *out = p;
   return EAGLE_OK;
 }
 
@@ -481,4 +522,13 @@ extern "C" eagle_status eagle_tree_build_noalloc(const float* draft_logits, int6
   EAGLE_CUDA(cudaMemsetAsync(ws, 0, L.off_rows, s));
   return build_impl(1, &draft_logits, row_stride, n_rows, vocab, top_k, depth, total_tokens,
                     &root_token, &out, ws, EAGLE_NOALLOC_SCRATCH_BYTES, s);
+}
+
+extern "C" eagle_status eagle_tree_build_noalloc_error(eagle_stream stream, int32_t* status,
+                                                       int32_t* detail) {
+  EAGLE_CHECK_ARG(status != nullptr);
+  void* ws = nullptr;
+  const eagle_status st = noalloc_scratch(&ws);
+  if (st != EAGLE_OK) return st;
+  return eagle_workspace_error(ws, stream, status, detail);
 }

@@ -107,6 +107,11 @@ typedef struct {
 const char* eagle_status_string(eagle_status status);
 int32_t eagle_version(void);
 
+/* Hash (16 hex digits) of the sources and compiler flags the library was
+ * built from; a build tool compares it with the sources on disk to tell a
+ * stale binary from a current one.  Static string, never NULL. */
+const char* eagle_build_id(void);
+
 /* Zero-fill a workspace (cudaMemsetAsync on `stream`). */
 eagle_status eagle_workspace_init(void* ws, size_t ws_bytes, eagle_stream stream);
 
@@ -167,15 +172,21 @@ eagle_status eagle_tree_build_batched(int32_t n_items, const float* const* draft
  * arguments and same output as eagle_tree_build, without `ws`.
  *
  * Scratch: a fixed array of EAGLE_NOALLOC_SCRATCH_BYTES in the library's own
- * static device memory (one per device, located once per device on first
- * use) -- the one piece of global state in the library.  The call allocates
- * nothing (no cudaMalloc / cudaFree / allocating library routine); it clears
- * the scratch's header and counters on `stream` before its launch, so stale
+ * static device memory (one per device) -- the one piece of global state in
+ * the library.  Its device address is looked up (cudaGetSymbolAddress) on
+ * the first call in each CUDA context, with that context's device current,
+ * and cached under the context's unique id, so a context created later (after
+ * cudaDeviceReset, or a separate driver-API context) gets its own lookup;
+ * make that first call before any stream capture.  The stream must belong to
+ * the calling thread's current context.  The call allocates nothing (no
+ * cudaMalloc / cudaFree / allocating library routine); it clears the
+ * scratch's header and counters on `stream` before its launch, so stale
  * contents from an earlier call (even one that recorded a device error) do
  * not matter.  Every call on a device shares that array: calls that overlap
  * on the GPU (different streams without ordering, or concurrent host
  * threads) race and give undefined results.  Device-side errors are recorded
- * in the shared scratch and are not reported.
+ * in the shared scratch's error word: eagle_tree_build_noalloc_error reads
+ * the last call's.
  * Limit: the workspace of the shape,
  *   eagle_tree_build_workspace_size(1, n_rows, vocab, top_k, depth, m),
  *   must fit in EAGLE_NOALLOC_SCRATCH_BYTES; larger shapes return
@@ -190,6 +201,13 @@ eagle_status eagle_tree_build_noalloc(const float* draft_logits, int64_t row_str
                                       int32_t n_rows, int32_t vocab, int32_t top_k,
                                       int32_t depth, int32_t total_tokens, int32_t root_token,
                                       eagle_tree out, eagle_stream stream);
+
+/* Synchronise `stream`, then read the error word of the static scratch as
+ * eagle_workspace_error does for a workspace: the device-side status of the
+ * last eagle_tree_build_noalloc call on the current device (EAGLE_OK,
+ * EAGLE_ERR_TIMEOUT or EAGLE_ERR_DEVICE_ASSERT).  Allocates nothing. */
+eagle_status eagle_tree_build_noalloc_error(eagle_stream stream, int32_t* status,
+                                            int32_t* detail);
 
 /* ------------------------------------------------------------------------
  * eagle_tree_build_policy -- tree shapes other than the dynamic top-k tree:

@@ -35,6 +35,13 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= set(eb.EXPORTS), set(names) - set(eb.EXPORTS)
 
 
+def test_build_id_is_the_hash_of_the_sources(lib):
+    from eagle_speculative_decoding_verify_gb300 import _build
+    bid = lib.eagle_build_id().decode()
+    assert len(bid) == 16 and bid == _build.source_hash()
+    assert _build.up_to_date()
+
+
 def test_status_strings_and_version(lib):
     assert lib.eagle_version() >= 1
     for code in range(7):

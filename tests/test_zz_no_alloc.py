@@ -69,3 +69,21 @@ def test_rejects_shapes_beyond_the_scratch():
     t = eb.eagle_tree_build(x, k, D, m, 0)
     torch.cuda.synchronize()
     assert int(t.parents[0]) == -1
+
+
+def test_reused_output_tree_and_error_word():
+    # a caller that cannot allocate also reuses its output arrays: two calls
+    # in stream order into the same tree with different roots, each result
+    # read before the next call, each equal to the workspace entry point's
+    w = wl.WORKLOADS["c1"]
+    x = wl.draft_logits(w).cuda()
+    out = eb.Tree(w.total_tokens)
+    for root in (17, 90210):
+        t = eb.eagle_tree_build_noalloc(x, w.top_k, w.depth, w.total_tokens, root, out=out)
+        assert t is out
+        ref = eb.eagle_tree_build(x, w.top_k, w.depth, w.total_tokens, root)
+        torch.cuda.synchronize()
+        _same(out, ref, f"root {root}")
+        assert int(out.tokens[0]) == root
+        # the static scratch's device error word is clear after a good call
+        assert eb.eagle_tree_build_noalloc_error() == (0, 0)
