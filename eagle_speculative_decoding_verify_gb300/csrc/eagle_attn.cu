@@ -195,8 +195,7 @@ static void plan_simt(AttnPlan& P, const eagle_attn_item* items, int n, int hq, 
   P.scale = scale != 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d));
   int64_t base = 0;
   for (int b = 0; b < n; ++b) base += static_cast<int64_t>(hkv) * items[b].m;
-  (void)sms;
-  const int64_t target = static_cast<int64_t>(kPlanSMs) * 8;
+  const int64_t target = static_cast<int64_t>(sms) * 8;
   int64_t units = 0, rows = 0, part = 0;
   for (int b = 0; b < n; ++b) {
     const eagle_attn_item& it = items[b];
@@ -238,7 +237,7 @@ static eagle_status attn_batched_impl(const eagle_attn_item* items, int32_t n, i
   eagle_status st = validate(items, n, hq, hkv, d, dtype);
   if (st != EAGLE_OK) return st;
   EAGLE_CHECK_ARG(ws != nullptr);
-  const int sms = kPlanSMs;
+  const int sms = plan_sms();
   for (int b0 = 0; b0 < n; b0 += kAttnMaxItems) {
     const int nb = (n - b0) < kAttnMaxItems ? (n - b0) : kAttnMaxItems;
     if (dtype == EAGLE_BF16 && tc_supported(d)) {
@@ -265,20 +264,21 @@ static eagle_status attn_batched_impl(const eagle_attn_item* items, int32_t n, i
 static size_t attn_ws_size(const eagle_attn_item* items, int32_t n, int32_t hq, int32_t hkv,
                            int32_t d, eagle_dtype dtype) {
   if (!items || n < 1 || hq < 1 || hkv < 1 || d < 1) return 0;
-  const int sms = kPlanSMs;
   size_t need = kWsHeader;
-  for (int b0 = 0; b0 < n; b0 += kAttnMaxItems) {
-    const int nb = (n - b0) < kAttnMaxItems ? (n - b0) : kAttnMaxItems;
-    size_t s;
-    if (dtype == EAGLE_BF16 && tc_supported(d)) {
-      s = attn_tc_ws_size(items + b0, nb, hq, hkv, d, sms);
-    } else {
-      AttnPlan P;
-      plan_simt(P, items + b0, nb, hq, hkv, d, 0.f, sms);
-      s = simt_ws(P);
+  // large enough for the plan of the current device and for the default one
+  for (const int sms : {kPlanSMs, plan_sms()})
+    for (int b0 = 0; b0 < n; b0 += kAttnMaxItems) {
+      const int nb = (n - b0) < kAttnMaxItems ? (n - b0) : kAttnMaxItems;
+      size_t s;
+      if (dtype == EAGLE_BF16 && tc_supported(d)) {
+        s = attn_tc_ws_size(items + b0, nb, hq, hkv, d, sms);
+      } else {
+        AttnPlan P;
+        plan_simt(P, items + b0, nb, hq, hkv, d, 0.f, sms);
+        s = simt_ws(P);
+      }
+      if (s > need) need = s;
     }
-    if (s > need) need = s;
-  }
   return need;
 }
 
@@ -289,10 +289,10 @@ static int32_t attn_num_launches(const eagle_attn_item* items, int32_t n, int32_
   for (int b0 = 0; b0 < n; b0 += kAttnMaxItems) {
     const int nb = (n - b0) < kAttnMaxItems ? (n - b0) : kAttnMaxItems;
     if (dtype == EAGLE_BF16 && tc_supported(d)) {
-      count += attn_tc_num_launches(items + b0, nb, hq, hkv, d);
+      count += attn_tc_num_launches(items + b0, nb, hq, hkv, d, plan_sms());
     } else {
       AttnPlan P;
-      plan_simt(P, items + b0, nb, hq, hkv, d, 0.f, kPlanSMs);
+      plan_simt(P, items + b0, nb, hq, hkv, d, 0.f, plan_sms());
       count += 1 + (P.part_floats > 0 ? 1 : 0);
     }
   }

@@ -10,9 +10,20 @@
 namespace eagle {
 
 constexpr int kAttnMaxItems = 32;  // items per launch (more are chunked)
-// Split plans are sized for a 152-SM part independently of the device the
-// call runs on, so workspace sizes do not depend on the device.
+// SM count the split plans assume when no device can be queried (a
+// workspace-size query on a host without a GPU); otherwise the plan fills the
+// current device's SMs, and workspace sizes cover both plans.
 constexpr int kPlanSMs = 152;
+
+inline int plan_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    return kPlanSMs;
+  }
+  return n;
+}
 
 // Floats per (row, split) partial: head_dim outputs, then max (log2 units)
 // and sum, padded to a 16-byte multiple.
@@ -50,7 +61,7 @@ eagle_status launch_attn_merge(const AttnPlan& P, cudaStream_t stream);
 // tensor-core path (eagle_attn_tc.cu)
 bool tc_supported(int head_dim);
 size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms);
-int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d);
+int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms);
 eagle_status attn_tc_launch(const eagle_attn_item* items, int n, int hq, int hkv, int d,
                             float scale, void* ws, size_t ws_bytes, cudaStream_t stream, int sms);
 

@@ -581,7 +581,7 @@ struct TcPlan {
 // prefix splits plus one tree split.  The span (in 128-key chunks) minimises
 // waves x (span + 2) -- the +2 for a CTA's fixed work (Q tiles, epilogue) --
 // plus a small charge per CTA for its partials' write and read.
-static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int d) {
+static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms) {
   TcPlan T;
   memset(&T, 0, sizeof(T));
   const int g = hq / hkv;
@@ -597,7 +597,7 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
       const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
       total += static_cast<int64_t>(hkv) * ((T.tiles[b] + 1) / 2) * ((nc + span - 1) / span + 1);
     }
-    const int64_t waves = (total + kPlanSMs - 1) / kPlanSMs;
+    const int64_t waves = (total + sms - 1) / sms;
     const double cost = static_cast<double>(waves * (span + 2)) + 0.04 * static_cast<double>(total);
     if (best_cost < 0.0 || cost <= best_cost) {
       best_cost = cost;
@@ -622,21 +622,21 @@ static size_t part_bytes(const TcPlan& T, int d) {
          align_up(sizeof(float2) * static_cast<size_t>(T.part_units) * 128, 256);
 }
 
-int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d) {
+int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms) {
   int count = 0;
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
-    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d);
+    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d, sms);
     count += 1 + (T.part_units > 0 ? 1 : 0);
   }
   return count;
 }
 
-size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int d, int) {
+size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms) {
   size_t need = kWsHeader;
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
-    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d);
+    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d, sms);
     need = std::max(need, kWsHeader + part_bytes(T, d));
   }
   return need;
@@ -646,14 +646,14 @@ size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int
 // of a paged prefix (null arrays: every item contiguous)
 template <int D>
 static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hkv, float scale,
-                             void* ws, size_t ws_bytes, cudaStream_t stream,
+                             void* ws, size_t ws_bytes, cudaStream_t stream, int sms,
                              const int32_t* const* tables = nullptr,
                              const int64_t* pool_rows = nullptr) {
   static_assert(sizeof(TcParams) < 32000, "kernel parameter block too large");
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
     const eagle_attn_item* its = items + b0;
-    const TcPlan T = plan_tc(its, nb, hq, hkv, D);
+    const TcPlan T = plan_tc(its, nb, hq, hkv, D, sms);
     if (ws_bytes < kWsHeader + part_bytes(T, D)) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
     TcParams P;
     memset(&P, 0, sizeof(P));
@@ -730,9 +730,9 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
 }
 
 eagle_status attn_tc_launch(const eagle_attn_item* items, int n, int hq, int hkv, int d,
-                            float scale, void* ws, size_t ws_bytes, cudaStream_t stream, int) {
-  if (d == 128) return launch_d<128>(items, n, hq, hkv, scale, ws, ws_bytes, stream);
-  if (d == 64) return launch_d<64>(items, n, hq, hkv, scale, ws, ws_bytes, stream);
+                            float scale, void* ws, size_t ws_bytes, cudaStream_t stream, int sms) {
+  if (d == 128) return launch_d<128>(items, n, hq, hkv, scale, ws, ws_bytes, stream, sms);
+  if (d == 64) return launch_d<64>(items, n, hq, hkv, scale, ws, ws_bytes, stream, sms);
   return EAGLE_ERR_UNSUPPORTED_SHAPE;
 }
 
@@ -786,7 +786,9 @@ extern "C" size_t eagle_tree_attn_paged_workspace_size(const eagle_attn_paged_it
   if (paged_items(items, n_items, n_q_heads, n_kv_heads, head_dim, flat.data(), tables.data(),
                   rows.data()) != EAGLE_OK)
     return 0;
-  return attn_tc_ws_size(flat.data(), n_items, n_q_heads, n_kv_heads, head_dim, kPlanSMs);
+  return std::max(attn_tc_ws_size(flat.data(), n_items, n_q_heads, n_kv_heads, head_dim, kPlanSMs),
+                  attn_tc_ws_size(flat.data(), n_items, n_q_heads, n_kv_heads, head_dim,
+                                  plan_sms()));
 }
 
 extern "C" eagle_status eagle_tree_attn_paged_batched(const eagle_attn_paged_item* items,
@@ -802,9 +804,10 @@ extern "C" eagle_status eagle_tree_attn_paged_batched(const eagle_attn_paged_ite
                                 tables.data(), rows.data());
   if (st != EAGLE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int sms = plan_sms();
   return head_dim == 128
              ? launch_d<128>(flat.data(), n_items, n_q_heads, n_kv_heads, scale, ws, ws_bytes, s,
-                             tables.data(), rows.data())
+                             sms, tables.data(), rows.data())
              : launch_d<64>(flat.data(), n_items, n_q_heads, n_kv_heads, scale, ws, ws_bytes, s,
-                            tables.data(), rows.data());
+                            sms, tables.data(), rows.data());
 }
