@@ -1,17 +1,19 @@
-// Tensor-core path of eagle_tree_attn for bf16 Q/K/V (head_dim 64 or 128).
+// Tensor-core path of eagle_tree_attn for bf16 Q/K/V: head_dim 128 runs the
+// 2-SM kernel (attn2_kernel, a cluster of two CTAs per work unit, tcgen05
+// .cta_group::2), head_dim 64 the 1-SM kernel below (attn_tc_kernel).
 //
 // Source: "EAGLE-2: Feature-Level Speculative Decoding Guide", "Single-Pass
 // Tree Verification" (one target pass over the tree; a token attends to its
 // ancestors and itself only) over the target's prefix KV cache.
 //
-// The m tree queries of one KV head times its g query heads form the M
-// dimension (row R = i*g + head-in-group), so the g heads that share a KV
-// head share every K/V byte.  One CTA = (item, kv head, pair of 128-row query
-// tiles, split): both tiles use every K/V chunk the CTA streams, so each K/V
-// byte crosses from L2 once per 256 rows.  Splits 0..n-2 each take a
-// contiguous span of prefix chunks (128 keys); the last split takes the tree
-// keys only (a CTA of its own, so the masked chunks with their two P fills
-// are off the prefix critical path).
+// Both kernels stack the m tree queries of one KV head times its g query
+// heads into the M dimension (row R = i*g + head-in-group), so the g heads
+// that share a KV head share every K/V byte, and every K/V chunk a work unit
+// streams serves two 128-row query tiles.
+//
+// 1-SM kernel (head_dim 64).  One CTA = (item, kv head, pair of 128-row
+// query tiles, split).  Splits 0..n-2 each take a contiguous span of prefix
+// chunks (128 keys); the last split takes the tree keys only.
 // Warp-specialised:
 //   warp 0      TMA producer: K and V chunks (K0 V0 K1 V1 ..., the order the
 //               MMAs consume them) into a 5-slot ring of 128-byte-swizzled
@@ -103,6 +105,7 @@ static_assert(TcSmem<128>::kAlloc <= 232448, "shared memory of the tensor-core k
 // after it must be executed by all 32 lanes).
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* err,
                                              volatile int* abort_flag, int where) {
+  if (mbar_try_wait(bar, parity)) return true;   // fast path: phase already complete
   bool ok = !*abort_flag && mbar_wait(bar, parity);
   if (!ok && !*abort_flag) {
     record_error(err, kDevTimeout, where);
@@ -471,6 +474,418 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ======================================================== 2-SM form (d 128)
+// One cluster of two CTAs = (item, kv head, pair of 128-row query tiles,
+// split); CTA r holds query tile 2 tp + r (128 rows) in its shared and tensor
+// memory.  The tensor cores of the pair work as one (tcgen05 .cta_group::2,
+// M = 256): for S = Q K^T each CTA holds 64 of a chunk's 128 keys (B split by
+// N), for O += P V each CTA holds 64 of the 128 value columns, so every CTA
+// loads half of each K / V chunk and every K / V byte still serves 256 rows.
+// Per CTA, tensor memory holds O (128 columns) and S / P triple-buffered
+// (3 x 128 columns): S of chunk j+3 is issued right after PV(j), so the
+// tensor core always has the next chunks' S queued and the softmax never
+// waits for it; each MMA instruction keeps the tensor core busy for 64
+// cycles per SM (N 128).
+// Warps per CTA: 0 TMA producer (its half of every chunk, completion on the
+// even CTA's barrier), 1 tensor-memory owner and, in the even CTA, the MMA
+// issuer; 4-7 and 8-11 softmax over keys 0-63 / 64-127 of each chunk, one
+// thread per query row, the two halves' row maxima exchanged through shared
+// memory at a named barrier.
+// A split covers a contiguous range of the item's chunk list (prefix chunks,
+// then the tree chunks), so the tree keys ride with the last split.
+constexpr int k2Threads = 384;
+constexpr int k2Slots = 10;                  // ring items (one CTA's half of a K or V chunk)
+constexpr int k2Bufs = 3;                    // S / P buffers
+constexpr uint32_t k2TmemCols = 512;         // O 128 + S 3 x 128
+
+struct Sm2 {
+  static constexpr int kQBytes = 128 * 128 * 2;   // one 128-row bf16 query tile (2 boxes)
+  static constexpr int kItem = 64 * 128 * 2;      // half of a K or V chunk: 16 KB
+  static constexpr int kQ = 0;
+  static constexpr int kRing = kQ + kQBytes;
+  static constexpr int kXch = kRing + k2Slots * kItem;   // [2][2][128] maxima, [2][128] sums
+  static constexpr int kBars = kXch + 4096;
+  static constexpr int kBytes = kBars + 512;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+static_assert(Sm2::kAlloc <= 232448, "shared memory of the 2-SM kernel");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
+    attn2_kernel(const __grid_constant__ TcParams P) {
+  constexpr int D = 128;
+  using L = Sm2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBars);   // [slot] (even CTA's)
+  uint64_t* empty = full + k2Slots;     // [slot] (each CTA: its producer may refill)
+  uint64_t* s_full = empty + k2Slots;   // [buffer] (each CTA)
+  uint64_t* o_done = s_full + k2Bufs;   // [buffer]: PV of a chunk of that buffer done
+  uint64_t* p_full = o_done + k2Bufs;   // [buffer] (even CTA's): 16 softmax warps
+  uint64_t* q_ready = p_full + k2Bufs;  // [1] (even CTA's): 8 warps wrote Q
+  uint64_t* drain = q_ready + 1;        // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xch = reinterpret_cast<float*>(smem + L::kXch);   // [parity][wg][row] maxima, at 512: [wg][row] sums
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = pair2::cta_rank();
+
+  // ---- work unit: (item, kv head, pair of query tiles, split)
+  const int unit = blockIdx.x >> 1;
+  int item = 0;
+  while (item + 1 < P.n_items && unit >= P.items[item + 1].unit_start) ++item;
+  const TcItem& it = P.items[item];
+  int u = unit - it.unit_start;
+  const int split = u % it.splits;
+  u /= it.splits;
+  const int tp = u % it.pairs;
+  const int kvh = u / it.pairs;
+  const int g = P.g;
+  const int M = it.m * g;
+  const int tile = 2 * tp + static_cast<int>(rank);
+  // chunk list of the item: nc prefix chunks, then the tree chunks; this
+  // split covers entries [v0, v1)
+  const int nc = (it.prefix_len + kChunk - 1) / kChunk;
+  const int nv = nc + (it.m + kChunk - 1) / kChunk;
+  const int v0 = split * P.span_chunks;
+  const int v1 = min(nv, v0 + P.span_chunks);
+  const int n_chunks = max(0, v1 - v0);
+
+  // ring item n: K (n even) or V (n odd) of chunk n >> 1, this CTA's half
+  auto issue_kv = [&](int n, uint32_t full_leader) {
+    const int slot = n % k2Slots;
+    const int j = n >> 1;
+    const bool is_v = n & 1;
+    uint8_t* dst = smem + L::kRing + slot * L::kItem;
+    const int v = v0 + j;
+    if (v < nc) {
+      int y = v * kChunk;
+      if (it.table) {   // paged prefix: a chunk is one page (a bad id reads page 0, reported)
+        int page = __ldg(it.table + v);
+        if (page < 0 || page >= it.pool_pages) {
+          record_error(P.err, kDevAssert, 60);
+          page = 0;
+        }
+        y = page * kChunk;
+      }
+      if (is_v) {
+        pair2::tma_load_3d(dst, &P.vmap[item], 64 * rank, y, kvh, full_leader);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          pair2::tma_load_3d(dst + h * 8192, &P.kmap[item], 64 * h, y + 64 * rank, kvh, full_leader);
+      }
+    } else {
+      const int z = (v - nc) * kChunk;
+      if (is_v) {
+        pair2::tma_load_3d(dst, &P.tvmap[item], 64 * rank, kvh, z, full_leader);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          pair2::tma_load_3d(dst + h * 8192, &P.tkmap[item], 64 * h, kvh, z + 64 * rank, full_leader);
+      }
+    }
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < k2Slots; ++s) {
+      mbar_init(&full[s], 1);   // the even CTA's producer arrives with both halves' bytes
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < k2Bufs; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&o_done[b], 1);
+      mbar_init(&p_full[b], 16);
+    }
+    mbar_init(q_ready, 8);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    pair2::tmem_alloc(tmem_slot, k2TmemCols);
+    pair2::tmem_relinquish();
+  }
+  tc_fence_before();
+  pair2::cluster_sync();   // both CTAs' barriers initialised, tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // tensor memory (each CTA): O in columns 0..127, S / P buffer b in 128 + 128 b ..
+
+  const int wg = warp >= 8 ? 1 : 0;          // softmax warpgroup: keys 64 wg .. of a chunk
+  const int row = (warp & 3) * 32 + lane;
+  const int R = 256 * tp + 128 * static_cast<int>(rank) + row;
+  const bool row_valid = tile < it.tiles && R < M;
+  if (warp >= 4 && warp < 8) {
+    // warpgroup 0 writes this CTA's Q tile (128-byte swizzle) while the
+    // producer streams K / V
+    const int qi = row_valid ? R / g : 0;
+    const int hl = row_valid ? R - qi * g : 0;
+    const int4* src = reinterpret_cast<const int4*>(it.q + (static_cast<int64_t>(qi) * P.hq + kvh * g + hl) * D);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      int4 qv[D / 16];
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c)
+        qv[c] = row_valid ? __ldg(src + half * (D / 16) + c) : make_int4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const int cg = half * (D / 16) + c;
+        const int box = cg >> 3, cc = cg & 7;
+        *reinterpret_cast<int4*>(smem + L::kQ + box * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = qv[c];
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) pair2::arrive_cluster(pair2::map_to(smem_addr(q_ready), 0));
+  }
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      const int n_items = 2 * n_chunks;
+      for (int n = 0; n < n_items; ++n) {
+        const int slot = n % k2Slots, use = n / k2Slots;
+        if (use > 0 && !bounded_wait(&empty[slot], (use - 1) & 1, P.err, abort_flag, 20)) break;
+        if (rank == 0) mbar_arrive_expect_tx(&full[slot], 2u * L::kItem);
+        issue_kv(n, pair2::map_to(smem_addr(&full[slot]), 0));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer (even CTA)
+    // prologue S(0), S(1), S(2); per chunk j: PV(j) into O, then S(j+3) into
+    // the buffer PV(j) has just read (the MMAs of one thread run in issue order)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(256, kChunk, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(256, D, true);
+      const uint32_t ring_base = smem_addr(smem + L::kRing);
+      const uint64_t qdesc0 = smem_desc_sw128(smem_addr(smem + L::kQ), 16, 1024);
+      const uint64_t kdesc0 = smem_desc_sw128(ring_base, 16, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(ring_base, 8192, 1024);
+      auto slot_of = [](int n) { return n % k2Slots; };
+      auto full_parity = [](int n) { return static_cast<uint32_t>((n / k2Slots) & 1); };
+      auto issue_s = [&](int j, int slot) {   // S(j) = Q K_j^T into buffer j % 3
+        const uint64_t kd = kdesc0 + static_cast<uint64_t>((slot * L::kItem) >> 4);
+        const uint32_t dst = tmem + 128 + 128 * (j % k2Bufs);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          pair2::mma_bf16(dst, qdesc0 + (((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4),
+                          kd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+      };
+      // O += P(j) V_j: keys 16kk.. in columns 8kk.. of the buffer (bf16
+      // pairs), the tree chunks' residual fill 64 columns further
+      auto issue_pv = [&](int j, int slot, int fill, bool acc) {
+        const uint32_t pa = tmem + 128 + 128 * (j % k2Bufs) + 64 * fill;
+        const uint64_t vd = vdesc0 + static_cast<uint64_t>((slot * L::kItem) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kChunk / 16; ++kk)
+          pair2::mma_bf16_ta(tmem, pa + 8 * kk, vd + ((kk * 2048) >> 4), idesc_o, (acc || kk > 0));
+      };
+      bool ok = n_chunks > 0 && bounded_wait(q_ready, 0, P.err, abort_flag, 29);
+      for (int j = 0; ok && j < k2Bufs && j < n_chunks; ++j) {   // S of the first three chunks
+        if (!bounded_wait(&full[slot_of(2 * j)], full_parity(2 * j), P.err, abort_flag, 30)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(j, slot_of(2 * j));
+        pair2::commit_both(&s_full[j]);
+        pair2::commit_both(&empty[slot_of(2 * j)]);
+      }
+      for (int j = 0; ok && j < n_chunks; ++j) {
+        const int b = j % k2Bufs;
+        const uint32_t ph = (j / k2Bufs) & 1;
+        const int nvi = 2 * j + 1, nki = 2 * (j + k2Bufs);
+        const int nf = v0 + j < nc ? 1 : 2;   // tree keys: P = hi + lo
+        if (!bounded_wait(&full[slot_of(nvi)], full_parity(nvi), P.err, abort_flag, 31) ||
+            !bounded_wait(&p_full[b], ph, P.err, abort_flag, 32))
+          break;
+        tc_fence_after();
+        for (int f = 0; f < nf; ++f) issue_pv(j, slot_of(nvi), f, j > 0 || f > 0);
+        pair2::commit_both(&o_done[b]);
+        pair2::commit_both(&empty[slot_of(nvi)]);
+        if (j + k2Bufs < n_chunks) {
+          if (!bounded_wait(&full[slot_of(nki)], full_parity(nki), P.err, abort_flag, 33)) break;
+          tc_fence_after();
+          issue_s(j + k2Bufs, slot_of(nki));
+          pair2::commit_both(&s_full[b]);
+          pair2::commit_both(&empty[slot_of(nki)]);
+        }
+      }
+      // every MMA of the pair has completed once `drain` flips
+      pair2::commit_local(drain);
+      mbar_wait(drain, 0, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ================================================================ softmax
+    // Every softmax thread runs all n_chunks iterations and meets its
+    // partner warpgroup at the named barrier in each; after a wait that ran
+    // out (`live` false) the iterations skip their work.
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t o_addr = tmem + lane_off + 64 * wg;   // this warpgroup's 64 O columns
+    const uint32_t s_addr = tmem + 128 + lane_off;       // S / P buffers of this row
+    const uint32_t p_full_leader = pair2::map_to(smem_addr(p_full), 0);
+    const float sl2 = P.scale_log2;
+    const uint64_t sl2x2 = f32x2(sl2, sl2);
+    const int W = (it.m + 63) >> 6;
+    const int64_t mrow = row_valid ? static_cast<int64_t>(R / g) * W : -1;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool live = n_chunks > 0;
+    for (int j = 0; j < n_chunks; ++j) {
+      const int b = j % k2Bufs;
+      const uint32_t sb = s_addr + 128 * b;
+      live = live && __all_sync(0xffffffffu, bounded_wait(&s_full[b], (j / k2Bufs) & 1, P.err, abort_flag, 40));
+      // keys 64 wg .. 64 wg + 63 of the chunk; only the prefix's last chunk
+      // and the tree chunks need a mask (key count, ancestor word)
+      const int v = v0 + j;
+      const bool pref = v < nc;
+      float x[64];
+      float mx = -INFINITY;
+      if (live) {
+        tc_fence_after();
+        const int k0 = (pref ? v : v - nc) * kChunk + 64 * wg;
+        const int nvalid = min(64, (pref ? it.prefix_len : it.m) - k0);
+        uint32_t ra[32], rb[32];
+        tmem_ld32(sb + 64 * wg, ra);
+        tmem_ld32(sb + 64 * wg + 32, rb);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(ra[c]);
+          x[32 + c] = __uint_as_float(rb[c]);
+        }
+        if (!pref || nvalid < 64) {
+          uint64_t wbits = ~0ull;
+          if (!pref) wbits = (mrow >= 0 && nvalid > 0) ? __ldg(it.mask + mrow + (k0 >> 6)) : 0ull;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (!((c < nvalid) & static_cast<bool>((wbits >> c) & 1ull))) x[c] = -INFINITY;
+        }
+        float m8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) m8[a] = fmax3(x[a], x[a + 8], x[a + 16]);
+#pragma unroll
+        for (int a = 0; a < 8; ++a) m8[a] = fmax3(m8[a], x[a + 24], x[a + 32]);
+#pragma unroll
+        for (int a = 0; a < 8; ++a) m8[a] = fmax3(m8[a], x[a + 40], x[a + 48]);
+#pragma unroll
+        for (int a = 0; a < 8; ++a) m8[a] = fmaxf(m8[a], x[a + 56]);
+        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+      }
+      // the other warpgroup's maximum of this row (both have their S values
+      // in registers by now, so P may overwrite any of the buffer after this)
+      xch[((j & 1) * 2 + wg) * 128 + row] = mx;
+      named_sync(1, 256);
+      if (!live) continue;
+      mx = sl2 * fmaxf(mx, xch[((j & 1) * 2 + (1 - wg)) * 128 + row]);   // scale > 0
+      const float m_new = fmaxf(m_run, mx);
+      const bool grow = (j == 0) || (m_new > m_run + 8.0f);
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O is rescaled once the previous PV has landed.  S(j) was issued
+        // after PV(j-3), so PV(j-3) is done here while PV(j-2), PV(j-1) may
+        // not be: one barrier per buffer keeps this wait within one phase.
+        live = __all_sync(0xffffffffu, bounded_wait(&o_done[(j - 1) % k2Bufs], ((j - 1) / k2Bufs) & 1,
+                                                    P.err, abort_flag, 41));
+        if (!live) continue;
+        tc_fence_after();
+        const float f = grow ? ex2(m_run - m_new) : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[16];
+          tmem_ld16(o_addr + 16 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+          tmem_st16(o_addr + 16 * c, r);
+        }
+        if (grow) l_run *= f;
+      }
+      if (grow) m_run = m_new;
+      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+      const uint64_t nm2 = f32x2(-mref, -mref);
+      // P = 2^(s sl2 - m) as bf16 pairs: keys 2c, 2c+1 of the chunk -> column
+      // c (this warpgroup: columns 32 wg ..); tree chunks put the rounding
+      // residual 64 columns further
+      uint32_t hi[32];
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float a0, a1;
+        f32x2_split(fma_x2(f32x2(x[2 * c], x[2 * c + 1]), sl2x2, nm2), a0, a1);
+        const float p0 = ex2(a0), p1 = ex2(a1);
+        const uint64_t pp = f32x2(p0, p1);
+        ls2[c & 3] = c < 4 ? pp : add_x2(ls2[c & 3], pp);
+        hi[c] = pack_bf16x2(p0, p1);
+        if (!pref) {
+          x[2 * c] = p0 - __uint_as_float(hi[c] << 16);
+          x[2 * c + 1] = p1 - __uint_as_float(hi[c] & 0xffff0000u);
+        }
+      }
+      tmem_st32(sb + 32 * wg, hi);
+      if (!pref) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) hi[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
+        tmem_st32(sb + 64 + 32 * wg, hi);
+      }
+      float s0, s1, s2, s3;
+      f32x2_split(add_x2(add_x2(ls2[0], ls2[1]), add_x2(ls2[2], ls2[3])), s0, s1);
+      l_run += s0 + s1;
+      (void)s2;
+      (void)s3;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) pair2::arrive_cluster(p_full_leader + 8 * b);
+    }
+    // ---- epilogue: row sum of both warpgroups, then this warpgroup's 64
+    // columns of O, normalised (one split) or as a partial
+    bool ok = live && __all_sync(0xffffffffu, bounded_wait(&o_done[(n_chunks - 1) % k2Bufs],
+                                                           ((n_chunks - 1) / k2Bufs) & 1, P.err,
+                                                           abort_flag, 42));
+    xch[512 + wg * 128 + row] = l_run;
+    named_sync(1, 256);
+    tc_fence_after();
+    if (ok) {
+      const float l_tot = l_run + xch[512 + (1 - wg) * 128 + row];
+      const int qi = row_valid ? R / g : 0, hl = row_valid ? R - qi * g : 0;
+      const int64_t orow = static_cast<int64_t>(qi) * P.hq + kvh * g + hl;
+      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+      const int64_t punit =
+          it.part_start + static_cast<int64_t>(kvh * it.tiles + tile) * it.splits + split;
+      float* po = P.part_o + (punit * D + 64 * wg) * 128 + row;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(o_addr + 32 * c, r);
+        tmem_wait_ld();
+        if (!row_valid) continue;
+        if (it.splits == 1) {
+          float4* dst = reinterpret_cast<float4*>(it.out + orow * D + 64 * wg + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                                 __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) po[(32 * c + e) * 128] = __uint_as_float(r[e]);
+        }
+      }
+      if (row_valid && it.splits > 1 && wg == 0) P.part_ml[punit * 128 + row] = make_float2(m_run, l_tot);
+    }
+  }
+
+  // ---- teardown: no MMA of the pair is in flight (the even CTA waited for
+  // its drain before reaching the barrier); tensor memory is freed by the
+  // warps that allocated it, in both CTAs together
+  tc_fence_before();
+  pair2::cluster_sync();
+  tc_fence_after();
+  if (warp == 1) pair2::tmem_dealloc(tmem, k2TmemCols);
+}
+
 // Split merge: one block per (kv head, 128-row tile, 32 rows, 32 columns);
 // lanes are rows, so every partial load is a coalesced 128-byte line; warp w
 // combines columns 4w..4w+3 online over the splits (running max in log2
@@ -577,28 +992,39 @@ struct TcPlan {
   int64_t part_units;   // 128-row partial blocks
 };
 
-// Splits per (kv head, pair of query tiles): ceil(prefix chunks / span)
-// prefix splits plus one tree split.  The span (in 128-key chunks) minimises
-// waves x (span + 2) -- the +2 for a CTA's fixed work (Q tiles, epilogue) --
-// plus a small charge per CTA for its partials' write and read.
+// Work units per (item, kv head, pair of query tiles).
+// head_dim 128 (the 2-SM kernel, a cluster of two CTAs per unit): a split
+// covers `span` entries of the item's chunk list (its prefix chunks, then its
+// tree chunks).  head_dim 64 (one CTA per unit): prefix splits of `span`
+// chunks plus one tree split.  The span minimises waves x (span + fixed work
+// of a unit, in chunks) plus a small charge per unit for its partials' write
+// and read.
 static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms) {
   TcPlan T;
   memset(&T, 0, sizeof(T));
+  const bool two = d == 128;
   const int g = hq / hkv;
-  int max_nc = 1;
+  int max_span = 1;
   for (int b = 0; b < n; ++b) {
     T.tiles[b] = (items[b].m * g + 127) / 128;
-    max_nc = std::max(max_nc, (items[b].prefix_len + kChunk - 1) / kChunk);
+    const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
+    const int nv = nc + (items[b].m + kChunk - 1) / kChunk;
+    max_span = std::max(max_span, two ? nv : nc);
   }
+  auto splits_of = [&](int b, int span) {
+    const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
+    if (two) return (nc + (items[b].m + kChunk - 1) / kChunk + span - 1) / span;
+    return (nc + span - 1) / span + 1;
+  };
   double best_cost = -1.0;
-  for (int span = 1; span <= max_nc; ++span) {
+  for (int span = 1; span <= max_span; ++span) {
     int64_t total = 0;
-    for (int b = 0; b < n; ++b) {
-      const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
-      total += static_cast<int64_t>(hkv) * ((T.tiles[b] + 1) / 2) * ((nc + span - 1) / span + 1);
-    }
-    const int64_t waves = (total + sms - 1) / sms;
-    const double cost = static_cast<double>(waves * (span + 2)) + 0.04 * static_cast<double>(total);
+    for (int b = 0; b < n; ++b)
+      total += static_cast<int64_t>(hkv) * ((T.tiles[b] + 1) / 2) * splits_of(b, span);
+    const int64_t slots = two ? 2 * total : total;
+    const int64_t waves = (slots + sms - 1) / sms;
+    const double cost = two ? static_cast<double>(waves * (span + 6)) + 0.02 * static_cast<double>(total)
+                            : static_cast<double>(waves * (span + 2)) + 0.04 * static_cast<double>(total);
     if (best_cost < 0.0 || cost <= best_cost) {
       best_cost = cost;
       T.span = span;
@@ -606,14 +1032,12 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
   }
   int64_t units = 0, part = 0;
   for (int b = 0; b < n; ++b) {
-    const int nc = (items[b].prefix_len + kChunk - 1) / kChunk;
-    T.splits[b] = (nc + T.span - 1) / T.span + 1;
+    T.splits[b] = splits_of(b, T.span);
     units += static_cast<int64_t>(hkv) * ((T.tiles[b] + 1) / 2) * T.splits[b];
     if (T.splits[b] > 1) part += static_cast<int64_t>(hkv) * T.tiles[b] * T.splits[b];
   }
   T.units = static_cast<int>(units);
   T.part_units = part;
-  (void)d;
   return T;
 }
 
@@ -667,10 +1091,14 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       const void* kbase = x.prefix_len ? x.k_cache : x.tree_k;
       const void* vbase = x.prefix_len ? x.v_cache : x.tree_v;
       const uint64_t hs = static_cast<uint64_t>(x.cache_head_stride) * 2;
-      if (!encode_3d(&P.kmap[b], kbase, D, S, hkv, D * 2, x.prefix_len ? hs : D * 2, kChunk, 1) ||
+      // boxes: the 2-SM kernel loads half a chunk per CTA (64 keys of K, 64
+      // value columns of V), the 1-SM kernel a whole chunk (128 keys)
+      const uint32_t kbox = D == 128 ? 64 : kChunk;
+      const uint64_t ts = static_cast<uint64_t>(hkv) * D * 2;
+      if (!encode_3d(&P.kmap[b], kbase, D, S, hkv, D * 2, x.prefix_len ? hs : D * 2, kbox, 1) ||
           !encode_3d(&P.vmap[b], vbase, D, S, hkv, D * 2, x.prefix_len ? hs : D * 2, kChunk, 1) ||
-          !encode_3d(&P.tkmap[b], x.tree_k, D, hkv, x.m, D * 2, static_cast<uint64_t>(hkv) * D * 2, 1, kChunk) ||
-          !encode_3d(&P.tvmap[b], x.tree_v, D, hkv, x.m, D * 2, static_cast<uint64_t>(hkv) * D * 2, 1, kChunk))
+          !encode_3d(&P.tkmap[b], x.tree_k, D, hkv, x.m, D * 2, ts, 1, kbox) ||
+          !encode_3d(&P.tvmap[b], x.tree_v, D, hkv, x.m, D * 2, ts, 1, kChunk))
         return EAGLE_ERR_CUDA;
       TcItem& ti = P.items[b];
       ti.q = static_cast<const __nv_bfloat16*>(x.q);
@@ -700,10 +1128,17 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     P.part_o = reinterpret_cast<float*>(pbase);
     P.part_ml = reinterpret_cast<float2*>(
         pbase + align_up(sizeof(float) * static_cast<size_t>(T.part_units) * 128 * D, 256));
-    const size_t smem = TcSmem<D>::kAlloc;
-    EAGLE_CUDA(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem)));
-    attn_tc_kernel<D><<<static_cast<unsigned>(units), kTcThreads, smem, stream>>>(P);
+    if constexpr (D == 128) {   // 2-SM kernel: a cluster of two CTAs per unit
+      const size_t smem = Sm2::kAlloc;
+      EAGLE_CUDA(cudaFuncSetAttribute(attn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+      attn2_kernel<<<static_cast<unsigned>(2 * units), k2Threads, smem, stream>>>(P);
+    } else {
+      const size_t smem = TcSmem<D>::kAlloc;
+      EAGLE_CUDA(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+      attn_tc_kernel<D><<<static_cast<unsigned>(units), kTcThreads, smem, stream>>>(P);
+    }
     eagle_status st = launch_status();
     if (st != EAGLE_OK) return st;
     if (part > 0) {

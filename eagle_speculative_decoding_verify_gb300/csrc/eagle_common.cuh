@@ -90,6 +90,7 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+
 // 1-D bulk copy global -> this CTA's shared memory; completes `bytes` of
 // transaction count on `bar`.  dst, src 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
@@ -193,6 +194,42 @@ __device__ __forceinline__ void warp_best(float& v, int& i) {
     v = t ? ov : v;
     i = t ? oi : i;
   }
+}
+
+}  // namespace eagle
+
+namespace eagle {
+
+// ------------------------------------------------ packed fp32 pairs, 3-way max
+// Two fp32 lanes in one 64-bit register (fma / add on both at once, one
+// instruction each), and the three-input maximum.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32) of this CTA.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace eagle
