@@ -482,15 +482,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 // N), for O += P V each CTA holds 64 of the 128 value columns, so every CTA
 // loads half of each K / V chunk and every K / V byte still serves 256 rows.
 // Per CTA, tensor memory holds O (128 columns) and S / P triple-buffered
-// (3 x 128 columns): S of chunk j+3 is issued right after PV(j), so the
-// tensor core always has the next chunks' S queued and the softmax never
-// waits for it; each MMA instruction keeps the tensor core busy for 64
-// cycles per SM (N 128).
+// (3 x 128 columns): S of chunk j+3 is issued as soon as PV(j) is done, so
+// the tensor core has the next chunks' S queued and the softmax does not
+// wait for it; each MMA instruction keeps the tensor core busy for 64 cycles
+// per SM (N 128).
 // Warps per CTA: 0 TMA producer (its half of every chunk, completion on the
-// even CTA's barrier), 1 tensor-memory owner and, in the even CTA, the MMA
-// issuer; 4-7 and 8-11 softmax over keys 0-63 / 64-127 of each chunk, one
-// thread per query row, the two halves' row maxima exchanged through shared
-// memory at a named barrier.
+// even CTA's barrier), 1 tensor-memory owner and, in the even CTA, the PV
+// issuer, 2 (even CTA) the S issuer; 4-7 and 8-11 softmax over keys 0-63 /
+// 64-127 of each chunk, one thread per query row, the two halves' row maxima
+// exchanged through shared memory at a named barrier.
 // A split covers a contiguous range of the item's chunk list (prefix chunks,
 // then the tree chunks), so the tree keys ride with the last split.
 constexpr int k2Threads = 384;
@@ -523,8 +523,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
   uint64_t* o_done = s_full + k2Bufs;   // [buffer]: PV of a chunk of that buffer done
   uint64_t* p_full = o_done + k2Bufs;   // [buffer] (even CTA's): 16 softmax warps
   uint64_t* q_ready = p_full + k2Bufs;  // [1] (even CTA's): 8 warps wrote Q
-  uint64_t* drain = q_ready + 1;        // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = q_ready + 1;        // [2]: each issuer's MMAs all done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xch = reinterpret_cast<float*>(smem + L::kXch);   // [parity][wg][row] maxima, at 512: [wg][row] sums
 
@@ -599,7 +599,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
       mbar_init(&p_full[b], 16);
     }
     mbar_init(q_ready, 8);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -653,70 +654,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer (even CTA)
-    // prologue S(0), S(1), S(2); per chunk j: PV(j) into O, then S(j+3) into
-    // the buffer PV(j) has just read (the MMAs of one thread run in issue order)
-    if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(256, kChunk, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(256, D, true);
+  } else if ((warp == 1 || warp == 2) && rank == 0) {
+    // ================================================================ MMA issuers (even CTA)
+    // Two threads issue, so that one MMA stream's instruction issue never
+    // waits behind the other's: warp 2 issues S(j) = Q K_j^T into buffer
+    // j % 3 once PV(j-3), the last reader of that buffer, has completed;
+    // warp 1 issues O += P(j) V_j once the softmax has written P(j).
+    if (lane == 0) {
       const uint32_t ring_base = smem_addr(smem + L::kRing);
-      const uint64_t qdesc0 = smem_desc_sw128(smem_addr(smem + L::kQ), 16, 1024);
-      const uint64_t kdesc0 = smem_desc_sw128(ring_base, 16, 1024);
-      const uint64_t vdesc0 = smem_desc_sw128(ring_base, 8192, 1024);
       auto slot_of = [](int n) { return n % k2Slots; };
       auto full_parity = [](int n) { return static_cast<uint32_t>((n / k2Slots) & 1); };
-      auto issue_s = [&](int j, int slot) {   // S(j) = Q K_j^T into buffer j % 3
-        const uint64_t kd = kdesc0 + static_cast<uint64_t>((slot * L::kItem) >> 4);
-        const uint32_t dst = tmem + 128 + 128 * (j % k2Bufs);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          pair2::mma_bf16(dst, qdesc0 + (((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4),
-                          kd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-      };
-      // O += P(j) V_j: keys 16kk.. in columns 8kk.. of the buffer (bf16
-      // pairs), the tree chunks' residual fill 64 columns further
-      auto issue_pv = [&](int j, int slot, int fill, bool acc) {
-        const uint32_t pa = tmem + 128 + 128 * (j % k2Bufs) + 64 * fill;
-        const uint64_t vd = vdesc0 + static_cast<uint64_t>((slot * L::kItem) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk)
-          pair2::mma_bf16_ta(tmem, pa + 8 * kk, vd + ((kk * 2048) >> 4), idesc_o, (acc || kk > 0));
-      };
-      bool ok = n_chunks > 0 && bounded_wait(q_ready, 0, P.err, abort_flag, 29);
-      for (int j = 0; ok && j < k2Bufs && j < n_chunks; ++j) {   // S of the first three chunks
-        if (!bounded_wait(&full[slot_of(2 * j)], full_parity(2 * j), P.err, abort_flag, 30)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_s(j, slot_of(2 * j));
-        pair2::commit_both(&s_full[j]);
-        pair2::commit_both(&empty[slot_of(2 * j)]);
-      }
-      for (int j = 0; ok && j < n_chunks; ++j) {
-        const int b = j % k2Bufs;
-        const uint32_t ph = (j / k2Bufs) & 1;
-        const int nvi = 2 * j + 1, nki = 2 * (j + k2Bufs);
-        const int nf = v0 + j < nc ? 1 : 2;   // tree keys: P = hi + lo
-        if (!bounded_wait(&full[slot_of(nvi)], full_parity(nvi), P.err, abort_flag, 31) ||
-            !bounded_wait(&p_full[b], ph, P.err, abort_flag, 32))
-          break;
-        tc_fence_after();
-        for (int f = 0; f < nf; ++f) issue_pv(j, slot_of(nvi), f, j > 0 || f > 0);
-        pair2::commit_both(&o_done[b]);
-        pair2::commit_both(&empty[slot_of(nvi)]);
-        if (j + k2Bufs < n_chunks) {
-          if (!bounded_wait(&full[slot_of(nki)], full_parity(nki), P.err, abort_flag, 33)) break;
+      if (warp == 2) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(256, kChunk, false);
+        const uint64_t qdesc0 = smem_desc_sw128(smem_addr(smem + L::kQ), 16, 1024);
+        const uint64_t kdesc0 = smem_desc_sw128(ring_base, 16, 1024);
+        bool ok = n_chunks > 0 && bounded_wait(q_ready, 0, P.err, abort_flag, 29);
+        for (int j = 0; ok && j < n_chunks; ++j) {
+          const int b = j % k2Bufs, nki = 2 * j;
+          if ((j >= k2Bufs &&
+               !bounded_wait(&o_done[b], ((j - k2Bufs) / k2Bufs) & 1, P.err, abort_flag, 34)) ||
+              !bounded_wait(&full[slot_of(nki)], full_parity(nki), P.err, abort_flag, 33))
+            break;
           tc_fence_after();
-          issue_s(j + k2Bufs, slot_of(nki));
+          const uint64_t kd = kdesc0 + static_cast<uint64_t>((slot_of(nki) * L::kItem) >> 4);
+          const uint32_t dst = tmem + 128 + 128 * b;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            pair2::mma_bf16(dst, qdesc0 + (((kk >> 2) * (128 * 128) + (kk & 3) * 32) >> 4),
+                            kd + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
           pair2::commit_both(&s_full[b]);
           pair2::commit_both(&empty[slot_of(nki)]);
         }
+        pair2::commit_local(&drain[1]);
+        mbar_wait(&drain[1], 0, 200000000ull);
+      } else {
+        constexpr uint32_t idesc_o = idesc_bf16_f32(256, D, true);
+        const uint64_t vdesc0 = smem_desc_sw128(ring_base, 8192, 1024);
+        for (int j = 0; j < n_chunks; ++j) {
+          const int b = j % k2Bufs, nvi = 2 * j + 1;
+          const int nf = v0 + j < nc ? 1 : 2;   // tree keys: P = hi + lo
+          if (!bounded_wait(&full[slot_of(nvi)], full_parity(nvi), P.err, abort_flag, 31) ||
+              !bounded_wait(&p_full[b], (j / k2Bufs) & 1, P.err, abort_flag, 32))
+            break;
+          tc_fence_after();
+          // keys 16kk.. of the chunk in columns 8kk.. of the buffer (bf16
+          // pairs), the tree chunks' residual fill 64 columns further
+          const uint64_t vd = vdesc0 + static_cast<uint64_t>((slot_of(nvi) * L::kItem) >> 4);
+          for (int f = 0; f < nf; ++f) {
+            const uint32_t pa = tmem + 128 + 128 * b + 64 * f;
+#pragma unroll
+            for (int kk = 0; kk < kChunk / 16; ++kk)
+              pair2::mma_bf16_ta(tmem, pa + 8 * kk, vd + ((kk * 2048) >> 4), idesc_o,
+                                 (j > 0 || f > 0 || kk > 0));
+          }
+          pair2::commit_both(&o_done[b]);
+          pair2::commit_both(&empty[slot_of(nvi)]);
+        }
+        pair2::commit_local(&drain[0]);
+        mbar_wait(&drain[0], 0, 200000000ull);
       }
-      // every MMA of the pair has completed once `drain` flips
-      pair2::commit_local(drain);
-      mbar_wait(drain, 0, 200000000ull);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -785,8 +781,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
       const bool grow = (j == 0) || (m_new > m_run + 8.0f);
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O is rescaled once the previous PV has landed.  S(j) was issued
-        // after PV(j-3), so PV(j-3) is done here while PV(j-2), PV(j-1) may
-        // not be: one barrier per buffer keeps this wait within one phase.
+        // after PV(j-3) completed, so PV(j-3) is done here while PV(j-2),
+        // PV(j-1) may not be: one barrier per buffer keeps this wait within
+        // one phase.
         live = __all_sync(0xffffffffu, bounded_wait(&o_done[(j - 1) % k2Bufs], ((j - 1) / k2Bufs) & 1,
                                                     P.err, abort_flag, 41));
         if (!live) continue;
