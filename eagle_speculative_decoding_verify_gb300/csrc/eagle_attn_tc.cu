@@ -59,7 +59,7 @@
 
 namespace eagle {
 
-constexpr int kTcMaxItems = 16;     // items per launch (tensor maps live in the params)
+constexpr int kTcMaxItems = 32;     // items per launch (tensor maps live in the params)
 constexpr int kTcThreads = 384;     // 12 warps
 constexpr int kChunk = 128;         // keys per K/V chunk
 constexpr int kSlots = 5;           // K/V ring depth
@@ -71,6 +71,7 @@ struct TcItem {
   const uint64_t* mask;
   int m, prefix_len, splits, tiles, pairs, unit_start;
   int64_t part_start;   // first partial unit of the item (units of 128 rows)
+  int cnt_start;        // first split-arrival counter of the item (2-SM kernel)
   const int32_t* table; // paged prefix: pool page of every 128-token page (null: contiguous)
   int pool_pages;       // pages in the pool (the table's entries must lie below)
 };
@@ -85,6 +86,8 @@ struct TcParams {
   float scale_log2;
   float* part_o;     // [unit][D][128 rows]
   float2* part_ml;   // [unit][128 rows] (max in log2 units, sum)
+  int32_t* counters; // [item][kv head][tile] splits arrived (2-SM kernel; left at zero)
+  int fuse_merge;    // 2-SM kernel: the last split of a tile merges (else a merge kernel runs)
   int32_t* err;
 };
 
@@ -872,6 +875,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
       }
       if (row_valid && it.splits > 1 && wg == 0) P.part_ml[punit * 128 + row] = make_float2(m_run, l_tot);
     }
+    // ---- split merge (few splits): the CTA whose partial of this (kv head,
+    // tile) lands last combines every split's (o, max, sum) for its 128 rows
+    // and writes the output; it leaves the arrival counter at zero for the
+    // next call.  With many splits, attn_tc_merge_kernel runs instead (one
+    // CTA reading many partials back is slower than a grid-wide pass).
+    if (P.fuse_merge && it.splits > 1 && tile < it.tiles) {
+      int* cnt = P.counters + it.cnt_start + kvh * it.tiles + tile;
+      volatile int* last = reinterpret_cast<volatile int*>(xch + 1000);
+      __threadfence();
+      named_sync(1, 256);
+      if (tid == 128) *last = atomicAdd(cnt, 1) == it.splits - 1;
+      named_sync(1, 256);
+      if (*last) {
+        __threadfence();
+        const int64_t pu0 = it.part_start + static_cast<int64_t>(kvh * it.tiles + tile) * it.splits;
+        if (row_valid) {
+          float mt = -INFINITY;
+          for (int sp = 0; sp < it.splits; ++sp) mt = fmaxf(mt, __ldcg(P.part_ml + (pu0 + sp) * 128 + row).x);
+          float acc[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+          float lt = 0.f;
+#pragma unroll 1
+          for (int sp = 0; sp < it.splits; ++sp) {
+            const float2 ml = __ldcg(P.part_ml + (pu0 + sp) * 128 + row);
+            const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - mt);
+            lt = fmaf(w, ml.y, lt);
+            const float* po = P.part_o + ((pu0 + sp) * D + 64 * wg) * 128 + row;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) acc[c] = fmaf(w, __ldcg(po + c * 128), acc[c]);
+          }
+          const float inv = lt > 0.f ? 1.f / lt : 0.f;
+          const int qi = R / g, hl = R - qi * g;
+          float4* dst = reinterpret_cast<float4*>(it.out + (static_cast<int64_t>(qi) * P.hq + kvh * g + hl) * D + 64 * wg);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            dst[e] = make_float4(acc[4 * e] * inv, acc[4 * e + 1] * inv, acc[4 * e + 2] * inv, acc[4 * e + 3] * inv);
+        }
+        if (tid == 128) *cnt = 0;
+      }
+    }
   }
 
   // ---- teardown: no MMA of the pair is in flight (the even CTA waited for
@@ -985,9 +1029,14 @@ struct TcPlan {
   int span;
   int splits[kTcMaxItems];
   int tiles[kTcMaxItems];
-  int units;            // CTAs
+  int units;            // CTAs (1-SM kernel) or CTA pairs (2-SM kernel)
   int64_t part_units;   // 128-row partial blocks
+  int64_t counters;     // split-arrival counters (2-SM kernel)
+  int max_splits;
 };
+
+// the 2-SM kernel merges splits in the kernel up to this many per tile
+constexpr int kFusedMergeMaxSplits = 4;
 
 // Work units per (item, kv head, pair of query tiles).
 // head_dim 128 (the 2-SM kernel, a cluster of two CTAs per unit): a split
@@ -1032,6 +1081,8 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
     T.splits[b] = splits_of(b, T.span);
     units += static_cast<int64_t>(hkv) * ((T.tiles[b] + 1) / 2) * T.splits[b];
     if (T.splits[b] > 1) part += static_cast<int64_t>(hkv) * T.tiles[b] * T.splits[b];
+    if (two && T.splits[b] > 1) T.counters += static_cast<int64_t>(hkv) * T.tiles[b];
+    T.max_splits = std::max(T.max_splits, T.splits[b]);
   }
   T.units = static_cast<int>(units);
   T.part_units = part;
@@ -1040,7 +1091,8 @@ static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int 
 
 static size_t part_bytes(const TcPlan& T, int d) {
   return align_up(sizeof(float) * static_cast<size_t>(T.part_units) * 128 * d, 256) +
-         align_up(sizeof(float2) * static_cast<size_t>(T.part_units) * 128, 256);
+         align_up(sizeof(float2) * static_cast<size_t>(T.part_units) * 128, 256) +
+         align_up(sizeof(int32_t) * static_cast<size_t>(T.counters), 256);
 }
 
 int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms) {
@@ -1048,7 +1100,7 @@ int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, i
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
     const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d, sms);
-    count += 1 + (T.part_units > 0 ? 1 : 0);
+    count += 1 + (T.part_units > 0 && (d != 128 || T.max_splits > kFusedMergeMaxSplits) ? 1 : 0);
   }
   return count;
 }
@@ -1078,7 +1130,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     if (ws_bytes < kWsHeader + part_bytes(T, D)) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
     TcParams P;
     memset(&P, 0, sizeof(P));
-    int64_t units = 0, part = 0;
+    int64_t units = 0, part = 0, cnt = 0;
     for (int b = 0; b < nb; ++b) {
       const eagle_attn_item& x = its[b];
       // rows the prefix maps cover: the prefix, or the whole pool of a paged item
@@ -1110,6 +1162,8 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       ti.pairs = (T.tiles[b] + 1) / 2;
       ti.unit_start = static_cast<int>(units);
       ti.part_start = part;
+      ti.cnt_start = static_cast<int>(cnt);
+      if (D == 128 && T.splits[b] > 1) cnt += static_cast<int64_t>(hkv) * T.tiles[b];
       units += static_cast<int64_t>(hkv) * ti.pairs * T.splits[b];
       if (T.splits[b] > 1) part += static_cast<int64_t>(hkv) * T.tiles[b] * T.splits[b];
     }
@@ -1125,6 +1179,10 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     P.part_o = reinterpret_cast<float*>(pbase);
     P.part_ml = reinterpret_cast<float2*>(
         pbase + align_up(sizeof(float) * static_cast<size_t>(T.part_units) * 128 * D, 256));
+    P.fuse_merge = D == 128 && T.max_splits <= kFusedMergeMaxSplits;
+    P.counters = reinterpret_cast<int32_t*>(
+        pbase + align_up(sizeof(float) * static_cast<size_t>(T.part_units) * 128 * D, 256) +
+        align_up(sizeof(float2) * static_cast<size_t>(T.part_units) * 128, 256));
     if constexpr (D == 128) {   // 2-SM kernel: a cluster of two CTAs per unit
       const size_t smem = Sm2::kAlloc;
       EAGLE_CUDA(cudaFuncSetAttribute(attn2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1138,7 +1196,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
     }
     eagle_status st = launch_status();
     if (st != EAGLE_OK) return st;
-    if (part > 0) {
+    if (part > 0 && !P.fuse_merge) {
       TcMergeParams MP;
       memset(&MP, 0, sizeof(MP));
       int blocks = 0;
