@@ -237,6 +237,150 @@ class Step:
                     for n in ("q", "tree_k", "tree_v")))
 
 
+class MultiStep:
+    """One verify step of any workload through the batched entry points: the
+    items' trees in one build launch, every attention problem (a layer of the
+    long-context workload, or a sequence of the ragged batch) in one batched
+    attention call, every item's walk in one verify launch."""
+
+    def __init__(self, w, dev, eb, wl):
+        import torch
+        self.torch, self.eb, self.w = torch, eb, w
+        n, m = w.items, w.total_tokens
+        self.draft = [wl.draft_logits(w, b).to(dev) for b in range(n)]
+        self.roots = [wl.root_token(w, b) for b in range(n)]
+        self.trees = [eb.Tree(m, dev) for _ in range(n)]
+        self.ws_build = eb.workspace(eb.eagle_tree_build_workspace_size(
+            n, w.n_rows, w.vocab, w.top_k, w.depth, m), dev)
+        self.build(torch.cuda.current_stream())          # untimed: the target logits need the trees
+        torch.cuda.synchronize()
+        self.target = [wl.target_logits(w, t.parents.cpu().tolist(), t.tokens.cpu().tolist(),
+                                        b).to(dev) for b, t in enumerate(self.trees)]
+        self.prefix = wl.prefix_lengths(w)
+        self.dtype = eb.EAGLE_BF16 if w.dtype == "bf16" else eb.EAGLE_F32
+        self.attn, self.outs, self.items = [], [], []
+        problems = ([(0, l) for l in range(w.layers)] if w.layers > 1 else
+                    [(b, 0) for b in range(n)])
+        for b, l in problems:
+            a = wl.attention_inputs(w, item=b, layer=l, device=dev, prefix=self.prefix[b])
+            o = torch.empty(m, w.n_q_heads, w.head_dim, device=dev)
+            self.attn.append(a)
+            self.outs.append(o)
+            self.items.append(eb.attn_item(a["q"], a["k_cache"], a["v_cache"], a["tree_k"],
+                                           a["tree_v"], self.trees[b].mask, o))
+        self.ws_attn = eb.workspace(eb.eagle_tree_attn_batched_workspace_size(
+            self.items, w.n_q_heads, w.n_kv_heads, w.head_dim, self.dtype), dev)
+        self.attn_launches = eb.eagle_tree_attn_num_launches(
+            self.items, w.n_q_heads, w.n_kv_heads, w.head_dim, self.dtype)
+        self.params = [eb.sampling(*w.sampling_of(b)) for b in range(n)]
+        self.seeds = [1234 + b for b in range(n)]
+        self.ws_verify = eb.workspace(eb.eagle_tree_verify_workspace_size(n, m, w.vocab), dev)
+        self.acc = [torch.zeros(m, dtype=torch.int32, device=dev) for _ in range(n)]
+        self.n_acc = torch.zeros(n, dtype=torch.int32, device=dev)
+        self.bonus = torch.zeros(n, dtype=torch.int32, device=dev)
+        self.launches = 1 + self.attn_launches + 1
+
+    def build(self, s):
+        w = self.w
+        self.eb.eagle_tree_build_batched(self.draft, w.top_k, w.depth, w.total_tokens, self.roots,
+                                         outs=self.trees, ws=self.ws_build, stream=s)
+
+    def attention(self, s):
+        w = self.w
+        self.eb.eagle_tree_attn_batched(self.items, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                        self.dtype, ws=self.ws_attn, stream=s)
+
+    def verify(self, s, step=0):
+        self.eb.eagle_tree_verify_batched(self.target, self.trees, self.params, self.seeds, step,
+                                          accepted=self.acc, n_accepted=self.n_acc,
+                                          bonus_tokens=self.bonus, ws=self.ws_verify, stream=s)
+
+    def run(self, s):
+        self.build(s)
+        self.attention(s)
+        self.verify(s)
+
+    def bytes_build(self):
+        w = self.w
+        return w.items * w.n_rows * w.vocab * 4
+
+    def bytes_verify(self):
+        w = self.w
+        return w.items * w.total_tokens * w.vocab * 4
+
+    def _problems(self):
+        w = self.w
+        return [(self.prefix[0], ) for _ in range(w.layers)] if w.layers > 1 else \
+            [(self.prefix[b], ) for b in range(w.items)]
+
+    def bytes_attn(self):
+        w = self.w
+        el = 2 if w.dtype == "bf16" else 4
+        m, hq, hkv, d = w.total_tokens, w.n_q_heads, w.n_kv_heads, w.head_dim
+        return sum(2 * S * hkv * d * el + m * hq * d * el + 2 * m * hkv * d * el + m * hq * d * 4
+                   for (S, ) in self._problems())
+
+    def flops_attn(self):
+        w = self.w
+        m, hq, d = w.total_tokens, w.n_q_heads, w.head_dim
+        return sum(4.0 * m * hq * (S + m) * d for (S, ) in self._problems())
+
+
+def config_bench(eb, wl, dev, key, flush, K):
+    """µs per verify step of one workload (CUDA graph, L2 flushed before every
+    step), the per-call split, and the step's roofline fraction (HBM time of
+    the logit passes plus the attention's larger of HBM and tensor time,
+    against the measured peaks)."""
+    import torch
+    w = wl.WORKLOADS[key]
+    st = MultiStep(w, dev, eb, wl)
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            flush.zero_()
+            st.run(s)
+    s.synchronize()
+    times, _ = _time_graph(torch, st, s, flush, K)
+    per = _time_kernels(torch, st, s, flush, K)
+    hbm, tf, _, peak_src = _peaks()
+    k_us = {k: statistics.mean(v) for k, v in per.items()}
+    roof_us = {"build": st.bytes_build() / (hbm * 1e3), "verify": st.bytes_verify() / (hbm * 1e3),
+               "attn": max(st.bytes_attn() / (hbm * 1e3), st.flops_attn() / (tf * 1e6))}
+    us = statistics.mean(times)
+    err = [eb.workspace_error(ws, s)[0] for ws in (st.ws_build, st.ws_attn, st.ws_verify)]
+    assert err == [0, 0, 0], f"{key}: device error words {err}"
+    res = {"workload": WORKLOAD_LABEL[key], "us_per_step": round(us, 2),
+           "spread_us": spread(times), "kernels_us": {k: round(v, 2) for k, v in k_us.items()},
+           "roofline_us": {k: round(v, 3) for k, v in roof_us.items()},
+           "step_roofline_us": round(sum(roof_us.values()), 3),
+           "step_roofline_frac": round(sum(roof_us.values()) / us, 4),
+           "attn_frac_hbm": round(st.bytes_attn() / (k_us["attn"] * 1e3) / hbm, 4),
+           "attn_frac_tensor": round(st.flops_attn() / (k_us["attn"] * 1e6) / tf, 4),
+           "bytes": {"build": st.bytes_build(), "attn": st.bytes_attn(),
+                     "verify": st.bytes_verify()},
+           "attn_gflop": round(st.flops_attn() / 1e9, 3), "launches": st.launches,
+           "items": w.items, "layers": w.layers, "steps": K, "peak_source": peak_src}
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_one_thread(key):
+    """The oracle's step on ONE host thread (BLAS pinned to one thread in a
+    child process, since the setting must precede numpy's import)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    code = ("import json, bench; r = bench.cpu_baseline(%r, samples=1); r['cores'] = 1; "
+            "print(json.dumps(r))" % key)
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                             text=True, timeout=600)
+        line = [ln for ln in out.stdout.splitlines() if ln.startswith("{")][-1]
+        return json.loads(line)
+    except Exception as exc:
+        return {"error": str(exc)[:200]}
+
+
 def attn_long(eb, wl, dev, reps=5, n_layers=None, paged=True):
     """Tree attention at long context: 32 independent layers of a
     llama-3-8b-shaped KV cache (8 kv heads, d 128, bf16 prefix 32768; 4.3 GB,
@@ -716,8 +860,14 @@ def run_ours(args, rank, world, local_rank):
         la["frac_tensor"] = round(la["achieved_tflops"] / tf, 4)
         la["peak_source"] = peak_src
         line["tree_attn_long"] = la
+    if not args.no_configs:
+        K = min(args.steps, 50)
+        line["configs"] = {key: config_bench(eb, wl, dev, key, flush, K)
+                           for key in ("c0", "c1", "c3", "c4")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, samples=1)
+        line["cpu_baseline_1thread_us"] = {key: oracle_one_thread(key).get("value")
+                                           for key in ("c0", "c1", "c2")}
     return line
 
 
@@ -806,6 +956,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c2", choices=["c0", "c1", "c2"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload step measurements of c0, c1, c3 and c4")
     ap.add_argument("--no-long-attn", action="store_true",
                     help="skip the 32-layer x 32K-context attention measurement")
     ap.add_argument("--long-attn-only", type=int, default=0, metavar="LAYERS",

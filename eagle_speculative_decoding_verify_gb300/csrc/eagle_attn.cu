@@ -29,10 +29,27 @@ __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// One CTA = (item, kv head, query i, split); warp w handles q heads
-// w, w+4, ... of the group; lanes own head_dim elements lane, lane+32, ...
+// One CTA = (item, kv head, query i, split).  The split's keys go through
+// shared memory in chunks of kSimtKeys: fp32 rows by 16-byte asynchronous
+// copies all issued at once (bf16 rows widened through registers), key rows
+// padded to d + 4 floats so that 16-byte reads of different rows by the
+// lanes of a quarter-warp fall on different banks.  The group's q vectors
+// (pre-scaled) sit in shared memory.  Warp w handles q heads w, w+4, ... of
+// the group; per 32-key step every lane scores its own key (float4 dot
+// products, four independent sums), the warp forms the online-softmax update,
+// the 32 weights go through shared memory, and lanes own head_dim columns
+// lane, lane+32, ... of the output.
+constexpr int kSimtKeys = 64;
+constexpr int kSimtHeadsPerWarp = 8;   // group size g <= 32
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
 template <typename T>
 __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ AttnPlan P) {
+  extern __shared__ __align__(16) float simt_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int item = 0;
   while (item + 1 < P.n_items && static_cast<int>(blockIdx.x) >= P.unit_start[item + 1]) ++item;
@@ -45,6 +62,11 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
   const int kvh = u / it.m;
   const int d = P.head_dim, g = P.n_q_heads / P.n_kv_heads;
   const int E = (d + 31) / 32;
+  const int ks = d + 4;                      // padded key row stride (floats, 16-byte rows)
+  float* Ks = simt_smem;                     // [kSimtKeys][d + 4]
+  float* Vs = Ks + kSimtKeys * ks;           // [kSimtKeys][d]
+  float* Qs = Vs + kSimtKeys * d;            // [g][d], pre-scaled
+  float* Ps = Qs + 32 * d;                   // [4 warps][32] weights of a step
   const int span = (it.prefix_len + splits - 1) / splits;
   const int j0 = min(it.prefix_len, split * span), j1 = min(it.prefix_len, j0 + span);
   const bool with_tree = (split == splits - 1);
@@ -54,58 +76,123 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
   const T* vc = static_cast<const T*>(it.v_cache) + static_cast<int64_t>(kvh) * it.cache_head_stride;
   const T* tk = static_cast<const T*>(it.tree_k);
   const T* tv = static_cast<const T*>(it.tree_v);
+  const uint64_t* mrow = it.mask + static_cast<int64_t>(i) * W;
 
-  for (int hl = warp; hl < g; hl += 4) {
-    const int h = kvh * g + hl;
-    const T* qrow = static_cast<const T*>(it.q) + (static_cast<int64_t>(i) * P.n_q_heads + h) * d;
-    float q[4], o[4];
+  const T* qg = static_cast<const T*>(it.q) + (static_cast<int64_t>(i) * P.n_q_heads + kvh * g) * d;
+  for (int x = threadIdx.x; x < g * d; x += blockDim.x) Qs[x] = to_f(__ldg(qg + x)) * qscale;
+
+  float o[kSimtHeadsPerWarp][4], mx[kSimtHeadsPerWarp], l[kSimtHeadsPerWarp];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e = r * 32 + lane;
-      q[r] = (r < E && e < d) ? to_f(qrow[e]) * qscale : 0.f;
-      o[r] = 0.f;
-    }
-    float mx = -INFINITY, l = 0.f;
-    auto visit = [&](const T* krow, const T* vrow) {
-      float s = 0.f;
+  for (int a = 0; a < kSimtHeadsPerWarp; ++a) {
+    mx[a] = -INFINITY;
+    l[a] = 0.f;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int e = r * 32 + lane;
-        if (r < E && e < d) s += q[r] * to_f(krow[e]);
+    for (int r = 0; r < 4; ++r) o[a][r] = 0.f;
+  }
+
+  // n keys whose rows start at element offsets row(k) (k < n) into K / V
+  auto stage = [&](int n, auto row, const T* ksrc, const T* vsrc) {
+    if constexpr (sizeof(T) == 4) {
+      const int q4 = d / 4;
+      for (int x = threadIdx.x; x < n * q4; x += blockDim.x) {
+        const int k = x / q4, c = x - k * q4;
+        const int64_t gi = row(k) + 4 * c;
+        cp_async16(Ks + k * ks + 4 * c, ksrc + gi);
+        cp_async16(Vs + k * d + 4 * c, vsrc + gi);
       }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (s > mx) {
-        const float c = exp2f(mx - s);
-        l *= c;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) o[r] *= c;
-        mx = s;
-      }
-      const float p = exp2f(s - mx);
-      l += p;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int e = r * 32 + lane;
-        if (r < E && e < d) o[r] += p * to_f(vrow[e]);
-      }
-    };
-    for (int j = j0; j < j1; ++j) visit(kc + static_cast<int64_t>(j) * d, vc + static_cast<int64_t>(j) * d);
-    if (with_tree) {
-      const uint64_t* mrow = it.mask + static_cast<int64_t>(i) * W;
-      for (int t = 0; t < it.m; ++t) {
-        if (!((mrow[t >> 6] >> (t & 63)) & 1ull)) continue;
-        const int64_t off = (static_cast<int64_t>(t) * P.n_kv_heads + kvh) * d;
-        visit(tk + off, tv + off);
+      cp_async_commit();
+      cp_async_wait_all();
+    } else {
+      for (int x = threadIdx.x; x < n * d; x += blockDim.x) {
+        const int k = x / d, e = x - k * d;
+        const int64_t gi = row(k) + e;
+        Ks[k * ks + e] = to_f(__ldg(ksrc + gi));
+        Vs[k * d + e] = to_f(__ldg(vsrc + gi));
       }
     }
-    const int64_t row = static_cast<int64_t>(i) * P.n_q_heads + h;
+  };
+
+  // one chunk of n keys in shared memory; bit k of valid: key k counts
+  auto consume = [&](int n, uint64_t valid) {
+    for (int sub = 0; sub < n; sub += 32) {
+      const int kk = sub + lane;
+      const bool ok = kk < n && ((valid >> (kk & 63)) & 1ull);
+      const float4* kr = reinterpret_cast<const float4*>(Ks + (kk < n ? kk : 0) * ks);
+#pragma unroll
+      for (int a = 0; a < kSimtHeadsPerWarp; ++a) {
+        const int hl = warp + 4 * a;
+        if (hl >= g) break;
+        const float4* qr = reinterpret_cast<const float4*>(Qs + hl * d);
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int c = 0; c < d / 4; ++c) {
+          const float4 qv = qr[c], kv = kr[c];
+          s4[0] = fmaf(qv.x, kv.x, s4[0]);
+          s4[1] = fmaf(qv.y, kv.y, s4[1]);
+          s4[2] = fmaf(qv.z, kv.z, s4[2]);
+          s4[3] = fmaf(qv.w, kv.w, s4[3]);
+        }
+        const float sc = ok ? (s4[0] + s4[1]) + (s4[2] + s4[3]) : -INFINITY;
+        const float m_new = fmaxf(mx[a], warp_max(sc));
+        if (m_new == -INFINITY) continue;   // nothing visible yet
+        const float c0 = exp2f(mx[a] - m_new);
+        const float p = ok ? exp2f(sc - m_new) : 0.f;
+        float ps = p;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+        l[a] = l[a] * c0 + ps;
+        mx[a] = m_new;
+        Ps[warp * 32 + lane] = p;
+        __syncwarp();
+        const int nk = min(32, n - sub);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int e = r * 32 + lane;
+          if (r >= E || e >= d) break;
+          float acc0 = o[a][r] * c0, acc1 = 0.f;
+#pragma unroll 8
+          for (int k = 0; k < 32; k += 2) {
+            if (k < nk) acc0 = fmaf(Ps[warp * 32 + k], Vs[(sub + k) * d + e], acc0);
+            if (k + 1 < nk) acc1 = fmaf(Ps[warp * 32 + k + 1], Vs[(sub + k + 1) * d + e], acc1);
+          }
+          o[a][r] = acc0 + acc1;
+        }
+        __syncwarp();
+      }
+    }
+  };
+
+  // prefix keys of this split
+  for (int c0 = j0; c0 < j1; c0 += kSimtKeys) {
+    const int n = min(kSimtKeys, j1 - c0);
+    __syncthreads();   // the previous chunk is consumed (and Qs written, the first time)
+    stage(n, [&](int k) { return static_cast<int64_t>(c0 + k) * d; }, kc, vc);
+    __syncthreads();
+    consume(n, ~0ull);
+  }
+  // tree keys (last split): the ancestor mask decides which count
+  if (with_tree) {
+    for (int c0 = 0; c0 < it.m; c0 += kSimtKeys) {
+      const int n = min(kSimtKeys, it.m - c0);
+      __syncthreads();
+      stage(n, [&](int k) { return (static_cast<int64_t>(c0 + k) * P.n_kv_heads + kvh) * d; },
+            tk, tv);
+      __syncthreads();
+      consume(n, mrow[c0 >> 6]);   // c0 is a multiple of 64: one mask word per chunk
+    }
+  }
+
+#pragma unroll
+  for (int a = 0; a < kSimtHeadsPerWarp; ++a) {
+    const int hl = warp + 4 * a;
+    if (hl >= g) break;
+    const int64_t row = static_cast<int64_t>(i) * P.n_q_heads + kvh * g + hl;
     if (splits == 1) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l[a] > 0.f ? 1.f / l[a] : 0.f;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int e = r * 32 + lane;
-        if (r < E && e < d) it.out[row * d + e] = o[r] * inv;
+        if (r < E && e < d) it.out[row * d + e] = o[a][r] * inv;
       }
     } else {
       float* part = P.partials + P.part_start[item] +
@@ -113,14 +200,18 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int e = r * 32 + lane;
-        if (r < E && e < d) part[e] = o[r];
+        if (r < E && e < d) part[e] = o[a][r];
       }
       if (lane == 0) {
-        part[d] = mx;
-        part[d + 1] = l;
+        part[d] = mx[a];
+        part[d + 1] = l[a];
       }
     }
   }
+}
+
+static size_t simt_smem_bytes(int d) {
+  return sizeof(float) * (kSimtKeys * (2 * d + 4) + 32 * d + 4 * 32);
 }
 
 // Combine split partials: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
@@ -169,6 +260,9 @@ static eagle_status validate(const eagle_attn_item* items, int n, int hq, int hk
   EAGLE_CHECK_ARG(hq >= 1 && hkv >= 1 && hq % hkv == 0 && d >= 1);
   EAGLE_CHECK_ARG(dtype == EAGLE_F32 || dtype == EAGLE_BF16);
   EAGLE_CHECK_SHAPE(d <= 128 && d % 4 == 0);
+  // the CUDA-core path (fp32, or a head_dim without tensor-core support)
+  // handles groups of up to 32 q heads per kv head
+  EAGLE_CHECK_SHAPE((dtype == EAGLE_BF16 && (d == 64 || d == 128)) || hq / hkv <= 32);
   for (int b = 0; b < n; ++b) {
     const eagle_attn_item& it = items[b];
     EAGLE_CHECK_ARG(it.m >= 1 && it.prefix_len >= 0);
@@ -251,10 +345,18 @@ static eagle_status attn_batched_impl(const eagle_attn_item* items, int32_t n, i
     P.err = static_cast<int32_t*>(ws);
     P.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
     const int grid = P.unit_start[nb];
-    if (dtype == EAGLE_F32)
-      attn_simt_kernel<float><<<grid, 128, 0, stream>>>(P);
-    else
-      attn_simt_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(P);
+    const size_t smem = simt_smem_bytes(d);
+    if (dtype == EAGLE_F32) {
+      EAGLE_CUDA(cudaFuncSetAttribute(attn_simt_kernel<float>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+      attn_simt_kernel<float><<<grid, 128, smem, stream>>>(P);
+    } else {
+      EAGLE_CUDA(cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+      attn_simt_kernel<__nv_bfloat16><<<grid, 128, smem, stream>>>(P);
+    }
     if ((st = launch_status()) != EAGLE_OK) return st;
     if (P.part_floats > 0 && (st = launch_attn_merge(P, stream)) != EAGLE_OK) return st;
   }
