@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libeagle.so
 
 EAGLE_OK = 0
 EAGLE_ERR_WORKSPACE_TOO_SMALL = 3
+EAGLE_ERR_TIMEOUT = 5
 EAGLE_ERR_DEVICE_ASSERT = 6
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape",
                 3: "workspace too small", 4: "CUDA error", 5: "device wait timed out",
@@ -182,6 +183,23 @@ def workspace(nbytes, device=None):
     """Zero-filled uint8 workspace of at least nbytes (256-byte aligned)."""
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8,
                        device=device or torch.device("cuda"))
+
+
+def eagle_workspace_init(ws, stream=None):
+    """Zero-fill a workspace on the stream (what every call's workspace needs
+    once, and again after a recorded device error)."""
+    _check(lib().eagle_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "eagle_workspace_init")
+
+
+def workspace_test_hook(ws, no_copies=False, wait_us=0):
+    """Set the workspace header's test hook (words 2 and 3): with no_copies the
+    attention kernel's producers issue no copy, so every consumer wait runs out
+    after wait_us microseconds and the call records EAGLE_ERR_TIMEOUT.  Test use
+    only; eagle_workspace_init clears it."""
+    hdr = ws[:16].view(torch.int32)
+    hdr[2] = 1 if no_copies else 0
+    hdr[3] = int(wait_us)
 
 
 def workspace_error(ws, stream=None):

@@ -107,9 +107,10 @@ static_assert(TcSmem<128>::kAlloc <= 232448, "shared memory of the tensor-core k
 // Bounded wait whose outcome is the same for the whole warp (tcgen05.ld/st
 // after it must be executed by all 32 lanes).
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int32_t* err,
-                                             volatile int* abort_flag, int where) {
+                                             volatile int* abort_flag, int where,
+                                             uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;   // fast path: phase already complete
-  bool ok = !*abort_flag && mbar_wait(bar, parity);
+  bool ok = !*abort_flag && mbar_wait(bar, parity, limit_ns);
   if (!ok && !*abort_flag) {
     record_error(err, kDevTimeout, where);
     *abort_flag = 1;
@@ -533,6 +534,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = pair2::cta_rank();
+  // the workspace header's test hook: a short wait limit, and producers that
+  // issue nothing (both zero in normal use)
+  const WsHeader* hdr = reinterpret_cast<const WsHeader*>(P.err);
+  const int32_t test_flags = hdr->test_flags;
+  const uint64_t wait_ns =
+      hdr->test_wait_us > 0 ? 1000ull * static_cast<uint64_t>(hdr->test_wait_us) : 2000000000ull;
 
   // ---- work unit: (item, kv head, pair of query tiles, split)
   const int unit = blockIdx.x >> 1;
@@ -648,10 +655,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0) {
-      const int n_items = 2 * n_chunks;
+      const int n_items = (test_flags & kTestNoCopies) ? 0 : 2 * n_chunks;
       for (int n = 0; n < n_items; ++n) {
         const int slot = n % k2Slots, use = n / k2Slots;
-        if (use > 0 && !bounded_wait(&empty[slot], (use - 1) & 1, P.err, abort_flag, 20)) break;
+        if (use > 0 && !bounded_wait(&empty[slot], (use - 1) & 1, P.err, abort_flag, 20, wait_ns)) break;
         if (rank == 0) mbar_arrive_expect_tx(&full[slot], 2u * L::kItem);
         issue_kv(n, pair2::map_to(smem_addr(&full[slot]), 0));
       }
@@ -671,12 +678,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         constexpr uint32_t idesc_s = idesc_bf16_f32(256, kChunk, false);
         const uint64_t qdesc0 = smem_desc_sw128(smem_addr(smem + L::kQ), 16, 1024);
         const uint64_t kdesc0 = smem_desc_sw128(ring_base, 16, 1024);
-        bool ok = n_chunks > 0 && bounded_wait(q_ready, 0, P.err, abort_flag, 29);
+        bool ok = n_chunks > 0 && bounded_wait(q_ready, 0, P.err, abort_flag, 29, wait_ns);
         for (int j = 0; ok && j < n_chunks; ++j) {
           const int b = j % k2Bufs, nki = 2 * j;
           if ((j >= k2Bufs &&
-               !bounded_wait(&o_done[b], ((j - k2Bufs) / k2Bufs) & 1, P.err, abort_flag, 34)) ||
-              !bounded_wait(&full[slot_of(nki)], full_parity(nki), P.err, abort_flag, 33))
+               !bounded_wait(&o_done[b], ((j - k2Bufs) / k2Bufs) & 1, P.err, abort_flag, 34, wait_ns)) ||
+              !bounded_wait(&full[slot_of(nki)], full_parity(nki), P.err, abort_flag, 33, wait_ns))
             break;
           tc_fence_after();
           const uint64_t kd = kdesc0 + static_cast<uint64_t>((slot_of(nki) * L::kItem) >> 4);
@@ -696,8 +703,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         for (int j = 0; j < n_chunks; ++j) {
           const int b = j % k2Bufs, nvi = 2 * j + 1;
           const int nf = v0 + j < nc ? 1 : 2;   // tree keys: P = hi + lo
-          if (!bounded_wait(&full[slot_of(nvi)], full_parity(nvi), P.err, abort_flag, 31) ||
-              !bounded_wait(&p_full[b], (j / k2Bufs) & 1, P.err, abort_flag, 32))
+          if (!bounded_wait(&full[slot_of(nvi)], full_parity(nvi), P.err, abort_flag, 31, wait_ns) ||
+              !bounded_wait(&p_full[b], (j / k2Bufs) & 1, P.err, abort_flag, 32, wait_ns))
             break;
           tc_fence_after();
           // keys 16kk.. of the chunk in columns 8kk.. of the buffer (bf16
@@ -736,7 +743,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
     for (int j = 0; j < n_chunks; ++j) {
       const int b = j % k2Bufs;
       const uint32_t sb = s_addr + 128 * b;
-      live = live && __all_sync(0xffffffffu, bounded_wait(&s_full[b], (j / k2Bufs) & 1, P.err, abort_flag, 40));
+      live = live && __all_sync(0xffffffffu, bounded_wait(&s_full[b], (j / k2Bufs) & 1, P.err, abort_flag, 40, wait_ns));
       // keys 64 wg .. 64 wg + 63 of the chunk; only the prefix's last chunk
       // and the tree chunks need a mask (key count, ancestor word)
       const int v = v0 + j;
@@ -788,7 +795,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         // PV(j-1) may not be: one barrier per buffer keeps this wait within
         // one phase.
         live = __all_sync(0xffffffffu, bounded_wait(&o_done[(j - 1) % k2Bufs], ((j - 1) / k2Bufs) & 1,
-                                                    P.err, abort_flag, 41));
+                                                    P.err, abort_flag, 41, wait_ns));
         if (!live) continue;
         tc_fence_after();
         const float f = grow ? ex2(m_run - m_new) : 1.0f;
@@ -844,7 +851,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
     // columns of O, normalised (one split) or as a partial
     bool ok = live && __all_sync(0xffffffffu, bounded_wait(&o_done[(n_chunks - 1) % k2Bufs],
                                                            ((n_chunks - 1) / k2Bufs) & 1, P.err,
-                                                           abort_flag, 42));
+                                                           abort_flag, 42, wait_ns));
     xch[512 + wg * 128 + row] = l_run;
     named_sync(1, 256);
     tc_fence_after();

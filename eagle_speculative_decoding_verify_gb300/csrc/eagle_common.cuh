@@ -15,8 +15,14 @@ namespace eagle {
 struct WsHeader {
   int32_t error;
   int32_t detail;
-  int32_t pad[62];
+  int32_t test_flags;     // test hook (zero in normal use): kTestNoCopies
+  int32_t test_wait_us;   // test hook: wait limit in microseconds (0: the default 2 s)
+  int32_t pad[60];
 };
+// test_flags bit: the attention kernel's producers issue no copy at all, so
+// every consumer wait runs out (with nothing in flight) -- how the tests make
+// a bounded device wait expire.
+constexpr int32_t kTestNoCopies = 1;
 constexpr size_t kWsHeader = sizeof(WsHeader);
 static_assert(kWsHeader == 256, "header size");
 

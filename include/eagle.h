@@ -35,6 +35,13 @@
  *   - Workspaces must be zero-filled once before first use (for example with
  *     eagle_workspace_init); every successful call leaves its workspace
  *     ready for the next call.  After a recorded device error, re-initialise.
+ *     A workspace starts with a 256-byte header: int32 words 0 and 1 are the
+ *     device error word and its detail; words 2 and 3 are a test hook that
+ *     must stay zero in normal use (for the head_dim 128 tensor-core
+ *     attention: word 2 = 1 makes its producers issue no copy, so that every
+ *     consumer wait runs out; word 3 = that wait's limit in microseconds,
+ *     0 = the default 2 s) -- how the tests make a bounded device wait
+ *     expire without a fault.
  *   - Floating-point inputs must be finite (no NaN / +-inf).
  */
 #ifndef EAGLE_H
