@@ -381,7 +381,7 @@ def oracle_one_thread(key):
         return {"error": str(exc)[:200]}
 
 
-def attn_long(eb, wl, dev, reps=5, n_layers=None, paged=True):
+def attn_long(eb, wl, dev, reps=5, n_layers=None, paged=True, fp8=True):
     """Tree attention at long context: 32 independent layers of a
     llama-3-8b-shaped KV cache (8 kv heads, d 128, bf16 prefix 32768; 4.3 GB,
     far above L2) for one 60-token tree, all layers in one batched call
@@ -460,6 +460,38 @@ def attn_long(eb, wl, dev, reps=5, n_layers=None, paged=True):
         res["paged"] = {"us": round(pt * 1e6, 1), "achieved_gbs": round(nbytes / pt / 1e9, 1),
                         "page_tokens": page, "pages_shuffled": True}
         del keep, pitems, pws
+    if fp8:   # the same prefixes as E4M3 codes with one scale per (kv head, 128-token page)
+        fitems, fkeep = [], []
+        for a, o in zip(layers, outs):
+            kc, ks = wl.fp8_kv(a["k_cache"])
+            vc, vs = wl.fp8_kv(a["v_cache"])
+            fkeep.append((kc, ks, vc, vs))
+            fitems.append(eb.attn_fp8_item(a["q"], kc, vc, ks, vs, a["tree_k"], a["tree_v"],
+                                           tree.mask, o, S))
+        fws = eb.workspace(eb.lib().eagle_tree_attn_fp8_workspace_size(
+            (eb.CAttnFp8Item * nl)(*fitems), nl, hq, hkv, d), dev)
+
+        def run_fp8():
+            eb.eagle_tree_attn_fp8_batched(fitems, hq, hkv, d, ws=fws, stream=s)
+
+        for _ in range(2):
+            run_fp8()
+        s.synchronize()
+        ftimes = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            run_fp8()
+            e1.record(s)
+            s.synchronize()
+            ftimes.append(e0.elapsed_time(e1) * 1e-3)
+        ft = statistics.median(ftimes)
+        fbytes = L * (2 * S * hkv * d * 1 + 2 * hkv * (S // 128) * 4 + m * hq * d * 2 +
+                      2 * m * hkv * d * 2 + m * hq * d * 4)
+        res["fp8"] = {"us": round(ft * 1e6, 1), "achieved_gbs": round(fbytes / ft / 1e9, 1),
+                      "bytes": fbytes, "achieved_tflops": round(flops / ft / 1e12, 1),
+                      "format": "E4M3 codes, one fp32 scale per (kv head, 128-token page)"}
+        del fkeep, fitems, fws
     del layers, outs, items, ws
     torch.cuda.empty_cache()
     return res
@@ -858,6 +890,9 @@ def run_ours(args, rank, world, local_rank):
         la = attn_long(eb, wl, dev)
         la["frac_hbm"] = round(la["achieved_gbs"] / hbm, 4)
         la["frac_tensor"] = round(la["achieved_tflops"] / tf, 4)
+        if "fp8" in la:
+            la["fp8"]["frac_hbm"] = round(la["fp8"]["achieved_gbs"] / hbm, 4)
+            la["fp8"]["frac_tensor"] = round(la["fp8"]["achieved_tflops"] / tf, 4)
         la["peak_source"] = peak_src
         line["tree_attn_long"] = la
     if not args.no_configs:
@@ -968,7 +1003,7 @@ def main():
         import torch
         from eagle_speculative_decoding_verify_gb300 import binding as eb, workloads as wl
         res = attn_long(eb, wl, torch.device("cuda"), reps=max(args.steps, 1),
-                        n_layers=args.long_attn_only, paged=False)
+                        n_layers=args.long_attn_only, paged=False, fp8=False)
         print(json.dumps(res), flush=True)
         return 0
     rank = int(os.environ.get("RANK", "0"))

@@ -66,6 +66,15 @@ class CAttnPagedItem(ctypes.Structure):
                 ("m", ctypes.c_int32)]
 
 
+class CAttnFp8Item(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("tree_k", ctypes.c_void_p), ("tree_v", ctypes.c_void_p), ("mask", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("cache_head_stride", ctypes.c_int64),
+                ("scale_head_stride", ctypes.c_int64), ("prefix_len", ctypes.c_int32),
+                ("m", ctypes.c_int32)]
+
+
 class CTreePolicy(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("width", ctypes.c_int32), ("depth", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("tau", ctypes.c_double)]
@@ -115,6 +124,8 @@ EXPORTS = {
                                          _P, _SZ, _P]),
     "eagle_tree_attn_paged_workspace_size": (_SZ, [_P, _I32, _I32, _I32, _I32]),
     "eagle_tree_attn_paged_batched": (_I32, [_P, _I32, _I32, _I32, _I32, _F, _P, _SZ, _P]),
+    "eagle_tree_attn_fp8_workspace_size": (_SZ, [_P, _I32, _I32, _I32, _I32]),
+    "eagle_tree_attn_fp8_batched": (_I32, [_P, _I32, _I32, _I32, _I32, _F, _P, _SZ, _P]),
     "eagle_tree_state_bytes": (_SZ, [_I32, _I32]),
     "eagle_tree_expand_workspace_size": (_SZ, [_I32, _I32]),
     "eagle_tree_expand": (_I32, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
@@ -544,4 +555,28 @@ def eagle_tree_attn_paged_batched(items, n_q_heads, n_kv_heads, head_dim, scale=
     _check(lib().eagle_tree_attn_paged_batched(arr, len(items), n_q_heads, n_kv_heads, head_dim,
                                                float(scale), _ptr(ws), ws.numel(),
                                                _stream(stream)), "eagle_tree_attn_paged_batched")
+    return ws
+
+
+# ------------------------------------------------------------- E4M3 prefix
+def attn_fp8_item(q, k_codes, v_codes, k_scale, v_scale, tree_k, tree_v, mask, out,
+                  prefix_len=None):
+    """C item for one attention problem over an E4M3 prefix cache: codes uint8
+    [Hkv, cap, d], scales float32 [Hkv, pages] (one per 128-token page)."""
+    S = k_codes.shape[1] if prefix_len is None else int(prefix_len)
+    return CAttnFp8Item(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(), k_scale.data_ptr(),
+                        v_scale.data_ptr(), tree_k.data_ptr(), tree_v.data_ptr(), mask.data_ptr(),
+                        out.data_ptr(), k_codes.stride(0), k_scale.stride(0), S, q.shape[0])
+
+
+def eagle_tree_attn_fp8_batched(items, n_q_heads, n_kv_heads, head_dim, scale=0.0, ws=None,
+                                stream=None, device=None):
+    """items: list of CAttnFp8Item (see attn_fp8_item)."""
+    arr = (CAttnFp8Item * len(items))(*items)
+    if ws is None:
+        ws = workspace(lib().eagle_tree_attn_fp8_workspace_size(arr, len(items), n_q_heads,
+                                                                n_kv_heads, head_dim), device)
+    _check(lib().eagle_tree_attn_fp8_batched(arr, len(items), n_q_heads, n_kv_heads, head_dim,
+                                             float(scale), _ptr(ws), ws.numel(), _stream(stream)),
+           "eagle_tree_attn_fp8_batched")
     return ws

@@ -74,6 +74,9 @@ struct TcItem {
   int cnt_start;        // first split-arrival counter of the item (2-SM kernel)
   const int32_t* table; // paged prefix: pool page of every 128-token page (null: contiguous)
   int pool_pages;       // pages in the pool (the table's entries must lie below)
+  const float* kscale;  // E4M3 prefix cache: scale of every (kv head, 128-token page)
+  const float* vscale;
+  int64_t sstride;      // scales between kv heads
 };
 
 struct TcParams {
@@ -91,18 +94,44 @@ struct TcParams {
   int32_t* err;
 };
 
-template <int D>
+// F8: the prefix comes from an E4M3 cache -- a staging ring of E4M3 chunks
+// (TMA) that two warps widen into the bf16 ring, which is shallower then.
+template <int D, bool F8 = false>
 struct TcSmem {
   static constexpr int kQTileBytes = 128 * D * 2;       // one 128-row bf16 query tile
   static constexpr int kKvBytes = kChunk * D * 2;       // one K or V chunk (128 keys)
   static constexpr int kBoxBytes = kChunk * 128;        // 128 rows x 64 elements (128 B)
+  static constexpr int kSlotsT = F8 ? 3 : kSlots;       // bf16 ring depth
+  static constexpr int kStage = F8 ? 4 : 0;             // E4M3 staging ring depth
+  static constexpr int kStageBytes = kChunk * D;        // one E4M3 chunk
   static constexpr int kQ = 0;                          // the CTA's two query tiles
   static constexpr int kRing = kQ + 2 * kQTileBytes;
-  static constexpr int kBars = kRing + kSlots * kKvBytes;
+  static constexpr int kStageOff = kRing + kSlotsT * kKvBytes;
+  static constexpr int kBars = kStageOff + kStage * kStageBytes;
   static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
 };
 static_assert(TcSmem<128>::kAlloc <= 232448, "shared memory of the tensor-core kernel");
+static_assert(TcSmem<128, true>::kAlloc <= 232448, "shared memory of the E4M3 kernel");
+
+// 16 E4M3 codes -> 16 bf16 (exact: every E4M3 value is a bf16 value); the
+// first code lands in the low half of out[0]
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 in, uint32_t (&out)[8]) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint16_t pair = static_cast<uint16_t>(w[q] >> (16 * h));
+      uint32_t f16x2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+      float lo, hi;
+      asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+          : "=f"(lo), "=f"(hi) : "r"(f16x2));
+      out[2 * q + h] = pack_bf16x2(lo, hi);
+    }
+  }
+}
 
 // Bounded wait whose outcome is the same for the whole warp (tcgen05.ld/st
 // after it must be executed by all 32 lanes).
@@ -118,9 +147,10 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int
   return ok;
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams P) {
-  using L = TcSmem<D>;
+  using L = TcSmem<D, F8>;
+  constexpr int kSlots = L::kSlotsT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -131,7 +161,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   uint64_t* o_done = p_full + 2;        // [query tile]: that tile's PV done
   uint64_t* drain = o_done + 2;         // [1]
   uint64_t* q_ready = drain + 1;        // [1] both Q tiles written (8 softmax warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
+  uint64_t* full8 = q_ready + 1;        // [kStage] E4M3 chunk landed (F8)
+  uint64_t* empty8 = full8 + 4;         // [kStage] E4M3 chunk widened (F8)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty8 + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -184,10 +216,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     }
   };
 
+  // E4M3 prefix (F8): item n of a prefix split is staged as codes, then
+  // widened into bf16 ring slot n % kSlots by the converter warps
+  const bool staged = F8 && !tree_split;
+  auto issue_stage = [&](int n) {
+    const int st = n % L::kStage;
+    const int j = n >> 1;
+    const CUtensorMap* map = (n & 1) ? &P.vmap[item] : &P.kmap[item];
+    mbar_arrive_expect_tx(&full8[st], static_cast<uint32_t>(L::kStageBytes));
+    tma_load_3d(smem + L::kStageOff + st * L::kStageBytes, map, 0, split_start + j * kChunk, kvh,
+                &full8[st]);
+  };
+
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < L::kStage; ++s) {
+      mbar_init(&full8[s], 1);
+      mbar_init(&empty8[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -199,7 +247,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     *abort_flag = 0;
     fence_barrier_init();
     // the producer (this thread) starts streaming before the CTA-wide barrier
-    for (int n = 0; n < kSlots && n < 2 * n_chunks; ++n) issue_kv(n);
+    if (staged) {
+      for (int n = 0; n < L::kStage && n < 2 * n_chunks; ++n) issue_stage(n);
+    } else {
+      for (int n = 0; n < kSlots && n < 2 * n_chunks; ++n) issue_kv(n);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -244,7 +296,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && staged) {
+      int issued = L::kStage < 2 * n_chunks ? L::kStage : 2 * n_chunks;   // the prologue's
+      for (int n = issued; n < 2 * n_chunks; ++n) {
+        const int st = n % L::kStage, use = n / L::kStage;
+        if (!bounded_wait(&empty8[st], (use - 1) & 1, P.err, abort_flag, 21)) break;
+        issue_stage(n);
+        issued = n + 1;
+      }
+      // make sure no copy of ours is still landing when the CTA leaves
+      for (int n = (issued > L::kStage ? issued - L::kStage : 0); n < issued; ++n)
+        mbar_wait(&full8[n % L::kStage], (n / L::kStage) & 1, 200000000ull);
+    } else if (lane == 0) {
       int issued = kSlots < 2 * n_chunks ? kSlots : 2 * n_chunks;   // the prologue's
       for (int n = issued; n < 2 * n_chunks; ++n) {
         const int slot = n % kSlots, use = n / kSlots;
@@ -255,6 +318,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // make sure no copy of ours is still landing when the CTA leaves
       for (int n = (issued > kSlots ? issued - kSlots : 0); n < issued; ++n)
         mbar_wait(&full[n % kSlots], (n / kSlots) & 1, 200000000ull);
+    }
+  } else if (staged && (warp == 2 || warp == 3)) {
+    // ================================================================ E4M3 -> bf16
+    // item n: the staged E4M3 chunk [128 keys][D codes] -> bf16 ring slot
+    // n % kSlots in the layout a bf16 TMA would have written (boxes of 64
+    // columns, 128-byte rows, 128-byte swizzle).  Both warps run every item
+    // and meet at a named barrier in each, also after a wait ran out.
+    const int ct = tid - 64;   // 0..63
+    bool live = true;
+    for (int n = 0; n < 2 * n_chunks; ++n) {
+      const int st = n % L::kStage, slot = n % kSlots;
+      live = live && __all_sync(0xffffffffu, bounded_wait(&full8[st], (n / L::kStage) & 1, P.err,
+                                                          abort_flag, 22));
+      if (live && n >= kSlots)
+        live = __all_sync(0xffffffffu, bounded_wait(&empty[slot], (n / kSlots - 1) & 1, P.err,
+                                                     abort_flag, 23));
+      if (live) {
+        const uint8_t* src = smem + L::kStageOff + st * L::kStageBytes;
+        uint8_t* dst = smem + L::kRing + slot * L::kKvBytes;
+        constexpr int kPieces = kChunk * D / 16;   // 16 codes each
+#pragma unroll 4
+        for (int pc = ct; pc < kPieces; pc += 64) {
+          const int r = pc / (D / 16), pp = pc - r * (D / 16);
+          const uint4 in = *reinterpret_cast<const uint4*>(src + r * D + 16 * pp);
+          uint32_t o[8];
+          e4m3x16_to_bf16(in, o);
+          const int col = 16 * pp, box = col >> 6, cc = (col & 63) >> 3;
+          uint8_t* rowp = dst + box * L::kBoxBytes + r * 128;
+          *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+      }
+      named_sync(2, 64);
+      if (ct == 0 && live) {
+        mbar_arrive(&full[slot]);
+        mbar_arrive(&empty8[st]);
+      }
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -344,6 +445,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // key validity: only the last prefix chunk of a split and the tree
       // chunks need a mask (key count, ancestor words for tree keys)
       const bool pref = j < n_pref;
+      // E4M3 prefix chunk: S carries the page's key scale, P the value scale
+      float sl2j = sl2, svj = 1.f, isvj = 1.f;
+      if (F8 && pref) {
+        const int64_t pg = static_cast<int64_t>(kvh) * it.sstride + split_start / kChunk + j;
+        sl2j = sl2 * __ldg(it.kscale + pg);
+        svj = __ldg(it.vscale + pg);
+        isvj = svj > 0.f ? 1.f / svj : 0.f;
+      }
       const int t0 = pref ? 0 : (j - n_pref) * kChunk;
       const int nvalid = pref ? min(kChunk, split_end - (split_start + j * kChunk)) : min(kChunk, it.m - t0);
       const bool masked = !pref || nvalid < kChunk;
@@ -385,7 +494,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                              fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
       }
-      mx *= sl2;   // scale > 0
+      mx *= sl2j;   // scale > 0
       const float m_new = fmaxf(m_run, mx);
       const bool grow = (j == 0) || (m_new > m_run + 8.0f);
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
@@ -419,10 +528,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(v[32 * q + 2 * e], sl2, -mref));
-            const float p1 = ex2(fmaf(v[32 * q + 2 * e + 1], sl2, -mref));
-            ls[e & 3] += p0 + p1;
-            hi[e] = pack_bf16x2(p0, p1);
+            const float p0 = ex2(fmaf(v[32 * q + 2 * e], sl2j, -mref));
+            const float p1 = ex2(fmaf(v[32 * q + 2 * e + 1], sl2j, -mref));
+            hi[e] = F8 ? pack_bf16x2(p0 * svj, p1 * svj) : pack_bf16x2(p0, p1);
+            // the row sum takes the weights the MMA uses: the bf16-rounded
+            // ones for prefix keys (a dominant key's rounding then cancels in
+            // the normalisation), hi + lo ~ p for tree keys
+            ls[e & 3] += pref ? (__uint_as_float(hi[e] << 16) + __uint_as_float(hi[e] & 0xffff0000u)) * isvj
+                              : p0 + p1;
             if (!pref) {
               const float r0 = p0 - __uint_as_float(hi[e] << 16);
               const float r1 = p1 - __uint_as_float(hi[e] & 0xffff0000u);
@@ -823,9 +936,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         float a0, a1;
         f32x2_split(fma_x2(f32x2(x[2 * c], x[2 * c + 1]), sl2x2, nm2), a0, a1);
         const float p0 = ex2(a0), p1 = ex2(a1);
-        const uint64_t pp = f32x2(p0, p1);
-        ls2[c & 3] = c < 4 ? pp : add_x2(ls2[c & 3], pp);
         hi[c] = pack_bf16x2(p0, p1);
+        // the row sum takes the weights the MMA uses: bf16-rounded for prefix
+        // keys (a dominant key's rounding cancels in the normalisation),
+        // hi + lo ~ p for tree keys
+        const uint64_t pp = pref ? f32x2(__uint_as_float(hi[c] << 16), __uint_as_float(hi[c] & 0xffff0000u))
+                                 : f32x2(p0, p1);
+        ls2[c & 3] = c < 4 ? pp : add_x2(ls2[c & 3], pp);
         if (!pref) {
           x[2 * c] = p0 - __uint_as_float(hi[c] << 16);
           x[2 * c + 1] = p1 - __uint_as_float(hi[c] & 0xffff0000u);
@@ -1030,6 +1147,21 @@ static bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D uint8 tensor map (E4M3 codes) with a (128 x rows_box x 1) box, no swizzle.
+static bool encode_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                         uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                         uint32_t box1) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1 ? d1 : 1, d2 ? d2 : 1};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {128, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_supported(int head_dim) { return head_dim == 64 || head_dim == 128; }
 
 struct TcPlan {
@@ -1046,16 +1178,16 @@ struct TcPlan {
 constexpr int kFusedMergeMaxSplits = 4;
 
 // Work units per (item, kv head, pair of query tiles).
-// head_dim 128 (the 2-SM kernel, a cluster of two CTAs per unit): a split
-// covers `span` entries of the item's chunk list (its prefix chunks, then its
-// tree chunks).  head_dim 64 (one CTA per unit): prefix splits of `span`
-// chunks plus one tree split.  The span minimises waves x (span + fixed work
+// two (the 2-SM kernel, a cluster of two CTAs per unit): a split covers
+// `span` entries of the item's chunk list (its prefix chunks, then its tree
+// chunks).  Otherwise (the 1-SM kernel, one CTA per unit): prefix splits of
+// `span` chunks plus one tree split.  The span minimises waves x (span + fixed work
 // of a unit, in chunks) plus a small charge per unit for its partials' write
 // and read.
-static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms) {
+static TcPlan plan_tc(const eagle_attn_item* items, int n, int hq, int hkv, int d, int sms,
+                      bool two) {
   TcPlan T;
   memset(&T, 0, sizeof(T));
-  const bool two = d == 128;
   const int g = hq / hkv;
   int max_span = 1;
   for (int b = 0; b < n; ++b) {
@@ -1106,7 +1238,7 @@ int attn_tc_num_launches(const eagle_attn_item* items, int n, int hq, int hkv, i
   int count = 0;
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
-    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d, sms);
+    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d, sms, d == 128);
     count += 1 + (T.part_units > 0 && (d != 128 || T.max_splits > kFusedMergeMaxSplits) ? 1 : 0);
   }
   return count;
@@ -1116,7 +1248,7 @@ size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int
   size_t need = kWsHeader;
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
-    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d, sms);
+    const TcPlan T = plan_tc(items + b0, nb, hq, hkv, d, sms, d == 128);
     need = std::max(need, kWsHeader + part_bytes(T, d));
   }
   return need;
@@ -1133,7 +1265,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
   for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
     const int nb = std::min(kTcMaxItems, n - b0);
     const eagle_attn_item* its = items + b0;
-    const TcPlan T = plan_tc(its, nb, hq, hkv, D, sms);
+    const TcPlan T = plan_tc(its, nb, hq, hkv, D, sms, D == 128);
     if (ws_bytes < kWsHeader + part_bytes(T, D)) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
     TcParams P;
     memset(&P, 0, sizeof(P));
@@ -1197,9 +1329,10 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       attn2_kernel<<<static_cast<unsigned>(2 * units), k2Threads, smem, stream>>>(P);
     } else {
       const size_t smem = TcSmem<D>::kAlloc;
-      EAGLE_CUDA(cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      EAGLE_CUDA(cudaFuncSetAttribute(attn_tc_kernel<D, false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-      attn_tc_kernel<D><<<static_cast<unsigned>(units), kTcThreads, smem, stream>>>(P);
+      attn_tc_kernel<D, false><<<static_cast<unsigned>(units), kTcThreads, smem, stream>>>(P);
     }
     eagle_status st = launch_status();
     if (st != EAGLE_OK) return st;
@@ -1231,6 +1364,118 @@ eagle_status attn_tc_launch(const eagle_attn_item* items, int n, int hq, int hkv
   if (d == 128) return launch_d<128>(items, n, hq, hkv, scale, ws, ws_bytes, stream, sms);
   if (d == 64) return launch_d<64>(items, n, hq, hkv, scale, ws, ws_bytes, stream, sms);
   return EAGLE_ERR_UNSUPPORTED_SHAPE;
+}
+
+// ------------------------------------------------------------ E4M3 prefix
+// The 1-SM kernel with its prefix chunks staged as E4M3 codes (head_dim 128);
+// the tree keys / values are bf16 and go through its tree split as usual.
+static eagle_status launch_fp8(const eagle_attn_fp8_item* items, int n, int hq, int hkv,
+                               float scale, void* ws, size_t ws_bytes, cudaStream_t stream,
+                               int sms) {
+  constexpr int D = 128;
+  std::vector<eagle_attn_item> flat(n);
+  for (int b = 0; b < n; ++b) {
+    flat[b].m = items[b].m;
+    flat[b].prefix_len = items[b].prefix_len;
+  }
+  for (int b0 = 0; b0 < n; b0 += kTcMaxItems) {
+    const int nb = std::min(kTcMaxItems, n - b0);
+    const TcPlan T = plan_tc(flat.data() + b0, nb, hq, hkv, D, sms, false);
+    if (ws_bytes < kWsHeader + part_bytes(T, D)) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+    TcParams P;
+    memset(&P, 0, sizeof(P));
+    int64_t units = 0, part = 0;
+    for (int b = 0; b < nb; ++b) {
+      const eagle_attn_fp8_item& x = items[b0 + b];
+      const uint64_t S = static_cast<uint64_t>(x.prefix_len);
+      const uint64_t ts = static_cast<uint64_t>(hkv) * D * 2;
+      const void* kb = x.prefix_len ? static_cast<const void*>(x.k_cache) : x.tree_k;
+      const void* vb = x.prefix_len ? static_cast<const void*>(x.v_cache) : x.tree_v;
+      const uint64_t hs = x.prefix_len ? static_cast<uint64_t>(x.cache_head_stride) : D;
+      if (!encode_3d_u8(&P.kmap[b], kb, D, S, hkv, D, hs, kChunk) ||
+          !encode_3d_u8(&P.vmap[b], vb, D, S, hkv, D, hs, kChunk) ||
+          !encode_3d(&P.tkmap[b], x.tree_k, D, hkv, x.m, D * 2, ts, 1, kChunk) ||
+          !encode_3d(&P.tvmap[b], x.tree_v, D, hkv, x.m, D * 2, ts, 1, kChunk))
+        return EAGLE_ERR_CUDA;
+      TcItem& ti = P.items[b];
+      ti.q = static_cast<const __nv_bfloat16*>(x.q);
+      ti.out = x.out;
+      ti.mask = x.mask;
+      ti.m = x.m;
+      ti.prefix_len = x.prefix_len;
+      ti.splits = T.splits[b];
+      ti.tiles = T.tiles[b];
+      ti.pairs = (T.tiles[b] + 1) / 2;
+      ti.unit_start = static_cast<int>(units);
+      ti.part_start = part;
+      ti.kscale = x.k_scale;
+      ti.vscale = x.v_scale;
+      ti.sstride = x.scale_head_stride;
+      units += static_cast<int64_t>(hkv) * ti.pairs * T.splits[b];
+      if (T.splits[b] > 1) part += static_cast<int64_t>(hkv) * T.tiles[b] * T.splits[b];
+    }
+    P.n_items = nb;
+    P.hq = hq;
+    P.hkv = hkv;
+    P.g = hq / hkv;
+    P.span_chunks = T.span;
+    P.total_units = static_cast<int>(units);
+    P.scale_log2 = (scale != 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D))) * 1.4426950408889634f;
+    P.err = static_cast<int32_t*>(ws);
+    char* pbase = static_cast<char*>(ws) + kWsHeader;
+    P.part_o = reinterpret_cast<float*>(pbase);
+    P.part_ml = reinterpret_cast<float2*>(
+        pbase + align_up(sizeof(float) * static_cast<size_t>(T.part_units) * 128 * D, 256));
+    const size_t smem = TcSmem<D, true>::kAlloc;
+    EAGLE_CUDA(cudaFuncSetAttribute(attn_tc_kernel<D, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem)));
+    attn_tc_kernel<D, true><<<static_cast<unsigned>(units), kTcThreads, smem, stream>>>(P);
+    eagle_status st = launch_status();
+    if (st != EAGLE_OK) return st;
+    if (part > 0) {
+      TcMergeParams MP;
+      memset(&MP, 0, sizeof(MP));
+      int blocks = 0;
+      for (int b = 0; b < nb; ++b) {
+        MP.items[b] = P.items[b];
+        MP.block_start[b] = blocks;
+        if (P.items[b].splits > 1) blocks += hkv * P.items[b].tiles * 4 * (D / 32);
+      }
+      MP.block_start[nb] = blocks;
+      MP.n_items = nb;
+      MP.hq = hq;
+      MP.hkv = hkv;
+      MP.g = hq / hkv;
+      MP.part_o = P.part_o;
+      MP.part_ml = P.part_ml;
+      attn_tc_merge_kernel<D><<<blocks, 256, 0, stream>>>(MP);
+      if ((st = launch_status()) != EAGLE_OK) return st;
+    }
+  }
+  return EAGLE_OK;
+}
+
+static eagle_status fp8_validate(const eagle_attn_fp8_item* items, int n, int hq, int hkv,
+                                 int d) {
+  EAGLE_CHECK_ARG(items && n >= 1 && n <= (1 << 20) && hq >= 1 && hkv >= 1 && hq % hkv == 0);
+  EAGLE_CHECK_SHAPE(d == 128);
+  for (int b = 0; b < n; ++b) {
+    const eagle_attn_fp8_item& x = items[b];
+    EAGLE_CHECK_ARG(x.m >= 1 && x.prefix_len >= 0);
+    EAGLE_CHECK_SHAPE(x.m <= EAGLE_MAX_TREE);
+    EAGLE_CHECK_ARG(x.q && x.tree_k && x.tree_v && x.mask && x.out);
+    EAGLE_CHECK_ARG(aligned16(x.q) && aligned16(x.tree_k) && aligned16(x.tree_v) &&
+                    aligned16(x.out));
+    if (x.prefix_len > 0) {
+      EAGLE_CHECK_ARG(x.k_cache && x.v_cache && x.k_scale && x.v_scale);
+      EAGLE_CHECK_ARG(aligned16(x.k_cache) && aligned16(x.v_cache));
+      EAGLE_CHECK_ARG(x.cache_head_stride % 16 == 0 &&
+                      x.cache_head_stride >= static_cast<int64_t>(x.prefix_len) * d);
+      EAGLE_CHECK_ARG(x.scale_head_stride >= (x.prefix_len + kChunk - 1) / kChunk);
+    }
+  }
+  return EAGLE_OK;
 }
 
 // ------------------------------------------------------------- paged prefix
@@ -1307,4 +1552,36 @@ extern "C" eagle_status eagle_tree_attn_paged_batched(const eagle_attn_paged_ite
                              sms, tables.data(), rows.data())
              : launch_d<64>(flat.data(), n_items, n_q_heads, n_kv_heads, scale, ws, ws_bytes, s,
                             sms, tables.data(), rows.data());
+}
+
+extern "C" size_t eagle_tree_attn_fp8_workspace_size(const eagle_attn_fp8_item* items,
+                                                     int32_t n_items, int32_t n_q_heads,
+                                                     int32_t n_kv_heads, int32_t head_dim) {
+  if (fp8_validate(items, n_items, n_q_heads, n_kv_heads, head_dim) != EAGLE_OK) return 0;
+  std::vector<eagle_attn_item> flat(n_items);
+  for (int b = 0; b < n_items; ++b) {
+    memset(&flat[b], 0, sizeof(flat[b]));
+    flat[b].m = items[b].m;
+    flat[b].prefix_len = items[b].prefix_len;
+  }
+  size_t need = kWsHeader;
+  for (const int sms : {kPlanSMs, plan_sms()})
+    for (int b0 = 0; b0 < n_items; b0 += kTcMaxItems) {
+      const int nb = std::min(kTcMaxItems, n_items - b0);
+      const TcPlan T = plan_tc(flat.data() + b0, nb, n_q_heads, n_kv_heads, head_dim, sms, false);
+      need = std::max(need, kWsHeader + part_bytes(T, head_dim));
+    }
+  return need;
+}
+
+extern "C" eagle_status eagle_tree_attn_fp8_batched(const eagle_attn_fp8_item* items,
+                                                    int32_t n_items, int32_t n_q_heads,
+                                                    int32_t n_kv_heads, int32_t head_dim,
+                                                    float scale, void* ws, size_t ws_bytes,
+                                                    eagle_stream stream) {
+  eagle_status st = fp8_validate(items, n_items, n_q_heads, n_kv_heads, head_dim);
+  if (st != EAGLE_OK) return st;
+  EAGLE_CHECK_ARG(ws != nullptr);
+  return launch_fp8(items, n_items, n_q_heads, n_kv_heads, scale, ws, ws_bytes,
+                    reinterpret_cast<cudaStream_t>(stream), plan_sms());
 }

@@ -136,6 +136,23 @@ def attention_inputs(w, item=0, layer=0, device="cpu", prefix=None):
     )
 
 
+def fp8_kv(cache, page=128):
+    """A key or value cache [Hkv, S, d] stored as E4M3 codes with one fp32
+    scale per (kv head, page of `page` tokens), as a cache writer would store
+    it: scale = the page's largest magnitude / 448, code = the value / scale
+    rounded by PyTorch's float8_e4m3fn conversion.  Returns (uint8 codes
+    [Hkv, S, d], float32 scales [Hkv, ceil(S / page)])."""
+    x = cache.to(torch.float32)
+    hkv, S, d = x.shape
+    n = (S + page - 1) // page
+    pad = torch.zeros(hkv, n * page, d, dtype=torch.float32, device=x.device)
+    pad[:, :S] = x
+    amax = pad.view(hkv, n, page * d).abs().amax(dim=2)
+    scales = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (pad.view(hkv, n, page, d) / scales[:, :, None, None]).to(torch.float8_e4m3fn)
+    return codes.view(torch.uint8).reshape(hkv, n * page, d)[:, :S].contiguous(), scales
+
+
 def target_logits(w, parents, tokens, item=0, device="cpu"):
     """fp32 [m, V]: N(0, 4) plus +8 at the first child's token (p = 0.8) or
     at a uniformly drawn token (otherwise, and always for leaves)."""

@@ -395,6 +395,50 @@ eagle_status eagle_tree_attn_paged_batched(const eagle_attn_paged_item* items, i
                                            int32_t head_dim, float scale, void* ws,
                                            size_t ws_bytes, eagle_stream stream);
 
+/* FP8 prefix cache (serving: half the bytes of a bf16 cache in the shared
+ * pool; [blog] production section).  The pages give no number format; this
+ * library reads it as E4M3 codes (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; subnormals m * 2^-9; the code S.1111.111 is not a number;
+ * largest magnitude 448) with one fp32 scale per (kv head, 128-token page):
+ * prefix element = decode(code) * scale.  The tree's own keys / values are
+ * bf16 (they are not cached yet when the tree is verified).
+ *
+ * k_cache,
+ * v_cache:           uint8 E4M3 codes [n_kv_heads][cache_head_stride]; each
+ *                    head's rows (head_dim codes each) contiguous; stride a
+ *                    multiple of 16, at least prefix_len * head_dim; 16-byte
+ *                    aligned.
+ * k_scale, v_scale:  fp32 [n_kv_heads][scale_head_stride]: entry p of head h
+ *                    scales prefix tokens 128 p .. 128 p + 127 of that head;
+ *                    scale_head_stride >= ceil(prefix_len / 128).
+ * q, tree_k, tree_v: bf16 as for eagle_tree_attn; out fp32.
+ * head_dim 128 only (EAGLE_ERR_UNSUPPORTED_SHAPE otherwise); everything else
+ * as for eagle_tree_attn_batched. */
+typedef struct {
+  const void*     q;
+  const uint8_t*  k_cache;
+  const uint8_t*  v_cache;
+  const float*    k_scale;
+  const float*    v_scale;
+  const void*     tree_k;
+  const void*     tree_v;
+  const uint64_t* mask;
+  float*          out;
+  int64_t         cache_head_stride;
+  int64_t         scale_head_stride;
+  int32_t         prefix_len;
+  int32_t         m;
+} eagle_attn_fp8_item;
+
+size_t eagle_tree_attn_fp8_workspace_size(const eagle_attn_fp8_item* items, int32_t n_items,
+                                          int32_t n_q_heads, int32_t n_kv_heads,
+                                          int32_t head_dim);
+
+eagle_status eagle_tree_attn_fp8_batched(const eagle_attn_fp8_item* items, int32_t n_items,
+                                         int32_t n_q_heads, int32_t n_kv_heads,
+                                         int32_t head_dim, float scale, void* ws,
+                                         size_t ws_bytes, eagle_stream stream);
+
 /* ------------------------------------------------------------------------
  * eagle_tree_verify -- [blog] "Single-Pass Tree Verification" (walk from the
  * root, accept matching tokens until the first discrepancy; lossless) and

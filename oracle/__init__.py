@@ -31,4 +31,4 @@ fixed independently of this code (hand-worked examples, closed forms, brute
 force, library routines, an external Philox implementation).
 """
 
-from . import philox, near_tie, tree_build, tree_attn, verify  # noqa: F401
+from . import philox, near_tie, tree_build, tree_attn, verify, kv_commit, kv_fp8  # noqa: F401

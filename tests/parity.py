@@ -15,6 +15,17 @@ import warnings
 import numpy as np
 
 ATTN_TOL = 2e-3     # max abs error of attention outputs (fp32 out, bf16/fp32 inputs)
+
+
+def peaked_tol(values):
+    """Error bound of the tensor-core attention when a few keys dominate a
+    row: the softmax weights enter the P V product as bf16, each within 2^-9
+    (relative) of its fp32 value, and the row sum uses the same rounded
+    weights, so the output moves by at most 2^-8 * max |v| (the weights'
+    errors sum to at most 2 * 2^-9 after normalisation).  For the workloads'
+    N(0, 1) inputs no key dominates and the 2e-3 bar applies."""
+    import numpy as np
+    return max(ATTN_TOL, 2.0 ** -8 * float(np.abs(np.asarray(values, dtype=np.float64)).max()))
 VALUE_TOL = 1e-5    # node values: fp32-derived on the GPU, fp64 in the oracle
 
 

@@ -9,7 +9,7 @@ from eagle_speculative_decoding_verify_gb300 import binding as eb
 from eagle_speculative_decoding_verify_gb300 import workloads as wl
 from oracle.tree_attn import tree_attention, tree_attention_rows
 from oracle.tree_build import build_draft_tree, tree_sizes
-from tests.parity import ATTN_TOL, max_abs, record_attn_error
+from tests.parity import ATTN_TOL, max_abs, peaked_tol, record_attn_error
 
 pytestmark = pytest.mark.gpu
 NAMES = ("q", "k_cache", "v_cache", "tree_k", "tree_v")
@@ -72,6 +72,20 @@ def test_shapes(dtype, m, hq, hkv, d, S):
     ref = _tree(10, 6, m, seed=m + S)
     a = _inputs(m, hq, hkv, d, S, dtype, seed=S + d)
     _check(a, ref, S)
+
+
+@pytest.mark.parametrize("S,kscale", [(2048, 40.0), (5000, 12.0), (300, 80.0)])
+def test_peaked_scores(S, kscale):
+    # keys scaled up: a few keys dominate every row, the case where the
+    # weights' bf16 rounding must cancel in the normalisation
+    m, hq, hkv, d = 60, 32, 8, 128
+    ref = _tree(10, 6, m, seed=S)
+    a = _inputs(m, hq, hkv, d, S, torch.bfloat16, seed=S + 1)
+    a["k_cache"] = (a["k_cache"].float() * kscale).to(torch.bfloat16)
+    a["tree_k"] = (a["tree_k"].float() * kscale).to(torch.bfloat16)
+    tol = peaked_tol(torch.cat([a["v_cache"].float().flatten(), a["tree_v"].float().flatten()]))
+    err = _check(a, ref, S, tol=tol)
+    record_attn_error(f"peaked scores S{S} x{kscale} (bound {tol:.2e})", err)
 
 
 def test_custom_scale_and_cache_capacity():
