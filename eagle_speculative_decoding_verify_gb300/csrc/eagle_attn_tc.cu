@@ -936,13 +936,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
         float a0, a1;
         f32x2_split(fma_x2(f32x2(x[2 * c], x[2 * c + 1]), sl2x2, nm2), a0, a1);
         const float p0 = ex2(a0), p1 = ex2(a1);
-        hi[c] = pack_bf16x2(p0, p1);
-        // the row sum takes the weights the MMA uses: bf16-rounded for prefix
-        // keys (a dominant key's rounding cancels in the normalisation),
-        // hi + lo ~ p for tree keys
-        const uint64_t pp = pref ? f32x2(__uint_as_float(hi[c] << 16), __uint_as_float(hi[c] & 0xffff0000u))
-                                 : f32x2(p0, p1);
+        const uint64_t pp = f32x2(p0, p1);
         ls2[c & 3] = c < 4 ? pp : add_x2(ls2[c & 3], pp);
+        hi[c] = pack_bf16x2(p0, p1);
         if (!pref) {
           x[2 * c] = p0 - __uint_as_float(hi[c] << 16);
           x[2 * c + 1] = p1 - __uint_as_float(hi[c] & 0xffff0000u);
