@@ -11,10 +11,10 @@
 // R draft rows -> per row the top_k (value desc, token id asc) and logsumexp.
 // Phase 2 (the CTA whose row of an item arrives last): candidate values
 // value = parent value + (logit - logsumexp), in fp64; per depth the top_k
-// frontier; the final best m-1 -- both by ranks across the sorted child lists
-// (binary search on order-preserving 64-bit keys, ties -> lower candidate
-// index); node ids by a block scan; ancestor mask by walking parent pointers
-// (depth <= 16).
+// frontier (ranks by counting within the depth); the final best m-1 (ranks
+// across the depths' sorted prefixes by binary search; order-preserving
+// 64-bit keys, ties -> lower candidate index); node ids by rank in candidate
+// order; ancestor mask by walking parent pointers (depth <= 16).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -30,6 +30,8 @@ struct BuildArgs {
   int root_token[kMaxItems];
   eagle_tree out[kMaxItems];
   char* warm;   // kWarmBytes of workspace for the code warm-up's own tree
+  char* swarm;  // the stream's code warm-up (stream_warm_bytes)
+  int warm_stream;  // 1: a stream code warm-up cluster follows the rows' (long rows)
 };
 
 // One tree assembly: the item's R row records and its outputs.
@@ -48,173 +50,180 @@ static_assert(16 + 3 * rec_bytes(kWarmK) + 4 * 16 + 8 * 4 <= kWarmBytes, "warm-u
 
 __device__ __forceinline__ int cand_depth(int a, int k) { return a < k ? 1 : 2 + (a - k) / (k * k); }
 
-// Block-wide exclusive scan of per-thread counts (blockDim == kThreads).
-static __device__ __noinline__ int block_excl_scan(int v, int* warp_tot, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  int off = 0;
-  total = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) off += warp_tot[w];
-    total += warp_tot[w];
-  }
-  __syncthreads();
-  return off + incl - v;
+// (key, candidate) a before (key, candidate) b: larger value first, then the
+// lower candidate index.
+__device__ __forceinline__ bool cand_before(uint64_t ka, int ia, uint64_t kb, int ib) {
+  return (ka > kb) | ((ka == kb) & (ia < ib));
 }
 
+// The tree assembly (all threads of one CTA).  Candidate a of level 1 is
+// entry a of row 0; candidate a = k + (l-2) k^2 + s k + c of level l >= 2 is
+// entry c of row 1 + (l-2) k + s, the row drafted from the s-th best of level
+// l-1 (its slot s): candidate a is row entry a, with offset w = logit -
+// logsumexp <= 0 of its row (each row's leader has put the logsumexp, at
+// least the row's max, in the record), so a child's value never exceeds its
+// parent's and it comes after its parent in (value desc, candidate asc).
+//
+// The result is the best need = m-1 candidates, kept level by level as a
+// sorted list B (the best need of the levels so far; B is a prefix of their
+// order).  A candidate of level l+1 can enter B only if its parent is in B:
+// otherwise the parent, and so the child, comes after B's last entry.  And a
+// candidate of level l in B has every candidate of level l before it in B,
+// so its rank in level l -- its slot, if below k -- is the number of level-l
+// entries of B before it.  Per level:
+//   children: every (B entry of level l with level rank s < k, c < k) gives
+//     candidate base + s k + c, value = parent value + w; it is kept (list Y)
+//     if it comes before B's last entry (or B is not yet full);
+//   merge: a Y entry's place in B u Y = (Y entries before it) + (B entries
+//     before it), a B entry's = its place + (Y entries before it), by
+//     counting; places below need form the new B, the Y entries with their
+//     level rank = the Y entries before them.
+// Node ids: 1 + the number of selected candidates of lower index.
 static __device__ __noinline__ void assemble_tree(const TreeJob J, StreamSmem& S) {
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int k = J.top_k, D = J.depth, m = J.total_tokens, C = J.n_cand;
-  const int R = 1 + (D - 1) * k;
   const int kk = k * k;
   const int rk = J.rec_k;
   const int rb = rec_bytes(rk);
+  const int need = m - 1;
   char* rows = J.rows;
   const eagle_tree out = J.out;
 
-  // scratch carved from the (now idle) ring and warp buffers; every array
-  // starts on a 16-byte boundary (<= 77 KB for C <= 2048; R k = C)
+  // scratch carved from the (now idle) ring; every array starts on a 16-byte
+  // boundary (about 32 C + 18 KB bytes)
   char* p = reinterpret_cast<char*>(S.ring);
   auto carve = [&p](size_t bytes) {
     char* q = p;
     p += align_up(bytes, 16);
     return q;
   };
-  uint64_t* key = reinterpret_cast<uint64_t*>(carve(sizeof(uint64_t) * C));  // value as order key
-  double* lse = reinterpret_cast<double*>(carve(sizeof(double) * R));
-  float* rv = reinterpret_cast<float*>(carve(sizeof(float) * C));   // row top-k logits
-  int* ri = reinterpret_cast<int*>(carve(sizeof(int) * C));         // row top-k tokens
+  double* w = reinterpret_cast<double*>(carve(sizeof(double) * C));      // logit - logsumexp
   int* tok = reinterpret_cast<int*>(carve(sizeof(int) * C));
-  int* par = reinterpret_cast<int*>(carve(sizeof(int) * C));
-  int* srt = reinterpret_cast<int*>(carve(sizeof(int) * C));    // candidates of each level, best first
-  int* lrank = reinterpret_cast<int*>(carve(sizeof(int) * C));  // rank of a candidate in its level
   int* node = reinterpret_cast<int*>(carve(sizeof(int) * C));
-  int* npar = reinterpret_cast<int*>(carve(sizeof(int) * EAGLE_MAX_TREE));
-  int* fr = reinterpret_cast<int*>(carve(sizeof(int) * 2 * kKMax));  // frontiers, by depth parity
-  int* warp_tot = reinterpret_cast<int*>(carve(sizeof(int) * EAGLE_MAX_DEPTH));
+  uint64_t* ykey = reinterpret_cast<uint64_t*>(carve(sizeof(uint64_t) * C));  // list Y
+  int* ycand = reinterpret_cast<int*>(carve(sizeof(int) * C));
+  int* ypar = reinterpret_cast<int*>(carve(sizeof(int) * C));
+  constexpr int T = EAGLE_MAX_TREE;
+  uint64_t* bkey = reinterpret_cast<uint64_t*>(carve(sizeof(uint64_t) * 2 * T));  // list B, x2
+  int* bcand = reinterpret_cast<int*>(carve(sizeof(int) * 2 * T));
+  int* bpar = reinterpret_cast<int*>(carve(sizeof(int) * 2 * T));
+  int* blr = reinterpret_cast<int*>(carve(sizeof(int) * 2 * T));   // level << 16 | level rank
+  int* npar = reinterpret_cast<int*>(carve(sizeof(int) * T));
+  int* ny = reinterpret_cast<int*>(carve(sizeof(int) * 2));        // |Y|, by level parity
 
-  // every row's statistics in one pass: logsumexp, top-k logits and tokens
-  for (int r = tid; r < R; r += kThreads) {
-    const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rows + r * rb);
-    lse[r] = static_cast<double>(h->max) + log_d(h->sum);
+  // every candidate's offset and token; level 1 (row 0's top-k, in order)
+  // is the first B
+  for (int a = tid; a < C; a += kThreads) {
+    const int r = a / k, c = a - r * k;
+    char* rec = rows + r * rb;
+    const double lse = __ldcg(&reinterpret_cast<const RecHead*>(rec)->sum);
+    const double wa = static_cast<double>(__ldcg(rec_val(rec) + c)) - lse;
+    w[a] = wa;
+    tok[a] = __ldcg(rec_idx(rec, rk) + c);
+    node[a] = 0;
+    if (a < k && a < need) {
+      bkey[a] = order_key(wa);
+      bcand[a] = a;
+      bpar[a] = -1;
+      blr[a] = (1 << 16) | a;
+    }
   }
-  for (int e = tid; e < C; e += kThreads) {
-    const int r = e / k, c = e - r * k;
-    rv[e] = __ldcg(rec_val(rows + r * rb) + c);
-    ri[e] = __ldcg(rec_idx(rows + r * rb, rk) + c);
-  }
+  if (tid < 2) ny[tid] = 0;
+  int nb = k < need ? k : need;   // |B|
+  int cur = 0;                    // which half of the B arrays holds it
   __syncthreads();
 
-  // Candidates are compared on (value desc, candidate index asc), values as
-  // order-preserving integer keys.  Level 1 = candidates 0..k-1 (the root's
-  // top_k, already in order); level j >= 2 = candidates k + (j-2) k^2 ..
-  // + k^2 - 1, ranked by counting with every thread of a warp reading the
-  // same keys (broadcast, no bank conflicts).
-  for (int c = tid; c < k; c += kThreads) {
-    key[c] = order_key(static_cast<double>(rv[c]) - lse[0]);
-    tok[c] = ri[c];
-    par[c] = -1;
-    fr[c] = c;
-    srt[c] = c;
-    lrank[c] = c;
-  }
-  __syncthreads();
-
-  // threads per candidate for the level ranks: a power of two <= 8
-  int tpc = kThreads / kk;
-  tpc = tpc >= 8 ? 8 : tpc >= 4 ? 4 : tpc >= 2 ? 2 : 1;
-  const int sub = tid & (tpc - 1);
-  const int stride = kThreads / tpc;
-  int base = k;   // first candidate of the level being built
-  for (int l = 1; l < D; ++l) {
-    const int* fcur = fr + ((l - 1) & 1) * kKMax;
-    int* fnext = fr + (l & 1) * kKMax;
-    for (int e = tid; e < kk; e += kThreads) {
-      const int s = e / k, c = e - s * k;
-      const int r = 1 + (l - 1) * k + s;
-      const int a = base + e;
-      const int pa = fcur[s];
-      key[a] = order_key(key_value(key[pa]) + (static_cast<double>(rv[r * k + c]) - lse[r]));
-      tok[a] = ri[r * k + c];
-      par[a] = pa;
+  for (int l = 1; l < D && need > 0; ++l) {
+    const int nbase = k + (l - 1) * kk;    // level l+1
+    const uint64_t* bk = bkey + cur * T;
+    const int* bc = bcand + cur * T;
+    const int* bl = blr + cur * T;
+    int* cnt_y = ny + (l & 1);
+    const bool full = nb == need;
+    const uint64_t tk = full ? bk[nb - 1] : 0ull;
+    const int tc = full ? bc[nb - 1] : 0;
+    // children of B's level-l entries of level rank < k that come before
+    // B's last entry
+    for (int t = tid; t < nb * k; t += kThreads) {
+      const int i = t / k, c = t - i * k;
+      const int lr = bl[i];
+      if ((lr >> 16) != l || (lr & 0xffff) >= k) continue;
+      const int a = nbase + (lr & 0xffff) * k + c;
+      const uint64_t kv = order_key(key_value(bk[i]) + w[a]);
+      if (full && !cand_before(kv, a, tk, tc)) continue;
+      const int y = atomicAdd(cnt_y, 1);
+      ykey[y] = kv;
+      ycand[y] = a;
+      ypar[y] = bc[i];
     }
     __syncthreads();
-    // full rank of every candidate within the level (tpc threads each)
-    const uint64_t* lk = key + base;
-    for (int e0 = 0; e0 < kk; e0 += stride) {
+    const int n_y = *cnt_y;
+    if (tid == 0) ny[(l + 1) & 1] = 0;     // the next level's counter
+    // merge: tpc threads per entry (a power of two), every thread of a warp
+    // reading the same list entries (broadcast)
+    const int ne = n_y + nb;
+    int tpc = ne > 0 ? kThreads / ne : 1;
+    tpc = tpc >= 8 ? 8 : tpc >= 4 ? 4 : tpc >= 2 ? 2 : 1;
+    const int sub = tid & (tpc - 1);
+    const int stride = kThreads / tpc;
+    uint64_t* nk = bkey + (cur ^ 1) * T;
+    int* nc = bcand + (cur ^ 1) * T;
+    int* np = bpar + (cur ^ 1) * T;
+    int* nl = blr + (cur ^ 1) * T;
+    const int* bp = bpar + cur * T;
+    for (int e0 = 0; e0 < ne; e0 += stride) {
       const int e = e0 + tid / tpc;
-      int cnt = 0;
-      if (e < kk) {
-        const uint64_t kv = lk[e];
-#pragma unroll 4
-        for (int f = sub; f < kk; f += tpc) {
-          const uint64_t o = lk[f];
-          cnt += ((o > kv) | ((o == kv) & (f < e))) ? 1 : 0;
+      uint64_t kv = 0;
+      int a = 0, before_y = 0, before_b = 0;
+      if (e < ne) {
+        kv = e < n_y ? ykey[e] : bk[e - n_y];
+        a = e < n_y ? ycand[e] : bc[e - n_y];
+        for (int f = sub; f < n_y; f += tpc) before_y += cand_before(ykey[f], ycand[f], kv, a) ? 1 : 0;
+        if (e < n_y)
+          for (int f = sub; f < nb; f += tpc) before_b += cand_before(bk[f], bc[f], kv, a) ? 1 : 0;
+      }
+      for (int o = tpc >> 1; o; o >>= 1) {
+        before_y += __shfl_xor_sync(0xffffffffu, before_y, o);
+        before_b += __shfl_xor_sync(0xffffffffu, before_b, o);
+      }
+      if (e < ne && sub == 0) {
+        if (e < n_y) {
+          const int pos = before_y + before_b;
+          if (pos < need) {
+            nk[pos] = kv;
+            nc[pos] = a;
+            np[pos] = ypar[e];
+            nl[pos] = ((l + 1) << 16) | before_y;
+          }
+        } else {
+          const int i = e - n_y;
+          const int pos = i + before_y;
+          if (pos < need) {
+            nk[pos] = kv;
+            nc[pos] = a;
+            np[pos] = bp[i];
+            nl[pos] = bl[i];
+          }
         }
       }
-      for (int o = tpc >> 1; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      if (e < kk && sub == 0) {
-        srt[base + cnt] = base + e;
-        lrank[base + e] = cnt;
-        if (cnt < k && l + 1 < D) fnext[cnt] = base + e;
-      }
     }
+    nb = nb + n_y < need ? nb + n_y : need;
+    cur ^= 1;
     __syncthreads();
-    base += kk;
   }
+  const uint64_t* sk = bkey + cur * T;   // the selected candidates, best first
+  const int* sel = bcand + cur * T;
+  const int* spar = bpar + cur * T;
+  if (tid == 0 && nb != (need > 0 ? need : 0)) record_error(J.err, kDevAssert, 10);
 
-  // final rerank: the best need = m-1 of the C candidates.  The global rank
-  // of a candidate is its rank in its own level plus, for every other level,
-  // the number of that level's entries before it (a binary search over the
-  // level's keys in sorted order, materialised over the row top-k scratch,
-  // which is no longer needed); it is kept if that rank is below need.
-  // Every candidate is ranked independently, all in parallel.
-  uint64_t* skey = reinterpret_cast<uint64_t*>(rv);   // rv and ri are contiguous: 8 C bytes
-  for (int i = tid; i < C; i += kThreads) skey[i] = key[srt[i]];
-  __syncthreads();
-  const int need = m - 1;
-  for (int a = tid; a < C; a += kThreads) {
-    const int la = a < k ? 0 : 1 + (a - k) / kk;
-    int rank = lrank[a];
-    const uint64_t kv = key[a];
-    for (int l = 0; l < D && rank < need; ++l) {
-      if (l == la) continue;
-      const int lb = l == 0 ? 0 : k + (l - 1) * kk;
-      int lo = 0, hi = l == 0 ? k : kk;   // entries of level l before (kv, a)
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        const uint64_t o = skey[lb + mid];
-        const bool go = (o > kv) | ((o == kv) & (srt[lb + mid] < a));
-        lo = go ? mid + 1 : lo;
-        hi = go ? hi : mid;
-      }
-      rank += lo;
-    }
-    node[a] = rank < need ? 1 : 0;
+  // node ids: selected candidates numbered 1.. in candidate order
+  for (int i = tid; i < nb; i += kThreads) {
+    const int a = sel[i];
+    int before_a = 0;
+    for (int q = 0; q < nb; ++q) before_a += sel[q] < a ? 1 : 0;
+    node[a] = 1 + before_a;
   }
   __syncthreads();
-  const int per = (C + kThreads - 1) / kThreads;
-  const int a0 = tid * per, a1 = min(C, a0 + per);
-  int cnt_local = 0;
-  for (int a = a0; a < a1; ++a) cnt_local += node[a];
-
-  // selection flags in candidate order -> node ids (1 + exclusive count)
-  int total = 0;
-  int off = block_excl_scan(cnt_local, warp_tot, total);
-  for (int a = a0; a < a1; ++a) {
-    if (node[a]) node[a] = 1 + off++;
-    else node[a] = 0;
-  }
-  __syncthreads();
-  if (tid == 0 && total != (need > 0 ? min(need, C) : 0)) record_error(J.err, kDevAssert, 10);
-  (void)lane;
 
   // node arrays
   if (tid == 0) {
@@ -225,23 +234,20 @@ static __device__ __noinline__ void assemble_tree(const TreeJob J, StreamSmem& S
     if (out.values) out.values[0] = 0.0;
     npar[0] = -1;
   }
-  for (int a = tid; a < C; a += kThreads) {
+  for (int i = tid; i < nb; i += kThreads) {
+    const int a = sel[i];
     const int n = node[a];
-    if (!n) continue;
     int pn = 0;
-    if (par[a] >= 0) {
-      pn = node[par[a]];
-      if (pn == 0) {
-        record_error(J.err, kDevAssert, 11);  // kept set not ancestor-closed
-        pn = 0;
-      }
+    if (spar[i] >= 0) {
+      pn = node[spar[i]];
+      if (pn == 0) record_error(J.err, kDevAssert, 11);  // kept set not ancestor-closed
     }
     const int dep = cand_depth(a, k);
     out.parents[n] = pn;
     out.tokens[n] = tok[a];
     out.depth[n] = dep;
     out.pos[n] = dep;
-    if (out.values) out.values[n] = key_value(key[a]);
+    if (out.values) out.values[n] = key_value(sk[i]);
     npar[n] = pn;
   }
   __syncthreads();
@@ -284,7 +290,7 @@ static __device__ __noinline__ void warm_assembly(char* warm, StreamSmem& S) {
   if (t < 3) {
     char* rec = rows + t * rb;
     RecHead* h = reinterpret_cast<RecHead*>(rec);
-    h->sum = 2.0;
+    h->sum = 1.0;   // stands for the row's logsumexp (any finite value)
     h->max = 0.f;
     h->count = kWarmK;
     rec_val(rec)[0] = 0.f;
@@ -314,18 +320,32 @@ static __device__ __noinline__ void warm_assembly(char* warm, StreamSmem& S) {
   assemble_tree(J, S);
 }
 
-// Grid: the rows' clusters, then one more cluster for the code warm-up.
+// Grid: the rows' clusters, then the clusters for the code warm-ups: (long
+// rows: stream_warm_up) one that streams the short warm-up row (see
+// warm_row_job), then one whose first CTA runs the tree assembly on its own
+// tree at launch.
 __global__ void __launch_bounds__(kThreads, 2) build_kernel(const __grid_constant__ BuildArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
-  const int64_t row_ctas =
-      static_cast<int64_t>(A.rs.n_items) * A.rs.rows_per_item * A.rs.ctas_per_row;
-  if (blockIdx.x >= row_ctas) {
-    if (blockIdx.x == row_ctas) warm_assembly(A.warm, S);
+  const int PC = A.rs.ctas_per_row;
+  const int64_t rows = static_cast<int64_t>(A.rs.n_items) * A.rs.rows_per_item;
+  const int64_t cl = blockIdx.x / PC;
+  const int rank = static_cast<int>(blockIdx.x - cl * PC);
+  if (cl >= rows + A.warm_stream) {
+    if (rank == 0) warm_assembly(A.warm, S);
     return;
   }
-  const RowCtx cx = stream_row(A.rs, S);
-  if (!cx.leader) return;
+  const bool warm = cl == rows;   // (only when warm_stream)
+  const RowJob R = warm ? warm_row_job(A.rs, A.swarm, rank) : row_job(A.rs, cl, rank);
+  const RowCtx cx = stream_row(R, S);
+  if (!cx.leader || warm) return;
+  // the row's logsumexp replaces the record's sum (the tree assembly needs
+  // only that; one fp64 log per row, here, in parallel over the rows).  The
+  // sum holds the max's own term 1, so its log is >= 0: kept so through the
+  // rounding of log_d, which makes every offset logit - logsumexp <= 0
+  if (threadIdx.x == 0)
+    reinterpret_cast<RecHead*>(R.rec)->sum =
+        static_cast<double>(S.rmax) + fmax(0.0, log_d(S.rsum));   // sum >= 1: log >= 0
   if (!item_arrive(A.rs, S, cx.item)) return;
   const int rb = rec_bytes(A.rs.rec_k);
   TreeJob J;
@@ -342,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 2) build_kernel(const __grid_constan
 }
 
 // tree assembly scratch (R = 1 + (depth-1) top_k <= 256 whenever C <= 2048)
-static_assert(kScratchBytes >= (8 + 4 * 7) * EAGLE_MAX_CANDIDATES + 8 * 256 +
-                                   4 * (EAGLE_MAX_TREE + 2 * kKMax + kWarps) + 16 * 16,
+static_assert(kScratchBytes >= (2 * 8 + 4 * 4) * EAGLE_MAX_CANDIDATES +
+                                   (2 * 8 + 3 * 2 * 4 + 4) * EAGLE_MAX_TREE + 16 * 16,
               "tree assembly scratch must fit in the stream's shared memory");
 
 static eagle_status build_impl(int32_t n_items, const float* const* logits, int64_t row_stride,
@@ -375,7 +395,7 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
   memset(&A, 0, sizeof(A));
   const int occ = stream_ctas_per_sm(build_kernel);
   if (occ <= 0) return EAGLE_ERR_CUDA;
-  const int ctas = stream_ctas_per_row(build_kernel, L, occ);
+  const int ctas = stream_ctas_per_row(build_kernel, L, occ, 2);
   if (ctas <= 0) return EAGLE_ERR_CUDA;
   fill_stream(A.rs, L, static_cast<char*>(ws), n_items, R, vocab, row_stride, ctas, false);
   for (int i = 0; i < n_items; ++i) {
@@ -391,7 +411,9 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
   A.total_tokens = total_tokens;
   A.n_cand = static_cast<int>(C);
   A.warm = static_cast<char*>(ws) + L.total;
-  return launch_stream(build_kernel, A, L.n_rows + 1, ctas, stream);
+  A.swarm = static_cast<char*>(ws) + L.off_warm;
+  A.warm_stream = stream_warm_up(L.tiles_per_row, ctas) ? 1 : 0;
+  return launch_stream(build_kernel, A, L.n_rows + 1 + A.warm_stream, ctas, stream);
 }
 
 // Scratch of the allocation-free entry point: fixed size, static device

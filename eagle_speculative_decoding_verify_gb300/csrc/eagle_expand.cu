@@ -148,7 +148,8 @@ static __device__ __noinline__ void expand_level(const ExpandArgs& A, StreamSmem
 __global__ void __launch_bounds__(kThreads, 2) expand_kernel(const __grid_constant__ ExpandArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
-  const RowCtx cx = stream_row(A.rs, S);
+  const int PC = A.rs.ctas_per_row;
+  const RowCtx cx = stream_row(row_job(A.rs, blockIdx.x / PC, static_cast<int>(blockIdx.x % PC)), S);
   if (!cx.leader) return;
   if (item_arrive(A.rs, S, cx.item)) expand_level(A, S);
 }

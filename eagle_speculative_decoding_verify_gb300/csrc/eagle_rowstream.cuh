@@ -43,7 +43,7 @@ namespace eagle {
 constexpr int kTile = 1024;                   // tokens per tile
 constexpr int kSlotTiles = 4;                 // tiles per ring slot
 constexpr int kSlotElems = kTile * kSlotTiles;  // 4096 floats = 16 KB
-constexpr int kSlots = 4;                     // ring depth
+constexpr int kSlots = 6;                     // ring depth
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVec = kSlotElems / kThreads / 4;  // float4 per thread per slot (4)
@@ -53,6 +53,7 @@ constexpr int kKMax = EAGLE_MAX_TOP_K;
 constexpr int kMaxItems = EAGLE_MAX_BATCH;
 constexpr int kMaxCluster = 8;                // CTAs per row
 constexpr int kTrackSlots = 64;               // slots per CTA with a recorded warp maximum
+constexpr int kCand = 5;                      // candidate slots per thread (second pass)
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { kWantSum = 1, kWantTileSums = 2 };
@@ -120,11 +121,13 @@ __device__ __forceinline__ Key warp_max_key(Key k) {
   return k;
 }
 
+static_assert(kKMax <= 127, "union_rank probes lists of at most 127 entries");
 static_assert(kWarps * kKMax >= kThreads, "the warp lists hold one key per thread (first-slot bound)");
 
 struct StreamSmem {
-  float ring[kSlots][kSlotElems];      // 64 KB; with wbuf reused by the final steps
-  Key wbuf[kWarps][kWarpCap];          // 16 KB warp survivor buffers
+  // 96 KB: the stream's ring; then (second pass) the warp survivor buffers,
+  // kWarpCap keys per warp at its start; then the callers' final steps
+  float ring[kSlots][kSlotElems];
   Key wlist[kWarps * kKMax];           // warp lists, stride K
   Key clist[kMaxCluster * kKMax];      // rank-0 CTA: the cluster's CTA lists, stride max(K, 1)
   Key rlist[kKMax];                    // rank-0 CTA: the row's list (best first)
@@ -148,8 +151,11 @@ struct StreamSmem {
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
 };
-// bytes of the contiguous region (ring + warp buffers) the final steps reuse
-constexpr size_t kScratchBytes = sizeof(float) * kSlots * kSlotElems + sizeof(Key) * kWarps * kWarpCap;
+// bytes of the region (the ring) the final steps reuse
+constexpr size_t kScratchBytes = sizeof(float) * kSlots * kSlotElems;
+static_assert(sizeof(Key) * kWarps * kWarpCap <= kScratchBytes, "warp buffers live in the ring");
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(2 * (sizeof(StreamSmem) + 1024) <= 228 * 1024, "two stream CTAs per SM");
 
 // ------------------------------------------------------------ cluster helpers
 __device__ __forceinline__ uint32_t map_rank0(const void* p) {
@@ -219,18 +225,23 @@ static __device__ __noinline__ int warp_select(const Key* buf, int n, int K, Key
   return n < K ? n : K;
 }
 
-// Rank of entry e in the union of nl <= 8 lists at stride `stride` with
-// counts cnt: the number of entries of all lists that come before it.  Every
-// thread of a warp reads the same entry at the same time (broadcast, no bank
-// conflicts); e itself never counts.
-__device__ __forceinline__ int union_rank(const Key* L, const int* cnt, int nl, int stride,
-                                          Key e) {
-  int r = 0;
+// Rank of entry c of list p in the union of nl <= 8 lists at stride
+// `stride` (each sorted best first, counts cnt, keys distinct): c plus, for
+// every other list, the length of its prefix of entries before it, found by
+// a branch-free binary search (7 probes: lists hold at most 64 entries).
+__device__ __forceinline__ int union_rank(const Key* L, const int* cnt, int nl, int stride, int p,
+                                          int c) {
+  const Key e = L[p * stride + c];
+  int r = c;
   for (int q = 0; q < nl; ++q) {
+    if (q == p) continue;
     const Key* lq = L + q * stride;
     const int n = cnt[q];
-#pragma unroll 4
-    for (int c = 0; c < n; ++c) r += lq[c] > e ? 1 : 0;
+    int pos = 0;   // entries of list q before e
+#pragma unroll
+    for (int s = 64; s; s >>= 1)
+      if (pos + s <= n && lq[pos + s - 1] > e) pos += s;
+    r += pos;
   }
   return r;
 }
@@ -277,28 +288,89 @@ struct RowCtx {
   bool leader;      // rank 0 of the row's cluster: holds the row result
 };
 
+// One cluster's row: where it is, what to compute, where the result goes.
+struct RowJob {
+  const float* src;   // the row's logits
+  char* rec;          // the row record
+  float2* tsums;      // the row's per-(tile, warp) sums (kWantTileSums)
+  int32_t* err;       // error word
+  int64_t row;        // global row (item * rows_per_item + row of the item)
+  int item, vocab, TR, PC, rank, K, flags, rec_k;
+  float c2;           // exp scale * log2(e)
+};
+
+// The job of CTA `rank` of the cluster that streams global row `row`.
+static __device__ __forceinline__ RowJob row_job(const RowStream& P, int64_t row, int rank) {
+  RowJob J;
+  J.row = row;
+  J.item = static_cast<int>(row / P.rows_per_item);
+  const int lrow = static_cast<int>(row - static_cast<int64_t>(J.item) * P.rows_per_item);
+  J.src = P.base[J.item] + lrow * P.row_stride;
+  J.rec = P.rows + row * rec_bytes(P.rec_k);
+  J.tsums = P.tile_sums ? P.tile_sums + row * P.tiles_per_row * kWarps : nullptr;
+  J.err = P.err;
+  J.vocab = P.vocab;
+  J.TR = P.tiles_per_row;
+  J.PC = P.ctas_per_row;
+  J.rank = rank;
+  J.K = P.topk[J.item];
+  J.flags = P.flags[J.item];
+  J.rec_k = P.rec_k;
+  J.c2 = P.exp_scale[J.item] * kLog2e;
+  return J;
+}
+
+// Code warm-up.  The code that runs once per row at its end (the CTA and row
+// merges, the callers' per-row and final steps) is not in L2 when the row's
+// data has just been flushed through it, and fetching it from HBM by the
+// leaders of every row at once costs several microseconds.  One extra
+// cluster streams a short row -- the first PC tiles of item 0's first row,
+// with item 0's statistics -- through the same code (same call sites) at
+// launch, with its results in a scratch area of its own (at `warm`: error
+// word, 16 bytes for the caller, the row record, tile sums of at most
+// kMaxCluster tiles; stream_warm_bytes), so that the code is in L2 when the
+// real rows reach it.  Only worth it when the rows are long enough for the
+// warm-up to run ahead of them (stream_warm_up); on short rows it would only
+// lengthen the launch.
+constexpr int kWarmMinTilesPerCta = 16;
+__host__ __device__ constexpr bool stream_warm_up(int tiles_per_row, int ctas_per_row) {
+  return tiles_per_row >= kWarmMinTilesPerCta * ctas_per_row;
+}
+__host__ __device__ constexpr size_t stream_warm_bytes(int rec_k, bool tile_sums) {
+  return 32 + static_cast<size_t>(rec_bytes(rec_k)) +
+         (tile_sums ? sizeof(float2) * kMaxCluster * kWarps : 0);
+}
+static __device__ __forceinline__ RowJob warm_row_job(const RowStream& P, char* warm, int rank) {
+  RowJob J = row_job(P, 0, rank);
+  J.vocab = min(P.vocab, P.ctas_per_row * kTile);
+  J.TR = (J.vocab + kTile - 1) / kTile;
+  J.err = reinterpret_cast<int32_t*>(warm);
+  J.rec = warm + 32;
+  J.tsums = J.tsums ? reinterpret_cast<float2*>(warm + 32 + rec_bytes(P.rec_k)) : nullptr;
+  return J;
+}
+
 // Streams this CTA's share of its row; on return the leader has written the
 // row record and holds it in S.rlist / rmax / rsum / rcount.  Every CTA of
 // the grid calls it exactly once (it contains cluster barriers).
-static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSmem& S) {
+static __device__ __forceinline__ RowCtx stream_row(const RowJob& Jb, StreamSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int PC = P.ctas_per_row;
+  const int PC = Jb.PC;
   RowCtx cx;
-  cx.row = blockIdx.x / PC;
-  const int rank = static_cast<int>(blockIdx.x - cx.row * PC);
+  cx.row = Jb.row;
+  const int rank = Jb.rank;
   cx.leader = rank == 0;
-  cx.item = static_cast<int>(cx.row / P.rows_per_item);
-  const int lrow = static_cast<int>(cx.row - static_cast<int64_t>(cx.item) * P.rows_per_item);
-  const float* src = P.base[cx.item] + lrow * P.row_stride;
-  const int TR = P.tiles_per_row;
+  cx.item = Jb.item;
+  const float* src = Jb.src;
+  const int TR = Jb.TR;
   const int tile0 = rank * TR / PC;
   const int e_begin = tile0 * kTile;
-  const int e_end = min(P.vocab, ((rank + 1) * TR / PC) * kTile);
+  const int e_end = min(Jb.vocab, ((rank + 1) * TR / PC) * kTile);
   const int n_el = e_end > e_begin ? e_end - e_begin : 0;
   const int n_slots = (n_el + kSlotElems - 1) / kSlotElems;
-  const int K = P.topk[cx.item];
-  const int flags = P.flags[cx.item];
-  const float c2 = P.exp_scale[cx.item] * kLog2e;
+  const int K = Jb.K;
+  const int flags = Jb.flags;
+  const float c2 = Jb.c2;
 
   auto issue = [&](int j) {  // thread 0: bulk copy of slot j
     const int off = j * kSlotElems;
@@ -327,19 +399,31 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
   cluster_arrive_relaxed();   // every CTA of the cluster has started (waited on at row end)
 
   float m_run = -INFINITY, s_run = 0.f;       // per-thread running max / sum
-  float tmax = -INFINITY;                      // per-thread maximum (K >= 2, first pass)
+  // K >= 2: this thread's kCand best slot maxima (cv, best first) and their
+  // slots (cs); a slot enters only with a larger maximum, so of equal maxima
+  // the earlier slot stays
+  float cv[kCand];
+  int cs[kCand];
+#pragma unroll
+  for (int r = 0; r < kCand; ++r) {
+    cv[r] = -INFINITY;
+    cs[r] = 0;
+  }
   float best_v = -INFINITY;                    // per-thread argmax (K == 1)
   int best_i = kNoIndex;
   float thr_v = INFINITY;                      // warp survivor bound (K >= 2): elements
   int thr_i = kNoIndex;                        // at or before (thr_v, thr_i)
   int wn = 0;                                  // entries in this warp's buffer
-  Key* wb = S.wbuf[warp];
+  // the warp's survivor buffer, in the ring: written only in the second pass,
+  // after the first pass's last CTA barrier (every thread has then read its
+  // last slot and no bulk copy is in flight)
+  Key* wb = reinterpret_cast<Key*>(S.ring) + warp * kWarpCap;
 
   for (int j = 0; j < n_slots; ++j) {
     const int b = j % kSlots;
     const uint32_t par = (j / kSlots) & 1;
     if (!mbar_wait(&S.full[b], par)) {
-      record_error(P.err, kDevTimeout, 1);
+      record_error(Jb.err, kDevTimeout, 1);
       mbar_wait(&S.full[b], par);  // give an in-flight copy a last chance to land
     }
     const int off = j * kSlotElems;
@@ -368,7 +452,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[b]);   // one arrival per warp
     if (tid == 0 && j + kSlots < n_slots) {    // refill once every warp has read the slot
-      if (!mbar_wait(&S.empty[b], par)) record_error(P.err, kDevTimeout, 2);
+      if (!mbar_wait(&S.empty[b], par)) record_error(Jb.err, kDevTimeout, 2);
       fence_proxy_async_smem();
       issue(j + kSlots);
     }
@@ -425,7 +509,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
 #pragma unroll
         for (int q = 0; q < kVec; ++q)
           if (q * kTile < nel)
-            P.tile_sums[(cx.row * TR + tile0 + j * kSlotTiles + q) * kWarps + warp] =
+            Jb.tsums[(tile0 + j * kSlotTiles + q) * kWarps + warp] =
                 make_float2(tm[q], ts[q]);
       }
     }
@@ -451,10 +535,22 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
     // maxima at or above it, by counting.  Values only: an element equal to
     // the bound survives whatever its token, which keeps a superset.
     if (K >= 2) {
-      tmax = fmaxf(tmax, lm);
+      {   // insert (lm, j): entry r takes entry r-1 if lm beats that, else lm if it beats r
+        bool g[kCand];
+#pragma unroll
+        for (int r = 0; r < kCand; ++r) g[r] = lm > cv[r];
+#pragma unroll
+        for (int r = kCand - 1; r > 0; --r) {
+          cv[r] = g[r - 1] ? cv[r - 1] : (g[r] ? lm : cv[r]);
+          cs[r] = g[r - 1] ? cs[r - 1] : (g[r] ? j : cs[r]);
+        }
+        cv[0] = g[0] ? lm : cv[0];
+        cs[0] = g[0] ? j : cs[0];
+      }
       const float wm = warp_max(lm);
       if (lane == 0 && j < kTrackSlots) S.wsmax[warp][j] = wm;
       if (j == n_slots - 1) {
+        const float tmax = cv[0];   // this thread's maximum
         const uint32_t c0 = tmax == -INFINITY ? 0u : fkey(tmax);
         const int q = (K + kWarps - 1) / kWarps;
         int ge = 0;
@@ -490,130 +586,161 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
     }
   }
 
-  // ---- second pass (K >= 2): only the warp-slots whose maximum reaches the
-  // bound can hold survivors (about K of the CTA's 8 x n_slots); each of
-  // those warps reloads its 512 elements of the slot, now from L2, with
-  // plain 16-byte loads in the ring's layout (slots past kTrackSlots have
-  // no recorded maximum and are always reloaded)
-  for (int j = 0; K >= 2 && j < n_slots; ++j) {
-    {
-      // the running bound: the best K-th entry any warp has cut to so far
-      const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
-      if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
-        thr_v = key_v(cb);
-        thr_i = key_i(cb);
-      }
-    }
-    const float wmax = j < kTrackSlots ? S.wsmax[warp][j] : INFINITY;
-    if (!(wmax >= thr_v)) continue;   // the same in every lane of the warp
-    const int off = j * kSlotElems;
-    int nel = n_el - off;
-    if (nel > kSlotElems) nel = kSlotElems;
-    const float* g0 = src + e_begin + off;
-    float x[kPer];
+  // ---- second pass (K >= 2): reload, now from L2, only what can hold
+  // survivors (elements at or before the bound).  Every survivor lies in a
+  // thread-slot (one thread's 16 elements of one slot) whose maximum reaches
+  // the bound, and a thread's kCand best slot maxima cover all its such slots
+  // unless the last of them reaches the bound as well.  So a warp none of whose
+  // threads is in that case reloads only its threads' qualifying candidate
+  // slots (about K thread-slots per CTA); otherwise it revisits every
+  // warp-slot whose recorded maximum reaches the bound, 512 elements each
+  // (slots past kTrackSlots have no recorded maximum and are always
+  // reloaded).
+  if (K >= 2) {
+    // this lane's 16 elements of slot j, in the ring's layout
+    auto load_slot = [&](int j, float (&x)[kPer]) {
+      const int off = j * kSlotElems;
+      int nel = n_el - off;
+      if (nel > kSlotElems) nel = kSlotElems;
+      const float* g0 = src + e_begin + off;
 #pragma unroll
-    for (int q = 0; q < kVec; ++q) {
-      const int e = (q * kThreads + tid) * 4;
-      float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      if (e + 4 <= nel) {
-        f = __ldcg(reinterpret_cast<const float4*>(g0 + e));
-      } else if (e < nel) {
-        const int avail = nel - e;
-        f.x = __ldcg(g0 + e);
-        if (avail > 1) f.y = __ldcg(g0 + e + 1);
-        if (avail > 2) f.z = __ldcg(g0 + e + 2);
-      }
-      x[4 * q + 0] = f.x;
-      x[4 * q + 1] = f.y;
-      x[4 * q + 2] = f.z;
-      x[4 * q + 3] = f.w;
-    }
-    const int tbase = e_begin + off + tid * 4;
-    float lm;
-    {
-      float m4[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) m4[a] = fmaxf(fmaxf(x[a], x[4 + a]), fmaxf(x[8 + a], x[12 + a]));
-      lm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    }
-    if (__any_sync(0xffffffffu, lm >= thr_v)) {
-      auto survives = [&](int e) {
-        const float xv = x[e];
-        const int xi = tbase + (e >> 2) * kTile + (e & 3);
-        return (xv != -INFINITY) & ((xv > thr_v) | ((xv == thr_v) & (xi <= thr_i)));
-      };
-      uint32_t pm = 0;
-      if (lm >= thr_v) {
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) pm |= survives(e) ? (1u << e) : 0u;
-      }
-      // common case: no lane holds more than one survivor.  A lone survivor
-      // has the lane maximum's value (any survivor of a lane whose maximum
-      // is above the bound is that maximum; at the bound all share its
-      // value); its token follows from its bit; positions from a ballot.
-      const unsigned one = __ballot_sync(0xffffffffu, pm != 0u);
-      if (__all_sync(0xffffffffu, (pm & (pm - 1u)) == 0u) && wn + __popc(one) <= kWarpCap) {
-        if (pm) {
-          const int e = __ffs(pm) - 1;
-          wb[wn + __popc(one & ((1u << lane) - 1u))] = mkkey(lm, tbase + (e >> 2) * kTile + (e & 3));
+      for (int q = 0; q < kVec; ++q) {
+        const int e = (q * kThreads + tid) * 4;
+        float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (e + 4 <= nel) {
+          f = __ldcg(reinterpret_cast<const float4*>(g0 + e));
+        } else if (e < nel) {
+          const int avail = nel - e;
+          f.x = __ldcg(g0 + e);
+          if (avail > 1) f.y = __ldcg(g0 + e + 1);
+          if (avail > 2) f.z = __ldcg(g0 + e + 2);
         }
-        wn += __popc(one);
-        __syncwarp();
-        pm = 0u;
+        x[4 * q + 0] = f.x;
+        x[4 * q + 1] = f.y;
+        x[4 * q + 2] = f.z;
+        x[4 * q + 3] = f.w;
       }
-      while (__any_sync(0xffffffffu, pm != 0u)) {
-        const int cntp = __popc(pm);
-        int incl = cntp;
+    };
+    // add this lane's survivors among x (tokens from tbase) to the warp buffer
+    auto absorb = [&](float (&x)[kPer], int tbase) {
+      float lm;
+      {
+        float m4[4];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        const bool fits = wn + total <= kWarpCap;
-        // append (all, or the first kWarpCap - wn in lane order)
-        int take = cntp;
-        if (!fits) take = max(0, min(cntp, kWarpCap - wn - (incl - cntp)));
-        int pos = wn + incl - cntp;
-        if (take) {
-          int taken = 0;
+        for (int a = 0; a < 4; ++a) m4[a] = fmaxf(fmaxf(x[a], x[4 + a]), fmaxf(x[8 + a], x[12 + a]));
+        lm = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
+      if (__any_sync(0xffffffffu, lm >= thr_v)) {
+        auto survives = [&](int e) {
+          const float xv = x[e];
+          const int xi = tbase + (e >> 2) * kTile + (e & 3);
+          return (xv != -INFINITY) & ((xv > thr_v) | ((xv == thr_v) & (xi <= thr_i)));
+        };
+        uint32_t pm = 0;
+        if (lm >= thr_v) {
 #pragma unroll
-          for (int e = 0; e < kPer; ++e)   // static indices keep x in registers
-            if (((pm >> e) & 1u) && taken < take) {
-              wb[pos++] = mkkey(x[e], tbase + (e >> 2) * kTile + (e & 3));
-              pm &= ~(1u << e);
-              ++taken;
-            }
+          for (int e = 0; e < kPer; ++e) pm |= survives(e) ? (1u << e) : 0u;
         }
-        __syncwarp();
-        if (fits) {
-          wn += total;
-          break;
+        // common case: no lane holds more than one survivor.  A lone survivor
+        // has the lane maximum's value (any survivor of a lane whose maximum
+        // is above the bound is that maximum; at the bound all share its
+        // value); its token follows from its bit; positions from a ballot.
+        const unsigned one = __ballot_sync(0xffffffffu, pm != 0u);
+        if (__all_sync(0xffffffffu, (pm & (pm - 1u)) == 0u) && wn + __popc(one) <= kWarpCap) {
+          if (pm) {
+            const int e = __ffs(pm) - 1;
+            wb[wn + __popc(one & ((1u << lane) - 1u))] = mkkey(lm, tbase + (e >> 2) * kTile + (e & 3));
+          }
+          wn += __popc(one);
+          __syncwarp();
+          pm = 0u;
         }
-        // buffer full: keep the best K, raise this warp's bound, drop what no
-        // longer survives, and go on with the rest of this slot
-        wn = warp_select(wb, kWarpCap, K, wb);
-        if (wn >= K && before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
+        while (__any_sync(0xffffffffu, pm != 0u)) {
+          const int cntp = __popc(pm);
+          int incl = cntp;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const int total = __shfl_sync(0xffffffffu, incl, 31);
+          const bool fits = wn + total <= kWarpCap;
+          // append (all, or the first kWarpCap - wn in lane order)
+          int take = cntp;
+          if (!fits) take = max(0, min(cntp, kWarpCap - wn - (incl - cntp)));
+          int pos = wn + incl - cntp;
+          if (take) {
+            int taken = 0;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e)   // static indices keep x in registers
+              if (((pm >> e) & 1u) && taken < take) {
+                wb[pos++] = mkkey(x[e], tbase + (e >> 2) * kTile + (e & 3));
+                pm &= ~(1u << e);
+                ++taken;
+              }
+          }
+          __syncwarp();
+          if (fits) {
+            wn += total;
+            break;
+          }
+          // buffer full: keep the best K, raise this warp's bound, drop what no
+          // longer survives, and go on with the rest of this slot
+          wn = warp_select(wb, kWarpCap, K, wb);
+          if (wn >= K && before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
+            thr_v = key_v(wb[K - 1]);
+            thr_i = key_i(wb[K - 1]);
+            if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
+          }
+          uint32_t keep = 0;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) keep |= survives(e) ? (1u << e) : 0u;
+          pm &= keep;
+          if (!__any_sync(0xffffffffu, pm != 0u)) break;
+        }
+      }
+      // keep the buffer short: past max(2K, 64) entries cut it to the best K,
+      // which raises this warp's bound and, through the shared running bound,
+      // every other warp's
+      if (wn > (2 * K > 64 ? 2 * K : 64)) {
+        wn = warp_select(wb, wn, K, wb);
+        if (before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
           thr_v = key_v(wb[K - 1]);
           thr_i = key_i(wb[K - 1]);
           if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
         }
-        uint32_t keep = 0;
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) keep |= survives(e) ? (1u << e) : 0u;
-        pm &= keep;
-        if (!__any_sync(0xffffffffu, pm != 0u)) break;
       }
-    }
-    // keep the buffer short: past max(2K, 64) entries cut it to the best K,
-    // which raises this warp's bound and, through the shared running bound,
-    // every other warp's
-    if (wn > (2 * K > 64 ? 2 * K : 64)) {
-      wn = warp_select(wb, wn, K, wb);
-      if (before(key_v(wb[K - 1]), key_i(wb[K - 1]), thr_v, thr_i)) {
-        thr_v = key_v(wb[K - 1]);
-        thr_i = key_i(wb[K - 1]);
-        if (lane == 0) atomicMax(&S.cta_bound, wb[K - 1]);
+    };
+    const bool over = cv[kCand - 1] != -INFINITY && cv[kCand - 1] >= thr_v;
+    if (!__any_sync(0xffffffffu, over)) {
+#pragma unroll
+      for (int r = 0; r < kCand; ++r) {
+        const bool q = cv[r] != -INFINITY && cv[r] >= thr_v;
+        if (!__any_sync(0xffffffffu, q)) break;
+        float x[kPer];
+        if (q) {
+          load_slot(cs[r], x);
+        } else {
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) x[e] = -INFINITY;
+        }
+        absorb(x, e_begin + cs[r] * kSlotElems + tid * 4);
+      }
+    } else {
+      for (int j = 0; j < n_slots; ++j) {
+        {
+          // the running bound: the best K-th entry any warp has cut to so far
+          const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
+          if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
+            thr_v = key_v(cb);
+            thr_i = key_i(cb);
+          }
+        }
+        const float wmax = j < kTrackSlots ? S.wsmax[warp][j] : INFINITY;
+        if (!(wmax >= thr_v)) continue;   // the same in every lane of the warp
+        float x[kPer];
+        load_slot(j, x);
+        absorb(x, e_begin + j * kSlotElems + tid * 4);
       }
     }
   }
@@ -651,7 +778,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
       const int w = e / K, c = e - w * K;
       if (c >= S.lcnt[w]) continue;
       const Key ent = S.wlist[e];
-      const int r = union_rank(S.wlist, S.lcnt, kWarps, K, ent);
+      const int r = union_rank(S.wlist, S.lcnt, kWarps, K, w, c);
       if (r < K) st_cluster(dst + 8u * static_cast<uint32_t>(r), ent);
     }
   }
@@ -688,8 +815,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
   if (!cx.leader) return cx;
 
   // ================================================================ row result (rank 0)
-  const int rb = rec_bytes(P.rec_k);
-  char* rec = P.rows + cx.row * rb;
+  char* rec = Jb.rec;
   if (K >= 2) {
     if (warp == 0) prune_lists(S.clist, S.ccnt, PC, K, K);
     __syncthreads();
@@ -697,11 +823,11 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
       const int p = e / K, c = e - p * K;
       if (c >= S.ccnt[p]) continue;
       const Key ent = S.clist[e];
-      const int r = union_rank(S.clist, S.ccnt, PC, K, ent);
+      const int r = union_rank(S.clist, S.ccnt, PC, K, p, c);
       if (r < K) {
         S.rlist[r] = ent;
         rec_val(rec)[r] = key_v(ent);
-        rec_idx(rec, P.rec_k)[r] = key_i(ent);
+        rec_idx(rec, Jb.rec_k)[r] = key_i(ent);
       }
     }
   }
@@ -723,7 +849,7 @@ static __device__ __forceinline__ RowCtx stream_row(const RowStream& P, StreamSm
       if (lane == 0) {
         S.rlist[0] = b;
         rec_val(rec)[0] = key_v(b);
-        rec_idx(rec, P.rec_k)[0] = key_i(b);
+        rec_idx(rec, Jb.rec_k)[0] = key_i(b);
       }
       cnt = 1;
     } else if (K >= 2) {

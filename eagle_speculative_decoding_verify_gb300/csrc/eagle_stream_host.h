@@ -11,11 +11,11 @@ struct StreamLayout {
   int64_t n_rows;       // rows of all items
   int tiles_per_row;
   int rec_k;
-  size_t off_item_cnt, off_rows, off_tiles, off_dec, total;
+  size_t off_item_cnt, off_rows, off_tiles, off_dec, off_warm, total;
 };
 
 // header | item counters | row records | per-(row, tile, warp) sums |
-// per-row decisions (verify)
+// per-row decisions (verify) | the code warm-up's scratch
 inline StreamLayout stream_layout(int n_items, int rows_per_item, int vocab, int rec_k,
                                   bool tile_sums, bool decisions) {
   StreamLayout L;
@@ -34,6 +34,9 @@ inline StreamLayout stream_layout(int n_items, int rows_per_item, int vocab, int
   off = align_up(off, 256);
   L.off_dec = off;
   if (decisions) off += sizeof(int2) * static_cast<size_t>(L.n_rows);
+  off = align_up(off, 256);
+  L.off_warm = off;
+  off += stream_warm_bytes(L.rec_k, tile_sums);
   L.total = align_up(off, 256);
   return L;
 }
@@ -69,11 +72,13 @@ inline cudaLaunchConfig_t stream_config(int64_t n_rows, int ctas, cudaStream_t s
 
 // CTAs per row (= cluster size): the largest size, at most kMaxCluster, at
 // most one CTA per tile and at most the GPU's CTA slots per row, for which
-// every row's cluster is resident at once (one wave); 1 when no size gives
-// one wave.  Returns 0 when the GPU cannot schedule the kernel at all.
+// every row's cluster and `extra` more clusters are resident at once (one
+// wave); 1 when no size gives one wave.  Returns 0 when the GPU cannot
+// schedule the kernel at all.
 template <typename Args>
-inline int stream_ctas_per_row(void (*kernel)(Args), const StreamLayout& L, int ctas_per_sm) {
-  const int64_t rows = L.n_rows > 0 ? L.n_rows : 1;
+inline int stream_ctas_per_row(void (*kernel)(Args), const StreamLayout& L, int ctas_per_sm,
+                               int extra = 0) {
+  const int64_t rows = (L.n_rows > 0 ? L.n_rows : 1) + extra;
   const int64_t slots = static_cast<int64_t>(sm_count()) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
   int64_t p = slots / rows;
   if (p > kMaxCluster) p = kMaxCluster;

@@ -46,6 +46,9 @@ struct VerifyArgs {
   int32_t* n_accepted;
   int32_t* bonus;
   int2* dec;                      // [rows] per-node decision: (accepted child or -1, bonus)
+  char* warm;                     // the stream code warm-up's scratch (stream_warm_bytes)
+  char* warm2;                    // the decision code warm-up's scratch (kDecisionWarmBytes)
+  int n_warm;                     // code warm-up clusters after the rows' (0 or 2)
 };
 
 __device__ __forceinline__ double warp_incl_scan_d(double v) {
@@ -64,24 +67,36 @@ __device__ __forceinline__ double full_prob(const float* lrow, int t, double row
   return exp_d((static_cast<double>(__ldg(lrow + t)) - rowmax) * invT) * inv_zsum;
 }
 
+// One node's decision: its row, its place in the tree, the sampling
+// parameters of its item, and where the decision goes.
+struct NodeJob {
+  const float* lrow;     // the node's target row
+  const float2* tsums;   // the row's per-(tile, warp) sums (full vocabulary)
+  int2* dec;             // out: (accepted child or -1, bonus)
+  double invT, top_p;
+  uint64_t seed, step;
+  float c2;              // 1/T * log2(e), the tile sums' exponent scale
+  int node, m, mode, K, TR, vocab;
+};
+
 // Decision of the walk at one node (warp 0 of the node's row leader): the
 // child accepted there (-1 if none) and the token emitted when the walk stops
 // there.  It depends only on the node's own row, its children and the
 // uniforms keyed by (seed, step, node, j), so every node decides on its own,
 // in parallel, and the item's final step follows the decisions from the root.
-static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t row, int item,
-                                                  StreamSmem& S) {
+// The tree (parents, tokens) is in S.aux.
+static __device__ __noinline__ void node_decision(const NodeJob& J, StreamSmem& S) {
   const int lane = threadIdx.x & 31;
-  const int m = A.m;
-  const int node = static_cast<int>(row - static_cast<int64_t>(item) * m);
-  const int mode = A.mode[item];
-  const double invT = A.inv_temperature[item];
-  const double top_p = static_cast<double>(A.top_p[item]);
-  const int K = A.top_k[item];
-  const uint64_t seed = A.seed[item];
+  const int m = J.m;
+  const int node = J.node;
+  const int mode = J.mode;
+  const double invT = J.invT;
+  const double top_p = J.top_p;
+  const int K = J.K;
+  const uint64_t seed = J.seed;
   const int* parents = S.aux;                   // prefetched at kernel start
   const int* tokens = S.aux + EAGLE_MAX_TREE;
-  const int TR = A.rs.tiles_per_row;
+  const int TR = J.TR;
 
   int* kn = reinterpret_cast<int*>(S.ring[0]);          // children (node ids), node order
   int* kt = kn + EAGLE_MAX_TREE;                         // their tokens
@@ -89,6 +104,8 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
   int* kid = reinterpret_cast<int*>(kp + kKMax);         // kept ids, by rank
   double* sp = reinterpret_cast<double*>(kid + kKMax);   // kept probabilities sorted by id
   int* sid = reinterpret_cast<int*>(sp + kKMax);
+  double* pc = reinterpret_cast<double*>(S.ring[2]);     // children probabilities (top-k mode)
+  int* krej = reinterpret_cast<int*>(pc + EAGLE_MAX_TREE);  // kept entry is a child's token
 
   // ---- the children of this node, in node order
   int nk = 0;
@@ -125,67 +142,75 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
     bonus = a;
   } else {
     // ---- the warped target distribution at this node
-    const float* lrow = A.rs.base[item] + static_cast<int64_t>(node) * A.rs.row_stride;
+    const float* lrow = J.lrow;
     double rowmax = 0.0, zsum = 1.0, izsum = 1.0;
     int nkeep = 0;
     if (mode == kModeTopK) {
+      // lane l holds the entries of rank 2l and 2l + 1: one scan of the pair
+      // sums gives every prefix mass and the total
       int cnt = S.rcount;
       if (cnt > K) cnt = K;
-      double z[2], pr[2];
-      int id[2];
+      const int ea = 2 * lane, eb = ea + 1;
       const double z0 = static_cast<double>(key_v(S.rlist[0])) * invT;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int e = lane + 32 * hh;
-        if (e < cnt) {
-          z[hh] = static_cast<double>(key_v(S.rlist[e])) * invT;
-          id[hh] = key_i(S.rlist[e]);
-          pr[hh] = exp_d(z[hh] - z0);
-        } else {
-          pr[hh] = 0.0;
-          id[hh] = kNoIndex;
-        }
+      double pa = 0.0, pb = 0.0;   // exp((z - z0)), unnormalised
+      int ia = kNoIndex, ib = kNoIndex;
+      if (ea < cnt) {
+        pa = exp_d(static_cast<double>(key_v(S.rlist[ea])) * invT - z0);
+        ia = key_i(S.rlist[ea]);
       }
-      const double itot = 1.0 / warp_sum_d(pr[0] + pr[1]);
-      pr[0] *= itot;
-      pr[1] *= itot;
+      if (eb < cnt) {
+        pb = exp_d(static_cast<double>(key_v(S.rlist[eb])) * invT - z0);
+        ib = key_i(S.rlist[eb]);
+      }
+      const double incl = warp_incl_scan_d(pa + pb);
+      double kept = __shfl_sync(0xffffffffu, incl, 31);
       nkeep = cnt;
       if (top_p < 1.0) {
         // entries are in probability order; keep the shortest prefix whose
-        // cumulative mass reaches top_p (the crossing entry included)
-        const double c0 = warp_incl_scan_d(pr[0]);
-        const double t0 = __shfl_sync(0xffffffffu, c0, 31);
-        const double c1 = warp_incl_scan_d(pr[1]) + t0;
-        const unsigned b0 = __ballot_sync(0xffffffffu, lane < cnt && c0 >= top_p);
-        const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < cnt && c1 >= top_p);
-        int last = cnt - 1;
-        if (b0) last = __ffs(b0) - 1;
-        else if (b1) last = 32 + __ffs(b1) - 1;
+        // normalised cumulative mass reaches top_p (the crossing entry included)
+        const double lim = top_p * kept;
+        const unsigned ba = __ballot_sync(0xffffffffu, ea < cnt && incl - pb >= lim);
+        const unsigned bb = __ballot_sync(0xffffffffu, eb < cnt && incl >= lim);
+        const int fa = ba ? 2 * (__ffs(ba) - 1) : cnt;
+        const int fb = bb ? 2 * (__ffs(bb) - 1) + 1 : cnt;
+        const int last = (fa < fb ? fa : fb) < cnt ? (fa < fb ? fa : fb) : cnt - 1;
         nkeep = last + 1;
-        if (lane > last) pr[0] = 0.0;
-        if (lane + 32 > last) pr[1] = 0.0;
-        const double itot2 = 1.0 / warp_sum_d(pr[0] + pr[1]);
-        pr[0] *= itot2;
-        pr[1] *= itot2;
+        const double at = __shfl_sync(0xffffffffu, (last & 1) ? incl : incl - pb, last >> 1);
+        kept = at;
       }
-      kp[lane] = pr[0];
-      kid[lane] = lane < nkeep ? id[0] : kNoIndex;
-      kp[lane + 32] = pr[1];
-      kid[lane + 32] = lane + 32 < nkeep ? id[1] : kNoIndex;
+      const double ik = 1.0 / kept;
+      const bool ka = ea < nkeep, kb = eb < nkeep;
+      kp[ea] = ka ? pa * ik : 0.0;
+      kid[ea] = ka ? ia : kNoIndex;
+      kp[eb] = kb ? pb * ik : 0.0;
+      kid[eb] = kb ? ib : kNoIndex;
+      // children probabilities: every kept entry looks for its token among
+      // the children (a child whose token is not kept has probability 0)
+      for (int j = lane; j < nk; j += 32) pc[j] = 0.0;
+      __syncwarp();
+      int ra = 0, rb = 0;
+      for (int r = 0; r < nk; ++r) {
+        const int t = kt[r];
+        if (ka && t == ia) {
+          pc[r] = pa * ik;
+          ra = 1;
+        }
+        if (kb && t == ib) {
+          pc[r] = pb * ik;
+          rb = 1;
+        }
+      }
+      krej[ea] = ra;
+      krej[eb] = rb;
       __syncwarp();
     } else {  // full vocabulary
       rowmax = static_cast<double>(S.rmax);
       zsum = S.rsum;
       izsum = 1.0 / zsum;
     }
-    auto prob_of = [&](int t) -> double {  // lane-local
-      if (mode == kModeTopK) {
-        double v = 0.0;
-        for (int e = 0; e < nkeep; ++e)
-          if (kid[e] == t) v = kp[e];
-        return v;
-      }
-      return full_prob(lrow, t, rowmax, invT, izsum);
+    auto prob_of = [&](int j) -> double {  // child j (lane-local)
+      if (mode == kModeTopK) return pc[j];
+      return full_prob(lrow, kt[j], rowmax, invT, izsum);
     };
 
     // ---- children in node order, 32 at a time: child j is accepted iff
@@ -195,10 +220,10 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
     for (int b = 0; b < nk && child < 0; b += 32) {
       const int j = b + lane;
       const bool valid = j < nk;
-      const double pt = valid ? prob_of(kt[j]) : 0.0;
+      const double pt = valid ? prob_of(j) : 0.0;
       const double incl = warp_incl_scan_d(pt);
       const double rho = rho_all + (incl - pt);
-      const double u = valid ? philox_uniform(seed, A.step, static_cast<uint32_t>(node),
+      const double u = valid ? philox_uniform(seed, J.step, static_cast<uint32_t>(node),
                                               static_cast<uint32_t>(j))
                              : 1.0;
       const unsigned bal = __ballot_sync(0xffffffffu, valid && (u * (1.0 - rho) < pt));
@@ -210,7 +235,7 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
       // ---- every child rejected (or a leaf): residual draw by inverse CDF
       // over ids ascending, the children's tokens removed
       const double thr =
-          philox_uniform(seed, A.step, static_cast<uint32_t>(node), kResidualChild) *
+          philox_uniform(seed, J.step, static_cast<uint32_t>(node), kResidualChild) *
           (1.0 - rho_all);
       auto is_rejected = [&](int t) {
         for (int r = 0; r < nk; ++r)
@@ -218,36 +243,42 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
         return false;
       };
       if (mode == kModeTopK) {
-        // kept entries sorted by token id (rank by counting)
+        // kept entries sorted by token id (rank by counting); the children's
+        // tokens (all rejected here) carry no mass
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int e = lane + 32 * hh;
+          const int e = 2 * lane + hh;
           if (e < nkeep) {
+            const int me = kid[e];
             int r = 0;
-            for (int f = 0; f < nkeep; ++f) r += kid[f] < kid[e] ? 1 : 0;
-            sid[r] = kid[e];
-            sp[r] = is_rejected(kid[e]) ? 0.0 : kp[e];
+            for (int f = 0; f < nkeep; ++f) r += kid[f] < me ? 1 : 0;
+            sid[r] = me;
+            sp[r] = krej[e] ? 0.0 : kp[e];
           }
         }
         __syncwarp();
-        int pick = -1, last = -1;
-        double cum = 0.0;
-        for (int hh = 0; hh < 2 && pick < 0; ++hh) {
-          const int r = lane + 32 * hh;
-          const double mass = r < nkeep ? sp[r] : 0.0;
-          const double incl = warp_incl_scan_d(mass) + cum;
-          const unsigned bal = __ballot_sync(0xffffffffu, r < nkeep && incl > thr);
-          if (bal) pick = 32 * hh + __ffs(bal) - 1;
-          const unsigned nz = __ballot_sync(0xffffffffu, r < nkeep && mass > 0.0);
-          if (nz) last = 32 * hh + 31 - __clz(nz);
-          cum = __shfl_sync(0xffffffffu, incl, 31);
+        // lane l holds sorted entries 2l and 2l + 1
+        const int ea = 2 * lane, eb = ea + 1;
+        const double ma = ea < nkeep ? sp[ea] : 0.0, mb = eb < nkeep ? sp[eb] : 0.0;
+        const double incl = warp_incl_scan_d(ma + mb);
+        const unsigned ba = __ballot_sync(0xffffffffu, ea < nkeep && incl - mb > thr);
+        const unsigned bb = __ballot_sync(0xffffffffu, eb < nkeep && incl > thr);
+        const int fa = ba ? 2 * (__ffs(ba) - 1) : kKMax;
+        const int fb = bb ? 2 * (__ffs(bb) - 1) + 1 : kKMax;
+        int pick = fa < fb ? fa : fb;
+        if (pick >= kKMax) {   // rounding: the last entry with mass
+          const unsigned nza = __ballot_sync(0xffffffffu, ea < nkeep && ma > 0.0);
+          const unsigned nzb = __ballot_sync(0xffffffffu, eb < nkeep && mb > 0.0);
+          const int la = nza ? 2 * (31 - __clz(nza)) : -1;
+          const int lb = nzb ? 2 * (31 - __clz(nzb)) + 1 : -1;
+          pick = la > lb ? la : lb;
+          if (pick < 0) pick = nkeep - 1;
         }
-        if (pick < 0) pick = last >= 0 ? last : nkeep - 1;
         bonus = sid[pick];
       } else {
         // tile masses (tile sums were taken relative to each tile's max)
-        const float2* ts = A.rs.tile_sums + row * TR * kWarps;
-        const double c2 = static_cast<double>(A.rs.exp_scale[item]) * 1.4426950408889634;
+        const float2* ts = J.tsums;
+        const double c2 = static_cast<double>(J.c2);
         double cum = 0.0;
         int tile = -1;
         double before_tile = 0.0;
@@ -291,7 +322,7 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
         for (int q = 0; q < 32; ++q) {
           const int t = v0 + q;
           double mass = 0.0;
-          if (t < A.rs.vocab && !is_rejected(t)) {
+          if (t < J.vocab && !is_rejected(t)) {
             const float x = __ldg(lrow + t);
             mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) * izsum;
           }
@@ -331,21 +362,42 @@ static __device__ __noinline__ void node_decision(const VerifyArgs& A, int64_t r
       }
     }
   }
-  if (lane == 0) A.dec[row] = make_int2(child, bonus);
+  if (lane == 0) *J.dec = make_int2(child, bonus);
   __syncwarp();
 }
 
-// The item's final step (warp 0 of the CTA whose row arrived last): follow
-// the decisions from the root.
-static __device__ __noinline__ void follow_path(const VerifyArgs& A, int item, StreamSmem& S) {
+// Warp 0 of a row leader, after its decision (written by lane 0): arrive on
+// the item's counter; true in the warp whose row arrives last.  Lane 0 wrote
+// the decision and performs the arrival itself, so the atomic's release
+// orders that write and its acquire (in the last arrival) makes every row's
+// decision visible to lane 0, and through the warp barrier to the warp.  The
+// last arrival resets the counter for the next launch.
+static __device__ __forceinline__ bool warp_item_arrive(const VerifyArgs& A, int item) {
   const int lane = threadIdx.x & 31;
-  const int m = A.m;
+  int last = 0;
+  if (lane == 0) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(A.rs.item_cnt + item)
+                 : "memory");
+    last = old == static_cast<uint32_t>(A.rs.rows_per_item - 1);
+    if (last) A.rs.item_cnt[item] = 0u;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  __syncwarp();
+  return last != 0;
+}
+
+// The item's final step (warp 0 of the CTA whose row arrived last): follow
+// the m decisions at `src` from the root into acc / n_acc / bonus.
+static __device__ __noinline__ void follow_path(const int2* src, int m, int32_t* acc,
+                                                int32_t* n_acc, int32_t* bonus, StreamSmem& S) {
+  const int lane = threadIdx.x & 31;
   int2* dec = reinterpret_cast<int2*>(S.ring[0]);
-  const int2* src = A.dec + static_cast<int64_t>(item) * m;
   for (int i = lane; i < m; i += 32) dec[i] = __ldcg(src + i);
   __syncwarp();
   if (lane == 0) {
-    int32_t* acc = A.accepted[item];
     int node = 0, n = 0;
     acc[0] = 0;
     for (int guard = 0; guard < m; ++guard) {
@@ -354,34 +406,125 @@ static __device__ __noinline__ void follow_path(const VerifyArgs& A, int item, S
       node = c;
       acc[++n] = node;
     }
-    A.n_accepted[item] = n;
-    A.bonus[item] = dec[node].y;
+    *n_acc = n;
+    *bonus = dec[node].y;
   }
   __syncwarp();
 }
 
+// Bytes of the decision code warm-up's scratch: decision, tile sums of one
+// tile, path outputs of a two-node tree.
+constexpr size_t kDecisionWarmBytes = 16 + sizeof(float2) * kWarps + 16;
+
+// The decision code warm-up (warp 0 of one CTA, at launch): node_decision
+// and follow_path on made-up inputs of item 0's mode -- the root of a
+// two-node tree, a row list of K entries with distinct tokens, item 0's
+// first row truncated to one tile for the full-vocabulary path, zero tile
+// sums -- with every output in its own scratch, so that their code is in L2
+// before the first real row reaches it (the L2 holds other data when a
+// verify step starts, and fetching the code from HBM after the row's stream
+// costs several microseconds).
+static __device__ __noinline__ void warm_decision(const VerifyArgs& A, StreamSmem& S) {
+  const int lane = threadIdx.x & 31;
+  char* w = A.warm2;
+  int2* dec = reinterpret_cast<int2*>(w);
+  float2* ts = reinterpret_cast<float2*>(w + 16);
+  int32_t* outs = reinterpret_cast<int32_t*>(w + 16 + sizeof(float2) * kWarps);
+  const int vocab = A.rs.vocab < kTile ? A.rs.vocab : kTile;
+  const int K = A.top_k[0];
+  if (lane < kWarps) ts[lane] = make_float2(0.f, 0.f);
+  for (int e = lane; e < kKMax; e += 32)
+    S.rlist[e] = e < K ? mkkey(-0.5f * static_cast<float>(e), (e * 7) % vocab) : 0ull;
+  if (lane == 0) {
+    S.aux[0] = -1;
+    S.aux[1] = 0;
+    S.aux[EAGLE_MAX_TREE] = 0;
+    S.aux[EAGLE_MAX_TREE + 1] = vocab - 1;
+    S.rcount = K > 1 ? K : 1;
+    S.rmax = 0.f;
+    S.rsum = 1.0;
+  }
+  __syncwarp();
+  NodeJob J;
+  J.lrow = A.rs.base[0];
+  J.tsums = ts;
+  J.dec = dec;
+  J.node = 0;
+  J.m = 2;
+  J.mode = A.mode[0];
+  J.K = K;
+  J.invT = A.inv_temperature[0];
+  J.top_p = static_cast<double>(A.top_p[0]);
+  J.seed = A.seed[0];
+  J.step = A.step;
+  J.c2 = A.rs.exp_scale[0] * kLog2e;
+  J.TR = 1;
+  J.vocab = vocab;
+  node_decision(J, S);
+  follow_path(dec, 1, outs, outs + 2, outs + 3, S);
+}
+
+// Grid: one cluster per row, then (long rows: stream_warm_up) two clusters
+// for the code warm-ups: the first streams the short warm-up row (see
+// warm_row_job) and decides node 0 of a two-node tree of its own on it,
+// stopping before the arrival; warp 0 of the first CTA of the second runs
+// warm_decision at launch.
 __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_constant__ VerifyArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
-  // the row leader's warp 0 prefetches its item's tree (parents, tokens)
-  // while the stream runs
   const int PC = A.rs.ctas_per_row;
-  if (blockIdx.x % PC == 0 && threadIdx.x < 32) {
-    const int item = static_cast<int>((blockIdx.x / PC) / A.m);
-    for (int i = threadIdx.x; i < A.m; i += 32) {
-      cp_async4(S.aux + i, A.parents[item] + i);
-      cp_async4(S.aux + EAGLE_MAX_TREE + i, A.tokens[item] + i);
+  const int64_t cl = blockIdx.x / PC;
+  const int rank = static_cast<int>(blockIdx.x - cl * PC);
+  const int64_t rows = static_cast<int64_t>(A.rs.n_items) * A.m;
+  if (cl > rows) {
+    if (rank == 0 && threadIdx.x < 32) warm_decision(A, S);
+    return;
+  }
+  const bool warm = cl == rows;
+  const RowJob R = warm ? warm_row_job(A.rs, A.warm, rank) : row_job(A.rs, cl, rank);
+  // the row leader's warp 0 prefetches its item's tree (parents, tokens)
+  // while the stream runs; the warm-up's tree is root -> one child
+  if (rank == 0 && threadIdx.x < 32) {
+    if (warm) {
+      if (threadIdx.x == 0) {
+        S.aux[0] = -1;
+        S.aux[1] = 0;
+        S.aux[EAGLE_MAX_TREE] = 0;
+        S.aux[EAGLE_MAX_TREE + 1] = R.vocab - 1;
+      }
+    } else {
+      for (int i = threadIdx.x; i < A.m; i += 32) {
+        cp_async4(S.aux + i, A.parents[R.item] + i);
+        cp_async4(S.aux + EAGLE_MAX_TREE + i, A.tokens[R.item] + i);
+      }
     }
     cp_async_commit();
   }
-  const RowCtx cx = stream_row(A.rs, S);
-  if (!cx.leader) return;
-  if (threadIdx.x < 32) {
-    cp_async_wait_all();
-    __syncwarp();
-    node_decision(A, cx.row, cx.item, S);
-  }
-  if (item_arrive(A.rs, S, cx.item) && threadIdx.x < 32) follow_path(A, cx.item, S);
+  const RowCtx cx = stream_row(R, S);
+  if (!cx.leader || threadIdx.x >= 32) return;   // warp 0 of the leader from here on
+  cp_async_wait_all();
+  __syncwarp();
+  NodeJob J;
+  const int item = cx.item;
+  J.lrow = R.src;
+  J.tsums = R.tsums;
+  J.node = warm ? 0 : static_cast<int>(cx.row - static_cast<int64_t>(item) * A.m);
+  J.m = warm ? 2 : A.m;
+  J.dec = warm ? reinterpret_cast<int2*>(A.warm + 16) : A.dec + cx.row;
+  J.mode = A.mode[item];
+  J.K = A.top_k[item];
+  J.invT = A.inv_temperature[item];
+  J.top_p = static_cast<double>(A.top_p[item]);
+  J.seed = A.seed[item];
+  J.step = A.step;
+  J.c2 = R.c2;
+  J.TR = R.TR;
+  J.vocab = R.vocab;
+  node_decision(J, S);
+  if (warm) return;
+  if (warp_item_arrive(A, item))
+    follow_path(A.dec + static_cast<int64_t>(item) * A.m, A.m, A.accepted[item],
+                A.n_accepted + item, A.bonus + item, S);
 }
 
 static eagle_status verify_impl(int32_t n_items, const float* const* logits, int64_t row_stride,
@@ -433,10 +576,10 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
   }
   (void)any_full;
   const StreamLayout L = stream_layout(n_items, m, vocab, kKMax, true, true);
-  if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < L.total + kDecisionWarmBytes) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
   const int occ = stream_ctas_per_sm(verify_kernel);
   if (occ <= 0) return EAGLE_ERR_CUDA;
-  const int ctas = stream_ctas_per_row(verify_kernel, L, occ);
+  const int ctas = stream_ctas_per_row(verify_kernel, L, occ, 2);
   if (ctas <= 0) return EAGLE_ERR_CUDA;
   fill_stream(A.rs, L, static_cast<char*>(ws), n_items, m, vocab, row_stride, ctas, true);
   A.m = m;
@@ -444,7 +587,10 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
   A.n_accepted = n_accepted;
   A.bonus = bonus;
   A.dec = reinterpret_cast<int2*>(static_cast<char*>(ws) + L.off_dec);
-  return launch_stream(verify_kernel, A, L.n_rows, ctas, stream);
+  A.warm = static_cast<char*>(ws) + L.off_warm;
+  A.warm2 = static_cast<char*>(ws) + L.total;
+  A.n_warm = stream_warm_up(L.tiles_per_row, ctas) ? 2 : 0;
+  return launch_stream(verify_kernel, A, L.n_rows + A.n_warm, ctas, stream);
 }
 
 }  // namespace eagle
@@ -453,7 +599,7 @@ using namespace eagle;
 
 extern "C" size_t eagle_tree_verify_workspace_size(int32_t n_items, int32_t m, int32_t vocab) {
   if (n_items < 1 || m < 1 || vocab < 1) return 0;
-  return stream_layout(n_items, m, vocab, kKMax, true, true).total;
+  return stream_layout(n_items, m, vocab, kKMax, true, true).total + kDecisionWarmBytes;
 }
 
 extern "C" eagle_status eagle_tree_verify(const float* target_logits, int64_t row_stride,
