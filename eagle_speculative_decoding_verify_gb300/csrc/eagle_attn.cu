@@ -49,6 +49,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 
 template <typename T>
 __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ AttnPlan P) {
+  pdl_trigger();   // let a dependent launch of the next kernel start (see pdl_attribute)
   extern __shared__ __align__(16) float simt_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int item = 0;
@@ -217,6 +218,7 @@ static size_t simt_smem_bytes(int d) {
 // Combine split partials: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s
 // (maxima are in log2 units).  One warp per (item, query row, q head).
 __global__ void __launch_bounds__(128) attn_merge_kernel(const __grid_constant__ AttnPlan P) {
+  pdl_trigger();   // let a dependent launch of the next kernel start (see pdl_attribute)
   const int lane = threadIdx.x & 31;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   int item = 0;

@@ -149,6 +149,7 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int
 
 template <int D, bool F8>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams P) {
+  pdl_trigger();   // let a dependent launch of the next kernel start (see pdl_attribute)
   using L = TcSmem<D, F8>;
   constexpr int kSlots = L::kSlotsT;
   extern __shared__ uint8_t smem_raw[];
@@ -629,6 +630,7 @@ static_assert(Sm2::kAlloc <= 232448, "shared memory of the 2-SM kernel");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
     attn2_kernel(const __grid_constant__ TcParams P) {
+  pdl_trigger();   // let a dependent launch of the next kernel start (see pdl_attribute)
   constexpr int D = 128;
   using L = Sm2;
   extern __shared__ uint8_t smem_raw[];
@@ -1063,6 +1065,7 @@ struct TcMergeParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcMergeParams P) {
+  pdl_trigger();   // let a dependent launch of the next kernel start (see pdl_attribute)
   __shared__ float tile[32][33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int item = 0;

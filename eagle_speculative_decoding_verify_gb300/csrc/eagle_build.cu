@@ -29,8 +29,6 @@ struct BuildArgs {
   int top_k, depth, total_tokens, n_cand;
   int root_token[kMaxItems];
   eagle_tree out[kMaxItems];
-  char* warm;   // kWarmBytes of workspace for the code warm-up's own tree
-  char* swarm;  // the stream's code warm-up (stream_warm_bytes)
   int warm_stream;  // 1: a stream code warm-up cluster follows the rows' (long rows)
 };
 
@@ -42,11 +40,13 @@ struct TreeJob {
   int rec_k, top_k, depth, total_tokens, n_cand, root_token;
 };
 
-// Workspace of the code warm-up: error word, 3 records of a top-2 row,
-// parents / tokens / depth / pos of 4 nodes, 4 mask words.
+// Scratch of the assembly's code warm-up (library-owned, see warm_row_job):
+// error word, 3 records of a top-2 row, parents / tokens / depth / pos of 4
+// nodes, 4 mask words.
 constexpr int kWarmK = 2;
 constexpr size_t kWarmBytes = 256;
-static_assert(16 + 3 * rec_bytes(kWarmK) + 4 * 16 + 8 * 4 <= kWarmBytes, "warm-up workspace");
+static_assert(16 + 3 * rec_bytes(kWarmK) + 4 * 16 + 8 * 4 <= kWarmBytes, "warm-up scratch");
+static __device__ __align__(16) char g_warm_tree[kWarmBytes];
 
 __device__ __forceinline__ int cand_depth(int a, int k) { return a < k ? 1 : 2 + (a - k) / (k * k); }
 
@@ -278,10 +278,12 @@ static __device__ __noinline__ void assemble_tree(const TreeJob J, StreamSmem& S
 // steps, after the target model's forward pass) each first use of a stretch
 // of its code is an instruction fetch from HBM, several microseconds in all.
 // The first CTA of one extra cluster runs the same function at launch, on a
-// tree of its own (three top-2 rows, depth 2, four nodes) in kWarmBytes of
-// workspace, so that the code is in L2 when the real assembly needs it.  It
-// reads and writes nothing else and has its own error word.
-static __device__ __noinline__ void warm_assembly(char* warm, StreamSmem& S) {
+// tree of its own (three top-2 rows, depth 2, four nodes) in the library's
+// g_warm_tree, so that the code is in L2 when the real assembly needs it.  It
+// reads and writes nothing else (no caller memory: it runs before the
+// launch's dependency wait) and has its own error word.
+static __device__ __noinline__ void warm_assembly(StreamSmem& S) {
+  char* warm = g_warm_tree;
   const int rb = rec_bytes(kWarmK);
   char* rows = warm + 16;
   int32_t* ints = reinterpret_cast<int32_t*>(rows + 3 * rb);
@@ -331,12 +333,14 @@ __global__ void __launch_bounds__(kThreads, 2) build_kernel(const __grid_constan
   const int64_t rows = static_cast<int64_t>(A.rs.n_items) * A.rs.rows_per_item;
   const int64_t cl = blockIdx.x / PC;
   const int rank = static_cast<int>(blockIdx.x - cl * PC);
+  pdl_trigger();
   if (cl >= rows + A.warm_stream) {
-    if (rank == 0) warm_assembly(A.warm, S);
+    if (rank == 0) warm_assembly(S);
     return;
   }
   const bool warm = cl == rows;   // (only when warm_stream)
-  const RowJob R = warm ? warm_row_job(A.rs, A.swarm, rank) : row_job(A.rs, cl, rank);
+  if (!warm) pdl_wait();          // the warm-ups touch no caller memory
+  const RowJob R = warm ? warm_row_job(A.rs, rank) : row_job(A.rs, cl, rank);
   const RowCtx cx = stream_row(R, S);
   if (!cx.leader || warm) return;
   // the row's logsumexp replaces the record's sum (the tree assembly needs
@@ -389,7 +393,7 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
     EAGLE_CHECK_ARG(t.m == total_tokens && t.mask_words == (total_tokens + 63) / 64);
   }
   const StreamLayout L = stream_layout(n_items, R, vocab, top_k, false, false);
-  if (ws_bytes < L.total + kWarmBytes) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
 
   BuildArgs A;
   memset(&A, 0, sizeof(A));
@@ -410,8 +414,6 @@ static eagle_status build_impl(int32_t n_items, const float* const* logits, int6
   A.depth = depth;
   A.total_tokens = total_tokens;
   A.n_cand = static_cast<int>(C);
-  A.warm = static_cast<char*>(ws) + L.total;
-  A.swarm = static_cast<char*>(ws) + L.off_warm;
   A.warm_stream = stream_warm_up(L.tiles_per_row, ctas) ? 1 : 0;
   return launch_stream(build_kernel, A, L.n_rows + 1 + A.warm_stream, ctas, stream);
 }
@@ -490,7 +492,7 @@ extern "C" size_t eagle_tree_build_workspace_size(int32_t n_items, int32_t n_row
   (void)total_tokens;
   if (n_items < 1 || vocab < 1 || top_k < 1 || depth < 1) return 0;
   const int R = 1 + (depth - 1) * top_k;
-  return stream_layout(n_items, R, vocab, top_k, false, false).total + kWarmBytes;
+  return stream_layout(n_items, R, vocab, top_k, false, false).total;
 }
 
 extern "C" eagle_status eagle_tree_build(const float* draft_logits, int64_t row_stride,
@@ -534,7 +536,7 @@ extern "C" eagle_status eagle_tree_build_noalloc(const float* draft_logits, int6
   EAGLE_CHECK_ARG(out.parents && out.tokens && out.depth && out.pos && out.mask);
   EAGLE_CHECK_ARG(out.m == total_tokens && out.mask_words == (total_tokens + 63) / 64);
   const StreamLayout L = stream_layout(1, R, vocab, top_k, false, false);
-  if (L.total + kWarmBytes > EAGLE_NOALLOC_SCRATCH_BYTES) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  if (L.total > EAGLE_NOALLOC_SCRATCH_BYTES) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   const eagle_status st = noalloc_scratch(&ws);
   if (st != EAGLE_OK) return st;

@@ -149,6 +149,8 @@ __global__ void __launch_bounds__(kThreads, 2) expand_kernel(const __grid_consta
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
   const int PC = A.rs.ctas_per_row;
+  pdl_trigger();
+  pdl_wait();
   const RowCtx cx = stream_row(row_job(A.rs, blockIdx.x / PC, static_cast<int>(blockIdx.x % PC)), S);
   if (!cx.leader) return;
   if (item_arrive(A.rs, S, cx.item)) expand_level(A, S);
@@ -177,6 +179,8 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const __grid_constan
   const int kk = k * k;
   const TreeState& T = A.st;
   const eagle_tree out = A.out;
+  pdl_trigger();   // one CTA
+  pdl_wait();
   if (*reinterpret_cast<volatile int*>(T.levels) != D) {   // not every depth expanded
     if (tid == 0) record_error(A.err, kDevAssert, 51);
     return;
@@ -347,6 +351,10 @@ extern "C" eagle_status eagle_tree_finalize(const void* state, int32_t top_k, in
   A.n_cand = static_cast<int>(C);
   A.root_token = root_token;
   A.err = static_cast<int32_t*>(ws);
-  finalize_kernel<<<1, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(A);
+  if (launch_pdl(finalize_kernel, dim3(1), dim3(kThreads), 0,
+                 reinterpret_cast<cudaStream_t>(stream), A) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return EAGLE_ERR_CUDA;
+  }
   return launch_status();
 }

@@ -39,6 +39,8 @@ struct KvParams {
 };
 
 __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(const __grid_constant__ KvParams P) {
+  pdl_trigger();   // dependent launch: see pdl_attribute
+  pdl_wait();
   const int item = blockIdx.x / P.n_kv_heads;
   const int h = blockIdx.x - item * P.n_kv_heads;
   const KvItem& it = P.items[item];
@@ -106,7 +108,8 @@ static eagle_status commit_impl(const eagle_kv_item* items, int32_t n_items, int
     P.n_kv_heads = n_kv_heads;
     P.row_bytes = static_cast<int>(row_bytes);
     P.err = static_cast<int32_t*>(ws);
-    kv_commit_kernel<<<static_cast<unsigned>(nb * n_kv_heads), kKvThreads, 0, stream>>>(P);
+    EAGLE_CUDA(launch_pdl(kv_commit_kernel, dim3(static_cast<unsigned>(nb * n_kv_heads)),
+                          dim3(kKvThreads), 0, stream, P));
     const eagle_status st = launch_status();
     if (st != EAGLE_OK) return st;
   }

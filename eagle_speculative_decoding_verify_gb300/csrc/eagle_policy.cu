@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(kThreads, 2) policy_kernel(const __grid_consta
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
   const int PC = A.rs.ctas_per_row;
+  pdl_trigger();
+  pdl_wait();
   const RowCtx cx = stream_row(row_job(A.rs, blockIdx.x / PC, static_cast<int>(blockIdx.x % PC)), S);
   if (!cx.leader) return;
   if (item_arrive(A.rs, S, cx.item)) assemble_policy(A, S);

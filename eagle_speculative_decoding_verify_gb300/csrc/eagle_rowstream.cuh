@@ -324,29 +324,38 @@ static __device__ __forceinline__ RowJob row_job(const RowStream& P, int64_t row
 // merges, the callers' per-row and final steps) is not in L2 when the row's
 // data has just been flushed through it, and fetching it from HBM by the
 // leaders of every row at once costs several microseconds.  One extra
-// cluster streams a short row -- the first PC tiles of item 0's first row,
-// with item 0's statistics -- through the same code (same call sites) at
-// launch, with its results in a scratch area of its own (at `warm`: error
-// word, 16 bytes for the caller, the row record, tile sums of at most
-// kMaxCluster tiles; stream_warm_bytes), so that the code is in L2 when the
-// real rows reach it.  Only worth it when the rows are long enough for the
-// warm-up to run ahead of them (stream_warm_up); on short rows it would only
-// lengthen the launch.
+// cluster streams a short row of its own through the same code (same call
+// sites) at launch, so that the code is in L2 when the real rows reach it.
+// Only worth it when the rows are long enough for the warm-up to run ahead of
+// them (stream_warm_up); on short rows it would only lengthen the launch.
+//
+// The warm-up reads and writes only library-owned static memory, never the
+// caller's buffers, so that it may run before the launch's dependency on
+// the previous kernel is resolved (pdl_wait): its row is one tile per CTA of
+// g_warm_row, written by that CTA (a descending ramp); its record, tile sums
+// and error word go to g_warm_out.  Launches that overlap write the same
+// values or outputs nothing reads.
 constexpr int kWarmMinTilesPerCta = 16;
 __host__ __device__ constexpr bool stream_warm_up(int tiles_per_row, int ctas_per_row) {
   return tiles_per_row >= kWarmMinTilesPerCta * ctas_per_row;
 }
-__host__ __device__ constexpr size_t stream_warm_bytes(int rec_k, bool tile_sums) {
-  return 32 + static_cast<size_t>(rec_bytes(rec_k)) +
-         (tile_sums ? sizeof(float2) * kMaxCluster * kWarps : 0);
-}
-static __device__ __forceinline__ RowJob warm_row_job(const RowStream& P, char* warm, int rank) {
+static __device__ __align__(16) float g_warm_row[kMaxCluster * kTile];
+static __device__ __align__(16) char g_warm_out[32 + rec_bytes(kKMax) + sizeof(float2) * kMaxCluster * kWarps];
+
+// CTA `rank` of the warm-up cluster: writes its tile of the warm-up row, and
+// returns its job (item 0's statistics, the cluster's PC tiles).
+static __device__ __forceinline__ RowJob warm_row_job(const RowStream& P, int rank) {
   RowJob J = row_job(P, 0, rank);
-  J.vocab = min(P.vocab, P.ctas_per_row * kTile);
-  J.TR = (J.vocab + kTile - 1) / kTile;
-  J.err = reinterpret_cast<int32_t*>(warm);
-  J.rec = warm + 32;
-  J.tsums = J.tsums ? reinterpret_cast<float2*>(warm + 32 + rec_bytes(P.rec_k)) : nullptr;
+  for (int i = threadIdx.x; i < kTile; i += kThreads)
+    g_warm_row[rank * kTile + i] = -static_cast<float>(rank * kTile + i) * (1.0f / 1024.0f);
+  fence_proxy_async_global();   // generic writes, then bulk-copy reads of them
+  __syncthreads();
+  J.src = g_warm_row;
+  J.vocab = P.ctas_per_row * kTile;
+  J.TR = P.ctas_per_row;
+  J.err = reinterpret_cast<int32_t*>(g_warm_out);
+  J.rec = g_warm_out + 32;
+  J.tsums = J.tsums ? reinterpret_cast<float2*>(g_warm_out + 32 + rec_bytes(kKMax)) : nullptr;
   return J;
 }
 

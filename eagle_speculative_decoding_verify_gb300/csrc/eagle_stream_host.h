@@ -11,11 +11,11 @@ struct StreamLayout {
   int64_t n_rows;       // rows of all items
   int tiles_per_row;
   int rec_k;
-  size_t off_item_cnt, off_rows, off_tiles, off_dec, off_warm, total;
+  size_t off_item_cnt, off_rows, off_tiles, off_dec, total;
 };
 
 // header | item counters | row records | per-(row, tile, warp) sums |
-// per-row decisions (verify) | the code warm-up's scratch
+// per-row decisions (verify)
 inline StreamLayout stream_layout(int n_items, int rows_per_item, int vocab, int rec_k,
                                   bool tile_sums, bool decisions) {
   StreamLayout L;
@@ -34,9 +34,6 @@ inline StreamLayout stream_layout(int n_items, int rows_per_item, int vocab, int
   off = align_up(off, 256);
   L.off_dec = off;
   if (decisions) off += sizeof(int2) * static_cast<size_t>(L.n_rows);
-  off = align_up(off, 256);
-  L.off_warm = off;
-  off += stream_warm_bytes(L.rec_k, tile_sums);
   L.total = align_up(off, 256);
   return L;
 }
@@ -54,6 +51,7 @@ inline int stream_ctas_per_sm(void (*kernel)(Args)) {
   return occ;
 }
 
+// attr: room for two attributes (cluster size; dependent launch)
 inline cudaLaunchConfig_t stream_config(int64_t n_rows, int ctas, cudaStream_t stream,
                                         cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -65,8 +63,9 @@ inline cudaLaunchConfig_t stream_config(int64_t n_rows, int ctas, cudaStream_t s
   attr[0].val.clusterDim.x = static_cast<unsigned>(ctas);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  pdl_attribute(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
@@ -86,7 +85,7 @@ inline int stream_ctas_per_row(void (*kernel)(Args), const StreamLayout& L, int 
   if (p < 1) p = 1;
   bool any = false;
   for (int c = static_cast<int>(p); c >= 1; --c) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = stream_config(c, c, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
@@ -118,7 +117,7 @@ inline void fill_stream(RowStream& rs, const StreamLayout& L, char* ws, int n_it
 template <typename Args>
 inline eagle_status launch_stream(void (*kernel)(Args), const Args& A, int64_t n_rows, int ctas,
                                   cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = stream_config(n_rows, ctas, stream, attr);
   if (cudaLaunchKernelEx(&cfg, kernel, A) != cudaSuccess) {
     (void)cudaGetLastError();

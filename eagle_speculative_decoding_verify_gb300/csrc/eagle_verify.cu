@@ -46,8 +46,6 @@ struct VerifyArgs {
   int32_t* n_accepted;
   int32_t* bonus;
   int2* dec;                      // [rows] per-node decision: (accepted child or -1, bonus)
-  char* warm;                     // the stream code warm-up's scratch (stream_warm_bytes)
-  char* warm2;                    // the decision code warm-up's scratch (kDecisionWarmBytes)
   int n_warm;                     // code warm-up clusters after the rows' (0 or 2)
 };
 
@@ -412,25 +410,26 @@ static __device__ __noinline__ void follow_path(const int2* src, int m, int32_t*
   __syncwarp();
 }
 
-// Bytes of the decision code warm-up's scratch: decision, tile sums of one
-// tile, path outputs of a two-node tree.
+// The decision code warm-up's scratch (library-owned, see warm_row_job):
+// decision, tile sums of one tile, path outputs of a two-node tree.
 constexpr size_t kDecisionWarmBytes = 16 + sizeof(float2) * kWarps + 16;
+static __device__ __align__(16) char g_warm_decision[kDecisionWarmBytes];
 
 // The decision code warm-up (warp 0 of one CTA, at launch): node_decision
 // and follow_path on made-up inputs of item 0's mode -- the root of a
-// two-node tree, a row list of K entries with distinct tokens, item 0's
-// first row truncated to one tile for the full-vocabulary path, zero tile
-// sums -- with every output in its own scratch, so that their code is in L2
-// before the first real row reaches it (the L2 holds other data when a
-// verify step starts, and fetching the code from HBM after the row's stream
-// costs several microseconds).
+// two-node tree, a row list of K entries with distinct tokens, the first tile
+// of the stream warm-up's row (g_warm_row) for the full-vocabulary path,
+// zero tile sums -- with every output in g_warm_decision, so that their code
+// is in L2 before the first real row reaches it (the L2 holds other data when
+// a verify step starts, and fetching the code from HBM after the row's
+// stream costs several microseconds).  It touches no caller memory.
 static __device__ __noinline__ void warm_decision(const VerifyArgs& A, StreamSmem& S) {
   const int lane = threadIdx.x & 31;
-  char* w = A.warm2;
+  char* w = g_warm_decision;
   int2* dec = reinterpret_cast<int2*>(w);
   float2* ts = reinterpret_cast<float2*>(w + 16);
   int32_t* outs = reinterpret_cast<int32_t*>(w + 16 + sizeof(float2) * kWarps);
-  const int vocab = A.rs.vocab < kTile ? A.rs.vocab : kTile;
+  const int vocab = kTile;
   const int K = A.top_k[0];
   if (lane < kWarps) ts[lane] = make_float2(0.f, 0.f);
   for (int e = lane; e < kKMax; e += 32)
@@ -446,7 +445,7 @@ static __device__ __noinline__ void warm_decision(const VerifyArgs& A, StreamSme
   }
   __syncwarp();
   NodeJob J;
-  J.lrow = A.rs.base[0];
+  J.lrow = g_warm_row;
   J.tsums = ts;
   J.dec = dec;
   J.node = 0;
@@ -476,12 +475,14 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_consta
   const int64_t cl = blockIdx.x / PC;
   const int rank = static_cast<int>(blockIdx.x - cl * PC);
   const int64_t rows = static_cast<int64_t>(A.rs.n_items) * A.m;
+  pdl_trigger();
   if (cl > rows) {
     if (rank == 0 && threadIdx.x < 32) warm_decision(A, S);
     return;
   }
   const bool warm = cl == rows;
-  const RowJob R = warm ? warm_row_job(A.rs, A.warm, rank) : row_job(A.rs, cl, rank);
+  if (!warm) pdl_wait();          // the warm-ups touch no caller memory
+  const RowJob R = warm ? warm_row_job(A.rs, rank) : row_job(A.rs, cl, rank);
   // the row leader's warp 0 prefetches its item's tree (parents, tokens)
   // while the stream runs; the warm-up's tree is root -> one child
   if (rank == 0 && threadIdx.x < 32) {
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_consta
   J.tsums = R.tsums;
   J.node = warm ? 0 : static_cast<int>(cx.row - static_cast<int64_t>(item) * A.m);
   J.m = warm ? 2 : A.m;
-  J.dec = warm ? reinterpret_cast<int2*>(A.warm + 16) : A.dec + cx.row;
+  J.dec = warm ? reinterpret_cast<int2*>(g_warm_decision) : A.dec + cx.row;
   J.mode = A.mode[item];
   J.K = A.top_k[item];
   J.invT = A.inv_temperature[item];
@@ -576,7 +577,7 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
   }
   (void)any_full;
   const StreamLayout L = stream_layout(n_items, m, vocab, kKMax, true, true);
-  if (ws_bytes < L.total + kDecisionWarmBytes) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
   const int occ = stream_ctas_per_sm(verify_kernel);
   if (occ <= 0) return EAGLE_ERR_CUDA;
   const int ctas = stream_ctas_per_row(verify_kernel, L, occ, 2);
@@ -587,8 +588,6 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
   A.n_accepted = n_accepted;
   A.bonus = bonus;
   A.dec = reinterpret_cast<int2*>(static_cast<char*>(ws) + L.off_dec);
-  A.warm = static_cast<char*>(ws) + L.off_warm;
-  A.warm2 = static_cast<char*>(ws) + L.total;
   A.n_warm = stream_warm_up(L.tiles_per_row, ctas) ? 2 : 0;
   return launch_stream(verify_kernel, A, L.n_rows + A.n_warm, ctas, stream);
 }
@@ -599,7 +598,7 @@ using namespace eagle;
 
 extern "C" size_t eagle_tree_verify_workspace_size(int32_t n_items, int32_t m, int32_t vocab) {
   if (n_items < 1 || m < 1 || vocab < 1) return 0;
-  return stream_layout(n_items, m, vocab, kKMax, true, true).total + kDecisionWarmBytes;
+  return stream_layout(n_items, m, vocab, kKMax, true, true).total;
 }
 
 extern "C" eagle_status eagle_tree_verify(const float* target_logits, int64_t row_stride,
