@@ -605,6 +605,41 @@ def tree_expand_bench(eb, wl, dev, step, s, flush, reps=50):
             "note": "L2 flushed before each round; rows of every depth from HBM"}
 
 
+def verify_nucleus_bench(eb, wl, dev, step, s, flush, reps=50):
+    """The step's verify with the nucleus over the whole vocabulary (T 0.7,
+    top_p 0.9, no top_k) instead of top_k 50: one call, replayed from a CUDA
+    graph with L2 flushed before every call, beside the same call with the
+    workload's own sampling."""
+    import torch
+    out = {}
+    for name, params in (("nucleus", eb.sampling(False, 0.7, 0, 0.9)), ("workload", step.params)):
+        def call():
+            eb.eagle_tree_verify(step.target, step.tree, params, 1234, 0, accepted=step.acc,
+                                 n_accepted=step.n_acc, bonus_token=step.bonus, ws=step.ws_verify,
+                                 stream=s)
+
+        for _ in range(3):
+            call()
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            call()
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            graph.replay()
+            e1.record(s)
+            s.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        assert eb.workspace_error(step.ws_verify, s)[0] == 0, "verify recorded a device error"
+        out[name + "_us"] = round(statistics.median(times), 2)
+    out["sampling"] = "nucleus: T 0.7, top_k 0, top_p 0.9; workload: T 0.7, top_k 50, top_p 0.9"
+    out["note"] = "L2 flushed before each call; one launch per call"
+    return out
+
+
 def tree_policy_bench(eb, wl, dev, step, s, flush, reps=50):
     """The tree-shape policies on the step's draft logits (51 rows of the
     vocabulary): the confidence-ratio tree (tau 2, up to 4 branches, depth <= 7,
@@ -886,6 +921,7 @@ def run_ours(args, rank, world, local_rank):
         line["kv_commit"] = kv_commit_bench(eb, wl, dev, step, s)
         line["tree_expand"] = tree_expand_bench(eb, wl, dev, step, s, flush)
         line["tree_policy"] = tree_policy_bench(eb, wl, dev, step, s, flush)
+        line["verify_nucleus"] = verify_nucleus_bench(eb, wl, dev, step, s, flush)
     if not args.no_long_attn:
         la = attn_long(eb, wl, dev)
         la["frac_hbm"] = round(la["achieved_gbs"] / hbm, 4)

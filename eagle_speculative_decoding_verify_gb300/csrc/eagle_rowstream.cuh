@@ -148,6 +148,8 @@ struct StreamSmem {
   float wsmax[kWarps][kTrackSlots];    // first pass: every warp's maximum of every slot
   Key cta_bound;                       // running bound: K-th best of the CTA so far
   int aux[2 * EAGLE_MAX_TREE];         // callers' own data (never touched by the stream)
+  unsigned long long aux_key;          // (callers' own)
+  double aux_d;                        // (callers' own)
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
 };

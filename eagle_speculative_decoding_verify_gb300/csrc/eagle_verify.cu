@@ -29,7 +29,7 @@
 
 namespace eagle {
 
-enum : int { kModeGreedy = 0, kModeTopK = 1, kModeFull = 2 };
+enum : int { kModeGreedy = 0, kModeTopK = 1, kModeFull = 2, kModeNucleus = 3 };
 
 struct VerifyArgs {
   RowStream rs;
@@ -59,10 +59,319 @@ __device__ __forceinline__ double warp_incl_scan_d(double v) {
   return v;
 }
 
-// p(t) under the full-vocabulary target distribution (lane-local).
-__device__ __forceinline__ double full_prob(const float* lrow, int t, double rowmax, double invT,
-                                            double inv_zsum) {
-  return exp_d((static_cast<double>(__ldg(lrow + t)) - rowmax) * invT) * inv_zsum;
+// ------------------------------------------------ nucleus over the vocabulary
+// (top_p < 1 without top_k).  The kept set is the shortest prefix of the
+// row in (probability desc, token asc) order -- the order of the 64-bit keys
+// mkkey(logit, token), larger first -- whose mass reaches top_p of the total,
+// the crossing token included.  Masses are exp((x - max) / T) as fixed-point
+// integers, units of 2^-31 of the max's, summed exactly in 64 bits, so sums
+// do not depend on their order.  The crossing token is found by bins of u = log2 of
+// the max's mass over the token's, (max - x) c2 >= 0, which is monotone in
+// the logit: 32 bins per unit of u, then 1024 sub-bins of the crossing bin,
+// then the crossing sub-bin's tokens (few unless many share a logit) ranked
+// by their keys; more than kNucCap of them are resolved by a radix select on
+// the key, 8 bits per pass.  All warps of the row's leader CTA, over the row
+// in L2 (the stream has just read it); the ring is their scratch.  Results:
+// S.aux_key = the crossing key (kept iff key >= it), S.aux_d = the kept mass
+// in units of the max's; per-tile kept masses at ring byte offset kNucTiles
+// (read by the residual draw).
+constexpr size_t kNucTiles = 65536;                  // u64 [tiles], after the histograms
+constexpr size_t kNucScratch = kScratchBytes - 128;  // the searches' scratch, at the ring's end
+constexpr int kNucMaxTiles = static_cast<int>((kNucScratch - kNucTiles) / 8);
+constexpr int kNucBins = 1024;                       // per warp, per level
+constexpr int kNucCap = 1024;                        // tokens ranked exactly
+constexpr float kQUnit = 2147483648.0f;              // 2^31: a token's mass fits 32 bits
+
+// Bin b of H[0..nb) (nb = kThreads * per, all threads) with above(b) < t <=
+// above(b) + H[b], above(b) = sum of H over the bins before b (bin 0 first);
+// scratch[kWarps] = b, scratch[kWarps + 1] = above(b), scratch[kWarps + 2] =
+// sum of H.
+static __device__ __forceinline__ void find_cut_bin(const unsigned long long* H, int nb, double t,
+                                                    unsigned long long* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = nb / kThreads;
+  const int lo = tid * per;   // this thread's bins [lo, lo + per)
+  unsigned long long cs = 0;
+  for (int b = lo; b < lo + per; ++b) cs += H[b];
+  unsigned long long incl = cs;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  if (tid == 0) {
+    scratch[kWarps] = static_cast<unsigned long long>(nb - 1);
+    scratch[kWarps + 1] = 0;
+  }
+  __syncthreads();
+  unsigned long long wbase = 0, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) wbase += scratch[w];
+    total += scratch[w];
+  }
+  const unsigned long long above = wbase + incl - cs;
+  if (cs > 0 && static_cast<double>(above) < t && t <= static_cast<double>(above + cs)) {
+    unsigned long long acc = above;
+    for (int b = lo; b < lo + per; ++b) {
+      if (H[b] > 0 && static_cast<double>(acc + H[b]) >= t) {
+        scratch[kWarps] = static_cast<unsigned long long>(b);
+        scratch[kWarps + 1] = acc;
+        break;
+      }
+      acc += H[b];
+    }
+  }
+  if (tid == 0) scratch[kWarps + 2] = total;
+  __syncthreads();
+}
+
+// Block sums (all threads) of three u64 and one int; every thread gets them.
+static __device__ __forceinline__ void block_sum4(unsigned long long& a, unsigned long long& b,
+                                                  unsigned long long& c, int& n,
+                                                  unsigned long long* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+    n += __shfl_xor_sync(0xffffffffu, n, o);
+  }
+  if (lane == 0) {
+    scratch[4 * warp] = a;
+    scratch[4 * warp + 1] = b;
+    scratch[4 * warp + 2] = c;
+    scratch[4 * warp + 3] = static_cast<unsigned long long>(n);
+  }
+  __syncthreads();
+  a = b = c = 0;
+  n = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    a += scratch[4 * w];
+    b += scratch[4 * w + 1];
+    c += scratch[4 * w + 2];
+    n += static_cast<int>(scratch[4 * w + 3]);
+  }
+  __syncthreads();
+}
+
+static __device__ __noinline__ void nucleus_cut(const float* row, int V, float M, float c2,
+                                                double top_p, StreamSmem& S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  char* ring = reinterpret_cast<char*>(S.ring);
+  float* fh = reinterpret_cast<float*>(ring);                             // [kWarps][kNucBins]
+  unsigned long long* wh = reinterpret_cast<unsigned long long*>(ring);   // (fallback) [kWarps][256]
+  unsigned long long* tiles = reinterpret_cast<unsigned long long*>(ring + kNucTiles);
+  unsigned long long* scr = reinterpret_cast<unsigned long long*>(ring + kNucScratch);
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(ring + kNucTiles - 512);  // [4 kWarps]
+  unsigned long long* lkey = reinterpret_cast<unsigned long long*>(ring + 32768);  // [kNucCap]
+  unsigned long long* lq = lkey + kNucCap;        // [kNucCap] their masses
+  unsigned long long* sq = lq + kNucCap;          // [kNucCap] masses in key order
+  int* ord = reinterpret_cast<int*>(sq + kNucCap);   // [kNucCap] entry of each rank
+  int* cnt = reinterpret_cast<int*>(scr + kWarps + 4);
+  const int TR = (V + kTile - 1) / kTile;
+  // every token of the row: f(x, token, u); x = -inf past the row's end.  A
+  // round loads kNucUnroll 16-byte pieces per thread before using any (the
+  // passes are bound by L2 latency otherwise); every lane of a warp runs the
+  // same rounds.
+  constexpr int kNucUnroll = 8;
+  const int Vr = (V + kThreads * 4 * kNucUnroll - 1) / (kThreads * 4 * kNucUnroll) * (kThreads * 4 * kNucUnroll);
+  auto load4 = [&](int i, float (&xs)[4]) {
+    if (i + 4 <= V) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(row + i));
+      xs[0] = v.x, xs[1] = v.y, xs[2] = v.z, xs[3] = v.w;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) xs[c] = i + c < V ? __ldcg(row + i + c) : -INFINITY;
+    }
+  };
+  auto for_each = [&](auto f) {
+    for (int i0 = tid * 4; i0 < Vr; i0 += kThreads * 4 * kNucUnroll) {
+      float xs[kNucUnroll][4];
+#pragma unroll
+      for (int j = 0; j < kNucUnroll; ++j) load4(i0 + j * kThreads * 4, xs[j]);
+#pragma unroll
+      for (int j = 0; j < kNucUnroll; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) f(xs[j][c], i0 + j * kThreads * 4 + c, (M - xs[j][c]) * c2);
+    }
+  };
+  auto qof = [&](float u) {   // (a 32-bit conversion: the 64-bit one is slow here)
+    return static_cast<unsigned long long>(__float2uint_rn(ex2(-u) * kQUnit));
+  };
+  auto bin1 = [&](float u) { return min(kNucBins - 1, __float2int_rz(u * 32.f)); };
+  // ---- approximate masses of the bins of u: token counts (32-bit atomics)
+  // times the mass at the bin's centre
+  uint32_t* ch = reinterpret_cast<uint32_t*>(fh);
+  for (int b = tid; b < kWarps * kNucBins; b += kThreads) ch[b] = 0u;
+  __syncthreads();
+  for_each([&](float x, int, float u) {
+    if (x != -INFINITY) atomicAdd(&ch[warp * kNucBins + bin1(u)], 1u);
+  });
+  __syncthreads();
+  for (int b = tid; b < kNucBins; b += kThreads) {
+    uint32_t c = 0;
+    for (int w = 0; w < kWarps; ++w) c += ch[w * kNucBins + b];
+    fh[b] = static_cast<float>(c) * ex2(-(static_cast<float>(b) + 0.5f) * (1.0f / 32.0f));
+  }
+  __syncthreads();
+  // crossing bin of the approximate cumulative masses (one warp)
+  if (warp == 0) {
+    double tot = 0.0;
+    for (int b = lane; b < kNucBins; b += 32) tot += fh[b];
+    tot = warp_sum_d(tot);
+    const double ta = top_p * tot;
+    double cum = 0.0;
+    int pick = kNucBins - 1;
+    for (int base = 0; base < kNucBins; base += 32) {
+      const double m = fh[base + lane];
+      const double incl = warp_incl_scan_d(m) + cum;
+      const unsigned bal = __ballot_sync(0xffffffffu, m > 0.0 && incl >= ta);
+      if (bal) {
+        pick = base + __ffs(bal) - 1;
+        break;
+      }
+      cum = __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) scr[kWarps] = static_cast<unsigned long long>(pick);
+  }
+  __syncthreads();
+  int b1 = static_cast<int>(scr[kWarps]);
+  __syncthreads();
+  // ---- exact masses (fixed point, register sums): above bin b1, in it, all;
+  // the crossing bin is b1 if above < t <= above + in, else a neighbour
+  unsigned long long above = 0, in = 0, Z = 0;
+  int n_in = 0;
+  double t = 0.0;
+  for (int guard = 0; guard < kNucBins; ++guard) {
+    above = in = Z = 0;
+    n_in = 0;
+    for_each([&](float x, int, float u) {
+      if (x == -INFINITY) return;
+      const unsigned long long q = qof(u);
+      const int b = bin1(u);
+      Z += q;
+      if (b < b1) above += q;
+      else if (b == b1) in += q, ++n_in;
+    });
+    block_sum4(above, in, Z, n_in, red);
+    t = top_p * static_cast<double>(Z);
+    if (static_cast<double>(above) >= t && b1 > 0) --b1;                       // cut earlier
+    else if (static_cast<double>(above + in) < t && b1 < kNucBins - 1) ++b1;   // cut later
+    else break;
+  }
+  unsigned long long kb = 0, keep = 0;
+  if (tid == 0) *cnt = 0;
+  __syncthreads();
+  if (n_in <= kNucCap) {
+    // ---- the crossing bin's tokens, ranked by key (distinct); masses in key
+    // order; the first prefix reaching t
+    for_each([&](float x, int id, float u) {
+      if (x == -INFINITY || bin1(u) != b1) return;
+      const int e = atomicAdd(cnt, 1);
+      if (e < kNucCap) {
+        lkey[e] = mkkey(x, id);
+        lq[e] = qof(u);
+      }
+    });
+    __syncthreads();
+    const int n = min(*cnt, kNucCap);
+    for (int e = tid; e < n; e += kThreads) {
+      const unsigned long long k = lkey[e];
+      int r = 0;
+      for (int f = 0; f < n; ++f) r += lkey[f] > k ? 1 : 0;
+      sq[r] = lq[e];
+      ord[r] = e;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long cum = above;
+      int pick = n - 1;
+      bool found = false;
+      for (int base = 0; base < n && !found; base += 32) {
+        const unsigned long long q = base + lane < n ? sq[base + lane] : 0ull;
+        unsigned long long incl = q;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned bal =
+            __ballot_sync(0xffffffffu, base + lane < n && static_cast<double>(cum + incl) >= t);
+        const int l = bal ? __ffs(bal) - 1 : 31;
+        if (bal) {
+          pick = base + l;
+          found = true;
+        }
+        cum += __shfl_sync(0xffffffffu, incl, l);
+      }
+      if (lane == 0) {
+        scr[kWarps + 1] = cum;
+        scr[kWarps + 3] = static_cast<unsigned long long>(pick);
+      }
+    }
+    __syncthreads();
+    keep = scr[kWarps + 1];
+    kb = lkey[ord[static_cast<int>(scr[kWarps + 3])]];
+  } else {
+    // many tokens share the crossing bin: radix select on the 64-bit key
+    // among them, 8 bits per pass from the top (exact 64-bit sums)
+    unsigned long long prefix = 0, pmask = 0;
+    for (int sh = 56; sh >= 0; sh -= 8) {
+      for (int b = tid; b < kWarps * 256; b += kThreads) wh[b] = 0ull;
+      __syncthreads();
+      for_each([&](float x, int id, float u) {
+        if (x == -INFINITY || bin1(u) != b1) return;
+        const unsigned long long k = mkkey(x, id);
+        if ((k & pmask) == prefix) atomicAdd(&wh[warp * 256 + static_cast<int>((k >> sh) & 255u)], qof(u));
+      });
+      __syncthreads();
+      unsigned long long* rev = wh + kWarps * 256;   // bins in key order, largest first
+      for (int b = tid; b < 256; b += kThreads) {
+        unsigned long long sum = 0;
+        for (int w = 0; w < kWarps; ++w) sum += wh[w * 256 + 255 - b];
+        rev[b] = sum;
+      }
+      __syncthreads();
+      find_cut_bin(rev, 256, t - static_cast<double>(above), scr);
+      const int b = 255 - static_cast<int>(scr[kWarps]);
+      above += scr[kWarps + 1];
+      prefix |= static_cast<unsigned long long>(b) << sh;
+      pmask |= 255ull << sh;
+      __syncthreads();
+    }
+    kb = prefix;   // one token (keys are distinct); its own mass completes the sum
+    for_each([&](float x, int id, float u) {
+      if (x != -INFINITY && mkkey(x, id) == kb) scr[kWarps + 1] = qof(u);
+    });
+    __syncthreads();
+    keep = above + scr[kWarps + 1];
+  }
+  // ---- kept mass of every tile (a warp's 128 tokens lie in one tile)
+  for (int b = tid; b < TR; b += kThreads) tiles[b] = 0ull;
+  __syncthreads();
+  for (int i0 = tid * 4; i0 < Vr; i0 += kThreads * 4 * kNucUnroll) {
+    float xs[kNucUnroll][4];
+#pragma unroll
+    for (int j = 0; j < kNucUnroll; ++j) load4(i0 + j * kThreads * 4, xs[j]);
+#pragma unroll
+    for (int j = 0; j < kNucUnroll; ++j) {
+      const int i = i0 + j * kThreads * 4;
+      unsigned long long q = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (xs[j][c] != -INFINITY && mkkey(xs[j][c], i + c) >= kb) q += qof((M - xs[j][c]) * c2);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+      if (lane == 0 && q) atomicAdd(&tiles[i / kTile], q);
+    }
+  }
+  if (tid == 0) {
+    S.aux_key = kb;
+    S.aux_d = static_cast<double>(keep) / static_cast<double>(kQUnit);
+  }
+  __syncthreads();
 }
 
 // One node's decision: its row, its place in the tree, the sampling
@@ -70,6 +379,7 @@ __device__ __forceinline__ double full_prob(const float* lrow, int t, double row
 struct NodeJob {
   const float* lrow;     // the node's target row
   const float2* tsums;   // the row's per-(tile, warp) sums (full vocabulary)
+  const unsigned long long* ntiles;   // per-tile kept masses (nucleus; see nucleus_cut)
   int2* dec;             // out: (accepted child or -1, bonus)
   double invT, top_p;
   uint64_t seed, step;
@@ -201,14 +511,20 @@ static __device__ __noinline__ void node_decision(const NodeJob& J, StreamSmem& 
       krej[ea] = ra;
       krej[eb] = rb;
       __syncwarp();
-    } else {  // full vocabulary
+    } else {  // full vocabulary, or its nucleus (kept mass and set from nucleus_cut)
       rowmax = static_cast<double>(S.rmax);
-      zsum = S.rsum;
+      zsum = mode == kModeNucleus ? S.aux_d : S.rsum;
       izsum = 1.0 / zsum;
     }
+    const unsigned long long kcut = mode == kModeNucleus ? S.aux_key : 0ull;
+    auto prob_tok = [&](int t) -> double {  // token t, full vocabulary or nucleus (lane-local)
+      const float x = __ldg(lrow + t);
+      if (mkkey(x, t) < kcut) return 0.0;   // outside the nucleus
+      return exp_d((static_cast<double>(x) - rowmax) * invT) * izsum;
+    };
     auto prob_of = [&](int j) -> double {  // child j (lane-local)
       if (mode == kModeTopK) return pc[j];
-      return full_prob(lrow, kt[j], rowmax, invT, izsum);
+      return prob_tok(kt[j]);
     };
 
     // ---- children in node order, 32 at a time: child j is accepted iff
@@ -283,7 +599,9 @@ static __device__ __noinline__ void node_decision(const NodeJob& J, StreamSmem& 
         for (int base = 0; base < TR && tile < 0; base += 32) {
           const int t = base + lane;
           double mass = 0.0;
-          if (t < TR) {
+          if (t < TR && mode == kModeNucleus) {
+            mass = static_cast<double>(J.ntiles[t]) * (1.0 / static_cast<double>(kQUnit)) * izsum;
+          } else if (t < TR) {
             // combine the per-warp partials of tile t (max, sum of 2^((x - max) c2))
             const float2* tw = ts + static_cast<int64_t>(t) * kWarps;
             for (int w = 0; w < kWarps; ++w) {
@@ -293,12 +611,14 @@ static __device__ __noinline__ void node_decision(const NodeJob& J, StreamSmem& 
                         static_cast<double>(ex2((v.x - static_cast<float>(rowmax)) * static_cast<float>(c2)));
             }
             mass *= izsum;
+          }
+          if (t < TR) {
             for (int r = 0; r < nk; ++r) {   // rejected tokens of this tile, each once
               const int rt = kt[r];
               if (rt / kTile != t) continue;
               bool first = true;
               for (int r2 = 0; r2 < r; ++r2) first &= kt[r2] != rt;
-              if (first) mass -= full_prob(lrow, rt, rowmax, invT, izsum);
+              if (first) mass -= prob_tok(rt);
             }
             if (mass < 0.0) mass = 0.0;
           }
@@ -322,7 +642,8 @@ static __device__ __noinline__ void node_decision(const NodeJob& J, StreamSmem& 
           double mass = 0.0;
           if (t < J.vocab && !is_rejected(t)) {
             const float x = __ldg(lrow + t);
-            mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) * izsum;
+            if (mkkey(x, t) >= kcut)
+              mass = static_cast<double>(exp2f((x - static_cast<float>(rowmax)) * static_cast<float>(c2))) * izsum;
           }
           lm[q] = mass;
           lsum += mass;
@@ -432,6 +753,12 @@ static __device__ __noinline__ void warm_decision(const VerifyArgs& A, StreamSme
   const int vocab = kTile;
   const int K = A.top_k[0];
   if (lane < kWarps) ts[lane] = make_float2(0.f, 0.f);
+  unsigned long long* ntiles = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(S.ring) + kNucTiles);
+  if (lane == 0) {
+    ntiles[0] = 0ull;
+    S.aux_key = 0ull;   // nucleus: every token kept, mass 1
+    S.aux_d = 1.0;
+  }
   for (int e = lane; e < kKMax; e += 32)
     S.rlist[e] = e < K ? mkkey(-0.5f * static_cast<float>(e), (e * 7) % vocab) : 0ull;
   if (lane == 0) {
@@ -447,6 +774,7 @@ static __device__ __noinline__ void warm_decision(const VerifyArgs& A, StreamSme
   NodeJob J;
   J.lrow = g_warm_row;
   J.tsums = ts;
+  J.ntiles = ntiles;
   J.dec = dec;
   J.node = 0;
   J.m = 2;
@@ -502,13 +830,17 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_consta
     cp_async_commit();
   }
   const RowCtx cx = stream_row(R, S);
-  if (!cx.leader || threadIdx.x >= 32) return;   // warp 0 of the leader from here on
+  if (!cx.leader) return;
+  if (A.mode[cx.item] == kModeNucleus)   // every warp of the leader
+    nucleus_cut(R.src, R.vocab, S.rmax, R.c2, static_cast<double>(A.top_p[cx.item]), S);
+  if (threadIdx.x >= 32) return;         // warp 0 of the leader from here on
   cp_async_wait_all();
   __syncwarp();
   NodeJob J;
   const int item = cx.item;
   J.lrow = R.src;
   J.tsums = R.tsums;
+  J.ntiles = reinterpret_cast<const unsigned long long*>(reinterpret_cast<char*>(S.ring) + kNucTiles);
   J.node = warm ? 0 : static_cast<int>(cx.row - static_cast<int64_t>(item) * A.m);
   J.m = warm ? 2 : A.m;
   J.dec = warm ? reinterpret_cast<int2*>(g_warm_decision) : A.dec + cx.row;
@@ -544,7 +876,6 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
   VerifyArgs A;
   memset(&A, 0, sizeof(A));
   int rec_k = 1;
-  bool any_full = false;
   for (int i = 0; i < n_items; ++i) {
     EAGLE_CHECK_ARG(logits[i] && aligned16(logits[i]) && accepted[i]);
     EAGLE_CHECK_ARG(trees[i].parents && trees[i].tokens && trees[i].m == m);
@@ -557,8 +888,8 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
       EAGLE_CHECK_ARG(p.temperature > 0.f && p.top_p > 0.f && p.top_p <= 1.f && p.top_k >= 0);
       k = p.top_k >= vocab ? (vocab <= kKMax ? vocab : 0) : p.top_k;
       EAGLE_CHECK_SHAPE(k <= kKMax);
-      EAGLE_CHECK_SHAPE(k > 0 || p.top_p >= 1.f);  // nucleus needs a top_k bound
-      mode = k > 0 ? kModeTopK : kModeFull;
+      mode = k > 0 ? kModeTopK : (p.top_p < 1.f ? kModeNucleus : kModeFull);
+      EAGLE_CHECK_SHAPE(mode != kModeNucleus || (vocab + kTile - 1) / kTile <= kNucMaxTiles);
     }
     A.mode[i] = mode;
     A.top_k[i] = k;
@@ -570,12 +901,10 @@ static eagle_status verify_impl(int32_t n_items, const float* const* logits, int
     A.seed[i] = seeds[i];
     A.rs.base[i] = logits[i];
     A.rs.exp_scale[i] = p.greedy ? 1.f : 1.f / p.temperature;
-    A.rs.topk[i] = static_cast<int16_t>(mode == kModeFull ? 0 : k);
-    A.rs.flags[i] = mode == kModeFull ? (kWantSum | kWantTileSums) : 0;
+    A.rs.topk[i] = static_cast<int16_t>(mode == kModeTopK || mode == kModeGreedy ? k : 0);
+    A.rs.flags[i] = mode == kModeFull ? (kWantSum | kWantTileSums) : mode == kModeNucleus ? kWantSum : 0;
     if (k > rec_k) rec_k = k;
-    any_full |= mode == kModeFull;
   }
-  (void)any_full;
   const StreamLayout L = stream_layout(n_items, m, vocab, kKMax, true, true);
   if (ws_bytes < L.total) return EAGLE_ERR_WORKSPACE_TOO_SMALL;
   const int occ = stream_ctas_per_sm(verify_kernel);

@@ -86,11 +86,17 @@ def test_build_rejects_bad_arguments_before_launch(lib, kwargs, status):
 
 def test_verify_rejects_bad_sampling(lib):
     fake = ctypes.c_void_p(1 << 20)
-    for samp, status in [(eb.sampling(False, 0.0), 1), (eb.sampling(False, 1.0, 0, 0.9), 2),
-                         (eb.sampling(False, 1.0, 65), 2), (eb.sampling(False, 1.0, 0, 1.5), 1)]:
+    for samp, status in [(eb.sampling(False, 0.0), 1), (eb.sampling(False, 1.0, 65), 2),
+                         (eb.sampling(False, 1.0, 0, 1.5), 1), (eb.sampling(False, 1.0, 0, 0.0), 1)]:
         st = lib.eagle_tree_verify(fake, 1000, 1000, _fake_tree(), ctypes.byref(samp), 0, 0, fake,
                                    fake, fake, ctypes.c_void_p(1 << 21), 1 << 30, None)
         assert st == status
+    # a nucleus over the whole vocabulary is limited to 4080 tiles of 1024 tokens
+    big = 4081 * 1024
+    samp = eb.sampling(False, 1.0, 0, 0.9)
+    st = lib.eagle_tree_verify(fake, big, big, _fake_tree(), ctypes.byref(samp), 0, 0, fake,
+                               fake, fake, ctypes.c_void_p(1 << 21), 1 << 40, None)
+    assert st == 2
 
 
 def test_attn_rejects_bad_arguments(lib):

@@ -127,8 +127,45 @@ def test_single_node_tree():
     assert n == 0 and bonus == int(torch.argmax(target[0]))
 
 
-def test_rejects_nucleus_without_top_k():
-    _, ref, target = _case("c0")
-    with pytest.raises(eb.EagleError) as e:
-        _verify(target, ref, False, 1.0, 0, 0.9)
-    assert e.value.status == 2
+# Nucleus over the whole vocabulary (top_p < 1, top_k = 0): the kept set is
+# cut by the library's radix select over exact fixed-point masses.
+@pytest.mark.parametrize("T,p,scale,vocab", [(1.0, 0.9, 0.7, 5003), (0.7, 0.5, 1.0, 5003),
+                                             (1.3, 0.99, 0.5, 12288), (1.0, 0.3, 3.0, 1000)])
+def test_nucleus_full_vocab_flat_rows(T, p, scale, vocab):
+    w = wl.WORKLOADS["c0"]
+    ref = build_draft_tree(wl.draft_logits(w).numpy(), w.top_k, w.depth, w.total_tokens, 5)
+    g = torch.Generator().manual_seed(23)
+    target = torch.randn(w.total_tokens, vocab, generator=g) * scale
+    for seed in range(10):
+        v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False,
+                        temperature=T, top_k=0, top_p=p, seed=seed, step=2)
+        acc, n, bonus = _verify(target, ref, False, T, 0, p, seed, 2)
+        path_matches(acc, n, bonus, v, f"nucleus T{T} p{p} seed{seed}", ref["parents"],
+                     ref["tokens"], target.numpy(), (0, T, 0, p))
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_nucleus_full_vocab_qwen7b(seed):
+    w, ref, target = _case("c2")
+    v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False, temperature=0.7,
+                    top_k=0, top_p=0.9, seed=seed, step=4)
+    acc, n, bonus = _verify(target, ref, False, 0.7, 0, 0.9, seed, 4)
+    path_matches(acc, n, bonus, v, f"nucleus c2 seed{seed}", ref["parents"], ref["tokens"],
+                 target.numpy(), (0, 0.7, 0, 0.9))
+
+
+def test_nucleus_full_vocab_tied_logits():
+    # logits on a grid of 1/8: hundreds of tokens share each value, so the
+    # crossing value is shared and the cut falls between equal logits
+    # (token ids ascending decide)
+    w = wl.WORKLOADS["c0"]
+    ref = build_draft_tree(wl.draft_logits(w).numpy(), w.top_k, w.depth, w.total_tokens, 5)
+    g = torch.Generator().manual_seed(29)
+    target = torch.round(torch.randn(w.total_tokens, 7001, generator=g) * 8.0) / 8.0
+    for p in (0.25, 0.6, 0.95):
+        for seed in range(6):
+            v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False,
+                            temperature=1.0, top_k=0, top_p=p, seed=seed, step=9)
+            acc, n, bonus = _verify(target, ref, False, 1.0, 0, p, seed, 9)
+            path_matches(acc, n, bonus, v, f"tied p{p} seed{seed}", ref["parents"],
+                         ref["tokens"], target.numpy(), (0, 1.0, 0, p))
