@@ -76,7 +76,7 @@ __device__ __forceinline__ double warp_incl_scan_d(double v) {
 // in units of the max's; per-tile kept masses at ring byte offset kNucTiles
 // (read by the residual draw).
 constexpr size_t kNucTiles = 65536;                  // u64 [tiles], after the histograms
-constexpr size_t kNucScratch = kScratchBytes - 128;  // the searches' scratch, at the ring's end
+constexpr size_t kNucScratch = kScratchBytes - 512;  // the searches' scratch, at the ring's end
 constexpr int kNucMaxTiles = static_cast<int>((kNucScratch - kNucTiles) / 8);
 constexpr int kNucBins = 1024;                       // per warp, per level
 constexpr int kNucCap = 1024;                        // tokens ranked exactly
@@ -156,27 +156,53 @@ static __device__ __forceinline__ void block_sum4(unsigned long long& a, unsigne
   __syncthreads();
 }
 
-static __device__ __noinline__ void nucleus_cut(const float* row, int V, float M, float c2,
-                                                double top_p, StreamSmem& S) {
+// The nucleus cut, by every CTA of the row's cluster over its own share of
+// the row (the tiles it streamed), the shares combined in the leader's
+// shared memory (distributed shared memory) between cluster barriers:
+//   1. approximate masses of the bins of u (32-bit sums of each token's mass
+//      relative to its bin's top, 2^-12 units) -> the leader's approximate
+//      crossing bin;
+//   2. exact fixed-point sums above / in the bin and the total -> the leader
+//      confirms the bin (or moves to a neighbour and the pass repeats);
+//   3. the bin's tokens appended to the leader's list, and every tile's mass
+//      above the bin written to the leader's tile array;
+// then the leader alone ranks the list (or, past kNucCap tokens, runs the
+// radix select on the key over the whole row) and completes the tiles.
+// Called by every CTA of the cluster after stream_row, the leader's row max
+// in place.
+struct NucShare {
+  uint32_t bin;          // leader: the bin under test / confirmed
+  uint32_t done;         // leader: 1 when confirmed
+  unsigned long long above, t_bits;   // leader: mass above the bin; t as double bits
+  unsigned long long part[4];         // every CTA: above, in, total, count of its share
+  uint32_t cnt;          // leader: tokens of the bin collected
+};
+
+static __device__ __noinline__ void nucleus_cut(const float* row, int V, int rank, int PC,
+                                                float c2, double top_p, StreamSmem& S) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool leader = rank == 0;
   char* ring = reinterpret_cast<char*>(S.ring);
-  float* fh = reinterpret_cast<float*>(ring);                             // [kWarps][kNucBins]
+  uint32_t* ch = reinterpret_cast<uint32_t*>(ring);                       // [kWarps][kNucBins]
+  float* fh = reinterpret_cast<float*>(ring + kWarps * kNucBins * 4);     // leader: [kNucBins]
   unsigned long long* wh = reinterpret_cast<unsigned long long*>(ring);   // (fallback) [kWarps][256]
   unsigned long long* tiles = reinterpret_cast<unsigned long long*>(ring + kNucTiles);
-  unsigned long long* scr = reinterpret_cast<unsigned long long*>(ring + kNucScratch);
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(ring + kNucTiles - 512);  // [4 kWarps]
-  unsigned long long* lkey = reinterpret_cast<unsigned long long*>(ring + 32768);  // [kNucCap]
+  unsigned long long* scr = reinterpret_cast<unsigned long long*>(ring + kNucScratch);  // [16]
+  NucShare* sh = reinterpret_cast<NucShare*>(ring + kNucScratch + 128);
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(ring + kNucScratch + 256);  // [4 kWarps]
+  unsigned long long* lkey = reinterpret_cast<unsigned long long*>(ring + 36864);  // [kNucCap]
   unsigned long long* lq = lkey + kNucCap;        // [kNucCap] their masses
   unsigned long long* sq = lq + kNucCap;          // [kNucCap] masses in key order
   int* ord = reinterpret_cast<int*>(sq + kNucCap);   // [kNucCap] entry of each rank
-  int* cnt = reinterpret_cast<int*>(scr + kWarps + 4);
+  const uint32_t lead_sh = map_rank(sh, 0);
+  auto lead = [&](const void* p) { return lead_sh + static_cast<uint32_t>(reinterpret_cast<const char*>(p) - reinterpret_cast<const char*>(sh)); };
+  const float M = __uint_as_float(ld_cluster_u32(map_rank(&S.rmax, 0)));
   const int TR = (V + kTile - 1) / kTile;
-  // every token of the row: f(x, token, u); x = -inf past the row's end.  A
-  // round loads kNucUnroll 16-byte pieces per thread before using any (the
-  // passes are bound by L2 latency otherwise); every lane of a warp runs the
-  // same rounds.
+  const int tile0 = rank * TR / PC, tile1 = (rank + 1) * TR / PC;   // this CTA's share
+  // the tokens of a range of tiles: f(x, token, u); x = -inf past the row's
+  // end.  A round loads kNucUnroll 16-byte pieces per thread before using
+  // any; every lane of a warp runs the same rounds.
   constexpr int kNucUnroll = 8;
-  const int Vr = (V + kThreads * 4 * kNucUnroll - 1) / (kThreads * 4 * kNucUnroll) * (kThreads * 4 * kNucUnroll);
   auto load4 = [&](int i, float (&xs)[4]) {
     if (i + 4 <= V) {
       const float4 v = __ldcg(reinterpret_cast<const float4*>(row + i));
@@ -186,11 +212,16 @@ static __device__ __noinline__ void nucleus_cut(const float* row, int V, float M
       for (int c = 0; c < 4; ++c) xs[c] = i + c < V ? __ldcg(row + i + c) : -INFINITY;
     }
   };
-  auto for_each = [&](auto f) {
-    for (int i0 = tid * 4; i0 < Vr; i0 += kThreads * 4 * kNucUnroll) {
+  auto for_tiles = [&](int t0, int t1, auto f) {
+    const int b0 = t0 * kTile, b1 = t1 * kTile;
+    for (int i0 = b0 + tid * 4; i0 < b1; i0 += kThreads * 4 * kNucUnroll) {
       float xs[kNucUnroll][4];
 #pragma unroll
-      for (int j = 0; j < kNucUnroll; ++j) load4(i0 + j * kThreads * 4, xs[j]);
+      for (int j = 0; j < kNucUnroll; ++j) {
+        const int i = i0 + j * kThreads * 4;
+        if (i < b1) load4(i, xs[j]);
+        else xs[j][0] = xs[j][1] = xs[j][2] = xs[j][3] = -INFINITY;
+      }
 #pragma unroll
       for (int j = 0; j < kNucUnroll; ++j)
 #pragma unroll
@@ -201,82 +232,167 @@ static __device__ __noinline__ void nucleus_cut(const float* row, int V, float M
     return static_cast<unsigned long long>(__float2uint_rn(ex2(-u) * kQUnit));
   };
   auto bin1 = [&](float u) { return min(kNucBins - 1, __float2int_rz(u * 32.f)); };
-  // ---- approximate masses of the bins of u: token counts (32-bit atomics)
-  // times the mass at the bin's centre
-  uint32_t* ch = reinterpret_cast<uint32_t*>(fh);
+
+  // ---- 1. approximate bin masses over the share: a token of bin b adds
+  // 2^(b/32 - u) in (2^-1/32, 1] in units of 2^-12 (a warp's bin would wrap
+  // past 2^20 tokens)
   for (int b = tid; b < kWarps * kNucBins; b += kThreads) ch[b] = 0u;
+  for (int b = tile0 + tid; b < tile1; b += kThreads) tiles[b] = 0ull;
+  if (leader && tid == 0) {
+    sh->cnt = 0u;
+    sh->done = 0u;
+  }
   __syncthreads();
-  for_each([&](float x, int, float u) {
-    if (x != -INFINITY) atomicAdd(&ch[warp * kNucBins + bin1(u)], 1u);
+  for_tiles(tile0, tile1, [&](float x, int, float u) {
+    if (x == -INFINITY) return;
+    const int b = bin1(u);
+    atomicAdd(&ch[warp * kNucBins + b],
+              __float2uint_rn(ex2(static_cast<float>(b) * (1.0f / 32.0f) - u) * 4096.0f));
   });
   __syncthreads();
-  for (int b = tid; b < kNucBins; b += kThreads) {
-    uint32_t c = 0;
-    for (int w = 0; w < kWarps; ++w) c += ch[w * kNucBins + b];
-    fh[b] = static_cast<float>(c) * ex2(-(static_cast<float>(b) + 0.5f) * (1.0f / 32.0f));
-  }
-  __syncthreads();
-  // crossing bin of the approximate cumulative masses (one warp)
-  if (warp == 0) {
-    double tot = 0.0;
-    for (int b = lane; b < kNucBins; b += 32) tot += fh[b];
-    tot = warp_sum_d(tot);
-    const double ta = top_p * tot;
-    double cum = 0.0;
-    int pick = kNucBins - 1;
-    for (int base = 0; base < kNucBins; base += 32) {
-      const double m = fh[base + lane];
-      const double incl = warp_incl_scan_d(m) + cum;
-      const unsigned bal = __ballot_sync(0xffffffffu, m > 0.0 && incl >= ta);
-      if (bal) {
-        pick = base + __ffs(bal) - 1;
-        break;
-      }
-      cum = __shfl_sync(0xffffffffu, incl, 31);
+  unsigned long long* ch64 = reinterpret_cast<unsigned long long*>(ring);   // [kNucBins] the CTA's sums
+  {
+    unsigned long long cs[kNucBins / kThreads];
+#pragma unroll
+    for (int k = 0; k < kNucBins / kThreads; ++k) {
+      cs[k] = 0;
+      for (int w = 0; w < kWarps; ++w) cs[k] += ch[w * kNucBins + tid + k * kThreads];
     }
-    if (lane == 0) scr[kWarps] = static_cast<unsigned long long>(pick);
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kNucBins / kThreads; ++k) ch64[tid + k * kThreads] = cs[k];
   }
-  __syncthreads();
-  int b1 = static_cast<int>(scr[kWarps]);
-  __syncthreads();
-  // ---- exact masses (fixed point, register sums): above bin b1, in it, all;
-  // the crossing bin is b1 if above < t <= above + in, else a neighbour
-  unsigned long long above = 0, in = 0, Z = 0;
-  int n_in = 0;
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait();
+  if (leader) {
+    for (int b = tid; b < kNucBins; b += kThreads) {
+      unsigned long long c = 0;
+      for (int r = 0; r < PC; ++r) c += ld_cluster_u64(map_rank(ch64 + b, static_cast<uint32_t>(r)));
+      fh[b] = static_cast<float>(c) * (1.0f / 4096.0f) * ex2(-static_cast<float>(b) * (1.0f / 32.0f));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      double tot = 0.0;
+      for (int b = lane; b < kNucBins; b += 32) tot += fh[b];
+      tot = warp_sum_d(tot);
+      const double ta = top_p * tot;
+      double cum = 0.0;
+      int pick = kNucBins - 1;
+      for (int base = 0; base < kNucBins; base += 32) {
+        const double m = fh[base + lane];
+        const double incl = warp_incl_scan_d(m) + cum;
+        const unsigned bal = __ballot_sync(0xffffffffu, m > 0.0 && incl >= ta);
+        if (bal) {
+          pick = base + __ffs(bal) - 1;
+          break;
+        }
+        cum = __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) sh->bin = static_cast<uint32_t>(pick);
+    }
+  }
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait();
+  // ---- 2. exact sums for the bin under test; the leader confirms or moves it
+  int b1 = 0;
+  unsigned long long above = 0;
   double t = 0.0;
   for (int guard = 0; guard < kNucBins; ++guard) {
-    above = in = Z = 0;
-    n_in = 0;
-    for_each([&](float x, int, float u) {
+    b1 = static_cast<int>(ld_cluster_u32(lead(&sh->bin)));
+    unsigned long long ab = 0, in = 0, Z = 0;
+    int n_in = 0;
+    for_tiles(tile0, tile1, [&](float x, int, float u) {
       if (x == -INFINITY) return;
       const unsigned long long q = qof(u);
       const int b = bin1(u);
       Z += q;
-      if (b < b1) above += q;
+      if (b < b1) ab += q;
       else if (b == b1) in += q, ++n_in;
     });
-    block_sum4(above, in, Z, n_in, red);
-    t = top_p * static_cast<double>(Z);
-    if (static_cast<double>(above) >= t && b1 > 0) --b1;                       // cut earlier
-    else if (static_cast<double>(above + in) < t && b1 < kNucBins - 1) ++b1;   // cut later
-    else break;
-  }
-  unsigned long long kb = 0, keep = 0;
-  if (tid == 0) *cnt = 0;
-  __syncthreads();
-  if (n_in <= kNucCap) {
-    // ---- the crossing bin's tokens, ranked by key (distinct); masses in key
-    // order; the first prefix reaching t
-    for_each([&](float x, int id, float u) {
-      if (x == -INFINITY || bin1(u) != b1) return;
-      const int e = atomicAdd(cnt, 1);
-      if (e < kNucCap) {
-        lkey[e] = mkkey(x, id);
-        lq[e] = qof(u);
+    block_sum4(ab, in, Z, n_in, red);
+    if (tid == 0) {
+      sh->part[0] = ab;
+      sh->part[1] = in;
+      sh->part[2] = Z;
+      sh->part[3] = static_cast<unsigned long long>(n_in);
+    }
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait();
+    if (leader && tid == 0) {
+      unsigned long long A = 0, I = 0, T = 0;
+      for (int r = 0; r < PC; ++r) {
+        A += ld_cluster_u64(map_rank(&sh->part[0], static_cast<uint32_t>(r)));
+        I += ld_cluster_u64(map_rank(&sh->part[1], static_cast<uint32_t>(r)));
+        T += ld_cluster_u64(map_rank(&sh->part[2], static_cast<uint32_t>(r)));
       }
-    });
-    __syncthreads();
-    const int n = min(*cnt, kNucCap);
+      const double tt = top_p * static_cast<double>(T);
+      sh->above = A;
+      sh->t_bits = static_cast<unsigned long long>(__double_as_longlong(tt));
+      if (static_cast<double>(A) >= tt && b1 > 0) sh->bin = static_cast<uint32_t>(b1 - 1);
+      else if (static_cast<double>(A + I) < tt && b1 < kNucBins - 1) sh->bin = static_cast<uint32_t>(b1 + 1);
+      else sh->done = 1u;
+    }
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait();
+    if (ld_cluster_u32(lead(&sh->done))) {
+      above = ld_cluster_u64(lead(&sh->above));
+      t = __longlong_as_double(static_cast<long long>(ld_cluster_u64(lead(&sh->t_bits))));
+      break;
+    }
+  }
+  // ---- 3. the bin's tokens to the leader's list; each tile's mass above the
+  // bin (a warp's 128 tokens of a piece lie in one tile: one add per warp and
+  // piece) into this CTA's own tile array, then copied to the leader's
+  for (int i0 = tile0 * kTile + tid * 4; i0 < tile1 * kTile; i0 += kThreads * 4 * kNucUnroll) {
+    float xs[kNucUnroll][4];
+#pragma unroll
+    for (int j = 0; j < kNucUnroll; ++j) {
+      const int i = i0 + j * kThreads * 4;
+      if (i < tile1 * kTile) load4(i, xs[j]);
+      else xs[j][0] = xs[j][1] = xs[j][2] = xs[j][3] = -INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < kNucUnroll; ++j) {
+      const int i = i0 + j * kThreads * 4;
+      unsigned long long q = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float x = xs[j][c];
+        if (x == -INFINITY) continue;
+        const float u = (M - x) * c2;
+        const int b = bin1(u);
+        if (b < b1) {
+          q += qof(u);
+        } else if (b == b1) {
+          const uint32_t e = atom_add_cluster_u32(lead(&sh->cnt), 1u);
+          if (e < static_cast<uint32_t>(kNucCap)) {
+            st_cluster(map_rank(lkey + e, 0), mkkey(x, i + c));
+            st_cluster(map_rank(lq + e, 0), static_cast<Key>(qof(u)));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+      if (lane == 0 && q && i < tile1 * kTile) atomicAdd(&tiles[i / kTile], q);
+    }
+  }
+  __syncthreads();
+  if (!leader)
+    for (int b = tile0 + tid; b < tile1; b += kThreads)
+      st_cluster(map_rank(tiles + b, 0), static_cast<Key>(tiles[b]));
+  __syncwarp();
+  cluster_arrive_release();
+  cluster_wait();
+  if (!leader) return;
+  const int n = static_cast<int>(sh->cnt);
+  unsigned long long kb = 0, keep = 0;
+  if (n <= kNucCap) {
+    // rank by counting (keys distinct), masses in key order, first prefix
+    // reaching t
     for (int e = tid; e < n; e += kThreads) {
       const unsigned long long k = lkey[e];
       int r = 0;
@@ -314,17 +430,21 @@ static __device__ __noinline__ void nucleus_cut(const float* row, int V, float M
     __syncthreads();
     keep = scr[kWarps + 1];
     kb = lkey[ord[static_cast<int>(scr[kWarps + 3])]];
+    // the bin's kept tokens complete their tiles
+    for (int e = tid; e < n; e += kThreads)
+      if (lkey[e] >= kb) atomicAdd(&tiles[static_cast<int>(~static_cast<uint32_t>(lkey[e])) / kTile], lq[e]);
   } else {
     // many tokens share the crossing bin: radix select on the 64-bit key
-    // among them, 8 bits per pass from the top (exact 64-bit sums)
+    // among them over the whole row, 8 bits per pass from the top (exact
+    // 64-bit sums), by the leader alone
     unsigned long long prefix = 0, pmask = 0;
-    for (int sh = 56; sh >= 0; sh -= 8) {
+    for (int shf = 56; shf >= 0; shf -= 8) {
       for (int b = tid; b < kWarps * 256; b += kThreads) wh[b] = 0ull;
       __syncthreads();
-      for_each([&](float x, int id, float u) {
+      for_tiles(0, TR, [&](float x, int id, float u) {
         if (x == -INFINITY || bin1(u) != b1) return;
         const unsigned long long k = mkkey(x, id);
-        if ((k & pmask) == prefix) atomicAdd(&wh[warp * 256 + static_cast<int>((k >> sh) & 255u)], qof(u));
+        if ((k & pmask) == prefix) atomicAdd(&wh[warp * 256 + static_cast<int>((k >> shf) & 255u)], qof(u));
       });
       __syncthreads();
       unsigned long long* rev = wh + kWarps * 256;   // bins in key order, largest first
@@ -337,34 +457,29 @@ static __device__ __noinline__ void nucleus_cut(const float* row, int V, float M
       find_cut_bin(rev, 256, t - static_cast<double>(above), scr);
       const int b = 255 - static_cast<int>(scr[kWarps]);
       above += scr[kWarps + 1];
-      prefix |= static_cast<unsigned long long>(b) << sh;
-      pmask |= 255ull << sh;
+      prefix |= static_cast<unsigned long long>(b) << shf;
+      pmask |= 255ull << shf;
       __syncthreads();
     }
     kb = prefix;   // one token (keys are distinct); its own mass completes the sum
-    for_each([&](float x, int id, float u) {
+    for_tiles(0, TR, [&](float x, int id, float u) {
       if (x != -INFINITY && mkkey(x, id) == kb) scr[kWarps + 1] = qof(u);
     });
     __syncthreads();
     keep = above + scr[kWarps + 1];
-  }
-  // ---- kept mass of every tile (a warp's 128 tokens lie in one tile)
-  for (int b = tid; b < TR; b += kThreads) tiles[b] = 0ull;
-  __syncthreads();
-  for (int i0 = tid * 4; i0 < Vr; i0 += kThreads * 4 * kNucUnroll) {
-    float xs[kNucUnroll][4];
-#pragma unroll
-    for (int j = 0; j < kNucUnroll; ++j) load4(i0 + j * kThreads * 4, xs[j]);
-#pragma unroll
-    for (int j = 0; j < kNucUnroll; ++j) {
-      const int i = i0 + j * kThreads * 4;
+    // the bin's kept tokens complete their tiles
+    for (int i0 = tid * 4; i0 < TR * kTile; i0 += kThreads * 4) {
+      float xs[4];
+      load4(i0, xs);
       unsigned long long q = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (xs[j][c] != -INFINITY && mkkey(xs[j][c], i + c) >= kb) q += qof((M - xs[j][c]) * c2);
+      for (int c = 0; c < 4; ++c) {
+        const float u = (M - xs[c]) * c2;
+        if (xs[c] != -INFINITY && bin1(u) == b1 && mkkey(xs[c], i0 + c) >= kb) q += qof(u);
+      }
 #pragma unroll
       for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
-      if (lane == 0 && q) atomicAdd(&tiles[i / kTile], q);
+      if (lane == 0 && q) atomicAdd(&tiles[i0 / kTile], q);
     }
   }
   if (tid == 0) {
@@ -830,9 +945,13 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_consta
     cp_async_commit();
   }
   const RowCtx cx = stream_row(R, S);
+  if (A.mode[cx.item] == kModeNucleus) {   // every CTA of the cluster, once the row max is in place
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait();
+    nucleus_cut(R.src, R.vocab, rank, R.PC, R.c2, static_cast<double>(A.top_p[cx.item]), S);
+  }
   if (!cx.leader) return;
-  if (A.mode[cx.item] == kModeNucleus)   // every warp of the leader
-    nucleus_cut(R.src, R.vocab, S.rmax, R.c2, static_cast<double>(A.top_p[cx.item]), S);
   if (threadIdx.x >= 32) return;         // warp 0 of the leader from here on
   cp_async_wait_all();
   __syncwarp();

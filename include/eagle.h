@@ -105,7 +105,7 @@ typedef struct {
  * keep the top_k largest (0 = all, at most EAGLE_MAX_TOP_K), softmax, then
  * nucleus top_p in (0, 1] (the shortest prefix in probability order, ties ->
  * lower token id, whose mass reaches top_p, the crossing token kept; with
- * top_k = 0 over the whole vocabulary, at most 4080 tiles of 1024 tokens),
+ * top_k = 0 over the whole vocabulary, at most 4032 tiles of 1024 tokens),
  * renormalise. */
 typedef struct {
   int32_t greedy;

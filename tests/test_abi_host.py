@@ -91,7 +91,7 @@ def test_verify_rejects_bad_sampling(lib):
         st = lib.eagle_tree_verify(fake, 1000, 1000, _fake_tree(), ctypes.byref(samp), 0, 0, fake,
                                    fake, fake, ctypes.c_void_p(1 << 21), 1 << 30, None)
         assert st == status
-    # a nucleus over the whole vocabulary is limited to 4080 tiles of 1024 tokens
+    # a nucleus over the whole vocabulary is limited to 4032 tiles of 1024 tokens
     big = 4081 * 1024
     samp = eb.sampling(False, 1.0, 0, 0.9)
     st = lib.eagle_tree_verify(fake, big, big, _fake_tree(), ctypes.byref(samp), 0, 0, fake,
