@@ -823,9 +823,9 @@ TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch on the c2
     # workload from one ncu capture, keyed by the kernel's source hash
     # (_kernel_source_hash)
-    "build:c2": ("780fe5897637", 31123456),
-    "verify:c2": ("122e946b2dc0", 36598528),
-    "attn:c2": ("d4abccd751ad", 17386496),
+    "build:c2": ("66ece9890652", 31668736),
+    "verify:c2": ("6227d054bb03", 37138944),
+    "attn:c2": ("b5a540d7fecd", 17385472),
 }
 
 
@@ -1034,12 +1034,14 @@ def main():
     ap.add_argument("--long-attn-only", type=int, default=0, metavar="LAYERS",
                     help="only time the long-context attention, on LAYERS layers "
                          "(a profiling case; prints its own JSON line)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="with --long-attn-only: also time the E4M3 prefix variant")
     args = ap.parse_args()
     if args.long_attn_only:
         import torch
         from eagle_speculative_decoding_verify_gb300 import binding as eb, workloads as wl
         res = attn_long(eb, wl, torch.device("cuda"), reps=max(args.steps, 1),
-                        n_layers=args.long_attn_only, paged=False, fp8=False)
+                        n_layers=args.long_attn_only, paged=False, fp8=args.fp8)
         print(json.dumps(res), flush=True)
         return 0
     rank = int(os.environ.get("RANK", "0"))
