@@ -95,7 +95,7 @@ struct TcParams {
 };
 
 // F8: the prefix comes from an E4M3 cache -- a staging ring of E4M3 chunks
-// (TMA) that two warps widen into the bf16 ring, which is shallower then.
+// (TMA) that two warps widen into the 16-bit ring, which is shallower then.
 template <int D, bool F8 = false>
 struct TcSmem {
   static constexpr int kQTileBytes = 128 * D * 2;       // one 128-row bf16 query tile
@@ -114,21 +114,17 @@ struct TcSmem {
 static_assert(TcSmem<128>::kAlloc <= 232448, "shared memory of the tensor-core kernel");
 static_assert(TcSmem<128, true>::kAlloc <= 232448, "shared memory of the E4M3 kernel");
 
-// 16 E4M3 codes -> 16 bf16 (exact: every E4M3 value is a bf16 value); the
-// first code lands in the low half of out[0]
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 in, uint32_t (&out)[8]) {
+// 16 E4M3 codes -> 16 fp16 (exact: every E4M3 value is an fp16 value; one
+// conversion per pair of codes); the first code lands in the low half of
+// out[0]
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 in, uint32_t (&out)[8]) {
   const uint32_t w[4] = {in.x, in.y, in.z, in.w};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint16_t pair = static_cast<uint16_t>(w[q] >> (16 * h));
-      uint32_t f16x2;
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
-      float lo, hi;
-      asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-          : "=f"(lo), "=f"(hi) : "r"(f16x2));
-      out[2 * q + h] = pack_bf16x2(lo, hi);
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out[2 * q + h]) : "h"(pair));
     }
   }
 }
@@ -218,7 +214,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   };
 
   // E4M3 prefix (F8): item n of a prefix split is staged as codes, then
-  // widened into bf16 ring slot n % kSlots by the converter warps
+  // widened to fp16 into ring slot n % kSlots by the converter warps.  A
+  // prefix split holds only prefix chunks and a tree split only tree chunks,
+  // so a staged split runs every MMA on fp16 operands (its query tiles are
+  // written as fp16, P is fp16) and the tree split stays bf16.
   const bool staged = F8 && !tree_split;
   auto issue_stage = [&](int n) {
     const int st = n % L::kStage;
@@ -287,7 +286,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       for (int c = 0; c < D / 16; ++c) {   // 16-byte chunks of the row
         const int cg = half * (D / 16) + c;
         const int box = cg >> 3, cc = cg & 7;
-        *reinterpret_cast<int4*>(qt + box * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = qv[c];
+        int4 x = qv[c];
+        if (staged) {
+          // fp16 (exact for magnitudes in [2^-14, 65504], the rest within
+          // 2^-25); a larger element is reported
+          const uint32_t w[4] = {static_cast<uint32_t>(x.x), static_cast<uint32_t>(x.y),
+                                 static_cast<uint32_t>(x.z), static_cast<uint32_t>(x.w)};
+          uint32_t h16[4];
+          bool big = false;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+            big |= fmaxf(fabsf(lo), fabsf(hi)) > 65504.f;
+            h16[e] = pack_f16x2(lo, hi);
+          }
+          if (big) record_error(P.err, kDevAssert, 61);
+          x = make_int4(static_cast<int>(h16[0]), static_cast<int>(h16[1]), static_cast<int>(h16[2]),
+                        static_cast<int>(h16[3]));
+        }
+        *reinterpret_cast<int4*>(qt + box * (128 * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = x;
       }
     }
     fence_proxy_async_smem();
@@ -338,17 +355,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       if (live) {
         const uint8_t* src = smem + L::kStageOff + st * L::kStageBytes;
         uint8_t* dst = smem + L::kRing + slot * L::kKvBytes;
-        constexpr int kPieces = kChunk * D / 16;   // 16 codes each
-#pragma unroll 4
-        for (int pc = ct; pc < kPieces; pc += 64) {
-          const int r = pc / (D / 16), pp = pc - r * (D / 16);
-          const uint4 in = *reinterpret_cast<const uint4*>(src + r * D + 16 * pp);
-          uint32_t o[8];
-          e4m3x16_to_bf16(in, o);
-          const int col = 16 * pp, box = col >> 6, cc = (col & 63) >> 3;
-          uint8_t* rowp = dst + box * L::kBoxBytes + r * 128;
-          *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        // piece pc = 16 codes at byte 16 pc of the staged chunk (key
+        // pc / (D / 16), columns 16 (pc % (D / 16)) ..); a group's pieces are
+        // all loaded before its first store (loads and stores share the
+        // address space, so the compiler would otherwise keep each piece's
+        // load behind the previous piece's stores)
+        constexpr int kPer = kChunk * D / 16 / 64;   // pieces per converter thread
+        constexpr int kGroup = 8;
+#pragma unroll 1
+        for (int g0 = 0; g0 < kPer; g0 += kGroup) {
+          uint4 in[kGroup];
+#pragma unroll
+          for (int i = 0; i < kGroup; ++i)
+            in[i] = *reinterpret_cast<const uint4*>(src + 16 * (ct + 64 * (g0 + i)));
+#pragma unroll
+          for (int i = 0; i < kGroup; ++i) {
+            const int pc = ct + 64 * (g0 + i);
+            const int r = pc / (D / 16), pp = pc - r * (D / 16);
+            uint32_t o[8];
+            e4m3x16_to_f16(in[i], o);
+            const int col = 16 * pp, box = col >> 6, cc = (col & 63) >> 3;
+            uint8_t* rowp = dst + box * L::kBoxBytes + r * 128;
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
         }
         fence_proxy_async_smem();
       }
@@ -363,8 +393,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     // per chunk j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) -- while the tensor
     // core works for one tile, the other tile's softmax runs
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kChunk, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      // a staged (E4M3 prefix) split: fp16 operands throughout
+      const uint32_t idesc_s = staged ? idesc_f16_f32(128, kChunk, false) : idesc_bf16_f32(128, kChunk, false);
+      const uint32_t idesc_o = staged ? idesc_f16_f32(128, D, true) : idesc_bf16_f32(128, D, true);
       const uint32_t q_base = smem_addr(smem + L::kQ);
       const uint32_t ring_base = smem_addr(smem + L::kRing);
       // descriptors built once; a k-step adds its byte offset / 16 to the
@@ -446,13 +477,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       // key validity: only the last prefix chunk of a split and the tree
       // chunks need a mask (key count, ancestor words for tree keys)
       const bool pref = j < n_pref;
-      // E4M3 prefix chunk: S carries the page's key scale, P the value scale
-      float sl2j = sl2, svj = 1.f, isvj = 1.f;
-      if (F8 && pref) {
+      // E4M3 prefix chunk: S carries the page's key scale, P (fp16: a value
+      // scale above 65504 is reported) the value scale
+      float sl2j = sl2, svj = 1.f;
+      if (staged) {
         const int64_t pg = static_cast<int64_t>(kvh) * it.sstride + split_start / kChunk + j;
         sl2j = sl2 * __ldg(it.kscale + pg);
         svj = __ldg(it.vscale + pg);
-        isvj = svj > 0.f ? 1.f / svj : 0.f;
+        if (svj > 65504.f && row == 0) record_error(P.err, kDevAssert, 62);
       }
       const int t0 = pref ? 0 : (j - n_pref) * kChunk;
       const int nvalid = pref ? min(kChunk, split_end - (split_start + j * kChunk)) : min(kChunk, it.m - t0);
@@ -531,12 +563,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
           for (int e = 0; e < 16; ++e) {
             const float p0 = ex2(fmaf(v[32 * q + 2 * e], sl2j, -mref));
             const float p1 = ex2(fmaf(v[32 * q + 2 * e + 1], sl2j, -mref));
-            hi[e] = F8 ? pack_bf16x2(p0 * svj, p1 * svj) : pack_bf16x2(p0, p1);
+            hi[e] = staged ? pack_f16x2(p0 * svj, p1 * svj) : pack_bf16x2(p0, p1);
             // the row sum takes the weights the MMA uses: the bf16-rounded
-            // ones for prefix keys (a dominant key's rounding then cancels in
-            // the normalisation), hi + lo ~ p for tree keys
-            ls[e & 3] += pref ? (__uint_as_float(hi[e] << 16) + __uint_as_float(hi[e] & 0xffff0000u)) * isvj
-                              : p0 + p1;
+            // ones for bf16 prefix keys (a dominant key's rounding then
+            // cancels in the normalisation), hi + lo ~ p for tree keys, p for
+            // E4M3 prefix keys (fp16 weights, 2^-11 relative)
+            ls[e & 3] += (pref && !staged)
+                             ? __uint_as_float(hi[e] << 16) + __uint_as_float(hi[e] & 0xffff0000u)
+                             : p0 + p1;
             if (!pref) {
               const float r0 = p0 - __uint_as_float(hi[e] << 16);
               const float r1 = p1 - __uint_as_float(hi[e] & 0xffff0000u);

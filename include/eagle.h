@@ -415,6 +415,12 @@ eagle_status eagle_tree_attn_paged_batched(const eagle_attn_paged_item* items, i
  *                    scales prefix tokens 128 p .. 128 p + 127 of that head;
  *                    scale_head_stride >= ceil(prefix_len / 128).
  * q, tree_k, tree_v: bf16 as for eagle_tree_attn; out fp32.
+ * The prefix's products run on fp16 tensor-core operands (codes widened
+ * exactly; the query as fp16, exact for magnitudes in [2^-14, 65504];
+ * softmax weights times the page's value scale as fp16): a query element
+ * above 65504 in magnitude is reported as EAGLE_ERR_DEVICE_ASSERT with
+ * detail 61, a value scale above 65504 with detail 62 (outputs then
+ * unspecified).
  * head_dim 128 only (EAGLE_ERR_UNSUPPORTED_SHAPE otherwise); everything else
  * as for eagle_tree_attn_batched. */
 typedef struct {

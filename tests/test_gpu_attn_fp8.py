@@ -38,7 +38,7 @@ def _oracle(a, ref, S):
                               ref["mask"], S)
 
 
-def _run(problems, hq, hkv):
+def _run(problems, hq, hkv, expect=(0, 0)):
     items, keep = [], []
     for a, ref, S in problems:
         dev = {k: v.cuda() for k, v in a.items()}
@@ -49,7 +49,7 @@ def _run(problems, hq, hkv):
         keep.append((dev, mask, out))
     ws = eb.eagle_tree_attn_fp8_batched(items, hq, hkv, 128, device=torch.device("cuda"))
     torch.cuda.synchronize()
-    assert eb.workspace_error(ws) == (0, 0)
+    assert eb.workspace_error(ws) == expect
     return [k[2].cpu().numpy() for k in keep]
 
 
@@ -59,6 +59,9 @@ def _run(problems, hq, hkv):
     (45, 8, 1, 4099),      # MQA, ragged prefix (last page partial)
     (16, 8, 2, 0),         # no prefix: tree keys only
     (100, 16, 4, 257),     # two tree chunks
+    (256, 8, 2, 1000),     # two full tree chunks after eight pages
+    (60, 8, 1, 40000),     # one kv head: many prefix splits
+    (24, 16, 2, 12345),    # a few prefix splits, ragged last page
 ])
 def test_fp8_prefix_matches_the_oracle(m, hq, hkv, S):
     a, ref = _problem(m, hq, hkv, S, seed=m + S)
@@ -84,6 +87,22 @@ def test_fp8_batched_ragged_items_with_different_scales():
                                  a["tree_v"].float().numpy().ravel()])
         tol = peaked_tol(values) if sk > 1.0 else ATTN_TOL
         assert err <= tol, (S, sk, err, tol)
+
+
+def test_fp8_reports_a_query_outside_the_fp16_range():
+    # the prefix's products are formed from an fp16 copy of the query: an
+    # element above 65504 in magnitude is reported (detail 61), not rounded
+    a, ref = _problem(16, 8, 2, 300, seed=5)
+    a["q"][3, 1, 7] = 1.0e5
+    _run([(a, ref, 300)], 8, 2, expect=(eb.EAGLE_ERR_DEVICE_ASSERT, 61))
+
+
+def test_fp8_reports_a_value_scale_outside_the_fp16_range():
+    # P carries the page's value scale in fp16: a scale above 65504 is
+    # reported (detail 62)
+    a, ref = _problem(16, 8, 2, 300, seed=6)
+    a["vs"][1, 2] = 1.0e5
+    _run([(a, ref, 300)], 8, 2, expect=(eb.EAGLE_ERR_DEVICE_ASSERT, 62))
 
 
 def test_fp8_rejects_other_head_dims():
