@@ -94,20 +94,18 @@ struct TcParams {
   int32_t* err;
 };
 
-// F8: the prefix comes from an E4M3 cache -- a staging ring of E4M3 chunks
-// (TMA) that two warps widen into the 16-bit ring, which is shallower then.
+// F8: the prefix comes from an E4M3 cache -- a chunk's codes land (TMA) in
+// the upper half of its ring slot, where two warps widen them in place.
 template <int D, bool F8 = false>
 struct TcSmem {
-  static constexpr int kQTileBytes = 128 * D * 2;       // one 128-row bf16 query tile
+  static constexpr int kQTileBytes = 128 * D * 2;       // one 128-row 16-bit query tile
   static constexpr int kKvBytes = kChunk * D * 2;       // one K or V chunk (128 keys)
   static constexpr int kBoxBytes = kChunk * 128;        // 128 rows x 64 elements (128 B)
-  static constexpr int kSlotsT = F8 ? 3 : kSlots;       // bf16 ring depth
-  static constexpr int kStage = F8 ? 4 : 0;             // E4M3 staging ring depth
-  static constexpr int kStageBytes = kChunk * D;        // one E4M3 chunk
+  static constexpr int kCodeBytes = kChunk * D;         // one E4M3 chunk
+  static constexpr int kCodeOff = kKvBytes - kCodeBytes;   // its place in the slot
   static constexpr int kQ = 0;                          // the CTA's two query tiles
   static constexpr int kRing = kQ + 2 * kQTileBytes;
-  static constexpr int kStageOff = kRing + kSlotsT * kKvBytes;
-  static constexpr int kBars = kStageOff + kStage * kStageBytes;
+  static constexpr int kBars = kRing + kSlots * kKvBytes;
   static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
 };
@@ -147,7 +145,6 @@ template <int D, bool F8>
 __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams P) {
   pdl_trigger();   // let a dependent launch of the next kernel start (see pdl_attribute)
   using L = TcSmem<D, F8>;
-  constexpr int kSlots = L::kSlotsT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -158,9 +155,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   uint64_t* o_done = p_full + 2;        // [query tile]: that tile's PV done
   uint64_t* drain = o_done + 2;         // [1]
   uint64_t* q_ready = drain + 1;        // [1] both Q tiles written (8 softmax warps)
-  uint64_t* full8 = q_ready + 1;        // [kStage] E4M3 chunk landed (F8)
-  uint64_t* empty8 = full8 + 4;         // [kStage] E4M3 chunk widened (F8)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty8 + 4);
+  uint64_t* full8 = q_ready + 1;        // [slot] E4M3 codes landed (F8)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full8 + kSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -220,12 +216,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   // written as fp16, P is fp16) and the tree split stays bf16.
   const bool staged = F8 && !tree_split;
   auto issue_stage = [&](int n) {
-    const int st = n % L::kStage;
+    const int slot = n % kSlots;
     const int j = n >> 1;
     const CUtensorMap* map = (n & 1) ? &P.vmap[item] : &P.kmap[item];
-    mbar_arrive_expect_tx(&full8[st], static_cast<uint32_t>(L::kStageBytes));
-    tma_load_3d(smem + L::kStageOff + st * L::kStageBytes, map, 0, split_start + j * kChunk, kvh,
-                &full8[st]);
+    mbar_arrive_expect_tx(&full8[slot], static_cast<uint32_t>(L::kCodeBytes));
+    tma_load_3d(smem + L::kRing + slot * L::kKvBytes + L::kCodeOff, map, 0, split_start + j * kChunk,
+                kvh, &full8[slot]);
   };
 
   if (tid == 0) {
@@ -233,10 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < L::kStage; ++s) {
-      mbar_init(&full8[s], 1);
-      mbar_init(&empty8[s], 1);
-    }
+    for (int s = 0; F8 && s < kSlots; ++s) mbar_init(&full8[s], 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);   // one arrival per warp of the tile's warpgroup
@@ -248,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
     fence_barrier_init();
     // the producer (this thread) starts streaming before the CTA-wide barrier
     if (staged) {
-      for (int n = 0; n < L::kStage && n < 2 * n_chunks; ++n) issue_stage(n);
+      for (int n = 0; n < kSlots && n < 2 * n_chunks; ++n) issue_stage(n);
     } else {
       for (int n = 0; n < kSlots && n < 2 * n_chunks; ++n) issue_kv(n);
     }
@@ -315,16 +308,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0 && staged) {
-      int issued = L::kStage < 2 * n_chunks ? L::kStage : 2 * n_chunks;   // the prologue's
+      int issued = kSlots < 2 * n_chunks ? kSlots : 2 * n_chunks;   // the prologue's
       for (int n = issued; n < 2 * n_chunks; ++n) {
-        const int st = n % L::kStage, use = n / L::kStage;
-        if (!bounded_wait(&empty8[st], (use - 1) & 1, P.err, abort_flag, 21)) break;
+        const int slot = n % kSlots, use = n / kSlots;
+        if (!bounded_wait(&empty[slot], (use - 1) & 1, P.err, abort_flag, 21)) break;
         issue_stage(n);
         issued = n + 1;
       }
       // make sure no copy of ours is still landing when the CTA leaves
-      for (int n = (issued > L::kStage ? issued - L::kStage : 0); n < issued; ++n)
-        mbar_wait(&full8[n % L::kStage], (n / L::kStage) & 1, 200000000ull);
+      for (int n = (issued > kSlots ? issued - kSlots : 0); n < issued; ++n)
+        mbar_wait(&full8[n % kSlots], (n / kSlots) & 1, 200000000ull);
     } else if (lane == 0) {
       int issued = kSlots < 2 * n_chunks ? kSlots : 2 * n_chunks;   // the prologue's
       for (int n = issued; n < 2 * n_chunks; ++n) {
@@ -338,55 +331,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const __grid_con
         mbar_wait(&full[n % kSlots], (n / kSlots) & 1, 200000000ull);
     }
   } else if (staged && (warp == 2 || warp == 3)) {
-    // ================================================================ E4M3 -> bf16
-    // item n: the staged E4M3 chunk [128 keys][D codes] -> bf16 ring slot
-    // n % kSlots in the layout a bf16 TMA would have written (boxes of 64
-    // columns, 128-byte rows, 128-byte swizzle).  Both warps run every item
-    // and meet at a named barrier in each, also after a wait ran out.
+    // ================================================================ E4M3 -> fp16
+    // item n: the codes [128 keys][D codes] in the upper half of ring slot
+    // n % kSlots -> fp16 in the whole slot, in the layout a 16-bit TMA would
+    // have written (boxes of 64 columns, 128-byte rows, 128-byte swizzle).
+    // Every code of the chunk is read into registers before the first store
+    // (a named barrier between), since the stores cover the codes.  Both
+    // warps run every item and meet at the barriers, also after a wait ran
+    // out.
     const int ct = tid - 64;   // 0..63
+    constexpr int kPer = kChunk * D / 16 / 64;   // pieces (16 codes) per converter thread
     bool live = true;
     for (int n = 0; n < 2 * n_chunks; ++n) {
-      const int st = n % L::kStage, slot = n % kSlots;
-      live = live && __all_sync(0xffffffffu, bounded_wait(&full8[st], (n / L::kStage) & 1, P.err,
+      const int slot = n % kSlots;
+      live = live && __all_sync(0xffffffffu, bounded_wait(&full8[slot], (n / kSlots) & 1, P.err,
                                                           abort_flag, 22));
-      if (live && n >= kSlots)
-        live = __all_sync(0xffffffffu, bounded_wait(&empty[slot], (n / kSlots - 1) & 1, P.err,
-                                                     abort_flag, 23));
+      uint8_t* dst = smem + L::kRing + slot * L::kKvBytes;
+      // piece pc = 16 codes at byte 16 pc of the codes (key pc / (D / 16),
+      // columns 16 (pc % (D / 16)) ..)
+      uint4 in[kPer];
       if (live) {
-        const uint8_t* src = smem + L::kStageOff + st * L::kStageBytes;
-        uint8_t* dst = smem + L::kRing + slot * L::kKvBytes;
-        // piece pc = 16 codes at byte 16 pc of the staged chunk (key
-        // pc / (D / 16), columns 16 (pc % (D / 16)) ..); a group's pieces are
-        // all loaded before its first store (loads and stores share the
-        // address space, so the compiler would otherwise keep each piece's
-        // load behind the previous piece's stores)
-        constexpr int kPer = kChunk * D / 16 / 64;   // pieces per converter thread
-        constexpr int kGroup = 8;
-#pragma unroll 1
-        for (int g0 = 0; g0 < kPer; g0 += kGroup) {
-          uint4 in[kGroup];
 #pragma unroll
-          for (int i = 0; i < kGroup; ++i)
-            in[i] = *reinterpret_cast<const uint4*>(src + 16 * (ct + 64 * (g0 + i)));
+        for (int i = 0; i < kPer; ++i)
+          in[i] = *reinterpret_cast<const uint4*>(dst + L::kCodeOff + 16 * (ct + 64 * i));
+      }
+      named_sync(2, 64);
+      if (live) {
 #pragma unroll
-          for (int i = 0; i < kGroup; ++i) {
-            const int pc = ct + 64 * (g0 + i);
-            const int r = pc / (D / 16), pp = pc - r * (D / 16);
-            uint32_t o[8];
-            e4m3x16_to_f16(in[i], o);
-            const int col = 16 * pp, box = col >> 6, cc = (col & 63) >> 3;
-            uint8_t* rowp = dst + box * L::kBoxBytes + r * 128;
-            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
+        for (int i = 0; i < kPer; ++i) {
+          const int pc = ct + 64 * i;
+          const int r = pc / (D / 16), pp = pc - r * (D / 16);
+          uint32_t o[8];
+          e4m3x16_to_f16(in[i], o);
+          const int col = 16 * pp, box = col >> 6, cc = (col & 63) >> 3;
+          uint8_t* rowp = dst + box * L::kBoxBytes + r * 128;
+          *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(rowp + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
         fence_proxy_async_smem();
       }
       named_sync(2, 64);
-      if (ct == 0 && live) {
-        mbar_arrive(&full[slot]);
-        mbar_arrive(&empty8[st]);
-      }
+      if (ct == 0 && live) mbar_arrive(&full[slot]);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
