@@ -121,7 +121,6 @@ __device__ __forceinline__ Key warp_max_key(Key k) {
   return k;
 }
 
-static_assert(kKMax <= 127, "union_rank probes lists of at most 127 entries");
 static_assert(kWarps * kKMax >= kThreads, "the warp lists hold one key per thread (first-slot bound)");
 
 struct StreamSmem {
@@ -248,10 +247,12 @@ static __device__ __noinline__ int warp_select(const Key* buf, int n, int K, Key
   return n < K ? n : K;
 }
 
-// Rank of entry c of list p in the union of nl <= 8 lists at stride
-// `stride` (each sorted best first, counts cnt, keys distinct): c plus, for
-// every other list, the length of its prefix of entries before it, found by
-// a branch-free binary search (7 probes: lists hold at most 64 entries).
+// Rank of entry c of list p in the union of nl lists at stride `stride`
+// (each sorted best first, counts cnt, keys distinct): c plus, for every
+// other list, the number of its entries before it -- counted over the whole
+// list with independent loads (a dependent binary-search probe costs ~90
+// cycles on this part, so a search over lists of up to 127 entries is slower
+// than the count).
 __device__ __forceinline__ int union_rank(const Key* L, const int* cnt, int nl, int stride, int p,
                                           int c) {
   const Key e = L[p * stride + c];
@@ -260,11 +261,10 @@ __device__ __forceinline__ int union_rank(const Key* L, const int* cnt, int nl, 
     if (q == p) continue;
     const Key* lq = L + q * stride;
     const int n = cnt[q];
-    int pos = 0;   // entries of list q before e
-#pragma unroll
-    for (int s = 64; s; s >>= 1)
-      if (pos + s <= n && lq[pos + s - 1] > e) pos += s;
-    r += pos;
+    int before = 0;
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) before += lq[i] > e ? 1 : 0;
+    r += before;
   }
   return r;
 }
@@ -293,13 +293,11 @@ __device__ __forceinline__ void prune_lists(const Key* L, int* cnt, int nl, int 
   if (tau == 0ull) return;
   if (lane < nl) {
     const Key* lq = L + lane * stride;
-    int lo = 0, hi = cnt[lane];   // entries at or before tau form a prefix
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (lq[mid] < tau) hi = mid;
-      else lo = mid + 1;
-    }
-    cnt[lane] = lo;
+    const int n = cnt[lane];   // entries at or before tau form a prefix: count them
+    int keep = 0;
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) keep += lq[i] >= tau ? 1 : 0;
+    cnt[lane] = keep;
   }
   __syncwarp();
 }
