@@ -823,8 +823,8 @@ TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch on the c2
     # workload from one ncu capture, keyed by the kernel's source hash
     # (_kernel_source_hash)
-    "build:c2": ("66ece9890652", 31668736),
-    "verify:c2": ("6227d054bb03", 37138944),
+    "build:c2": ("0f1a8ab75a63", 31661824),
+    "verify:c2": ("b5d0d9c135ae", 37131520),
     "attn:c2": ("b5a540d7fecd", 17385472),
 }
 

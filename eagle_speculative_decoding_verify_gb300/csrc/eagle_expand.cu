@@ -87,6 +87,16 @@ static __device__ __noinline__ void expand_level(const ExpandArgs& A, StreamSmem
   float* rv = reinterpret_cast<float*>(lse + kKMax);              // [kKMax * kKMax]
   int* ri = reinterpret_cast<int*>(rv + kKMax * kKMax);           // [kKMax * kKMax]
   uint64_t* lk = reinterpret_cast<uint64_t*>(ri + kKMax * kKMax); // [kKMax * kKMax]
+  int* nf = reinterpret_cast<int*>(lk + kKMax * kKMax);           // [kKMax] next frontier
+  int* pf = nf + kKMax;                                            // [kKMax] frontier slots
+  uint64_t* pkey = reinterpret_cast<uint64_t*>(pf + kKMax);       // [kKMax] their keys
+  // the frontier and its keys load beside the row records (not after them)
+  if (L > 0 && tid >= kThreads - k) {
+    const int sl = tid - (kThreads - k);
+    const int pa = T.frontier[sl];
+    pf[sl] = pa;
+    pkey[sl] = T.key[pa];
+  }
   for (int r = tid; r < n; r += kThreads) {
     const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rows + r * rb);
     lse[r] = static_cast<double>(h->max) + log_d(h->sum);
@@ -109,8 +119,8 @@ static __device__ __noinline__ void expand_level(const ExpandArgs& A, StreamSmem
       pa = -1;
     } else {
       const int s = e / k, c = e - s * k;
-      pa = T.frontier[s];
-      key = order_key(key_value(T.key[pa]) + (static_cast<double>(rv[s * k + c]) - lse[s]));
+      pa = pf[s];
+      key = order_key(key_value(pkey[s]) + (static_cast<double>(rv[s * k + c]) - lse[s]));
     }
     lk[e] = key;
     T.key[base + e] = key;
@@ -119,7 +129,6 @@ static __device__ __noinline__ void expand_level(const ExpandArgs& A, StreamSmem
   }
   __syncthreads();
   // rank within the depth by counting; the best top_k form the next frontier
-  int* nf = reinterpret_cast<int*>(lk + kKMax * kKMax);           // [kKMax]
   for (int e = tid; e < cnt; e += kThreads) {
     const uint64_t kv = lk[e];
     int r = 0;
@@ -156,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 2) expand_kernel(const __grid_consta
   if (item_arrive(A.rs, S, cx.item)) expand_level(A, S);
 }
 
-static_assert(kScratchBytes >= 8 * kKMax + (4 + 4 + 8) * kKMax * kKMax + 4 * kKMax,
+static_assert(kScratchBytes >= 8 * kKMax + (4 + 4 + 8) * kKMax * kKMax + (4 + 4 + 8) * kKMax,
               "expand scratch must fit in the stream's shared memory");
 
 struct FinalArgs {
@@ -171,6 +180,7 @@ __device__ __forceinline__ int depth_of(int a, int k) { return a < k ? 1 : 2 + (
 // The final top-(m-1) cut over all depths and the tree arrays (one CTA).
 __global__ void __launch_bounds__(kThreads) finalize_kernel(const __grid_constant__ FinalArgs A) {
   __shared__ uint64_t skey[EAGLE_MAX_CANDIDATES];
+  __shared__ int sidx[EAGLE_MAX_CANDIDATES];
   __shared__ int node[EAGLE_MAX_CANDIDATES];
   __shared__ int npar[EAGLE_MAX_TREE];
   __shared__ int warp_tot[kWarps];
@@ -187,8 +197,14 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const __grid_constan
   }
   // a candidate is kept iff fewer than need = m - 1 candidates come before it:
   // its rank in its own depth plus, for every other depth, the entries before
-  // it (binary search over that depth's keys in sorted order)
-  for (int i = tid; i < C; i += kThreads) skey[i] = T.key[T.srt[i]];
+  // it (binary search over that depth's keys in sorted order, keys and
+  // candidate ids both in shared memory: a probe that waited on a global load
+  // would cost an L2 round trip)
+  for (int i = tid; i < C; i += kThreads) {
+    const int c = T.srt[i];
+    sidx[i] = c;
+    skey[i] = T.key[c];
+  }
   __syncthreads();
   const int need = m - 1;
   for (int a = tid; a < C; a += kThreads) {
@@ -202,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const __grid_constan
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         const uint64_t o = skey[lb + mid];
-        const bool go = (o > kv) | ((o == kv) & (T.srt[lb + mid] < a));
+        const bool go = (o > kv) | ((o == kv) & (sidx[lb + mid] < a));
         lo = go ? mid + 1 : lo;
         hi = go ? hi : mid;
       }

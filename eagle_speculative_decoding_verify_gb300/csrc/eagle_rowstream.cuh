@@ -906,20 +906,24 @@ static __device__ __forceinline__ RowCtx stream_row(const RowJob& Jb, StreamSmem
 
 // The row's leader arrives on its item's counter after the caller's per-row
 // step; true for the one CTA whose row arrives last (it then runs the item's
-// final step and may read every row result of the item).
+// final step and may read every row result of the item).  One
+// acquire-release atomic at GPU scope orders both ways: the CTA barrier before
+// it puts every thread's row writes before the release (cumulative), and the
+// barrier after it puts the acquire before every thread's later reads.
 static __device__ __forceinline__ bool item_arrive(const RowStream& P, StreamSmem& S, int item) {
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const uint32_t old = atomicAdd(&P.item_cnt[item], 1u);
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(P.item_cnt + item)
+                 : "memory");
     const bool last = old == static_cast<uint32_t>(P.rows_per_item - 1);
     if (last) P.item_cnt[item] = 0u;
     S.flag = last ? 1 : 0;
   }
   __syncthreads();
-  const bool last = S.flag != 0;
-  if (last) __threadfence();
-  return last;
+  return S.flag != 0;
 }
 
 }  // namespace eagle
