@@ -66,6 +66,7 @@ struct ExpandArgs {
   RowStream rs;
   TreeState st;
   int top_k, depth, level;
+  int warm_stream;      // 1: a stream code warm-up cluster follows the rows' (long rows)
   int32_t* front_out;   // [2][top_k]: tokens and parent slots of the new frontier, or null
 };
 
@@ -154,14 +155,22 @@ static __device__ __noinline__ void expand_level(const ExpandArgs& A, StreamSmem
   if (tid == 0) *T.levels = L + 1;
 }
 
+// Grid: the rows' clusters, then (long rows: stream_warm_up) one cluster that
+// streams the short warm-up row through the same code at launch (see
+// warm_row_job): after an L2 flush the first launch of a round would
+// otherwise fetch that code from HBM in every row's cluster at once.
 __global__ void __launch_bounds__(kThreads, 2) expand_kernel(const __grid_constant__ ExpandArgs A) {
   extern __shared__ __align__(128) char smem_raw[];
   StreamSmem& S = *reinterpret_cast<StreamSmem*>(smem_raw);
   const int PC = A.rs.ctas_per_row;
+  const int64_t rows = static_cast<int64_t>(A.rs.n_items) * A.rs.rows_per_item;
+  const int64_t cl = blockIdx.x / PC;
+  const int rank = static_cast<int>(blockIdx.x - cl * PC);
   pdl_trigger();
-  pdl_wait();
-  const RowCtx cx = stream_row(row_job(A.rs, blockIdx.x / PC, static_cast<int>(blockIdx.x % PC)), S);
-  if (!cx.leader) return;
+  const bool warm = cl >= rows;   // (only when warm_stream)
+  if (!warm) pdl_wait();          // the warm-up touches no caller memory
+  const RowCtx cx = stream_row(warm ? warm_row_job(A.rs, rank) : row_job(A.rs, cl, rank), S);
+  if (!cx.leader || warm) return;
   if (item_arrive(A.rs, S, cx.item)) expand_level(A, S);
 }
 
@@ -330,7 +339,7 @@ extern "C" eagle_status eagle_tree_expand(const float* rows, int64_t row_stride,
   memset(&A, 0, sizeof(A));
   const int occ = stream_ctas_per_sm(expand_kernel);
   if (occ <= 0) return EAGLE_ERR_CUDA;
-  const int ctas = stream_ctas_per_row(expand_kernel, L, occ);
+  const int ctas = stream_ctas_per_row(expand_kernel, L, occ, 1);
   if (ctas <= 0) return EAGLE_ERR_CUDA;
   fill_stream(A.rs, L, static_cast<char*>(ws), 1, n_rows, vocab, row_stride, ctas, false);
   A.rs.base[0] = rows;
@@ -342,7 +351,9 @@ extern "C" eagle_status eagle_tree_expand(const float* rows, int64_t row_stride,
   A.depth = depth;
   A.level = level;
   A.front_out = frontier_out;
-  return launch_stream(expand_kernel, A, L.n_rows, ctas, reinterpret_cast<cudaStream_t>(stream));
+  A.warm_stream = stream_warm_up(L.tiles_per_row, ctas) ? 1 : 0;
+  return launch_stream(expand_kernel, A, L.n_rows + A.warm_stream, ctas,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" eagle_status eagle_tree_finalize(const void* state, int32_t top_k, int32_t depth,
