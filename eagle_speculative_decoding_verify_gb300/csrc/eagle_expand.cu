@@ -98,10 +98,8 @@ static __device__ __noinline__ void expand_level(const ExpandArgs& A, StreamSmem
     pf[sl] = pa;
     pkey[sl] = T.key[pa];
   }
-  for (int r = tid; r < n; r += kThreads) {
-    const volatile RecHead* h = reinterpret_cast<volatile RecHead*>(rows + r * rb);
-    lse[r] = static_cast<double>(h->max) + log_d(h->sum);
-  }
+  for (int r = tid; r < n; r += kThreads)   // each row's leader put its logsumexp in the record
+    lse[r] = reinterpret_cast<const volatile RecHead*>(rows + r * rb)->sum;
   for (int e = tid; e < n * k; e += kThreads) {
     const int r = e / k, c = e - r * k;
     rv[e] = __ldcg(rec_val(rows + r * rb) + c);
@@ -150,8 +148,7 @@ static __device__ __noinline__ void expand_level(const ExpandArgs& A, StreamSmem
       A.front_out[k + tid] = L == 0 ? 0 : e / k;
     }
   }
-  __threadfence();
-  __syncthreads();
+  // the next call reads the state after this kernel has completed
   if (tid == 0) *T.levels = L + 1;
 }
 
@@ -169,8 +166,15 @@ __global__ void __launch_bounds__(kThreads, 2) expand_kernel(const __grid_consta
   pdl_trigger();
   const bool warm = cl >= rows;   // (only when warm_stream)
   if (!warm) pdl_wait();          // the warm-up touches no caller memory
-  const RowCtx cx = stream_row(warm ? warm_row_job(A.rs, rank) : row_job(A.rs, cl, rank), S);
+  const RowJob R = warm ? warm_row_job(A.rs, rank) : row_job(A.rs, cl, rank);
+  const RowCtx cx = stream_row(R, S);
   if (!cx.leader || warm) return;
+  // the row's logsumexp replaces the record's sum, here in parallel over the
+  // rows, as in the one-shot build (the sum holds the max's own term 1, so its
+  // log is >= 0, kept so through the rounding of log_d)
+  if (threadIdx.x == 0)
+    reinterpret_cast<RecHead*>(R.rec)->sum =
+        static_cast<double>(S.rmax) + fmax(0.0, log_d(S.rsum));
   if (item_arrive(A.rs, S, cx.item)) expand_level(A, S);
 }
 
