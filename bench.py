@@ -825,7 +825,7 @@ TRAFFIC = {
     # (_kernel_source_hash)
     "build:c2": ("0f1a8ab75a63", 31661824),
     "verify:c2": ("b5d0d9c135ae", 37131520),
-    "attn:c2": ("b5a540d7fecd", 17385472),
+    "attn:c2": ("c9246df8275b", 17385472),
 }
 
 
@@ -1019,6 +1019,34 @@ def run_reference(args):
     }
 
 
+def profile_calls(case):
+    """Three untimed iterations of one workload's library calls (a case for
+    a profiler's launch filter)."""
+    import torch
+    from eagle_speculative_decoding_verify_gb300 import _build
+    _build.build()
+    from eagle_speculative_decoding_verify_gb300 import binding as eb, workloads as wl
+    dev = torch.device("cuda")
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        if case == "c4":
+            st = MultiStep(wl.WORKLOADS["c4"], dev, eb, wl)
+            for _ in range(3):
+                st.run(s)
+        elif case in ("policy", "kv"):
+            st = Step(wl.WORKLOADS["c2"], dev, eb, wl)
+            if case == "policy":
+                tree_policy_bench(eb, wl, dev, st, s, L2Flush(dev), reps=2)
+            else:
+                kv_commit_bench(eb, wl, dev, st, s, reps=3)
+        else:
+            st = Step(wl.WORKLOADS[case], dev, eb, wl)
+            for _ in range(3):
+                st.run(s)
+    s.synchronize()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1036,7 +1064,14 @@ def main():
                          "(a profiling case; prints its own JSON line)")
     ap.add_argument("--fp8", action="store_true",
                     help="with --long-attn-only: also time the E4M3 prefix variant")
+    ap.add_argument("--profile-calls", default="", metavar="CASE",
+                    choices=["", "c0", "c1", "c2", "c4", "policy", "kv"],
+                    help="run three untimed iterations of one workload's calls (c0-c2, c4: "
+                         "build, attention, verify; policy: the tree policies on c2's draft "
+                         "rows; kv: the KV commits) for a profiler, and print no JSON line")
     args = ap.parse_args()
+    if args.profile_calls:
+        return profile_calls(args.profile_calls)
     if args.long_attn_only:
         import torch
         from eagle_speculative_decoding_verify_gb300 import binding as eb, workloads as wl
