@@ -825,7 +825,7 @@ TRAFFIC = {
     # (_kernel_source_hash)
     "build:c2": ("0f1a8ab75a63", 31661824),
     "verify:c2": ("b5d0d9c135ae", 37131520),
-    "attn:c2": ("c9246df8275b", 17385472),
+    "attn:c2": ("8e891d4a011d", 17385472),
 }
 
 

@@ -1070,9 +1070,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(k2Threads, 1)
 
 // Split merge: one block per (kv head, 128-row tile, 32 rows, 32 columns);
 // lanes are rows, so every partial load is a coalesced 128-byte line; warp w
-// combines columns 4w..4w+3 online over the splits (running max in log2
-// units); the 32 x 32 result leaves row by row through a shared-memory
-// transpose.  Partials: o column-major [unit][d][128 rows], (max, sum)
+// combines columns 4w..4w+3 over the splits; the 32 x 32 result leaves row
+// by row through a shared-memory transpose.  kOnce (up to kMergeOnce splits,
+// a grid of at most one wave at its occupancy): every partial is loaded at
+// once, then the splits' maximum and the weighted sum, so the loads cost one
+// round trip, at ~110 registers a thread; otherwise online over the splits
+// (running max in log2 units, 32 registers: many blocks per SM for large
+// grids).  Partials: o column-major [unit][d][128 rows], (max, sum)
 // [unit][128 rows].
 struct TcMergeParams {
   TcItem items[kTcMaxItems];
@@ -1082,7 +1086,9 @@ struct TcMergeParams {
   const float2* part_ml;
 };
 
-template <int D>
+constexpr int kMergeOnce = 16;
+
+template <int D, bool kOnce>
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constant__ TcMergeParams P) {
   pdl_trigger();   // let a dependent launch of the next kernel start (see pdl_attribute)
   __shared__ float tile[32][33];
@@ -1103,7 +1109,30 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const __grid_constan
   const int64_t u0 = it.part_start + static_cast<int64_t>(pair) * S;
   float mx = -INFINITY, l = 0.f;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (128 * tp + rb * 32 < M) {
+  constexpr int kPre = kMergeOnce;
+  if (kOnce && 128 * tp + rb * 32 < M) {
+    float2 ml[kPre];
+    float o[kPre][4];
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+      if (s < S) {
+        ml[s] = __ldcg(P.part_ml + (u0 + s) * 128 + r);
+        const float* po = P.part_o + ((u0 + s) * D + c0) * 128 + r;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[s][e] = __ldcg(po + e * 128);
+      }
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+      if (s < S) mx = fmaxf(mx, ml[s].x);
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+      if (s < S) {
+        const float w = ml[s].x == -INFINITY ? 0.f : ex2(ml[s].x - mx);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = fmaf(w, o[s][e], acc[e]);
+        l = fmaf(w, ml[s].y, l);
+      }
+  } else if (!kOnce && 128 * tp + rb * 32 < M) {
 #pragma unroll 4
     for (int s = 0; s < S; ++s) {
       const float2 ml = __ldcg(P.part_ml + (u0 + s) * 128 + r);
@@ -1272,6 +1301,17 @@ size_t attn_tc_ws_size(const eagle_attn_item* items, int n, int hq, int hkv, int
   return need;
 }
 
+// The split merge in its one-round form when every tile's splits fit and the
+// grid is one wave at that form's occupancy (two blocks per SM), else online.
+template <int D>
+static void launch_merge(const TcMergeParams& MP, int blocks, int max_splits, int sms,
+                         cudaStream_t stream) {
+  if (max_splits <= kMergeOnce && blocks <= 2 * sms)
+    attn_tc_merge_kernel<D, true><<<blocks, 256, 0, stream>>>(MP);
+  else
+    attn_tc_merge_kernel<D, false><<<blocks, 256, 0, stream>>>(MP);
+}
+
 // tables / pool_rows: per item, the block table and the pool's rows per head
 // of a paged prefix (null arrays: every item contiguous)
 template <int D>
@@ -1370,7 +1410,7 @@ static eagle_status launch_d(const eagle_attn_item* items, int n, int hq, int hk
       MP.g = hq / hkv;
       MP.part_o = P.part_o;
       MP.part_ml = P.part_ml;
-      attn_tc_merge_kernel<D><<<blocks, 256, 0, stream>>>(MP);
+      launch_merge<D>(MP, blocks, T.max_splits, sms, stream);
       if ((st = launch_status()) != EAGLE_OK) return st;
     }
   }
@@ -1467,7 +1507,7 @@ static eagle_status launch_fp8(const eagle_attn_fp8_item* items, int n, int hq, 
       MP.g = hq / hkv;
       MP.part_o = P.part_o;
       MP.part_ml = P.part_ml;
-      attn_tc_merge_kernel<D><<<blocks, 256, 0, stream>>>(MP);
+      launch_merge<D>(MP, blocks, T.max_splits, sms, stream);
       if ((st = launch_status()) != EAGLE_OK) return st;
     }
   }
