@@ -944,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const __grid_consta
     }
     cp_async_commit();
   }
-  const RowCtx cx = stream_row(R, S);
+  const RowCtx cx = stream_row<true>(R, S);
   if (A.mode[cx.item] == kModeNucleus) {   // every CTA of the cluster, once the row max is in place
     __syncwarp();
     cluster_arrive_release();
