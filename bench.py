@@ -824,7 +824,7 @@ TRAFFIC = {
     # workload from one ncu capture, keyed by the kernel's source hash
     # (_kernel_source_hash)
     "build:c2": ("4c6a3a648a66", 31661824),
-    "verify:c2": ("b5d0d9c135ae", 37131520),
+    "verify:c2": ("a5769f8446cb", 36646400),
     "attn:c2": ("8e891d4a011d", 17385472),
 }
 
