@@ -1,6 +1,9 @@
 // Tensor-core path of eagle_tree_attn for bf16 Q/K/V: head_dim 128 runs the
 // 2-SM kernel (attn2_kernel, a cluster of two CTAs per work unit, tcgen05
-// .cta_group::2), head_dim 64 the 1-SM kernel below (attn_tc_kernel).
+// .cta_group::2), head_dim 64 the 1-SM kernel below (attn_tc_kernel).  An
+// E4M3 prefix cache (eagle_tree_attn_fp8_batched, head_dim 128) runs the
+// 1-SM kernel with its prefix chunks widened to fp16 in shared memory and
+// those splits' MMAs on fp16 operands (see TcSmem and the converter warps).
 //
 // Source: "EAGLE-2: Feature-Level Speculative Decoding Guide", "Single-Pass
 // Tree Verification" (one target pass over the tree; a token attends to its
