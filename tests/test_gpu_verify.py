@@ -169,3 +169,30 @@ def test_nucleus_full_vocab_tied_logits():
             acc, n, bonus = _verify(target, ref, False, 1.0, 0, p, seed, 9)
             path_matches(acc, n, bonus, v, f"tied p{p} seed{seed}", ref["parents"],
                          ref["tokens"], target.numpy(), (0, 1.0, 0, p))
+
+
+# Sampling over target rows built to stress the row stream's top-k (a single
+# lane holding a row's best entries, 100 exact copies of a row's maximum, the
+# best entries in the unaligned tail of a row): the verify kernel's second
+# pass reloads its threads' candidate slots ahead of absorbing them, which
+# these rows exercise at the tie rules' edges.
+@pytest.mark.parametrize("kind,V,k,p", [
+    ("one_lane", 40000, 50, 1.0),
+    ("one_lane", 152064, 2, 1.0),
+    ("duplicates", 30000, 50, 1.0),
+    ("duplicates", 152064, 64, 0.9),
+    ("tail", 5003, 64, 1.0),
+    ("tail", 152063, 16, 0.95),
+])
+def test_sampling_on_adversarial_target_rows(kind, V, k, p):
+    from tests.test_gpu_build import _adversarial
+    g = torch.Generator().manual_seed(V + k)
+    draft = torch.randn(51, V, generator=g) * 2.0
+    ref = build_draft_tree(draft.numpy(), 10, 6, 60, 3)
+    target = _adversarial(kind, 60, V, k, 17)
+    for seed in range(2):
+        v = verify_tree(target.numpy(), ref["parents"], ref["tokens"], greedy=False,
+                        temperature=1.0, top_k=k, top_p=p, seed=seed, step=3)
+        acc, n, bonus = _verify(target, ref, False, 1.0, k, p, seed, 3)
+        path_matches(acc, n, bonus, v, f"{kind} V{V} k{k} seed{seed}", ref["parents"],
+                     ref["tokens"], target.numpy(), (0, 1.0, k, p))
