@@ -201,9 +201,9 @@ eagle_status eagle_tree_build_batched(int32_t n_items, const float* const* draft
  *   eagle_tree_build_workspace_size(1, n_rows, vocab, top_k, depth, m),
  *   must fit in EAGLE_NOALLOC_SCRATCH_BYTES; larger shapes return
  *   EAGLE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The size
- *   is about 1.2 KB + R * (16 + 8*top_k, rounded up to 16) bytes, R = 1 +
+ *   is about 0.7 KB + R * (16 + 8*top_k, rounded up to 16) bytes, R = 1 +
  *   (depth-1)*top_k rows: every shape with top_k <= 10 fits; e.g. top_k
- *   12, depth 13 does not (17,408 bytes).
+ *   12, depth 13 does not (16,896 bytes).
  * ------------------------------------------------------------------------ */
 #define EAGLE_NOALLOC_SCRATCH_BYTES (16u * 1024u)
 

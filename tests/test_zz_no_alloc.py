@@ -57,7 +57,7 @@ def test_repeat_after_a_larger_shape_leaves_no_stale_state():
 
 
 def test_rejects_shapes_beyond_the_scratch():
-    k, D, m = 12, 13, 64                       # workspace 17,408 bytes
+    k, D, m = 12, 13, 64                       # workspace 16,896 bytes
     R = 1 + (D - 1) * k
     assert eb.eagle_tree_build_workspace_size(1, R, 1000, k, D, m) > \
         eb.EAGLE_NOALLOC_SCRATCH_BYTES
