@@ -10,11 +10,12 @@
 // Phase 1 (one cluster per row, eagle_rowstream.cuh): one HBM pass over the
 // R draft rows -> per row the top_k (value desc, token id asc) and logsumexp.
 // Phase 2 (the CTA whose row of an item arrives last): candidate values
-// value = parent value + (logit - logsumexp), in fp64; per depth the top_k
-// frontier (ranks by counting within the depth); the final best m-1 (ranks
-// across the depths' sorted prefixes by binary search; order-preserving
-// 64-bit keys, ties -> lower candidate index); node ids by rank in candidate
-// order; ancestor mask by walking parent pointers (depth <= 16).
+// value = parent value + (logit - logsumexp), in fp64; the best m-1 kept
+// level by level as one sorted list, merged with each level's children by
+// counting (order-preserving 64-bit keys, ties -> lower candidate index); a
+// candidate's slot in its level's frontier is its rank among that level's
+// kept entries; node ids by rank in candidate order; ancestor mask by
+// walking parent pointers (depth <= 16).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -178,9 +179,14 @@ static __device__ __noinline__ void assemble_tree(const TreeJob J, StreamSmem& S
       if (e < ne) {
         kv = e < n_y ? ykey[e] : bk[e - n_y];
         a = e < n_y ? ycand[e] : bc[e - n_y];
+        // unrolled: a thread's shared loads go out together, not one per
+        // dependent round
+#pragma unroll 4
         for (int f = sub; f < n_y; f += tpc) before_y += cand_before(ykey[f], ycand[f], kv, a) ? 1 : 0;
-        if (e < n_y)
+        if (e < n_y) {
+#pragma unroll 4
           for (int f = sub; f < nb; f += tpc) before_b += cand_before(bk[f], bc[f], kv, a) ? 1 : 0;
+        }
       }
       for (int o = tpc >> 1; o; o >>= 1) {
         before_y += __shfl_xor_sync(0xffffffffu, before_y, o);
@@ -220,6 +226,7 @@ static __device__ __noinline__ void assemble_tree(const TreeJob J, StreamSmem& S
   for (int i = tid; i < nb; i += kThreads) {
     const int a = sel[i];
     int before_a = 0;
+#pragma unroll 8
     for (int q = 0; q < nb; ++q) before_a += sel[q] < a ? 1 : 0;
     node[a] = 1 + before_a;
   }
