@@ -779,20 +779,47 @@ static __device__ __forceinline__ RowCtx stream_row(const RowJob& Jb, StreamSmem
         }
       }
     } else {
-      for (int j = 0; j < n_slots; ++j) {
-        {
-          // the running bound: the best K-th entry any warp has cut to so far
-          const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
-          if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
-            thr_v = key_v(cb);
-            thr_i = key_i(cb);
-          }
+      // the running bound: the best K-th entry any warp has cut to so far
+      auto refresh = [&]() {
+        const Key cb = *reinterpret_cast<volatile Key*>(&S.cta_bound);
+        if (cb != 0ull && before(key_v(cb), key_i(cb), thr_v, thr_i)) {
+          thr_v = key_v(cb);
+          thr_i = key_i(cb);
         }
-        const float wmax = j < kTrackSlots ? S.wsmax[warp][j] : INFINITY;
-        if (!(wmax >= thr_v)) continue;   // the same in every lane of the warp
-        float x[kPer];
-        load_slot(j, x);
-        absorb(x, e_begin + j * kSlotElems + tid * 4);
+      };
+      if constexpr (kOverlapReload) {
+        // the next warp-slot at or after j whose recorded maximum reaches
+        // the bound (n_slots: none), the same in every lane of the warp.  It
+        // is loaded before the current slot is absorbed, so the L2 round
+        // trips overlap; the bound it was chosen with may since have risen,
+        // which only loads a slot whose elements then all fail the bound.
+        auto next_slot = [&](int j) {
+          refresh();
+          for (; j < n_slots; ++j)
+            if ((j < kTrackSlots ? S.wsmax[warp][j] : INFINITY) >= thr_v) break;
+          return j;
+        };
+        float xa[kPer], xb[kPer];
+        int j = next_slot(0);
+        if (j < n_slots) load_slot(j, xa);
+        while (j < n_slots) {
+          const int j1 = next_slot(j + 1);
+          if (j1 < n_slots) load_slot(j1, xb);
+          absorb(xa, e_begin + j * kSlotElems + tid * 4);
+          if (j1 >= n_slots) break;
+          j = next_slot(j1 + 1);
+          if (j < n_slots) load_slot(j, xa);
+          absorb(xb, e_begin + j1 * kSlotElems + tid * 4);
+        }
+      } else {
+        for (int j = 0; j < n_slots; ++j) {
+          refresh();
+          const float wmax = j < kTrackSlots ? S.wsmax[warp][j] : INFINITY;
+          if (!(wmax >= thr_v)) continue;   // the same in every lane of the warp
+          float x[kPer];
+          load_slot(j, x);
+          absorb(x, e_begin + j * kSlotElems + tid * 4);
+        }
       }
     }
   }
