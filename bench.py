@@ -823,8 +823,8 @@ TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch on the c2
     # workload from one ncu capture, keyed by the kernel's source hash
     # (_kernel_source_hash)
-    "build:c2": ("9b3de7b6b7ee", 31663360),
-    "verify:c2": ("a5769f8446cb", 36646400),
+    "build:c2": ("c75e3b8f121a", 31664128),
+    "verify:c2": ("7c14c3a06102", 36639232),
     "attn:c2": ("8e891d4a011d", 17385472),
 }
 
