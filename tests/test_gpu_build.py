@@ -132,6 +132,14 @@ def _adversarial(kind, R, V, k, seed):
         # the best k in the last elements of a row whose length is no
         # multiple of 4 (read element-wise by the stream)
         x[:, V - k:] = 100.0 + torch.rand(R, k, generator=g)
+    elif kind == "slots":
+        # one element of every 4096-element slot (16 KB of a row) raised to
+        # 5 + U(0, 1): the thread that reads that place of each slot has
+        # every slot at or above the second pass's bound, more than the five
+        # candidate slots a thread records, so its warp revisits every
+        # qualifying slot of its CTA's share
+        pos = torch.arange(0, V, 4096)
+        x[:, pos] = 5.0 + torch.rand(R, len(pos), generator=g)
     elif kind == "negative":
         x = x - 1000.0
     return x
@@ -145,6 +153,8 @@ def _adversarial(kind, R, V, k, seed):
     ("tail", 5003, 10, 3, 40),
     ("tail", 152063, 64, 1, 65),
     ("negative", 20000, 8, 3, 30),
+    ("slots", 152064, 10, 6, 60),    # row shares of 5+ slots: the fallback runs
+    ("slots", 152064, 16, 4, 60),
     ("plain", 100, 64, 1, 65),       # fewer valid lanes than the bound needs: no bound
 ])
 def test_adversarial_top_k_rows(kind, V, k, D, m):

@@ -173,9 +173,11 @@ def test_nucleus_full_vocab_tied_logits():
 
 # Sampling over target rows built to stress the row stream's top-k (a single
 # lane holding a row's best entries, 100 exact copies of a row's maximum, the
-# best entries in the unaligned tail of a row): the verify kernel's second
-# pass reloads its threads' candidate slots ahead of absorbing them, which
-# these rows exercise at the tie rules' edges.
+# best entries in the unaligned tail of a row, one lane with a raised element
+# in every slot): the verify kernel's second pass reloads its threads'
+# candidate slots, or for a lane with more qualifying slots than it records
+# every qualifying slot of its warp, ahead of absorbing them, which these
+# rows exercise at the tie rules' edges.
 @pytest.mark.parametrize("kind,V,k,p", [
     ("one_lane", 40000, 50, 1.0),
     ("one_lane", 152064, 2, 1.0),
@@ -183,6 +185,8 @@ def test_nucleus_full_vocab_tied_logits():
     ("duplicates", 152064, 64, 0.9),
     ("tail", 5003, 64, 1.0),
     ("tail", 152063, 16, 0.95),
+    ("slots", 152064, 50, 1.0),
+    ("slots", 152064, 8, 0.9),
 ])
 def test_sampling_on_adversarial_target_rows(kind, V, k, p):
     from tests.test_gpu_build import _adversarial
