@@ -12,13 +12,18 @@
 //     fp32 factors and fp64 accumulation;
 //   * the exact top-K (value desc, token id asc), K <= 64, in two passes
 //     over the CTA's share.  The first (the stream itself) keeps each
-//     thread's maximum and each warp's maximum of every slot; at its end the
-//     K-th largest of the CTA's 256 thread maxima (K distinct elements reach
-//     it) becomes the bound.  The second revisits only the warp-slots whose
-//     maximum reaches the bound (about K of them), reloading their elements
-//     from L2, and each warp keeps the elements at or above the bound in a
-//     private buffer: about K per CTA, where a one-pass running bound lets
-//     some K ln(n / K) through, nearly one per warp and slot.  A warp whose
+//     thread's five best slot maxima (its candidate slots) and each warp's
+//     maximum of every slot; at its end the K-th largest of the CTA's 256
+//     thread maxima (K distinct elements reach it) becomes the bound.  The
+//     second reloads from L2 each thread's candidate slots that reach the
+//     bound (about K thread-slots per CTA); a warp with a lane whose fifth
+//     candidate slot reaches the bound as well (it may have more) revisits
+//     instead every warp-slot whose maximum reaches the bound.  In the
+//     verify kernel the next slot's load overlaps the current slot's
+//     absorption on both routes.  Each warp keeps the elements at or above
+//     the bound in a private buffer: about K per CTA, where a one-pass
+//     running bound lets some K ln(n / K) through, nearly one per warp and
+//     slot.  A warp whose
 //     buffer grows past max(2K, 64) entries cuts it to its best K, which
 //     raises its bound to its exact K-th best; that entry is also published
 //     as the CTA's running bound (shared-memory atomicMax on the 64-bit
