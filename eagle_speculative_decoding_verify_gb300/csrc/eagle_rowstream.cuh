@@ -4,7 +4,7 @@
 // Work split: every row is streamed by one thread-block cluster of P CTAs
 // (P <= 8, chosen on the host so that one wave fills the GPU).  CTA p of the
 // cluster takes the p-th contiguous share of the row's 1024-element tiles
-// and streams it through a four-slot shared-memory ring (16 KB slots) filled
+// and streams it through a six-slot shared-memory ring (16 KB slots) filled
 // by 1-D bulk (TMA) copies; a slot is released through an mbarrier that each
 // warp arrives on once it holds its elements in registers, so no CTA barrier
 // is taken per slot.  Per CTA:
