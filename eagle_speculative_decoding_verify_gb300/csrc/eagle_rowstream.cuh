@@ -23,11 +23,10 @@
 //     absorption on both routes.  Each warp keeps the elements at or above
 //     the bound in a private buffer: about K per CTA, where a one-pass
 //     running bound lets some K ln(n / K) through, nearly one per warp and
-//     slot.  A warp whose
-//     buffer grows past max(2K, 64) entries cuts it to its best K, which
-//     raises its bound to its exact K-th best; that entry is also published
-//     as the CTA's running bound (shared-memory atomicMax on the 64-bit
-//     key), which every warp reads once per slot;
+//     slot.  A warp whose buffer grows past max(2K, 64) entries cuts it to
+//     its best K, which raises its bound to its exact K-th best; that entry
+//     is also published as the CTA's running bound (shared-memory atomicMax
+//     on the 64-bit key), which every warp reads once per slot;
 //   * the argmax (K = 1);
 //   * optionally per-tile (max, sum) of every warp for inverse-CDF sampling.
 // Row end: every warp ranks its survivors by counting into a sorted list of at
