@@ -34,15 +34,17 @@ def _sdpa_one(q, keys, vals, scale):
     return out[0, 0, 0]
 
 
-@pytest.mark.parametrize("Hq,Hkv,S", [(4, 2, 16), (6, 3, 0), (8, 1, 33)])
-def test_each_node_equals_causal_attention_over_its_chain(Hq, Hkv, S):
+@pytest.mark.parametrize("Hq,Hkv,S,scale", [(4, 2, 16, None), (6, 3, 0, None), (8, 1, 33, None),
+                                            (4, 2, 16, 0.05), (2, 1, 9, 0.7)])
+def test_each_node_equals_causal_attention_over_its_chain(Hq, Hkv, S, scale):
+    # scale None: the default 1/sqrt(d); otherwise the caller's score scale
     t = _tree(Hq + S)
     m, d = t["m"], 16
     q, kc, vc, tk, tv = _inputs(S, m, Hq, Hkv, d, S)
     out = tree_attention(q.numpy(), kc.numpy(), vc.numpy(), tk.numpy(), tv.numpy(),
-                         t["mask"], S)
+                         t["mask"], S, scale=scale)
     g = Hq // Hkv
-    scale = 1.0 / np.sqrt(d)
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
     for i in range(m):
         chain = []
         n = i
@@ -58,7 +60,7 @@ def test_each_node_equals_causal_attention_over_its_chain(Hq, Hkv, S):
             np.testing.assert_allclose(out[i, h], ref.numpy(), rtol=1e-12, atol=1e-12)
     rows = [(0, 0), (m - 1, Hq - 1), (m // 2, 1)]
     sampled = tree_attention_rows(q.numpy(), kc.numpy(), vc.numpy(), tk.numpy(), tv.numpy(),
-                                  t["mask"], S, rows)
+                                  t["mask"], S, rows, scale=scale)
     for n, (i, h) in enumerate(rows):
         np.testing.assert_allclose(sampled[n], out[i, h], rtol=1e-12, atol=1e-12)
 
